@@ -1,0 +1,238 @@
+/*
+ * zc.h -- C ABI of libzc: lossless BF16 exponent coding on one GB300 (sm_103a).
+ *
+ * The method is the one described in the technical summary of "ZipCCL:
+ * Efficient Lossless Data Compression of Communication Collectives for
+ * Accelerating LLM Training" (Lin, Pan, Fan, Shi, Chu, 2026), cited below as
+ * [ZipCCL §x]:
+ *   §2.A  LLM tensors are near-Gaussian, so BF16 exponents concentrate: the
+ *         seven most frequent exponents cover about 97% of values, and they
+ *         can be predicted from the layer's standard deviation sigma instead
+ *         of an online histogram.
+ *   §2.B  each value is split into sign-mantissa bits and exponent bits; an
+ *         exponent among the top 7 becomes a 3-bit code 001..111, any other
+ *         exponent becomes code 000 and its full 8 bits go to a separate
+ *         escape ("zero-point") array; 16 -> 11 bits per value.
+ *   §2.C  the 3-bit codes are kept as three 1-bit arrays in a column-major
+ *         layout, blocks padded to 128-byte boundaries.
+ *   §2.D  a zipped reduce-scatter is an all-to-all of compressed shards plus a
+ *         local reduction; MoE all-to-all sends a fixed-size part first and a
+ *         variable-size part after it.
+ *
+ * ------------------------------------------------------------------------
+ * Stream format "ZC1" (all integers little-endian)
+ * ------------------------------------------------------------------------
+ * A tensor of n bfloat16 values (n < 2^32) becomes two buffers:
+ *
+ * MAIN stream, exactly zc_main_bytes(n) = 128 + R + 5632 * ntiles bytes,
+ * ntiles = ceil(n / 4096), R = roundup(4 * ntiles, 128).  Its size depends on
+ * n alone, so it can be sent before the escape stream's size is known (the
+ * fixed-size part of [ZipCCL §2.D]).
+ *   [0, 128)     header: u32 magic 0x3142435A (bytes "ZCB1") @0, u16 version 1
+ *                @4, u16 flags 0 @6, u64 n @8, u32 tile_elems 4096 @16,
+ *                u32 ntiles @20, u64 n_esc @24, u8 codebook[7] @32, zeros to 128.
+ *   [128, 128+R) u32 esc_off[ntiles]: exclusive prefix sum of the per-tile
+ *                escape counts; zero padding up to R.
+ *   tiles        tile t at 128 + R + 5632 t holds elements [4096 t, 4096 t + 4096)
+ *                as four 1408-byte blocks of 1024 elements.  Block layout:
+ *                  [0, 1024)     sign-mantissa byte of element i = sign<<7 | mantissa
+ *                  [1024, 1152)  code plane 0 (bit 0 of every code)
+ *                  [1152, 1280)  code plane 1
+ *                  [1280, 1408)  code plane 2
+ *                A plane is a 4 x 32 byte matrix stored column-major: plane
+ *                byte q, bit j (LSB first) belongs to block element
+ *                256 * (q % 4) + 8 * (q / 4) + j.
+ *                Positions >= n in the last tile hold sign-mantissa 0 and code
+ *                0 and are not escapes.
+ * ESCAPE stream, n_esc bytes (header field): the 8-bit exponents of all values
+ *   whose exponent is not in the codebook.  Tile t's escapes occupy
+ *   [esc_off[t], esc_off[t] + count_t); inside a tile, blocks in order, inside
+ *   a block in ascending plane-bit position (q, j).
+ * CODEBOOK: 7 distinct exponent bytes in rank order; codebook[k] <-> code k+1,
+ *   code 0 <-> escape.  It travels in the header, so decoding needs no codebook.
+ *
+ * ------------------------------------------------------------------------
+ * Conventions for every entry point
+ * ------------------------------------------------------------------------
+ * - Pointers named d_* are device pointers owned by the caller (for example
+ *   tensors allocated by PyTorch); h_* are host pointers.  libzc never
+ *   allocates, never frees and never synchronises the host.  All device work
+ *   is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ * - Alignment: bfloat16 buffers, main streams and escape streams must be
+ *   16-byte aligned; the workspace 16-byte aligned; d_status 4-byte aligned.
+ * - Argument errors are returned synchronously and enqueue nothing.  A failed
+ *   kernel launch returns ZC_ERR_CUDA.
+ * - Data-dependent errors (corrupt stream, escape overflow, ...) cannot be
+ *   known on the host without a synchronisation, so the device writes them to
+ *   *d_status.  The caller zeroes that int32 before use; the first error wins
+ *   and later errors do not overwrite it.  Read it (after the stream has
+ *   finished) when convenient.
+ * - Workspace: calls that need one take (d_ws, ws_bytes).  Size it with
+ *   zc_workspace_size and fill it with zeros ONCE before its first use; every
+ *   call that completes without a device error leaves it ready for the next
+ *   call (no per-call memset is needed).  After a call that reported a device
+ *   error, zero it again.  Calls that share a workspace must be ordered on one
+ *   stream; concurrent calls need separate workspaces.
+ */
+#ifndef ZC_H
+#define ZC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZC_TILE_ELEMS 4096
+#define ZC_BLOCK_ELEMS 1024
+#define ZC_BLOCK_BYTES 1408
+#define ZC_TILE_BYTES 5632
+#define ZC_HEADER_BYTES 128
+#define ZC_MAGIC 0x3142435Au
+#define ZC_VERSION 1
+#define ZC_MAX_SHARDS 64
+#define ZC_WORKSPACE_HEADER_BYTES 4096
+#define ZC_WORKSPACE_BYTES_PER_TILE 16
+
+typedef enum zc_status {
+  ZC_OK = 0,
+  /* synchronous (returned) */
+  ZC_ERR_INVALID_ARG = 1,     /* null pointer, bad count, sigma not finite and positive, ... */
+  ZC_ERR_ALIGNMENT = 2,       /* a pointer violates the alignment rules above */
+  ZC_ERR_TOO_LARGE = 3,       /* n >= 2^32 */
+  ZC_ERR_WORKSPACE = 4,       /* ws_bytes smaller than zc_workspace_size */
+  ZC_ERR_CODEBOOK = 5,        /* host codebook with duplicate entries */
+  ZC_ERR_CUDA = 6,            /* a CUDA runtime call or kernel launch failed */
+  /* asynchronous (written to *d_status by the device) */
+  ZC_ERR_ESCAPE_OVERFLOW = 7, /* more escapes than esc_capacity; the count in the header is still exact */
+  ZC_ERR_BAD_HEADER = 8,      /* magic, version, tile size, ntiles, codebook or n_esc invalid */
+  ZC_ERR_CORRUPT_STREAM = 9,  /* offset table inconsistent with the code planes or the escape stream */
+  ZC_ERR_SIZE_MISMATCH = 10,  /* header n differs from the n passed in */
+  ZC_ERR_TIMEOUT = 11,        /* an inter-block wait gave up (about one second); output invalid */
+  ZC_ERR_DUP_CODEBOOK = 12    /* a device codebook holds a repeated exponent; nothing was encoded */
+} zc_status;
+
+/* Human-readable name of a status value (static string, never NULL). */
+const char* zc_status_string(int status);
+
+/* Version of the library and of the stream format, as "libzc <x.y> ZC1". */
+const char* zc_version(void);
+
+/*
+ * sigma -> codebook, the closed form of [ZipCCL §2.A] (host arithmetic, pure).
+ * The pages derive the top-7 exponents from the layer's weight standard
+ * deviation without printing the formula; libzc takes the plainest reading:
+ * p_e = P(exponent field of RNE_bf16(X) == e) for X ~ N(0, sigma^2), with the
+ * binade edges moved down by half an ulp for round-to-nearest-even, computed
+ * in double with erf/erfc; the 7 exponents with the largest p_e (ties: the
+ * smaller exponent first) in rank order.
+ * sigma must be finite and > 0 (else ZC_ERR_INVALID_ARG).  cb_out: 7 bytes, host.
+ */
+zc_status zc_codebook_from_sigma(double sigma, uint8_t cb_out[7]);
+
+/*
+ * Sizes of the two streams for n elements (pure).  *main_bytes is exact (see
+ * the format above); *max_escape_bytes = n is the worst case (every value an
+ * escape).  Either output pointer may be NULL.  n >= 2^32 -> ZC_ERR_TOO_LARGE.
+ */
+zc_status zc_compressed_size(uint64_t n, uint64_t* main_bytes, uint64_t* max_escape_bytes);
+
+/*
+ * Workspace bytes needed by a call that encodes `count` tensors of sizes
+ * h_ns[0..count-1] (compress, compress_batched, decompress_reduce with
+ * re-encoding) or computes a histogram (count = 1, any n):
+ * ZC_WORKSPACE_HEADER_BYTES + ZC_WORKSPACE_BYTES_PER_TILE * sum(ceil(n_i / 4096)).
+ */
+zc_status zc_workspace_size(const uint64_t* h_ns, int count, uint64_t* bytes);
+
+/*
+ * Exact exponent histogram -> top-7 codebook, the online alternative that
+ * [ZipCCL §2.A] avoids; kept for tensors whose sigma is unknown and for
+ * non-Gaussian payloads.  Counts all n exponent fields (0 and 255 included),
+ * orders (count desc, exponent asc) and writes the first 7 to d_cb_out (7
+ * bytes, device).  d_hist_out (256 x u32, device) receives the counts when
+ * not NULL.  One launch; the codebook never leaves the device, so it can feed
+ * zc_compress without a host round trip.  n = 0 yields codebook 0..6.
+ * d_in: n bf16 values, 16-byte aligned.  Workspace: zc_workspace_size(&n, 1).
+ */
+zc_status zc_histogram_topk(const void* d_in, uint64_t n, uint8_t* d_cb_out, uint32_t* d_hist_out,
+                            void* d_ws, uint64_t ws_bytes, int32_t* d_status, void* stream);
+
+/*
+ * Encode n bf16 values [ZipCCL §2.B, §2.C] into the ZC1 main stream d_main
+ * (zc_main_bytes(n) bytes, fully written, padding included) and the escape
+ * stream d_esc (esc_capacity bytes available).  d_cb: 7 distinct exponents,
+ * DEVICE memory (from zc_histogram_topk, or zc_codebook_from_sigma copied
+ * over).  The escape count is the header's n_esc; if it exceeds esc_capacity,
+ * only the first esc_capacity escapes are stored and *d_status gets
+ * ZC_ERR_ESCAPE_OVERFLOW.  A codebook with repeated entries sets
+ * ZC_ERR_DUP_CODEBOOK and writes nothing else.  One kernel launch: per-tile
+ * escape offsets come from a single-pass decoupled look-back scan whose waits
+ * are bounded (ZC_ERR_TIMEOUT).
+ */
+zc_status zc_compress(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_main, void* d_esc,
+                      uint64_t esc_capacity, void* d_ws, uint64_t ws_bytes, int32_t* d_status,
+                      void* stream);
+
+/*
+ * Decode a ZC1 stream back to n bf16 values, bit for bit (the inverse of
+ * zc_compress).  esc_bytes: the readable size of d_esc (at least the header's
+ * n_esc).  The header and every tile's escape range are validated on the
+ * device before use; a bad header writes nothing, a corrupt tile skips that
+ * tile; errors go to *d_status.  No workspace.
+ */
+zc_status zc_decompress(const void* d_main, const void* d_esc, uint64_t esc_bytes, uint64_t n,
+                        void* d_out, int32_t* d_status, void* stream);
+
+/*
+ * Local stage of a zipped reduce-scatter [ZipCCL §2.D]: decode P received
+ * shards of n elements each, add them in fp32 in rank order 0..P-1
+ * (acc = x_0; acc += x_r; IEEE round-to-nearest, subnormals kept), round to
+ * bf16 (round-to-nearest-even; a NaN sum becomes 0x7FC0), and optionally
+ * re-encode the result with the output codebook d_out_cb.
+ *   h_mains, h_escs, h_esc_bytes: host arrays of P device pointers / sizes.
+ *   d_out: n bf16 results, or NULL to skip writing them.
+ *   d_out_cb: device codebook for re-encoding, or NULL for no re-encoding (then
+ *     d_out must be non-NULL and d_out_main/d_out_esc/d_ws may be NULL).
+ *   d_out_main / d_out_esc / out_esc_capacity: as in zc_compress.
+ * 1 <= P <= ZC_MAX_SHARDS.  Every shard's header must carry n
+ * (ZC_ERR_SIZE_MISMATCH otherwise).  One fused kernel launch.
+ */
+zc_status zc_decompress_reduce(int P, const void* const* h_mains, const void* const* h_escs,
+                               const uint64_t* h_esc_bytes, uint64_t n, void* d_out,
+                               const uint8_t* d_out_cb, void* d_out_main, void* d_out_esc,
+                               uint64_t out_esc_capacity, void* d_ws, uint64_t ws_bytes,
+                               int32_t* d_status, void* stream);
+
+/*
+ * One tensor of a batched call.  compress: bf16 = input (n values), main/esc =
+ * outputs, esc_bytes = escape capacity, cb = device codebook.  decompress:
+ * main/esc = inputs, esc_bytes = readable escape bytes, bf16 = output, cb unused.
+ */
+typedef struct zc_tensor {
+  void* bf16;
+  void* main;
+  void* esc;
+  const uint8_t* cb;
+  uint64_t n;
+  uint64_t esc_bytes;
+} zc_tensor;
+
+/*
+ * Encode / decode many tensors in one launch over the flattened tile space,
+ * each tensor with its own codebook and its own escape scan (the per-layer
+ * bucket of [ZipCCL §4]'s Llama3-8B runs, or the per-destination chunks of an
+ * MoE all-to-all).  h_tensors: host array of `count` descriptors (count >= 1);
+ * the library splits very large counts into several launches.
+ * compress_batched needs a workspace of zc_workspace_size over all n.
+ */
+zc_status zc_compress_batched(int count, const zc_tensor* h_tensors, void* d_ws, uint64_t ws_bytes,
+                              int32_t* d_status, void* stream);
+zc_status zc_decompress_batched(int count, const zc_tensor* h_tensors, int32_t* d_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZC_H */

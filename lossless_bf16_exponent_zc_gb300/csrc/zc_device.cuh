@@ -1,0 +1,600 @@
+// zc_device.cuh -- device building blocks shared by the libzc kernels (sm_103a).
+//
+// Format constants, the per-warp TMA/mbarrier pipeline primitives, the bounded
+// decoupled look-back that gives every tile its escape offset, and the
+// per-tile encode and decode routines of ZC1 (layout in include/zc.h).
+// Method: [ZipCCL §2.B] field split, 3-bit codes, escape array; [ZipCCL §2.C]
+// three 1-bit code arrays, column-major, 128-byte blocks.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zc.h"
+
+namespace zc {
+
+constexpr uint32_t kTile = ZC_TILE_ELEMS;          // 4096 elements
+constexpr uint32_t kBlock = ZC_BLOCK_ELEMS;        // 1024 elements
+constexpr uint32_t kTileBytes = ZC_TILE_BYTES;     // 5632
+constexpr uint32_t kBlockBytes = ZC_BLOCK_BYTES;   // 1408
+constexpr uint32_t kHeader = ZC_HEADER_BYTES;      // 128
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+// Upper bound on any inter-block wait (look-back, TMA completion).  Normal
+// waits last microseconds; after this the kernel records ZC_ERR_TIMEOUT.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+// ---------------------------------------------------------------- workspace
+// The caller zero-fills the workspace once.  Every kernel returns it to a
+// reusable state: tickets and exit counters are reset by the last warp to
+// leave, look-back flags are tagged with a per-launch epoch so stale flags of
+// earlier launches never match, and histogram bins are cleared by the last CTA.
+struct WsHeader {
+  uint32_t ticket;     // next tile ticket of the running encoding launch
+  uint32_t exited;     // warps of the running encoding launch that have left
+  uint32_t epoch;      // epoch tag of the last finished encoding launch
+  uint32_t max_tiles;  // largest flag range ever used (cleared when the epoch wraps)
+  uint32_t hist_done;  // CTAs of the running histogram launch that have finished
+  uint32_t pad[27];
+  uint32_t hist[256];  // global exponent bins, all zero between calls
+};
+static_assert(sizeof(WsHeader) <= ZC_WORKSPACE_HEADER_BYTES, "workspace header too large");
+
+// Look-back flag of one tile: {epoch << 32 | escape count of the tile,
+// epoch << 32 | inclusive escape prefix}.  Each half is written once per
+// launch with a single 64-bit store, so a reader sees it whole or stale.
+struct __align__(16) Flag {
+  unsigned long long agg;
+  unsigned long long incl;
+};
+
+// ---------------------------------------------------------------- small helpers
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+__device__ __forceinline__ void set_status(int32_t* status, int code) {
+  atomicCAS(reinterpret_cast<int*>(status), 0, code);
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ ulonglong2 ld_relaxed_v2(const Flag* f) {
+  ulonglong2 v;
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];"
+               : "=l"(v.x), "=l"(v.y)
+               : "l"(f)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// ---------------------------------------------------------------- mbarrier + TMA
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (TMA) accesses to the same buffer.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, at most kWaitLimitNs.  Returns
+// false (and records ZC_ERR_TIMEOUT) if the limit is reached.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) {
+      set_status(status, ZC_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// One-dimensional TMA bulk copy global -> shared, completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 16-byte asynchronous copy that reads only `src_bytes` (0..16) and zero-fills
+// the rest; src and dst 16-byte aligned.
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+// Arrive on `bar` once all of this thread's earlier cp.async copies land; the
+// arrival counts toward the barrier's expected count.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// ---------------------------------------------------------------- warp scans
+__device__ __forceinline__ uint32_t warp_inclusive_scan(uint32_t v) {
+  const uint32_t lane = lane_id();
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t u = __shfl_up_sync(kFull, v, d);
+    if (lane >= static_cast<uint32_t>(d)) v += u;
+  }
+  return v;
+}
+
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
+  return v;
+}
+
+// ---------------------------------------------------------------- format helpers
+__host__ __device__ __forceinline__ uint64_t num_tiles(uint64_t n) { return (n + kTile - 1) / kTile; }
+__host__ __device__ __forceinline__ uint64_t table_bytes(uint64_t ntiles) { return (4 * ntiles + 127) / 128 * 128; }
+__host__ __device__ __forceinline__ uint64_t main_bytes(uint64_t n) {
+  return kHeader + table_bytes(num_tiles(n)) + static_cast<uint64_t>(kTileBytes) * num_tiles(n);
+}
+__device__ __forceinline__ uint8_t* tile_ptr(uint8_t* main, uint64_t ntiles, uint64_t t) {
+  return main + kHeader + table_bytes(ntiles) + static_cast<uint64_t>(kTileBytes) * t;
+}
+__device__ __forceinline__ const uint8_t* tile_ptr(const uint8_t* main, uint64_t ntiles, uint64_t t) {
+  return main + kHeader + table_bytes(ntiles) + static_cast<uint64_t>(kTileBytes) * t;
+}
+
+// Valid-element mask of this lane in block `blk` of a tile holding `n_tile`
+// valid elements: bit 8k + j <-> block element 256k + 8*lane + j.
+__device__ __forceinline__ uint32_t lane_valid_mask(uint32_t blk, uint32_t n_tile, uint32_t lane) {
+  if (n_tile >= kTile) return kFull;
+  uint32_t v = 0;
+#pragma unroll
+  for (uint32_t k = 0; k < 4; k++) {
+    const int start = static_cast<int>(blk * kBlock + k * 256 + lane * 8);
+    int c = static_cast<int>(n_tile) - start;
+    c = c < 0 ? 0 : (c > 8 ? 8 : c);
+    v |= ((1u << c) - 1u) << (8 * k);
+  }
+  return v;
+}
+
+// ---------------------------------------------------------------- encode side
+// Encoder lookup table, one u32 per exponent e: bit 0 / 8 / 16 = bits 0 / 1 / 2
+// of e's code, bit 24 = "escape".  Shifting an entry left by j (0..7) and
+// adding moves element j's bits into bit j of four byte lanes at once.
+__device__ __forceinline__ uint32_t enc_lut_entry(uint32_t code) {
+  return code ? ((code & 1u) | (((code >> 1) & 1u) << 8) | (((code >> 2) & 1u) << 16)) : (1u << 24);
+}
+
+// Builds the per-warp encoder table from a device codebook; returns false if
+// the codebook repeats an exponent.  Ends with __syncwarp().
+__device__ __forceinline__ bool build_enc_lut(uint32_t* lut, const uint8_t* cb_dev) {
+  const uint32_t lane = lane_id();
+  uint32_t cb[7];
+#pragma unroll
+  for (int k = 0; k < 7; k++) cb[k] = __ldg(cb_dev + k);
+  bool dup = false;
+#pragma unroll
+  for (int a = 0; a < 7; a++)
+#pragma unroll
+    for (int b = a + 1; b < 7; b++) dup |= (cb[a] == cb[b]);
+  for (uint32_t e = lane; e < 256; e += 32) {
+    uint32_t code = 0;
+#pragma unroll
+    for (int k = 0; k < 7; k++) code = (cb[k] == e) ? static_cast<uint32_t>(k + 1) : code;
+    lut[e] = enc_lut_entry(code);
+  }
+  __syncwarp();
+  return !dup;
+}
+
+// Per-lane escape bookkeeping of one encoded tile.
+struct TileEsc {
+  uint32_t mask[4];  // bit 8k + j: block element 256k + 8*lane + j is an escape
+  uint32_t base[4];  // tile-local rank of this lane's first escape in each block
+  uint32_t total;    // escapes in the tile (same in every lane)
+};
+
+// Encodes one tile held in shared memory (`tb`: 4096 bf16 bit patterns, zero
+// beyond n_tile) into its 5632-byte ZC1 tile at `out` (global).  One warp.
+// Lane l of group k handles block elements 256k + 8l .. 256k + 8l + 7 (one
+// 16-byte vector); its 4 groups' code bits form one plane word per plane,
+// which is exactly the column-major plane layout (byte 4l + k).
+__device__ __forceinline__ void encode_tile(const uint16_t* tb, uint32_t n_tile, const uint32_t* lut,
+                                            uint8_t* out, TileEsc& te) {
+  const uint32_t lane = lane_id();
+  uint32_t run = 0;
+#pragma unroll
+  for (uint32_t blk = 0; blk < 4; blk++) {
+    uint32_t acc[4];
+    uint2 smv[4];
+#pragma unroll
+    for (uint32_t k = 0; k < 4; k++) {
+      const uint4 v = *reinterpret_cast<const uint4*>(tb + blk * kBlock + k * 256 + lane * 8);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t a = 0;
+#pragma unroll
+      for (int h = 0; h < 4; h++) {
+        a += lut[(w[h] >> 7) & 0xFFu] << (2 * h);
+        a += lut[(w[h] >> 23) & 0xFFu] << (2 * h + 1);
+      }
+      acc[k] = a;
+      // sign-mantissa bytes: low byte of each value holds 7 mantissa bits,
+      // high byte holds the sign in bit 7
+      const uint32_t lo01 = __byte_perm(w[0], w[1], 0x6420), hi01 = __byte_perm(w[0], w[1], 0x7531);
+      const uint32_t lo23 = __byte_perm(w[2], w[3], 0x6420), hi23 = __byte_perm(w[2], w[3], 0x7531);
+      smv[k] = make_uint2((lo01 & 0x7F7F7F7Fu) | (hi01 & 0x80808080u), (lo23 & 0x7F7F7F7Fu) | (hi23 & 0x80808080u));
+    }
+    uint8_t* ob = out + blk * kBlockBytes;
+#pragma unroll
+    for (uint32_t k = 0; k < 4; k++) *reinterpret_cast<uint2*>(ob + k * 256 + lane * 8) = smv[k];
+    // transpose: byte k of plane word b = byte b of acc[k]
+    const uint32_t t01 = __byte_perm(acc[0], acc[1], 0x5140), t23 = __byte_perm(acc[2], acc[3], 0x5140);
+    const uint32_t u01 = __byte_perm(acc[0], acc[1], 0x7362), u23 = __byte_perm(acc[2], acc[3], 0x7362);
+    uint32_t w0 = __byte_perm(t01, t23, 0x5410);
+    uint32_t w1 = __byte_perm(t01, t23, 0x7632);
+    uint32_t w2 = __byte_perm(u01, u23, 0x5410);
+    uint32_t x = __byte_perm(u01, u23, 0x7632);
+    const uint32_t valid = lane_valid_mask(blk, n_tile, lane);
+    w0 &= valid;
+    w1 &= valid;
+    w2 &= valid;
+    x &= valid;
+    *reinterpret_cast<uint32_t*>(ob + 1024 + lane * 4) = w0;
+    *reinterpret_cast<uint32_t*>(ob + 1152 + lane * 4) = w1;
+    *reinterpret_cast<uint32_t*>(ob + 1280 + lane * 4) = w2;
+    const uint32_t c = __popc(x);
+    const uint32_t inc = warp_inclusive_scan(c);
+    te.mask[blk] = x;
+    te.base[blk] = run + inc - c;
+    run += __shfl_sync(kFull, inc, 31);
+  }
+  te.total = run;
+}
+
+// Writes the tile's escapes (their 8-bit exponents, read back from the tile
+// in shared memory) at global positions prefix + rank, skipping positions at
+// or beyond `cap`.  Escapes of a lane are consecutive, in bit order.
+__device__ __forceinline__ void write_escapes(const uint16_t* tb, const TileEsc& te, uint64_t prefix, uint8_t* esc,
+                                              uint64_t cap) {
+  const uint32_t lane = lane_id();
+#pragma unroll
+  for (uint32_t blk = 0; blk < 4; blk++) {
+    uint32_t m = te.mask[blk];
+    uint64_t pos = prefix + te.base[blk];
+    while (m) {
+      const uint32_t p = __ffs(m) - 1;
+      m &= m - 1;
+      const uint32_t i = blk * kBlock + (p >> 3) * 256 + lane * 8 + (p & 7);
+      const uint32_t e = (tb[i] >> 7) & 0xFFu;
+      if (pos < cap) esc[pos] = static_cast<uint8_t>(e);
+      pos++;
+    }
+  }
+}
+
+// Decoupled look-back (single pass): returns the exclusive escape prefix of
+// tile g, whose tensor starts at global tile g0, by summing the aggregates of
+// preceding tiles until one carrying an inclusive prefix is found.  Tiles are
+// handed out by an atomic ticket in increasing order and every ticket holder
+// is resident, so predecessors always make progress; the wait is still
+// bounded (ZC_ERR_TIMEOUT, prefix then meaningless).  `*timed_out` is set.
+__device__ __forceinline__ uint64_t lookback(const Flag* flags, uint32_t g, uint32_t g0, uint32_t epoch,
+                                             int32_t* status, bool* timed_out) {
+  const uint32_t lane = lane_id();
+  uint64_t prefix = 0;
+  int64_t end = g;  // exclusive end of the window
+  unsigned long long t0 = 0;
+  *timed_out = false;
+  while (true) {
+    const int64_t idx = end - 1 - static_cast<int64_t>(lane);
+    uint32_t st = 2, val = 0;
+    if (idx >= static_cast<int64_t>(g0)) {
+      const ulonglong2 f = ld_relaxed_v2(flags + idx);
+      if (static_cast<uint32_t>(f.y >> 32) == epoch) {
+        st = 2;
+        val = static_cast<uint32_t>(f.y);
+      } else if (static_cast<uint32_t>(f.x >> 32) == epoch) {
+        st = 1;
+        val = static_cast<uint32_t>(f.x);
+      } else {
+        st = 0;
+      }
+    }
+    const uint32_t incl_lanes = __ballot_sync(kFull, st == 2);
+    const uint32_t missing = __ballot_sync(kFull, st == 0);
+    const uint32_t first = incl_lanes ? static_cast<uint32_t>(__ffs(incl_lanes) - 1) : 31u;
+    const uint32_t upto = (first == 31) ? kFull : ((2u << first) - 1u);
+    if (missing & upto) {
+      unsigned long long now = 0;
+      if (lane == 0) now = global_ns();
+      now = __shfl_sync(kFull, now, 0);
+      if (t0 == 0) t0 = now;
+      if (now - t0 > kWaitLimitNs) {
+        if (lane == 0) set_status(status, ZC_ERR_TIMEOUT);
+        *timed_out = true;
+        return prefix;
+      }
+      __nanosleep(64);
+      continue;
+    }
+    prefix += warp_sum(lane <= first ? val : 0u);
+    if (incl_lanes) return prefix;
+    end -= 32;
+  }
+}
+
+// ---------------------------------------------------------------- decode side
+// Spread tables: spread[b][v] puts bit j of byte v at bit 4j + b, so
+// spread[0][p0] | spread[1][p1] | spread[2][p2] is a byte-permute selector
+// whose nibble j is the 3-bit code of element j.
+__device__ __forceinline__ void build_spread_tables(uint32_t* spread /* 3 x 256 */) {
+  for (uint32_t i = threadIdx.x; i < 768; i += blockDim.x) {
+    const uint32_t b = i >> 8, v = i & 255u;
+    uint32_t s = 0;
+#pragma unroll
+    for (int j = 0; j < 8; j++) s |= ((v >> j) & 1u) << (4 * j + b);
+    spread[i] = s;
+  }
+}
+
+// Code -> exponent table as two words for __byte_perm: byte c of (t0, t1) is
+// the exponent of code c (byte 0, code 0 = escape, is a placeholder 0).
+struct DecTable {
+  uint32_t t0, t1;
+};
+
+__device__ __forceinline__ DecTable make_dec_table(const uint8_t cb[7]) {
+  DecTable d;
+  d.t0 = (static_cast<uint32_t>(cb[0]) << 8) | (static_cast<uint32_t>(cb[1]) << 16) |
+         (static_cast<uint32_t>(cb[2]) << 24);
+  d.t1 = static_cast<uint32_t>(cb[3]) | (static_cast<uint32_t>(cb[4]) << 8) | (static_cast<uint32_t>(cb[5]) << 16) |
+         (static_cast<uint32_t>(cb[6]) << 24);
+  return d;
+}
+
+// Two packed bf16 values from bytes x = [sm0, e0, sm1, e1] (16-bit lanes e<<8 | sm):
+// value = sign << 15 | e << 7 | mantissa.
+__device__ __forceinline__ uint32_t join_pair(uint32_t x) {
+  return ((x >> 1) & 0x7F807F80u) | (x & 0x007F007Fu) | ((x << 8) & 0x80008000u);
+}
+
+// Source of escape bytes for one (tile, stream): the first `staged` ranks sit
+// in shared memory at `smem`, the rest are read from global at `glob`; ranks at
+// or beyond `count` are invalid (corrupt stream) and read as 0.
+struct EscSource {
+  const uint8_t* smem;
+  const uint8_t* glob;
+  uint32_t staged;
+  uint32_t count;
+};
+
+__device__ __forceinline__ uint32_t esc_byte(const EscSource& s, uint32_t rank) {
+  if (rank < s.staged) return s.smem[rank];
+  if (rank < s.count) return __ldg(s.glob + rank);
+  return 0;
+}
+
+// Decodes block `blk` of a ZC1 tile held in shared memory (`tile`: 5632 B) for
+// this lane: out[k] (k = 0..3) receives 4 words = 8 bf16 values of block
+// elements 256k + 8*lane + 0..7.  `scratch` is this warp's 1 KB exponent
+// scratch.  `run` is the tile-local rank of the block's first escape and is
+// advanced past the block.  Returns the number of code-0 positions (escapes).
+__device__ __forceinline__ uint32_t decode_block(const uint8_t* tile, uint32_t blk, uint32_t n_tile,
+                                                 const uint32_t* spread, DecTable dt, const EscSource& es,
+                                                 uint32_t& run, uint8_t* scratch, uint4 out[4]) {
+  const uint32_t lane = lane_id();
+  const uint8_t* b = tile + blk * kBlockBytes;
+  const uint32_t w0 = *reinterpret_cast<const uint32_t*>(b + 1024 + lane * 4);
+  const uint32_t w1 = *reinterpret_cast<const uint32_t*>(b + 1152 + lane * 4);
+  const uint32_t w2 = *reinterpret_cast<const uint32_t*>(b + 1280 + lane * 4);
+  const uint32_t z = ~(w0 | w1 | w2) & lane_valid_mask(blk, n_tile, lane);
+  const uint32_t c = __popc(z);
+  const uint32_t inc = warp_inclusive_scan(c);
+  uint32_t rank = run + inc - c;
+  run += __shfl_sync(kFull, inc, 31);
+
+  // exponents of the 32 elements, 4 per word: ex[2k] = elements 0..3 of group k
+  uint32_t ex[8];
+#pragma unroll
+  for (uint32_t k = 0; k < 4; k++) {
+    const uint32_t sel = spread[(w0 >> (8 * k)) & 0xFFu] | spread[256 + ((w1 >> (8 * k)) & 0xFFu)] |
+                         spread[512 + ((w2 >> (8 * k)) & 0xFFu)];
+    ex[2 * k] = __byte_perm(dt.t0, dt.t1, sel & 0xFFFFu);
+    ex[2 * k + 1] = __byte_perm(dt.t0, dt.t1, sel >> 16);
+  }
+  if (__any_sync(kFull, z != 0)) {
+    // patch escapes through shared memory (bit p of z <-> byte p of ex)
+    uint4* sp = reinterpret_cast<uint4*>(scratch + lane * 32);
+    sp[0] = make_uint4(ex[0], ex[1], ex[2], ex[3]);
+    sp[1] = make_uint4(ex[4], ex[5], ex[6], ex[7]);
+    uint32_t m = z;
+    while (m) {
+      const uint32_t p = __ffs(m) - 1;
+      m &= m - 1;
+      scratch[lane * 32 + p] = static_cast<uint8_t>(esc_byte(es, rank));
+      rank++;
+    }
+    const uint4 a = sp[0], bq = sp[1];
+    ex[0] = a.x; ex[1] = a.y; ex[2] = a.z; ex[3] = a.w;
+    ex[4] = bq.x; ex[5] = bq.y; ex[6] = bq.z; ex[7] = bq.w;
+    __syncwarp();
+  }
+#pragma unroll
+  for (uint32_t k = 0; k < 4; k++) {
+    const uint2 sm = *reinterpret_cast<const uint2*>(b + k * 256 + lane * 8);
+    out[k].x = join_pair(__byte_perm(sm.x, ex[2 * k], 0x5140));
+    out[k].y = join_pair(__byte_perm(sm.x, ex[2 * k], 0x7362));
+    out[k].z = join_pair(__byte_perm(sm.y, ex[2 * k + 1], 0x5140));
+    out[k].w = join_pair(__byte_perm(sm.y, ex[2 * k + 1], 0x7362));
+  }
+  return c;
+}
+
+// Stores 8 bf16 values (one 16-byte vector) at element index `idx` of a tensor
+// of n elements, element by element past the end.
+__device__ __forceinline__ void store8_guarded(uint16_t* out, uint64_t idx, uint64_t n, uint4 v) {
+  if (idx + 8 <= n) {
+    *reinterpret_cast<uint4*>(out + idx) = v;
+  } else if (idx < n) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (uint32_t j = 0; idx + j < n; j++) out[idx + j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+  }
+}
+
+// Writes the 128-byte ZC1 header words of a tensor except n_esc (bytes 24..31).
+// Lane i writes word i.
+__device__ __forceinline__ void write_header_words(uint8_t* main, uint64_t n, const uint8_t* cb_dev) {
+  const uint32_t lane = lane_id();
+  const uint64_t nt = num_tiles(n);
+  uint32_t w = 0;
+  switch (lane) {
+    case 0: w = ZC_MAGIC; break;
+    case 1: w = ZC_VERSION; break;  // flags 0 in the high half
+    case 2: w = static_cast<uint32_t>(n); break;
+    case 3: w = static_cast<uint32_t>(n >> 32); break;
+    case 4: w = kTile; break;
+    case 5: w = static_cast<uint32_t>(nt); break;
+    case 8:
+      w = static_cast<uint32_t>(__ldg(cb_dev)) | (static_cast<uint32_t>(__ldg(cb_dev + 1)) << 8) |
+          (static_cast<uint32_t>(__ldg(cb_dev + 2)) << 16) | (static_cast<uint32_t>(__ldg(cb_dev + 3)) << 24);
+      break;
+    case 9:
+      w = static_cast<uint32_t>(__ldg(cb_dev + 4)) | (static_cast<uint32_t>(__ldg(cb_dev + 5)) << 8) |
+          (static_cast<uint32_t>(__ldg(cb_dev + 6)) << 16);
+      break;
+    default: w = 0;
+  }
+  if (lane != 6 && lane != 7) reinterpret_cast<uint32_t*>(main)[lane] = w;
+}
+
+// Writes n_esc into the header and zeroes the offset table's padding.  Warp.
+__device__ __forceinline__ void write_header_tail(uint8_t* main, uint64_t ntiles, uint64_t n_esc) {
+  const uint32_t lane = lane_id();
+  if (lane == 0) *reinterpret_cast<unsigned long long*>(main + 24) = n_esc;
+  const uint64_t first = kHeader + 4 * ntiles, last = kHeader + table_bytes(ntiles);
+  for (uint64_t o = first + 4 * lane; o < last; o += 128) *reinterpret_cast<uint32_t*>(main + o) = 0;
+}
+
+// The epoch tag used by a launch: one more than the last finished launch's,
+// never 0 (the value of a zero-filled workspace).
+__device__ __forceinline__ uint32_t launch_epoch(const WsHeader* ws) {
+  const uint32_t e = *reinterpret_cast<const volatile uint32_t*>(&ws->epoch) + 1u;
+  return e == 0 ? 1u : e;
+}
+
+// Exit protocol of a ticketed launch: every warp calls this once, after its
+// last use of a ticket.  The last warp resets the ticket and exit counters and
+// publishes the epoch; when the epoch wraps it clears every flag first, so a
+// flag written 2^32 launches earlier can never pass for a current one.
+__device__ __forceinline__ void ticket_exit(WsHeader* ws, Flag* flags, uint32_t epoch, uint32_t total_tiles,
+                                            uint32_t total_warps) {
+  const uint32_t lane = lane_id();
+  uint32_t last = 0;
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    last = (atomicAdd(&ws->exited, 1u) == total_warps - 1) ? 1u : 0u;
+  }
+  last = __shfl_sync(kFull, last, 0);
+  if (!last) return;
+  __threadfence();
+  const uint32_t maxt = max(*reinterpret_cast<volatile uint32_t*>(&ws->max_tiles), total_tiles);
+  if (epoch == 0xFFFFFFFFu) {
+    for (uint32_t i = lane; i < maxt; i += 32) flags[i] = Flag{0ull, 0ull};
+    __threadfence();
+  }
+  if (lane == 0) {
+    ws->max_tiles = maxt;
+    ws->ticket = 0;
+    ws->exited = 0;
+    ws->epoch = (epoch == 0xFFFFFFFFu) ? 0u : epoch;
+    __threadfence();
+  }
+}
+
+__device__ __forceinline__ uint32_t draw_ticket(WsHeader* ws) {
+  uint32_t t = 0;
+  if (lane_id() == 0) t = atomicAdd(&ws->ticket, 1u);
+  return __shfl_sync(kFull, t, 0);
+}
+
+
+// After encode_tile: publish the tile's escape count, find its escape offset by
+// look-back, write the offset-table entry, the header parts this tile owns
+// (tile 0: everything but n_esc; last tile: n_esc and table padding) and the
+// escapes themselves.  Tile g of the launch is local tile lt of its tensor,
+// whose first global tile is g - lt.  Warp-wide.
+__device__ __forceinline__ void publish_tile(Flag* flags, uint32_t g, uint32_t lt, uint32_t epoch, const TileEsc& te,
+                                             const uint16_t* tb, uint8_t* main, uint64_t n, const uint8_t* cb,
+                                             uint8_t* esc, uint64_t esc_cap, int32_t* status) {
+  const uint32_t lane = lane_id();
+  const uint64_t ntiles = num_tiles(n);
+  const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
+  uint64_t prefix = 0;
+  if (lt == 0) {
+    if (lane == 0) st_relaxed(&flags[g].incl, tag | te.total);
+  } else {
+    if (lane == 0) st_relaxed(&flags[g].agg, tag | te.total);
+    bool timed_out;
+    prefix = lookback(flags, g, g - lt, epoch, status, &timed_out);
+    if (lane == 0) st_relaxed(&flags[g].incl, tag | static_cast<uint32_t>(prefix + te.total));
+  }
+  if (lane == 0) *reinterpret_cast<uint32_t*>(main + kHeader + 4ull * lt) = static_cast<uint32_t>(prefix);
+  if (lt == 0) write_header_words(main, n, cb);
+  if (lt + 1 == ntiles) {
+    const uint64_t n_esc = prefix + te.total;
+    write_header_tail(main, ntiles, n_esc);
+    if (lane == 0 && n_esc > esc_cap) set_status(status, ZC_ERR_ESCAPE_OVERFLOW);
+  }
+  write_escapes(tb, te, prefix, esc, esc_cap);
+}
+
+// bfloat16 bits of f, rounded to nearest even (IEEE-754 definition: add half
+// an ulp minus one plus the kept lowest bit, then truncate); NaN -> 0x7FC0.
+__device__ __forceinline__ uint32_t f32_to_bf16_rne(float f) {
+  const uint32_t a = __float_as_uint(f);
+  if ((a & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0u;
+  return (a + 0x7FFFu + ((a >> 16) & 1u)) >> 16;
+}
+
+}  // namespace zc

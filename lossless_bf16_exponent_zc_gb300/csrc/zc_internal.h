@@ -1,0 +1,61 @@
+// zc_internal.h -- launch interface between the C ABI (zc_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zc.h"
+
+namespace zc {
+
+struct WsHeader;
+struct Flag;
+
+// Largest number of tensors one batched launch carries in its parameters;
+// larger batches are split into several launches by the host.
+constexpr int kMaxBatch = 32;
+
+struct EncTensor {
+  const uint16_t* in;
+  uint8_t* main;
+  uint8_t* esc;
+  const uint8_t* cb;
+  uint64_t n;
+  uint64_t esc_cap;
+};
+
+struct DecTensor {
+  const uint8_t* main;
+  const uint8_t* esc;
+  uint16_t* out;
+  uint64_t n;
+  uint64_t esc_bytes;
+};
+
+struct Shard {
+  const uint8_t* main;
+  const uint8_t* esc;
+  uint64_t esc_bytes;
+};
+
+struct DeviceInfo {
+  int sm_count;
+};
+
+cudaError_t device_info(DeviceInfo* info);
+
+// count <= kMaxBatch; flags = workspace flag array (one per tile of the launch).
+cudaError_t launch_encode(const EncTensor* ts, int count, WsHeader* ws, Flag* flags, int32_t* status,
+                          cudaStream_t stream, const DeviceInfo& dev);
+
+cudaError_t launch_decode(const DecTensor* ts, int count, int32_t* status, cudaStream_t stream,
+                          const DeviceInfo& dev);
+
+cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out, const uint8_t* out_cb,
+                          uint8_t* out_main, uint8_t* out_esc, uint64_t out_cap, WsHeader* ws, Flag* flags,
+                          int32_t* status, cudaStream_t stream, const DeviceInfo& dev);
+
+cudaError_t launch_histogram(const uint16_t* in, uint64_t n, uint8_t* cb_out, uint32_t* hist_out, WsHeader* ws,
+                             cudaStream_t stream, const DeviceInfo& dev);
+
+}  // namespace zc

@@ -1,0 +1,258 @@
+"""Thin Python binding of libzc (the C ABI in include/zc.h).
+
+Argument marshalling only: every step runs in libzc's CUDA kernels on the
+caller's current torch stream.  Tensors are passed as raw device pointers;
+bfloat16 data may be given as ``torch.bfloat16``, ``torch.int16`` or
+``torch.uint16`` tensors (the bits are what matters).  There is no CPU path:
+if libzc cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Sequence
+
+import numpy as np
+import torch
+
+from . import _build
+
+TILE = 4096
+HEADER_BYTES = 128
+WORKSPACE_HEADER_BYTES = 4096
+WORKSPACE_BYTES_PER_TILE = 16
+MAX_SHARDS = 64
+
+STATUS_NAMES = [
+    "ZC_OK", "ZC_ERR_INVALID_ARG", "ZC_ERR_ALIGNMENT", "ZC_ERR_TOO_LARGE", "ZC_ERR_WORKSPACE",
+    "ZC_ERR_CODEBOOK", "ZC_ERR_CUDA", "ZC_ERR_ESCAPE_OVERFLOW", "ZC_ERR_BAD_HEADER",
+    "ZC_ERR_CORRUPT_STREAM", "ZC_ERR_SIZE_MISMATCH", "ZC_ERR_TIMEOUT", "ZC_ERR_DUP_CODEBOOK",
+]
+for _i, _name in enumerate(STATUS_NAMES):
+    globals()[_name[3:]] = _i   # OK, ERR_INVALID_ARG, ...
+
+
+class ZcError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+        self.code = code
+
+
+class ZcTensor(ctypes.Structure):
+    _fields_ = [("bf16", ctypes.c_void_p), ("main", ctypes.c_void_p), ("esc", ctypes.c_void_p),
+                ("cb", ctypes.c_void_p), ("n", ctypes.c_uint64), ("esc_bytes", ctypes.c_uint64)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libzc.so (building it in-tree first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libzc not found at {path}")
+    lib = ctypes.CDLL(path)
+    vp, u64, i32 = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int
+    u64p = ctypes.POINTER(ctypes.c_uint64)
+    lib.zc_status_string.argtypes = [i32]
+    lib.zc_status_string.restype = ctypes.c_char_p
+    lib.zc_version.argtypes = []
+    lib.zc_version.restype = ctypes.c_char_p
+    lib.zc_codebook_from_sigma.argtypes = [ctypes.c_double, ctypes.POINTER(ctypes.c_uint8)]
+    lib.zc_compressed_size.argtypes = [u64, u64p, u64p]
+    lib.zc_workspace_size.argtypes = [u64p, i32, u64p]
+    lib.zc_histogram_topk.argtypes = [vp, u64, vp, vp, vp, u64, vp, vp]
+    lib.zc_compress.argtypes = [vp, u64, vp, vp, vp, u64, vp, u64, vp, vp]
+    lib.zc_decompress.argtypes = [vp, vp, u64, u64, vp, vp, vp]
+    lib.zc_decompress_reduce.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), u64p, u64, vp, vp, vp, vp,
+                                         u64, vp, u64, vp, vp]
+    lib.zc_compress_batched.argtypes = [i32, ctypes.POINTER(ZcTensor), vp, u64, vp, vp]
+    lib.zc_decompress_batched.argtypes = [i32, ctypes.POINTER(ZcTensor), vp, vp]
+    for name in ("zc_codebook_from_sigma", "zc_compressed_size", "zc_workspace_size", "zc_histogram_topk",
+                 "zc_compress", "zc_decompress", "zc_decompress_reduce", "zc_compress_batched",
+                 "zc_decompress_batched"):
+        getattr(lib, name).restype = i32
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().zc_status_string(int(code)).decode()
+
+
+def version() -> str:
+    return load().zc_version().decode()
+
+
+def _check(code: int, where: str) -> None:
+    if code != OK:  # noqa: F821 - defined from STATUS_NAMES
+        raise ZcError(code, where)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libzc takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("libzc takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream: torch.cuda.Stream | None = None) -> int:
+    return (stream or torch.cuda.current_stream()).cuda_stream
+
+
+def _nelem16(x: torch.Tensor) -> int:
+    if x.element_size() != 2:
+        raise ValueError("bfloat16 data must be a 2-byte dtype (bfloat16, int16 or uint16)")
+    return x.numel()
+
+
+# ------------------------------------------------------------------ host-side pure functions
+def codebook_from_sigma(sigma: float) -> np.ndarray:
+    cb = (ctypes.c_uint8 * 7)()
+    _check(load().zc_codebook_from_sigma(float(sigma), cb), "zc_codebook_from_sigma")
+    return np.frombuffer(bytes(cb), np.uint8).copy()
+
+
+def compressed_size(n: int) -> tuple[int, int]:
+    m, e = ctypes.c_uint64(), ctypes.c_uint64()
+    _check(load().zc_compressed_size(int(n), ctypes.byref(m), ctypes.byref(e)), "zc_compressed_size")
+    return m.value, e.value
+
+
+def workspace_size(ns: Sequence[int] | int) -> int:
+    ns = [int(ns)] if isinstance(ns, (int, np.integer)) else [int(v) for v in ns]
+    arr = (ctypes.c_uint64 * len(ns))(*ns)
+    out = ctypes.c_uint64()
+    _check(load().zc_workspace_size(arr, len(ns), ctypes.byref(out)), "zc_workspace_size")
+    return out.value
+
+
+def workspace(ns: Sequence[int] | int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace (zero it again only after a call reported a device error)."""
+    return torch.zeros(workspace_size(ns), dtype=torch.uint8, device=device)
+
+
+def new_status(device="cuda") -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def codebook_to_device(cb, device="cuda") -> torch.Tensor:
+    return torch.as_tensor(np.asarray(cb, np.uint8).reshape(7), dtype=torch.uint8).to(device)
+
+
+# ------------------------------------------------------------------ device entry points
+def histogram_topk(x: torch.Tensor, ws: torch.Tensor, status: torch.Tensor, cb_out: torch.Tensor | None = None,
+                   hist_out: torch.Tensor | None = None, stream=None):
+    """Exact exponent histogram -> device codebook (7 x uint8) [+ 256 x int32 counts]."""
+    n = _nelem16(x)
+    if cb_out is None:
+        cb_out = torch.empty(7, dtype=torch.uint8, device=x.device)
+    rc = load().zc_histogram_topk(_ptr(x), n, _ptr(cb_out), _ptr(hist_out), _ptr(ws), ws.numel(), _ptr(status),
+                                  _stream(stream))
+    _check(rc, "zc_histogram_topk")
+    return cb_out, hist_out
+
+
+def compress(x: torch.Tensor, cb: torch.Tensor, ws: torch.Tensor, status: torch.Tensor,
+             main: torch.Tensor | None = None, esc: torch.Tensor | None = None, stream=None):
+    """Encode x into (main stream, escape buffer); the escape count is in the main header."""
+    n = _nelem16(x)
+    mb, eb = compressed_size(n)
+    if main is None:
+        main = torch.empty(mb, dtype=torch.uint8, device=x.device)
+    if esc is None:
+        esc = torch.empty(max(eb, 16), dtype=torch.uint8, device=x.device)
+    rc = load().zc_compress(_ptr(x), n, _ptr(cb), _ptr(main), _ptr(esc), esc.numel(), _ptr(ws), ws.numel(),
+                            _ptr(status), _stream(stream))
+    _check(rc, "zc_compress")
+    return main, esc
+
+
+def decompress(main: torch.Tensor, esc: torch.Tensor, n: int, status: torch.Tensor,
+               out: torch.Tensor | None = None, esc_bytes: int | None = None, stream=None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty(n, dtype=torch.int16, device=main.device)
+    eb = esc.numel() if esc_bytes is None else int(esc_bytes)
+    rc = load().zc_decompress(_ptr(main), _ptr(esc) if esc is not None else None, eb, int(n), _ptr(out),
+                              _ptr(status), _stream(stream))
+    _check(rc, "zc_decompress")
+    return out
+
+
+def decompress_reduce(mains: Sequence[torch.Tensor], escs: Sequence[torch.Tensor], n: int, status: torch.Tensor,
+                      out: torch.Tensor | None = None, out_cb: torch.Tensor | None = None,
+                      out_main: torch.Tensor | None = None, out_esc: torch.Tensor | None = None,
+                      ws: torch.Tensor | None = None, want_out: bool = True, esc_bytes: Sequence[int] | None = None,
+                      stream=None):
+    P = len(mains)
+    dev = mains[0].device
+    if out is None and want_out:
+        out = torch.empty(n, dtype=torch.int16, device=dev)
+    if out_cb is not None:
+        mb, eb = compressed_size(n)
+        if out_main is None:
+            out_main = torch.empty(mb, dtype=torch.uint8, device=dev)
+        if out_esc is None:
+            out_esc = torch.empty(max(eb, 16), dtype=torch.uint8, device=dev)
+    mp = (ctypes.c_void_p * P)(*[_ptr(m) for m in mains])
+    ep = (ctypes.c_void_p * P)(*[_ptr(e) for e in escs])
+    sizes = [e.numel() for e in escs] if esc_bytes is None else list(esc_bytes)
+    eb_arr = (ctypes.c_uint64 * P)(*sizes)
+    rc = load().zc_decompress_reduce(P, mp, ep, eb_arr, int(n), _ptr(out), _ptr(out_cb), _ptr(out_main),
+                                     _ptr(out_esc), out_esc.numel() if out_esc is not None else 0,
+                                     _ptr(ws), ws.numel() if ws is not None else 0, _ptr(status), _stream(stream))
+    _check(rc, "zc_decompress_reduce")
+    return out, out_main, out_esc
+
+
+@dataclass
+class BatchItem:
+    bf16: torch.Tensor
+    main: torch.Tensor
+    esc: torch.Tensor
+    cb: torch.Tensor | None = None
+    esc_bytes: int | None = None
+
+
+def _descs(items: Sequence[BatchItem]):
+    arr = (ZcTensor * len(items))()
+    for i, it in enumerate(items):
+        arr[i].bf16 = _ptr(it.bf16)
+        arr[i].main = _ptr(it.main)
+        arr[i].esc = _ptr(it.esc)
+        arr[i].cb = _ptr(it.cb)
+        arr[i].n = it.bf16.numel()
+        arr[i].esc_bytes = it.esc.numel() if it.esc_bytes is None else int(it.esc_bytes)
+    return arr
+
+
+def compress_batched(items: Sequence[BatchItem], ws: torch.Tensor, status: torch.Tensor, stream=None) -> None:
+    arr = _descs(items)
+    _check(load().zc_compress_batched(len(items), arr, _ptr(ws), ws.numel(), _ptr(status), _stream(stream)),
+           "zc_compress_batched")
+
+
+def decompress_batched(items: Sequence[BatchItem], status: torch.Tensor, stream=None) -> None:
+    arr = _descs(items)
+    _check(load().zc_decompress_batched(len(items), arr, _ptr(status), _stream(stream)), "zc_decompress_batched")
+
+
+# ------------------------------------------------------------------ small host helpers
+def header_n_esc(main: torch.Tensor) -> int:
+    """Escape count from a main stream's header (a device-to-host read of 8 bytes)."""
+    return int.from_bytes(main[24:32].cpu().numpy().tobytes(), "little")
+
+
+def status_value(status: torch.Tensor) -> int:
+    return int(status.item())

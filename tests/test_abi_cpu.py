@@ -1,0 +1,101 @@
+"""CPU-side checks of libzc: it loads, exports every entry point include/zc.h declares, and its host logic
+(sigma closed form, sizes, argument validation) behaves -- no kernel is launched here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from lossless_bf16_exponent_zc_gb300 import zc
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "zc.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(zc_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = zc.load()
+    names = declared_functions()
+    assert {"zc_codebook_from_sigma", "zc_histogram_topk", "zc_compress", "zc_decompress", "zc_decompress_reduce",
+            "zc_compressed_size", "zc_workspace_size", "zc_compress_batched", "zc_decompress_batched",
+            "zc_status_string", "zc_version"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings():
+    assert zc.version().startswith("libzc")
+    for i, name in enumerate(zc.STATUS_NAMES):
+        assert zc.status_string(i) == name
+    assert zc.status_string(999) == "ZC_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("sigma", list(np.exp(np.linspace(np.log(1e-6), np.log(10.0), 120))) + [1e-38, 1e30])
+def test_sigma_closed_form_matches_oracle(sigma):
+    assert np.array_equal(zc.codebook_from_sigma(sigma), oracle.codebook_from_sigma(sigma))
+
+
+def test_sigma_rejects_bad_values():
+    for s in (0.0, -1.0, float("nan"), float("inf")):
+        with pytest.raises(zc.ZcError) as ei:
+            zc.codebook_from_sigma(s)
+        assert ei.value.code == zc.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("n", [0, 1, 4095, 4096, 4097, 1 << 20, 67108864, 218103808 // 9, (1 << 32) - 1])
+def test_sizes_match_oracle(n):
+    mb, eb = zc.compressed_size(n)
+    assert mb == oracle.main_bytes(n) and eb == n
+
+
+def test_too_large():
+    with pytest.raises(zc.ZcError) as ei:
+        zc.compressed_size(1 << 32)
+    assert ei.value.code == zc.ERR_TOO_LARGE
+
+
+def test_workspace_size_formula():
+    assert zc.workspace_size(0) == 4096
+    assert zc.workspace_size([4096, 4097, 1]) == 4096 + 16 * (1 + 2 + 1)
+    assert zc.workspace_size(1 << 26) == 4096 + 16 * (1 << 14)
+
+
+def _raw(name, *args):
+    return getattr(zc.load(), name)(*args)
+
+
+def test_argument_errors_are_synchronous():
+    """Bad arguments are rejected on the host before anything is enqueued (no GPU needed)."""
+    E = zc
+    # null pointers
+    assert _raw("zc_compress", None, 10, None, None, None, 0, None, 0, None, None) == E.ERR_INVALID_ARG
+    assert _raw("zc_decompress", None, None, 0, 10, None, None, None) == E.ERR_INVALID_ARG
+    assert _raw("zc_histogram_topk", None, 10, None, None, None, 0, None, None) == E.ERR_INVALID_ARG
+    # misaligned pointers (never dereferenced)
+    fake = 0x10000
+    status = 0x20000
+    assert _raw("zc_compress", fake + 2, 10, fake, fake, fake, 10, fake, 1 << 20, status, None) == E.ERR_ALIGNMENT
+    assert _raw("zc_decompress", fake + 8, fake, 10, 10, fake, status, None) == E.ERR_ALIGNMENT
+    assert _raw("zc_compress", fake, 10, fake, fake, fake, 10, fake, 1 << 20, status + 2, None) == E.ERR_ALIGNMENT
+    # workspace too small
+    assert _raw("zc_compress", fake, 1 << 20, fake, fake, fake, 10, fake, 4096, status, None) == E.ERR_WORKSPACE
+    # n too large
+    assert _raw("zc_compress", fake, 1 << 32, fake, fake, fake, 10, fake, 1 << 40, status, None) == E.ERR_TOO_LARGE
+    # shard count out of range
+    arr = (ctypes.c_void_p * 1)(fake)
+    sz = (ctypes.c_uint64 * 1)(0)
+    assert _raw("zc_decompress_reduce", 0, arr, arr, sz, 10, fake, None, None, None, 0, None, 0, status,
+                None) == E.ERR_INVALID_ARG
+    assert _raw("zc_decompress_reduce", 65, arr, arr, sz, 10, fake, None, None, None, 0, None, 0, status,
+                None) == E.ERR_INVALID_ARG
+    # neither output requested
+    assert _raw("zc_decompress_reduce", 1, arr, arr, sz, 10, None, None, None, None, 0, None, 0, status,
+                None) == E.ERR_INVALID_ARG
+    # batched: empty batch
+    assert _raw("zc_compress_batched", 0, None, None, 0, status, None) == E.ERR_INVALID_ARG

@@ -1,0 +1,353 @@
+"""GPU parity: libzc's CUDA kernels against the CPU oracle, byte for byte.
+
+Every case runs the product path through the C ABI (the ctypes binding) and the
+oracle on the same seeded inputs; compressed main and escape streams, decoded
+tensors, histogram codebooks and reduced / re-encoded outputs must be
+bit-identical (integer work: no tolerance).  Sizes span several tiles with
+ragged tails; the five workload configurations run at full size.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(x: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda()
+
+
+def host_u16(t: torch.Tensor) -> np.ndarray:
+    return t.cpu().numpy().view(np.uint16)
+
+
+def host_u8(t: torch.Tensor) -> np.ndarray:
+    return t.cpu().numpy().view(np.uint8)
+
+
+def gpu_compress(zc, x: np.ndarray, cb, ws=None):
+    st = zc.new_status()
+    ws = zc.workspace(x.size) if ws is None else ws
+    main, esc = zc.compress(dev(x), zc.codebook_to_device(cb), ws, st)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0, zc.status_string(zc.status_value(st))
+    n_esc = zc.header_n_esc(main)
+    return host_u8(main), host_u8(esc)[:n_esc], main, esc
+
+
+def assert_stream_equal(got_main, got_esc, want_main, want_esc):
+    assert got_main.size == want_main.size
+    d = np.nonzero(got_main != want_main)[0]
+    assert d.size == 0, f"{d.size} main bytes differ, first at {d[:8]}: {got_main[d[:8]]} vs {want_main[d[:8]]}"
+    assert got_esc.size == want_esc.size, (got_esc.size, want_esc.size)
+    assert np.array_equal(got_esc, want_esc)
+
+
+def roundtrip_check(zc, x, cb):
+    gm, ge, main_t, esc_t = gpu_compress(zc, x, cb)
+    om, oe = oracle.compress(x, cb)
+    assert_stream_equal(gm, ge, om, oe)
+    st = zc.new_status()
+    out = zc.decompress(main_t, esc_t, x.size, st)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0, zc.status_string(zc.status_value(st))
+    assert np.array_equal(host_u16(out), x)
+    return gm, ge
+
+
+# ------------------------------------------------------------------ small and ragged cases
+def test_gaussian_2pow20_roundtrip(zc):
+    """The 2^20-element N(0, 0.02) case with the sigma codebook."""
+    x = workloads.gaussian()
+    cb = oracle.codebook_from_sigma(0.02)
+    assert np.array_equal(zc.codebook_from_sigma(0.02), cb)
+    roundtrip_check(zc, x, cb)
+
+
+@pytest.mark.parametrize("n", [1, 7, 31, 32, 255, 256, 257, 1023, 1024, 1025, 2047, 4095, 4096, 4097,
+                               3 * 4096 + 5, 100_003, 1 << 18])
+def test_ragged_sizes(zc, n):
+    x = workloads.gradient(n=n, sigma=1e-3, seed=n % 1000 + 7)
+    roundtrip_check(zc, x, oracle.codebook_from_sigma(1e-3))
+
+
+def test_empty_tensor(zc):
+    x = np.zeros(0, np.uint16)
+    st = zc.new_status()
+    ws = zc.workspace(0)
+    cb = oracle.codebook_from_sigma(0.02)
+    main, esc = zc.compress(torch.empty(0, dtype=torch.int16, device="cuda"), zc.codebook_to_device(cb), ws, st)
+    torch.cuda.synchronize()
+    om, oe = oracle.compress(x, cb)
+    assert zc.status_value(st) == 0
+    assert_stream_equal(host_u8(main), host_u8(esc)[:0], om, oe)
+
+
+@pytest.mark.parametrize("cb", [
+    [121, 120, 119, 122, 118, 117, 116],
+    [255, 0, 127, 1, 254, 128, 126],
+    [140, 141, 142, 143, 144, 145, 146],
+])
+def test_all_65536_patterns(zc, cb):
+    x = workloads.all_bf16_patterns()
+    roundtrip_check(zc, x, np.array(cb, np.uint8))
+    # shuffled, so that every tile mixes NaN payloads, infinities, zeros and subnormals
+    rng = np.random.default_rng(3)
+    roundtrip_check(zc, rng.permutation(np.tile(x, 3)), np.array(cb, np.uint8))
+
+
+def test_all_escape_and_no_escape(zc):
+    cb = np.array([120, 121, 122, 123, 124, 125, 126], np.uint8)
+    x = workloads.all_bf16_patterns()
+    all_esc = x[~np.isin((x >> 7) & 0xFF, cb)]
+    gm, ge = roundtrip_check(zc, all_esc, cb)
+    assert ge.size == all_esc.size
+    rng = np.random.default_rng(4)
+    n = 5 * 4096 + 17
+    e = cb[rng.integers(0, 7, n)].astype(np.uint16)
+    none = (rng.integers(0, 2, n).astype(np.uint16) << 15) | (e << 7) | rng.integers(0, 128, n).astype(np.uint16)
+    gm, ge = roundtrip_check(zc, none, cb)
+    assert ge.size == 0
+
+
+def test_worked_example_fixture(zc):
+    import json, os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "worked_example_n1030.json")) as f:
+        fx = json.load(f)
+    x = np.full(fx["n"], int(fx["default_bits"], 16), np.uint16)
+    for k, v in fx["elements"].items():
+        x[int(k)] = int(v["bits"], 16)
+    gm, ge = roundtrip_check(zc, x, np.array(fx["codebook"], np.uint8))
+    assert ge.tolist() == fx["escapes"]
+
+
+# ------------------------------------------------------------------ histogram
+@pytest.mark.parametrize("n", [0, 1, 9, 4096 * 3 + 3, 1 << 20])
+def test_histogram_small(zc, n):
+    x = workloads.gradient(n=n, seed=21) if n else np.zeros(0, np.uint16)
+    st = zc.new_status()
+    ws = zc.workspace(n)
+    hist = torch.zeros(256, dtype=torch.int32, device="cuda")
+    xt = dev(x) if n else torch.empty(0, dtype=torch.int16, device="cuda")
+    cb, _ = zc.histogram_topk(xt, ws, st, hist_out=hist)
+    torch.cuda.synchronize()
+    ocb, oh = oracle.histogram_topk(x)
+    assert np.array_equal(host_u8(cb), ocb)
+    assert np.array_equal(hist.cpu().numpy().astype(np.uint64), oh)
+    # the workspace is left clean: a second call gives the same answer
+    cb2, _ = zc.histogram_topk(xt, ws, st, hist_out=hist)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_u8(cb2), ocb)
+    assert np.array_equal(hist.cpu().numpy().astype(np.uint64), oh)
+
+
+def test_histogram_ties(zc):
+    """Equal counts: the smaller exponent ranks first."""
+    e = np.repeat(np.array([200, 7, 90, 50, 51, 52, 53, 54], np.uint16), [5, 5, 1, 3, 3, 3, 3, 3])
+    x = (e << 7).astype(np.uint16)
+    st = zc.new_status()
+    cb, _ = zc.histogram_topk(dev(x), zc.workspace(x.size), st)
+    torch.cuda.synchronize()
+    assert host_u8(cb).tolist() == oracle.histogram_topk(x)[0].tolist() == [7, 200, 50, 51, 52, 53, 54]
+
+
+# ------------------------------------------------------------------ workload configurations at full size
+@pytest.mark.slow
+def test_config_gradient_64M_histogram_and_sigma(zc):
+    """64M gradient tensor with outliers and special values; histogram vs sigma codebooks, both round-tripped."""
+    x = workloads.gradient()
+    st = zc.new_status()
+    ws = zc.workspace(x.size)
+    xt = dev(x)
+    cb_dev, _ = zc.histogram_topk(xt, ws, st)
+    torch.cuda.synchronize()
+    ocb, _ = oracle.histogram_topk(x)
+    assert np.array_equal(host_u8(cb_dev), ocb)
+    for cb in (ocb, oracle.codebook_from_sigma(1e-3)):
+        main, esc = zc.compress(xt, zc.codebook_to_device(cb), ws, st)
+        out = zc.decompress(main, esc, x.size, st)
+        torch.cuda.synchronize()
+        assert zc.status_value(st) == 0
+        om, oe = oracle.compress(x, cb)
+        n_esc = zc.header_n_esc(main)
+        assert_stream_equal(host_u8(main), host_u8(esc)[:n_esc], om, oe)
+        assert np.array_equal(host_u16(out), x)
+
+
+def _llama_items(zc, bucket):
+    items = []
+    for name, x, sigma in bucket:
+        mb, eb = zc.compressed_size(x.size)
+        items.append(zc.BatchItem(bf16=dev(x), main=torch.empty(mb, dtype=torch.uint8, device="cuda"),
+                                  esc=torch.empty(max(eb, 16), dtype=torch.uint8, device="cuda"),
+                                  cb=zc.codebook_to_device(oracle.codebook_from_sigma(sigma))))
+    return items
+
+
+@pytest.mark.parametrize("scale", [pytest.param(1.0, marks=pytest.mark.slow), 1 / 512])
+def test_config_llama_bucket_batched(zc, scale):
+    """Nine Llama-3-8B layer tensors, per-tensor sigma codebooks, one batched launch each way."""
+    bucket = workloads.llama_bucket(scale=scale)
+    items = _llama_items(zc, bucket)
+    st = zc.new_status()
+    ws = zc.workspace([x.size for _, x, _ in bucket])
+    zc.compress_batched(items, ws, st)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0
+    outs = []
+    for it, (name, x, sigma) in zip(items, bucket):
+        om, oe = oracle.compress(x, oracle.codebook_from_sigma(sigma))
+        n_esc = zc.header_n_esc(it.main)
+        assert_stream_equal(host_u8(it.main), host_u8(it.esc)[:n_esc], om, oe)
+        outs.append(zc.BatchItem(bf16=torch.empty(x.size, dtype=torch.int16, device="cuda"), main=it.main,
+                                 esc=it.esc))
+    zc.decompress_batched(outs, st)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0
+    for o, (name, x, sigma) in zip(outs, bucket):
+        assert np.array_equal(host_u16(o.bf16), x), name
+
+
+@pytest.mark.slow
+def test_config_moe_payload_chunks(zc):
+    """16384 x 4096 Student-t payload: one histogram codebook, 8 Zipf-sized destination chunks batched."""
+    x, counts = workloads.moe_payload()
+    st = zc.new_status()
+    xt = dev(x)
+    ws = zc.workspace([c * 4096 for c in counts])
+    cb_dev, _ = zc.histogram_topk(xt, ws, st)
+    torch.cuda.synchronize()
+    ocb, _ = oracle.histogram_topk(x)
+    assert np.array_equal(host_u8(cb_dev), ocb)
+    items, start = [], 0
+    for c in counts:
+        n = c * 4096
+        mb, eb = zc.compressed_size(n)
+        items.append(zc.BatchItem(bf16=xt[start:start + n], main=torch.empty(mb, dtype=torch.uint8, device="cuda"),
+                                  esc=torch.empty(eb, dtype=torch.uint8, device="cuda"), cb=cb_dev))
+        start += n
+    zc.compress_batched(items, ws, st)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0
+    start = 0
+    outs = []
+    for it, c in zip(items, counts):
+        n = c * 4096
+        om, oe = oracle.compress(x[start:start + n], ocb)
+        mb = zc.compressed_size(n)[0]
+        assert mb == om.size            # the fixed-size part is known before encoding
+        n_esc = zc.header_n_esc(it.main)
+        assert_stream_equal(host_u8(it.main), host_u8(it.esc)[:n_esc], om, oe)
+        outs.append(zc.BatchItem(bf16=torch.empty(n, dtype=torch.int16, device="cuda"), main=it.main, esc=it.esc,
+                                 esc_bytes=n_esc))
+        start += n
+    zc.decompress_batched(outs, st)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0
+    assert np.array_equal(np.concatenate([host_u16(o.bf16) for o in outs]), x)
+
+
+def _reduce_case(zc, P, m, sigma=1e-3, reencode=True, seed=5):
+    shards = workloads.rs_shards(P=P, m=m, sigma=sigma, seed=seed)
+    cb_in = oracle.codebook_from_sigma(sigma)
+    cb_out = oracle.codebook_from_sigma(sigma * math.sqrt(P))
+    st = zc.new_status()
+    ws = zc.workspace(m)
+    mains, escs, omains, oescs = [], [], [], []
+    for s in shards:
+        main, esc = zc.compress(dev(s), zc.codebook_to_device(cb_in), ws, st)
+        mains.append(main)
+        escs.append(esc)
+        om, oe = oracle.compress(s, cb_in)
+        omains.append(om)
+        oescs.append(oe)
+    y, om_t, oe_t = zc.decompress_reduce(mains, escs, m, st, out_cb=zc.codebook_to_device(cb_out) if reencode else None,
+                                         ws=ws if reencode else None)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0, zc.status_string(zc.status_value(st))
+    if reencode:
+        oy, orm, ore = oracle.decompress_reduce(omains, oescs, m, cb_out)
+        n_esc = zc.header_n_esc(om_t)
+        assert_stream_equal(host_u8(om_t), host_u8(oe_t)[:n_esc], orm, ore)
+    else:
+        oy = oracle.decompress_reduce(omains, oescs, m)
+    assert np.array_equal(host_u16(y), oy)
+
+
+@pytest.mark.parametrize("P,m", [(1, 5000), (2, 4096), (3, 3 * 4096 + 77), (8, 1 << 16), (64, 9000), (33, 4097)])
+@pytest.mark.parametrize("reencode", [True, False])
+def test_decompress_reduce_small(zc, P, m, reencode):
+    _reduce_case(zc, P, m, reencode=reencode, seed=P * 7 + m % 13)
+
+
+def test_decompress_reduce_special_values(zc):
+    """Infinities of both signs (NaN sums), overflow to inf, signed zeros and subnormals across shards."""
+    P, m = 4, 3 * 4096 + 11
+    rng = np.random.default_rng(17)
+    shards = []
+    for r in range(P):
+        x = workloads.gradient(n=m, sigma=1e-3, seed=40 + r)
+        x[rng.integers(0, m, 300)] = 0x7F7F
+        x[rng.integers(0, m, 50)] = 0xFF80
+        x[rng.integers(0, m, 300)] = rng.integers(1, 128, 300).astype(np.uint16)
+        x[rng.integers(0, m, 100)] = 0x8000
+        shards.append(x)
+    cb = oracle.codebook_from_sigma(1e-3)
+    st = zc.new_status()
+    ws = zc.workspace(m)
+    mains, escs, om, oe = [], [], [], []
+    for s in shards:
+        a, b = zc.compress(dev(s), zc.codebook_to_device(cb), ws, st)
+        mains.append(a); escs.append(b)
+        c, d = oracle.compress(s, cb)
+        om.append(c); oe.append(d)
+    y, m_t, e_t = zc.decompress_reduce(mains, escs, m, st, out_cb=zc.codebook_to_device(cb), ws=ws)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0
+    oy, orm, ore = oracle.decompress_reduce(om, oe, m, cb)
+    assert np.array_equal(host_u16(y), oy)
+    assert_stream_equal(host_u8(m_t), host_u8(e_t)[:zc.header_n_esc(m_t)], orm, ore)
+    assert (oy == 0x7FC0).sum() > 0
+
+
+@pytest.mark.slow
+def test_config_reduce_scatter_8x32M(zc):
+    """P = 8 shards of 2^25 elements, shared input codebook, sqrt(8)*sigma output codebook."""
+    _reduce_case(zc, 8, 1 << 25)
+
+
+# ------------------------------------------------------------------ workspace reuse
+def test_workspace_reused_without_rezeroing(zc):
+    ws = zc.workspace(1 << 18)
+    cb = oracle.codebook_from_sigma(1e-3)
+    for i, n in enumerate([1 << 18, 4096 * 5 + 1, 100, 1 << 17, 1 << 18]):
+        x = workloads.gradient(n=n, seed=200 + i)
+        gm, ge, _, _ = gpu_compress(zc, x, cb, ws=ws)
+        om, oe = oracle.compress(x, cb)
+        assert_stream_equal(gm, ge, om, oe)
+    hdr = host_u8(ws[:16]).view(np.uint32)
+    assert hdr[0] == 0 and hdr[1] == 0 and hdr[2] == 5   # ticket, exit count reset; epoch = launches
+
+
+def test_epoch_wraparound(zc):
+    """The look-back epoch tag wraps after 2^32 - 1 launches; the wrap clears every flag first.
+
+    The first launch leaves flags tagged with epoch 1 holding other escape
+    counts; if the wrap did not clear them, the launch tagged 1 after the wrap
+    would pick them up and write wrong escape offsets."""
+    ws = zc.workspace(1 << 16)
+    cb = oracle.codebook_from_sigma(1e-3)
+    other = workloads.gradient(n=1 << 16, seed=301, outlier_frac=0.2)
+    gpu_compress(zc, other, cb, ws=ws)         # flags tagged with epoch 1
+    ws[8:12] = torch.tensor([0xFE, 0xFF, 0xFF, 0xFF], dtype=torch.uint8, device="cuda")  # epoch = 2^32 - 2
+    x = workloads.gradient(n=1 << 16, seed=300)
+    om, oe = oracle.compress(x, cb)
+    for epoch_after in (0, 1, 2):              # launches tagged 2^32 - 1 (wrap), 1, 2
+        gm, ge, _, _ = gpu_compress(zc, x, cb, ws=ws)
+        assert_stream_equal(gm, ge, om, oe)
+        assert int(host_u8(ws[8:12]).view(np.uint32)[0]) == epoch_after
