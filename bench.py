@@ -52,7 +52,12 @@ def parse_args(argv=None):
     p.add_argument("--ref-sample-log2", type=int, default=20, help="elements per reference-arm step")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    return p.parse_args(argv)
+    p.add_argument("--profile", action="store_true",
+                   help="for profiler runs: no clock sampling, no soak, no e2e or CPU legs")
+    a = p.parse_args(argv)
+    if a.profile:
+        a.no_e2e = a.no_cpu_baseline = True
+    return a
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -269,11 +274,12 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
     clocks = ClockSampler(local)
-    clocks.start()
-    # keep the GPU busy ~1 s so clock samples reflect load
-    t_soak = time.perf_counter()
-    while time.perf_counter() - t_soak < 1.0:
-        step()
+    if not args.profile:
+        clocks.start()
+        # keep the GPU busy ~1 s so clock samples reflect load
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < 1.0:
+            step()
     torch.cuda.synchronize()
 
     evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in ops]

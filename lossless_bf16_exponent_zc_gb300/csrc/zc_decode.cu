@@ -4,12 +4,12 @@
 // -> next byte of the escape ("zero-point") array; the exponent is joined with
 // the sign-mantissa byte.
 //
-// Design on sm_103a: a persistent grid of 8-warp CTAs.  Warp w owns tiles
+// Design on sm_103a: a persistent grid of 16-warp CTAs, one per SM.  Warp w owns tiles
 // w, w + W, w + 2W, ... (W = warps in the grid); no tile waits on another.
 // Per tile, one TMA bulk copy stages the 5632-byte tile into shared memory and
 // 16-byte cp.async copies stage the tile's escape bytes (up to 512 of them;
 // any excess is read straight from global memory), all completing on one
-// mbarrier; three stages are in flight per warp.  Code -> exponent goes
+// mbarrier; two stages are in flight per warp.  Code -> exponent goes
 // through byte permutes on an 8-byte table held in registers, with a 3 x 256
 // spread table in shared memory turning the three plane bytes into a permute
 // selector.  Output is written with 16-byte vector stores.
@@ -18,12 +18,15 @@
 
 namespace zc {
 
-constexpr int kDecWarps = 8;
-constexpr int kDecStages = 3;
+constexpr int kDecWarps = 16;
+constexpr int kDecStages = 2;
 constexpr uint32_t kDecEscCap = 512;  // escape bytes staged per tile (multiple of 16)
 constexpr uint32_t kDecStageBytes = kTileBytes + kDecEscCap;
-constexpr uint32_t kDecWarpSmem = kDecStages * kDecStageBytes + 1024 + 64;  // stages, scratch, barriers
-constexpr uint32_t kDecSmem = 3 * 256 * 4 + kDecWarps * kDecWarpSmem;
+// (after 1 KB alignment) spread tables 3 KB, per-warp scratch 1 KB, barriers, stages
+constexpr uint32_t kDecScratchOff = 3 * 1024;
+constexpr uint32_t kDecBarOff = kDecScratchOff + kDecWarps * 1024;
+constexpr uint32_t kDecStageOff = kDecBarOff + kDecWarps * 16;
+constexpr uint32_t kDecSmem = 1024 + kDecStageOff + kDecWarps * kDecStages * kDecStageBytes;
 
 template <int MAXB>
 struct DecParams {
@@ -116,11 +119,14 @@ __device__ __forceinline__ uint32_t stage_escapes(uint8_t* dst, const uint8_t* e
 template <int MAXB>
 __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_constant__ DecParams<MAXB> p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint32_t* spread = reinterpret_cast<uint32_t*>(smem);
   const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
-  uint8_t* wbase = smem + 3 * 256 * 4 + warp * kDecWarpSmem;
-  uint8_t* scratch = wbase + kDecStages * kDecStageBytes;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(scratch + 1024);
+  const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;
+  uint8_t* gbase = smem + (sbase - smem_u32(smem));
+  uint32_t* spread = reinterpret_cast<uint32_t*>(gbase);
+  uint8_t* scratch = gbase + kDecScratchOff + warp * 1024;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(gbase + kDecBarOff + warp * 16);
+  uint8_t* wstage = gbase + kDecStageOff + warp * kDecStages * kDecStageBytes;
+  const uint32_t wstage_s = sbase + kDecStageOff + warp * kDecStages * kDecStageBytes;
 
   build_spread_tables(spread);
   if (lane == 0) {
@@ -132,7 +138,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
 
   const uint32_t total_warps = gridDim.x * kDecWarps;
   const uint32_t gw = blockIdx.x * kDecWarps + warp;
-  auto stage_ptr = [&](int s) { return wbase + s * kDecStageBytes; };
+  auto stage_ptr = [&](int s) { return wstage + s * kDecStageBytes; };
 
   HdrInfo issue_hdr;
   issue_hdr.ti = -1;
@@ -180,6 +186,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
       const uint64_t rem = T.n - static_cast<uint64_t>(lt) * kTile;
       const uint32_t n_tile = rem >= kTile ? kTile : static_cast<uint32_t>(rem);
       const uint8_t* tile = stage_ptr(s);
+      const uint32_t tile_s = wstage_s + s * kDecStageBytes;
 
       mbar_wait_bounded(&bar[s], (phase >> s) & 1u, p.status);
       phase ^= 1u << s;
@@ -195,7 +202,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
 #pragma unroll 1
         for (uint32_t blk = 0; blk < 4; blk++) {
           uint4 v[4];
-          decode_block(tile, blk, n_tile, spread, hdr.dt, es, run, scratch, v);
+          decode_block(tile_s, blk, n_tile, sbase, hdr.dt, es, run, scratch, v);
 #pragma unroll
           for (uint32_t k = 0; k < 4; k++) store8_guarded(out, blk * kBlock + k * 256 + lane * 8, n_left, v[k]);
         }

@@ -65,6 +65,29 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Shared-memory loads by 32-bit shared address.  volatile keeps them after
+// the mbarrier waits that publish TMA data (those carry a memory clobber).
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+
 __device__ __forceinline__ ulonglong2 ld_relaxed_v2(const Flag* f) {
   ulonglong2 v;
   asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];"
@@ -227,6 +250,12 @@ __device__ __forceinline__ bool build_enc_lut(uint32_t* lut, const uint8_t* cb_d
   return !dup;
 }
 
+// Table entries of the low / high value of a 32-bit word holding two bf16.
+// `lut` is the table's shared address, 1 KB aligned, so the byte offset
+// (exponent * 4) can be OR-ed in.
+__device__ __forceinline__ uint32_t lut_lo(uint32_t w, uint32_t lut) { return lds32(((w >> 5) & 0x3FCu) | lut); }
+__device__ __forceinline__ uint32_t lut_hi(uint32_t w, uint32_t lut) { return lds32(((w >> 21) & 0x3FCu) | lut); }
+
 // Per-lane escape bookkeeping of one encoded tile.
 struct TileEsc {
   uint32_t mask[4];  // bit 8k + j: block element 256k + 8*lane + j is an escape
@@ -234,13 +263,13 @@ struct TileEsc {
   uint32_t total;    // escapes in the tile (same in every lane)
 };
 
-// Encodes one tile held in shared memory (`tb`: 4096 bf16 bit patterns, zero
-// beyond n_tile) into its 5632-byte ZC1 tile at `out` (global).  One warp.
-// Lane l of group k handles block elements 256k + 8l .. 256k + 8l + 7 (one
-// 16-byte vector); its 4 groups' code bits form one plane word per plane,
-// which is exactly the column-major plane layout (byte 4l + k).
-__device__ __forceinline__ void encode_tile(const uint16_t* tb, uint32_t n_tile, const uint32_t* lut,
-                                            uint8_t* out, TileEsc& te) {
+// Encodes one tile held in shared memory (shared address `tb`: 4096 bf16 bit
+// patterns, zero beyond n_tile) into its 5632-byte ZC1 tile at `out`
+// (global).  One warp.  Lane l of group k handles block elements
+// 256k + 8l .. 256k + 8l + 7 (one 16-byte vector); its 4 groups' code bits
+// form one plane word per plane, which is exactly the column-major plane
+// layout (byte 4l + k).
+__device__ __forceinline__ void encode_tile(uint32_t tb, uint32_t n_tile, uint32_t lut, uint8_t* out, TileEsc& te) {
   const uint32_t lane = lane_id();
   uint32_t run = 0;
 #pragma unroll
@@ -249,19 +278,14 @@ __device__ __forceinline__ void encode_tile(const uint16_t* tb, uint32_t n_tile,
     uint2 smv[4];
 #pragma unroll
     for (uint32_t k = 0; k < 4; k++) {
-      const uint4 v = *reinterpret_cast<const uint4*>(tb + blk * kBlock + k * 256 + lane * 8);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t a = 0;
-#pragma unroll
-      for (int h = 0; h < 4; h++) {
-        a += lut[(w[h] >> 7) & 0xFFu] << (2 * h);
-        a += lut[(w[h] >> 23) & 0xFFu] << (2 * h + 1);
-      }
-      acc[k] = a;
+      const uint4 v = lds128(tb + 2 * (blk * kBlock + k * 256 + lane * 8));
+      const uint32_t e0 = lut_lo(v.x, lut), e1 = lut_hi(v.x, lut), e2 = lut_lo(v.y, lut), e3 = lut_hi(v.y, lut);
+      const uint32_t e4 = lut_lo(v.z, lut), e5 = lut_hi(v.z, lut), e6 = lut_lo(v.w, lut), e7 = lut_hi(v.w, lut);
+      acc[k] = (e0 + (e1 << 1)) + ((e2 << 2) + (e3 << 3)) + ((e4 << 4) + (e5 << 5)) + ((e6 << 6) + (e7 << 7));
       // sign-mantissa bytes: low byte of each value holds 7 mantissa bits,
       // high byte holds the sign in bit 7
-      const uint32_t lo01 = __byte_perm(w[0], w[1], 0x6420), hi01 = __byte_perm(w[0], w[1], 0x7531);
-      const uint32_t lo23 = __byte_perm(w[2], w[3], 0x6420), hi23 = __byte_perm(w[2], w[3], 0x7531);
+      const uint32_t lo01 = __byte_perm(v.x, v.y, 0x6420), hi01 = __byte_perm(v.x, v.y, 0x7531);
+      const uint32_t lo23 = __byte_perm(v.z, v.w, 0x6420), hi23 = __byte_perm(v.z, v.w, 0x7531);
       smv[k] = make_uint2((lo01 & 0x7F7F7F7Fu) | (hi01 & 0x80808080u), (lo23 & 0x7F7F7F7Fu) | (hi23 & 0x80808080u));
     }
     uint8_t* ob = out + blk * kBlockBytes;
@@ -274,11 +298,13 @@ __device__ __forceinline__ void encode_tile(const uint16_t* tb, uint32_t n_tile,
     uint32_t w1 = __byte_perm(t01, t23, 0x7632);
     uint32_t w2 = __byte_perm(u01, u23, 0x5410);
     uint32_t x = __byte_perm(u01, u23, 0x7632);
-    const uint32_t valid = lane_valid_mask(blk, n_tile, lane);
-    w0 &= valid;
-    w1 &= valid;
-    w2 &= valid;
-    x &= valid;
+    if (n_tile < kTile) {
+      const uint32_t valid = lane_valid_mask(blk, n_tile, lane);
+      w0 &= valid;
+      w1 &= valid;
+      w2 &= valid;
+      x &= valid;
+    }
     *reinterpret_cast<uint32_t*>(ob + 1024 + lane * 4) = w0;
     *reinterpret_cast<uint32_t*>(ob + 1152 + lane * 4) = w1;
     *reinterpret_cast<uint32_t*>(ob + 1280 + lane * 4) = w2;
@@ -292,32 +318,47 @@ __device__ __forceinline__ void encode_tile(const uint16_t* tb, uint32_t n_tile,
 }
 
 // Writes the tile's escapes (their 8-bit exponents, read back from the tile
-// in shared memory) at global positions prefix + rank, skipping positions at
-// or beyond `cap`.  Escapes of a lane are consecutive, in bit order.
-__device__ __forceinline__ void write_escapes(const uint16_t* tb, const TileEsc& te, uint64_t prefix, uint8_t* esc,
+// in shared memory at shared address `tb`) at global positions prefix + rank,
+// skipping positions at or beyond `cap`.  Escapes of a lane are consecutive,
+// in bit order.
+__device__ __forceinline__ void write_escapes(uint32_t tb, const TileEsc& te, uint64_t prefix, uint8_t* esc,
                                               uint64_t cap) {
   const uint32_t lane = lane_id();
+  const bool fits = prefix + te.total <= cap;
+  const uint32_t lane_off = tb + 16 * lane;
 #pragma unroll
   for (uint32_t blk = 0; blk < 4; blk++) {
     uint32_t m = te.mask[blk];
-    uint64_t pos = prefix + te.base[blk];
-    while (m) {
-      const uint32_t p = __ffs(m) - 1;
-      m &= m - 1;
-      const uint32_t i = blk * kBlock + (p >> 3) * 256 + lane * 8 + (p & 7);
-      const uint32_t e = (tb[i] >> 7) & 0xFFu;
-      if (pos < cap) esc[pos] = static_cast<uint8_t>(e);
-      pos++;
+    uint8_t* dst = esc + prefix + te.base[blk];
+    const uint32_t src = lane_off + 2 * blk * kBlock;
+    if (fits) {
+      while (m) {
+        const uint32_t p = __ffs(m) - 1;
+        m &= m - 1;
+        *dst++ = static_cast<uint8_t>(lds_u16(src + 512 * (p >> 3) + 2 * (p & 7)) >> 7);
+      }
+    } else {
+      uint64_t pos = prefix + te.base[blk];
+      while (m) {
+        const uint32_t p = __ffs(m) - 1;
+        m &= m - 1;
+        if (pos < cap) esc[pos] = static_cast<uint8_t>(lds_u16(src + 512 * (p >> 3) + 2 * (p & 7)) >> 7);
+        pos++;
+      }
     }
   }
 }
 
 // Decoupled look-back (single pass): returns the exclusive escape prefix of
 // tile g, whose tensor starts at global tile g0, by summing the aggregates of
-// preceding tiles until one carrying an inclusive prefix is found.  Tiles are
-// handed out by an atomic ticket in increasing order and every ticket holder
-// is resident, so predecessors always make progress; the wait is still
-// bounded (ZC_ERR_TIMEOUT, prefix then meaningless).  `*timed_out` is set.
+// preceding tiles until one carrying an inclusive prefix is found.  Each step
+// reads the flags of the 128 nearest unresolved predecessors (4 per lane) so
+// the resolved front moves quickly even with ~1,800 tiles in flight.  Tiles
+// are handed out by an atomic ticket in increasing order and every ticket
+// holder is resident, so predecessors always make progress; the wait is still
+// bounded (ZC_ERR_TIMEOUT, prefix then meaningless).
+constexpr int kLookbackPerLane = 4;
+
 __device__ __forceinline__ uint64_t lookback(const Flag* flags, uint32_t g, uint32_t g0, uint32_t epoch,
                                              int32_t* status, bool* timed_out) {
   const uint32_t lane = lane_id();
@@ -326,25 +367,41 @@ __device__ __forceinline__ uint64_t lookback(const Flag* flags, uint32_t g, uint
   unsigned long long t0 = 0;
   *timed_out = false;
   while (true) {
-    const int64_t idx = end - 1 - static_cast<int64_t>(lane);
-    uint32_t st = 2, val = 0;
-    if (idx >= static_cast<int64_t>(g0)) {
-      const ulonglong2 f = ld_relaxed_v2(flags + idx);
-      if (static_cast<uint32_t>(f.y >> 32) == epoch) {
-        st = 2;
-        val = static_cast<uint32_t>(f.y);
-      } else if (static_cast<uint32_t>(f.x >> 32) == epoch) {
-        st = 1;
-        val = static_cast<uint32_t>(f.x);
-      } else {
-        st = 0;
+    uint32_t st[kLookbackPerLane], val[kLookbackPerLane];
+#pragma unroll
+    for (int q = 0; q < kLookbackPerLane; q++) {
+      const int64_t idx = end - 1 - static_cast<int64_t>(lane + 32 * q);  // distance lane + 32q
+      st[q] = 2;
+      val[q] = 0;
+      if (idx >= static_cast<int64_t>(g0)) {
+        const ulonglong2 f = ld_relaxed_v2(flags + idx);
+        if (static_cast<uint32_t>(f.y >> 32) == epoch) {
+          val[q] = static_cast<uint32_t>(f.y);
+        } else if (static_cast<uint32_t>(f.x >> 32) == epoch) {
+          st[q] = 1;
+          val[q] = static_cast<uint32_t>(f.x);
+        } else {
+          st[q] = 0;
+        }
       }
     }
-    const uint32_t incl_lanes = __ballot_sync(kFull, st == 2);
-    const uint32_t missing = __ballot_sync(kFull, st == 0);
-    const uint32_t first = incl_lanes ? static_cast<uint32_t>(__ffs(incl_lanes) - 1) : 31u;
-    const uint32_t upto = (first == 31) ? kFull : ((2u << first) - 1u);
-    if (missing & upto) {
+    // nearest predecessor carrying an inclusive prefix: distance `first`
+    uint32_t first = 32 * kLookbackPerLane - 1;
+    bool found = false, missing = false;
+#pragma unroll
+    for (int q = 0; q < kLookbackPerLane; q++) {
+      const uint32_t inc = __ballot_sync(kFull, st[q] == 2);
+      const uint32_t mis = __ballot_sync(kFull, st[q] == 0);
+      if (!found) {
+        const uint32_t upto = inc ? ((2u << (__ffs(inc) - 1)) - 1u) : kFull;  // lanes up to the inclusive one
+        missing |= (mis & upto) != 0;
+        if (inc) {
+          found = true;
+          first = 32 * q + (__ffs(inc) - 1);
+        }
+      }
+    }
+    if (missing) {
       unsigned long long now = 0;
       if (lane == 0) now = global_ns();
       now = __shfl_sync(kFull, now, 0);
@@ -354,12 +411,14 @@ __device__ __forceinline__ uint64_t lookback(const Flag* flags, uint32_t g, uint
         *timed_out = true;
         return prefix;
       }
-      __nanosleep(64);
       continue;
     }
-    prefix += warp_sum(lane <= first ? val : 0u);
-    if (incl_lanes) return prefix;
-    end -= 32;
+    uint32_t part = 0;
+#pragma unroll
+    for (int q = 0; q < kLookbackPerLane; q++) part += (lane + 32 * q <= first) ? val[q] : 0u;
+    prefix += warp_sum(part);
+    if (found) return prefix;
+    end -= 32 * kLookbackPerLane;
   }
 }
 
@@ -414,20 +473,29 @@ __device__ __forceinline__ uint32_t esc_byte(const EscSource& s, uint32_t rank) 
   return 0;
 }
 
-// Decodes block `blk` of a ZC1 tile held in shared memory (`tile`: 5632 B) for
-// this lane: out[k] (k = 0..3) receives 4 words = 8 bf16 values of block
-// elements 256k + 8*lane + 0..7.  `scratch` is this warp's 1 KB exponent
-// scratch.  `run` is the tile-local rank of the block's first escape and is
-// advanced past the block.  Returns the number of code-0 positions (escapes).
-__device__ __forceinline__ uint32_t decode_block(const uint8_t* tile, uint32_t blk, uint32_t n_tile,
-                                                 const uint32_t* spread, DecTable dt, const EscSource& es,
-                                                 uint32_t& run, uint8_t* scratch, uint4 out[4]) {
+// Spread-table lookup for byte k of plane word w: table b lives at shared
+// address `spread` + 1024 b (1 KB aligned, so the offset can be OR-ed in).
+__device__ __forceinline__ uint32_t spread_at(uint32_t w, uint32_t k, uint32_t table) {
+  const uint32_t off = k == 0 ? (w << 2) : (w >> (8 * k - 2));
+  return lds32((off & 0x3FCu) | table);
+}
+
+// Decodes block `blk` of a ZC1 tile held in shared memory (shared address
+// `tile`: 5632 B) for this lane: out[k] (k = 0..3) receives 4 words = 8 bf16
+// values of block elements 256k + 8*lane + 0..7.  `scratch` is this warp's
+// 1 KB exponent scratch.  `run` is the tile-local rank of the block's first
+// escape and is advanced past the block.  Returns the number of code-0
+// positions (escapes).
+__device__ __forceinline__ uint32_t decode_block(uint32_t tile, uint32_t blk, uint32_t n_tile, uint32_t spread,
+                                                 DecTable dt, const EscSource& es, uint32_t& run, uint8_t* scratch,
+                                                 uint4 out[4]) {
   const uint32_t lane = lane_id();
-  const uint8_t* b = tile + blk * kBlockBytes;
-  const uint32_t w0 = *reinterpret_cast<const uint32_t*>(b + 1024 + lane * 4);
-  const uint32_t w1 = *reinterpret_cast<const uint32_t*>(b + 1152 + lane * 4);
-  const uint32_t w2 = *reinterpret_cast<const uint32_t*>(b + 1280 + lane * 4);
-  const uint32_t z = ~(w0 | w1 | w2) & lane_valid_mask(blk, n_tile, lane);
+  const uint32_t b = tile + blk * kBlockBytes;
+  const uint32_t w0 = lds32(b + 1024 + lane * 4);
+  const uint32_t w1 = lds32(b + 1152 + lane * 4);
+  const uint32_t w2 = lds32(b + 1280 + lane * 4);
+  uint32_t z = ~(w0 | w1 | w2);
+  if (n_tile < kTile) z &= lane_valid_mask(blk, n_tile, lane);
   const uint32_t c = __popc(z);
   const uint32_t inc = warp_inclusive_scan(c);
   uint32_t rank = run + inc - c;
@@ -437,8 +505,7 @@ __device__ __forceinline__ uint32_t decode_block(const uint8_t* tile, uint32_t b
   uint32_t ex[8];
 #pragma unroll
   for (uint32_t k = 0; k < 4; k++) {
-    const uint32_t sel = spread[(w0 >> (8 * k)) & 0xFFu] | spread[256 + ((w1 >> (8 * k)) & 0xFFu)] |
-                         spread[512 + ((w2 >> (8 * k)) & 0xFFu)];
+    const uint32_t sel = spread_at(w0, k, spread) | spread_at(w1, k, spread + 1024) | spread_at(w2, k, spread + 2048);
     ex[2 * k] = __byte_perm(dt.t0, dt.t1, sel & 0xFFFFu);
     ex[2 * k + 1] = __byte_perm(dt.t0, dt.t1, sel >> 16);
   }
@@ -461,7 +528,7 @@ __device__ __forceinline__ uint32_t decode_block(const uint8_t* tile, uint32_t b
   }
 #pragma unroll
   for (uint32_t k = 0; k < 4; k++) {
-    const uint2 sm = *reinterpret_cast<const uint2*>(b + k * 256 + lane * 8);
+    const uint2 sm = lds64(b + k * 256 + lane * 8);
     out[k].x = join_pair(__byte_perm(sm.x, ex[2 * k], 0x5140));
     out[k].y = join_pair(__byte_perm(sm.x, ex[2 * k], 0x7362));
     out[k].z = join_pair(__byte_perm(sm.y, ex[2 * k + 1], 0x5140));
@@ -565,7 +632,7 @@ __device__ __forceinline__ uint32_t draw_ticket(WsHeader* ws) {
 // escapes themselves.  Tile g of the launch is local tile lt of its tensor,
 // whose first global tile is g - lt.  Warp-wide.
 __device__ __forceinline__ void publish_tile(Flag* flags, uint32_t g, uint32_t lt, uint32_t epoch, const TileEsc& te,
-                                             const uint16_t* tb, uint8_t* main, uint64_t n, const uint8_t* cb,
+                                             uint32_t tb, uint8_t* main, uint64_t n, const uint8_t* cb,
                                              uint8_t* esc, uint64_t esc_cap, int32_t* status) {
   const uint32_t lane = lane_id();
   const uint64_t ntiles = num_tiles(n);

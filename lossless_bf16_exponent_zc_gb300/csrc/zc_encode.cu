@@ -5,24 +5,28 @@
 // aligned blocks, asynchronous global->shared staging with double (here
 // triple) buffering.
 //
-// Design on sm_103a: a persistent grid of 8-warp CTAs, one CTA per SM.  Each
+// Design on sm_103a: a persistent grid of 12-warp CTAs, one CTA per SM.  Each
 // warp is its own producer/consumer pipeline: it draws tile tickets from an
 // atomic counter, stages each 8 KB input tile into shared memory with one TMA
-// bulk copy (3 stages in flight per warp, ~200 KB per SM), encodes the tile
-// from shared memory, publishes the tile's escape count, and finds its escape
-// offset with a decoupled look-back over the preceding tiles' flags.  The
-// tile stays in shared memory until its escapes are written at their final
-// global positions, so the escape stream needs no second pass.
+// bulk copy (2 stages per warp, 192 KB per SM), encodes the tile from shared
+// memory, publishes the tile's escape count, and finds its escape offset with
+// a decoupled look-back over the preceding tiles' flags.  The tile stays in
+// shared memory until its escapes are written at their final global
+// positions, so the escape stream needs no second pass.  The next ticket is
+// drawn before the tile is encoded, hiding the atomic's round trip.
 #include "zc_device.cuh"
 #include "zc_internal.h"
 
 namespace zc {
 
-constexpr int kEncWarps = 8;
-constexpr int kEncStages = 3;
-constexpr uint32_t kEncStageBytes = kTile * 2;                                  // 8192
-constexpr uint32_t kEncWarpSmem = kEncStages * kEncStageBytes + 1024 + 64;      // stages, LUT, barriers
-constexpr uint32_t kEncSmem = kEncWarps * kEncWarpSmem;
+constexpr int kEncWarps = 12;
+constexpr int kEncStages = 2;
+constexpr uint32_t kEncStageBytes = kTile * 2;  // 8192
+// 1 KB alignment slack, per-warp LUTs (1 KB each, 1 KB aligned), barriers, stages
+constexpr uint32_t kEncLutOff = 0;
+constexpr uint32_t kEncBarOff = kEncWarps * 1024;
+constexpr uint32_t kEncStageOff = kEncBarOff + 256;
+constexpr uint32_t kEncSmem = 1024 + kEncStageOff + kEncWarps * kEncStages * kEncStageBytes;
 
 template <int MAXB>
 struct EncParams {
@@ -47,9 +51,13 @@ template <int MAXB>
 __global__ void __launch_bounds__(kEncWarps * 32, 1) encode_kernel(const __grid_constant__ EncParams<MAXB> p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
-  uint8_t* wbase = smem + warp * kEncWarpSmem;
-  uint32_t* lut = reinterpret_cast<uint32_t*>(wbase + kEncStages * kEncStageBytes);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(wbase + kEncStages * kEncStageBytes + 1024);
+  const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;  // 1 KB aligned shared address
+  uint8_t* gbase = smem + (sbase - smem_u32(smem));           // its generic pointer
+  uint32_t* lut = reinterpret_cast<uint32_t*>(gbase + kEncLutOff + warp * 1024);
+  const uint32_t lut_s = sbase + kEncLutOff + warp * 1024;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(gbase + kEncBarOff + warp * 16);
+  uint8_t* wstage = gbase + kEncStageOff + warp * kEncStages * kEncStageBytes;
+  const uint32_t wstage_s = sbase + kEncStageOff + warp * kEncStages * kEncStageBytes;
   const uint32_t epoch = launch_epoch(p.ws);
   const uint32_t total_warps = gridDim.x * kEncWarps;
 
@@ -74,7 +82,7 @@ __global__ void __launch_bounds__(kEncWarps * 32, 1) encode_kernel(const __grid_
     }
   }
 
-  auto stage_ptr = [&](int s) { return reinterpret_cast<uint16_t*>(wbase + s * kEncStageBytes); };
+  auto stage_ptr = [&](int s) { return reinterpret_cast<uint16_t*>(wstage + s * kEncStageBytes); };
   auto issue = [&](int s, uint32_t g) {
     const uint32_t ti = locate(p, g);
     const uint32_t lt = g - p.tile_start[ti];
@@ -116,6 +124,10 @@ __global__ void __launch_bounds__(kEncWarps * 32, 1) encode_kernel(const __grid_
       const uint64_t rem = T.n - static_cast<uint64_t>(lt) * kTile;
       const uint32_t n_tile = rem >= kTile ? kTile : static_cast<uint32_t>(rem);
       uint16_t* tb = stage_ptr(s);
+      const uint32_t tb_s = wstage_s + s * kEncStageBytes;
+      // draw the ticket that refills this stage now; the atomic completes while the tile is encoded
+      uint32_t next_raw = 0;
+      if (lane == 0) next_raw = atomicAdd(&p.ws->ticket, 1u);
 
       mbar_wait_bounded(&bar[s], (phase >> s) & 1u, p.status);
       phase ^= 1u << s;
@@ -131,11 +143,11 @@ __global__ void __launch_bounds__(kEncWarps * 32, 1) encode_kernel(const __grid_
       }
       if (cb_ok) {
         TileEsc te;
-        encode_tile(tb, n_tile, lut, tile_ptr(T.main, ntiles, lt), te);
-        publish_tile(p.flags, g, lt, epoch, te, tb, T.main, T.n, T.cb, T.esc, T.esc_cap, p.status);
+        encode_tile(tb_s, n_tile, lut_s, tile_ptr(T.main, ntiles, lt), te);
+        publish_tile(p.flags, g, lt, epoch, te, tb_s, T.main, T.n, T.cb, T.esc, T.esc_cap, p.status);
       }
       __syncwarp();
-      tk[s] = draw_ticket(p.ws);
+      tk[s] = __shfl_sync(kFull, next_raw, 0);
       if (tk[s] < p.total_tiles) issue(s, tk[s]);
     }
   }

@@ -20,10 +20,15 @@ constexpr int kRedWarps = 8;
 constexpr int kRedStages = 2;
 constexpr uint32_t kRedEscCap = 512;
 constexpr uint32_t kRedStageBytes = kTileBytes + kRedEscCap;  // 6144
-// per warp: stages, y tile (8 KB), exponent scratch (1 KB), encoder LUT (1 KB), barriers
-constexpr uint32_t kRedWarpSmem = kRedStages * kRedStageBytes + 8192 + 1024 + 1024 + 64;
-constexpr uint32_t kRedShared = 3 * 256 * 4 + ZC_MAX_SHARDS * 16 + 16;  // spread tables, shard tables, flag
-constexpr uint32_t kRedSmem = kRedShared + kRedWarps * kRedWarpSmem;
+// After 1 KB alignment: spread tables (3 KB), per-warp encoder LUTs (1 KB each,
+// 1 KB aligned), shard tables, a flag, then per warp: stages, y tile (8 KB),
+// exponent scratch (1 KB), barriers.
+constexpr uint32_t kRedLutOff = 3 * 1024;
+constexpr uint32_t kRedShardOff = kRedLutOff + kRedWarps * 1024;
+constexpr uint32_t kRedFlagOff = kRedShardOff + ZC_MAX_SHARDS * 16;
+constexpr uint32_t kRedWarpOff = kRedFlagOff + 16;
+constexpr uint32_t kRedWarpSmem = kRedStages * kRedStageBytes + 8192 + 1024 + 64;
+constexpr uint32_t kRedSmem = 1024 + kRedWarpOff + kRedWarps * kRedWarpSmem;
 
 struct RedParams {
   Shard s[ZC_MAX_SHARDS];
@@ -93,15 +98,20 @@ __device__ __forceinline__ uint4 round_pack(const float (&acc)[8]) {
 template <bool REENC>
 __global__ void __launch_bounds__(kRedWarps * 32, 1) reduce_kernel(const __grid_constant__ RedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint32_t* spread = reinterpret_cast<uint32_t*>(smem);
-  ShardInfo* si = reinterpret_cast<ShardInfo*>(smem + 3 * 256 * 4);
-  int* bad = reinterpret_cast<int*>(smem + 3 * 256 * 4 + ZC_MAX_SHARDS * 16);
   const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
-  uint8_t* wbase = smem + kRedShared + warp * kRedWarpSmem;
+  const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;
+  uint8_t* gbase = smem + (sbase - smem_u32(smem));
+  uint32_t* spread = reinterpret_cast<uint32_t*>(gbase);
+  uint32_t* lut = reinterpret_cast<uint32_t*>(gbase + kRedLutOff + warp * 1024);
+  const uint32_t lut_s = sbase + kRedLutOff + warp * 1024;
+  ShardInfo* si = reinterpret_cast<ShardInfo*>(gbase + kRedShardOff);
+  int* bad = reinterpret_cast<int*>(gbase + kRedFlagOff);
+  uint8_t* wbase = gbase + kRedWarpOff + warp * kRedWarpSmem;
+  const uint32_t wbase_s = sbase + kRedWarpOff + warp * kRedWarpSmem;
   uint16_t* ytile = reinterpret_cast<uint16_t*>(wbase + kRedStages * kRedStageBytes);
+  const uint32_t ytile_s = wbase_s + kRedStages * kRedStageBytes;
   uint8_t* scratch = wbase + kRedStages * kRedStageBytes + 8192;
-  uint32_t* lut = reinterpret_cast<uint32_t*>(scratch + 1024);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(scratch + 2048);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(scratch + 1024);
 
   build_spread_tables(spread);
   if (threadIdx.x == 0) *bad = 0;
@@ -239,6 +249,7 @@ __global__ void __launch_bounds__(kRedWarps * 32, 1) reduce_kernel(const __grid_
             for (int j = 0; j < 8; j++) acc[b][k][j] = -0.0f;  // -0 + x == x for every x
       }
       const uint8_t* tile = stage_ptr(s);
+      const uint32_t tile_s = wbase_s + s * kRedStageBytes;
       mbar_wait_bounded(&bar[s], (phase >> s) & 1u, p.status);
       phase ^= 1u << s;
       {
@@ -254,7 +265,7 @@ __global__ void __launch_bounds__(kRedWarps * 32, 1) reduce_kernel(const __grid_
 #pragma unroll
         for (uint32_t blk = 0; blk < 4; blk++) {
           uint4 v[4];
-          decode_block(tile, blk, n_tile, spread, dt, es, run, scratch, v);
+          decode_block(tile_s, blk, n_tile, sbase, dt, es, run, scratch, v);
 #pragma unroll
           for (int k = 0; k < 4; k++) accumulate(acc[blk][k], v[k]);
         }
@@ -282,8 +293,8 @@ __global__ void __launch_bounds__(kRedWarps * 32, 1) reduce_kernel(const __grid_
         if (REENC) {
           __syncwarp();
           TileEsc te;
-          encode_tile(ytile, n_tile, lut, tile_ptr(p.out_main, p.ntiles, g), te);
-          publish_tile(p.flags, g, g, epoch, te, ytile, p.out_main, p.n, p.out_cb, p.out_esc, p.out_cap, p.status);
+          encode_tile(ytile_s, n_tile, lut_s, tile_ptr(p.out_main, p.ntiles, g), te);
+          publish_tile(p.flags, g, g, epoch, te, ytile_s, p.out_main, p.n, p.out_cb, p.out_esc, p.out_cap, p.status);
         }
       }
       __syncwarp();

@@ -1,0 +1,144 @@
+"""Device-side error reporting: corrupt or inconsistent streams, escape overflow, bad codebooks and the
+bounded inter-block wait.  Every failure is produced on the host (corrupted bytes, a pre-advanced ticket);
+nothing here faults or hangs the GPU: kernels finish and report through the status word."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda()
+
+
+def _stream(zc, n=3 * 4096 + 100, seed=1):
+    x = workloads.gradient(n=n, sigma=1e-3, seed=seed)
+    cb = oracle.codebook_from_sigma(1e-3)
+    st = zc.new_status()
+    main, esc = zc.compress(dev(x), zc.codebook_to_device(cb), zc.workspace(n), st)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0
+    return x, cb, main, esc
+
+
+def _decode_status(zc, main, esc, n, esc_bytes=None):
+    st = zc.new_status()
+    out = torch.full((n,), 0x1234, dtype=torch.int16, device="cuda")
+    zc.decompress(main, esc, n, st, out=out, esc_bytes=esc_bytes)
+    torch.cuda.synchronize()
+    return zc.status_value(st), out
+
+
+def test_bad_magic_writes_nothing(zc):
+    x, cb, main, esc = _stream(zc)
+    bad = main.clone()
+    bad[0] ^= 1
+    code, out = _decode_status(zc, bad, esc, x.size)
+    assert code == zc.ERR_BAD_HEADER
+    assert bool((out == 0x1234).all())
+
+
+def test_size_mismatch(zc):
+    x, cb, main, esc = _stream(zc)
+    code, _ = _decode_status(zc, main, esc, x.size + 1)   # same tile count, different n
+    assert code == zc.ERR_SIZE_MISMATCH
+
+
+def test_escape_count_beyond_buffer(zc):
+    x, cb, main, esc = _stream(zc)
+    n_esc = zc.header_n_esc(main)
+    code, _ = _decode_status(zc, main, esc, x.size, esc_bytes=n_esc - 1)
+    assert code == zc.ERR_BAD_HEADER
+
+
+def test_corrupt_offset_table(zc):
+    x, cb, main, esc = _stream(zc)
+    bad = main.clone()
+    bad[128 + 4:128 + 8] = torch.tensor(list((10 ** 6).to_bytes(4, "little")), dtype=torch.uint8, device="cuda")
+    code, _ = _decode_status(zc, bad, esc, x.size)
+    assert code == zc.ERR_CORRUPT_STREAM
+
+
+def test_offsets_inconsistent_with_planes(zc):
+    """Tile 1 claims one escape fewer than its planes hold: detected, and no read leaves the escape range."""
+    x, cb, main, esc = _stream(zc)
+    bad = main.clone()
+    off = int.from_bytes(bad[128 + 8:128 + 12].cpu().numpy().tobytes(), "little")
+    bad[128 + 8:128 + 12] = torch.tensor(list((off - 1).to_bytes(4, "little")), dtype=torch.uint8, device="cuda")
+    code, _ = _decode_status(zc, bad, esc, x.size)
+    assert code == zc.ERR_CORRUPT_STREAM
+
+
+def test_duplicate_codebook_in_header(zc):
+    x, cb, main, esc = _stream(zc)
+    bad = main.clone()
+    bad[33] = bad[32]
+    code, _ = _decode_status(zc, bad, esc, x.size)
+    assert code == zc.ERR_BAD_HEADER
+
+
+def test_escape_overflow_keeps_exact_count(zc):
+    x = workloads.gradient(n=5 * 4096 + 9, sigma=1e-3, seed=3)
+    cb = oracle.codebook_from_sigma(1e-3)
+    om, oe = oracle.compress(x, cb)
+    cap = 48     # 16-byte multiple, far below the escape count
+    st = zc.new_status()
+    main = torch.empty(om.size, dtype=torch.uint8, device="cuda")
+    esc = torch.zeros(cap, dtype=torch.uint8, device="cuda")
+    zc.compress(dev(x), zc.codebook_to_device(cb), zc.workspace(x.size), st, main=main, esc=esc)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == zc.ERR_ESCAPE_OVERFLOW
+    assert zc.header_n_esc(main) == oe.size
+    assert np.array_equal(main.cpu().numpy(), om)
+    assert np.array_equal(esc.cpu().numpy(), oe[:cap])
+
+
+def test_duplicate_device_codebook(zc):
+    x = workloads.gradient(n=4096, seed=4)
+    st = zc.new_status()
+    main = torch.full((zc.compressed_size(x.size)[0],), 0xAB, dtype=torch.uint8, device="cuda")
+    zc.compress(dev(x), zc.codebook_to_device([1, 2, 3, 4, 5, 6, 6]), zc.workspace(x.size), st, main=main)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == zc.ERR_DUP_CODEBOOK
+    assert bool((main == 0xAB).all())
+
+
+def test_reduce_shard_size_mismatch(zc):
+    a = _stream(zc, n=4096 * 2, seed=5)
+    b = _stream(zc, n=4096 * 2 + 3, seed=6)
+    st = zc.new_status()
+    zc.decompress_reduce([a[2], b[2]], [a[3], b[3]], 4096 * 2, st)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) in (zc.ERR_SIZE_MISMATCH, zc.ERR_BAD_HEADER)
+
+
+def test_lookback_wait_is_bounded(zc):
+    """A workspace whose ticket counter is pre-advanced never produces tile 0, so tile 1's look-back has a
+    flag nobody sets: the wait gives up after about a second with ZC_ERR_TIMEOUT and the kernel returns.
+    The context stays usable and the workspace counters are reset."""
+    import time
+    n = 3 * 4096
+    x = workloads.gradient(n=n, seed=7)
+    cb = oracle.codebook_from_sigma(1e-3)
+    ws = zc.workspace(n)
+    ws[0:4] = torch.tensor([1, 0, 0, 0], dtype=torch.uint8, device="cuda")   # ticket = 1
+    st = zc.new_status()
+    t0 = time.time()
+    zc.compress(dev(x), zc.codebook_to_device(cb), ws, st)
+    torch.cuda.synchronize()
+    dt = time.time() - t0
+    assert zc.status_value(st) == zc.ERR_TIMEOUT
+    assert 0.5 < dt < 30
+    hdr = ws[:8].cpu().numpy().view(np.uint32)
+    assert hdr[0] == 0 and hdr[1] == 0          # ticket and exit counters reset by the last warp
+    # the same workspace works again
+    st2 = zc.new_status()
+    main, esc = zc.compress(dev(x), zc.codebook_to_device(cb), ws, st2)
+    torch.cuda.synchronize()
+    assert zc.status_value(st2) == 0
+    om, oe = oracle.compress(x, cb)
+    assert np.array_equal(main.cpu().numpy(), om)

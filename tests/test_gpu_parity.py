@@ -297,6 +297,13 @@ def test_decompress_reduce_special_values(zc):
         x[rng.integers(0, m, 300)] = rng.integers(1, 128, 300).astype(np.uint16)
         x[rng.integers(0, m, 100)] = 0x8000
         shards.append(x)
+    # fixed positions: +inf + -inf (NaN), max + max (overflow to inf), all -0, subnormal sums, a NaN payload
+    shards[0][0], shards[1][0] = 0x7F80, 0xFF80
+    shards[0][1], shards[1][1], shards[2][1], shards[3][1] = 0x7F7F, 0x7F7F, 0x0000, 0x0000
+    for r in range(P):
+        shards[r][2] = 0x8000
+        shards[r][3] = 0x0001 + r
+    shards[2][4] = 0xFFC3
     cb = oracle.codebook_from_sigma(1e-3)
     st = zc.new_status()
     ws = zc.workspace(m)
@@ -312,7 +319,7 @@ def test_decompress_reduce_special_values(zc):
     oy, orm, ore = oracle.decompress_reduce(om, oe, m, cb)
     assert np.array_equal(host_u16(y), oy)
     assert_stream_equal(host_u8(m_t), host_u8(e_t)[:zc.header_n_esc(m_t)], orm, ore)
-    assert (oy == 0x7FC0).sum() > 0
+    assert oy[0] == 0x7FC0 and oy[1] == 0x7F80 and oy[2] == 0x8000 and oy[3] == 0x000A and oy[4] == 0x7FC0
 
 
 @pytest.mark.slow
