@@ -26,12 +26,13 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
 // ---------------------------------------------------------------- workspace
 // The caller zero-fills the workspace once.  Every kernel returns it to a
-// reusable state: tickets and exit counters are reset by the last warp to
-// leave, look-back flags are tagged with a per-launch epoch so stale flags of
+// reusable state: the exit counter is reset by the last CTA to leave, look-back flags are tagged with a per-launch epoch so stale flags of
 // earlier launches never match, and histogram bins are cleared by the last CTA.
 struct WsHeader {
-  uint32_t ticket;     // next tile ticket of the running encoding launch
-  uint32_t exited;     // warps of the running encoding launch that have left
+  uint32_t hold_tile;  // test hook for the bounded waits: if non-zero, look-back unit hold_tile - 1
+                       // publishes no flag, so its successor's look-back must time out; the
+                       // last CTA of the launch resets it to 0
+  uint32_t exited;     // CTAs of the running encoding launch that have left
   uint32_t epoch;      // epoch tag of the last finished encoding launch
   uint32_t max_tiles;  // largest flag range ever used (cleared when the epoch wraps)
   uint32_t hist_done;  // CTAs of the running histogram launch that have finished
@@ -353,10 +354,11 @@ __device__ __forceinline__ void write_escapes(uint32_t tb, const TileEsc& te, ui
 // tile g, whose tensor starts at global tile g0, by summing the aggregates of
 // preceding tiles until one carrying an inclusive prefix is found.  Each step
 // reads the flags of the 128 nearest unresolved predecessors (4 per lane) so
-// the resolved front moves quickly even with ~1,800 tiles in flight.  Tiles
-// are handed out by an atomic ticket in increasing order and every ticket
-// holder is resident, so predecessors always make progress; the wait is still
-// bounded (ZC_ERR_TIMEOUT, prefix then meaningless).
+// the resolved front moves quickly even with ~1,800 tiles in flight.  Every
+// warp owns a fixed set of tiles, visits them in increasing order, and all
+// warps are resident (cooperative launch), so predecessors always make
+// progress; the wait is still bounded (ZC_ERR_TIMEOUT, prefix then
+// meaningless).
 constexpr int kLookbackPerLane = 4;
 
 __device__ __forceinline__ uint64_t lookback(const Flag* flags, uint32_t g, uint32_t g0, uint32_t epoch,
@@ -584,47 +586,44 @@ __device__ __forceinline__ void write_header_tail(uint8_t* main, uint64_t ntiles
 
 // The epoch tag used by a launch: one more than the last finished launch's,
 // never 0 (the value of a zero-filled workspace).
+__device__ __forceinline__ uint32_t launch_hold(const WsHeader* ws) {
+  return *reinterpret_cast<const volatile uint32_t*>(&ws->hold_tile);
+}
+
 __device__ __forceinline__ uint32_t launch_epoch(const WsHeader* ws) {
   const uint32_t e = *reinterpret_cast<const volatile uint32_t*>(&ws->epoch) + 1u;
   return e == 0 ? 1u : e;
 }
 
-// Exit protocol of a ticketed launch: every warp calls this once, after its
-// last use of a ticket.  The last warp resets the ticket and exit counters and
-// publishes the epoch; when the epoch wraps it clears every flag first, so a
-// flag written 2^32 launches earlier can never pass for a current one.
-__device__ __forceinline__ void ticket_exit(WsHeader* ws, Flag* flags, uint32_t epoch, uint32_t total_tiles,
-                                            uint32_t total_warps) {
-  const uint32_t lane = lane_id();
-  uint32_t last = 0;
-  __syncwarp();
-  if (lane == 0) {
+// Exit protocol of a launch that uses look-back flags: every thread of every
+// CTA calls this once, after its last flag access.  The last CTA to leave
+// resets the exit counter and publishes the epoch; when the epoch wraps it
+// clears every flag first, so a flag written 2^32 launches earlier can never
+// pass for a current one.  One atomic per CTA.
+__device__ __forceinline__ void cta_exit(WsHeader* ws, Flag* flags, uint32_t epoch, uint32_t total_tiles) {
+  __shared__ int last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
     __threadfence();
-    last = (atomicAdd(&ws->exited, 1u) == total_warps - 1) ? 1u : 0u;
+    last = atomicAdd(&ws->exited, 1u) == gridDim.x - 1;
   }
-  last = __shfl_sync(kFull, last, 0);
+  __syncthreads();
   if (!last) return;
   __threadfence();
   const uint32_t maxt = max(*reinterpret_cast<volatile uint32_t*>(&ws->max_tiles), total_tiles);
   if (epoch == 0xFFFFFFFFu) {
-    for (uint32_t i = lane; i < maxt; i += 32) flags[i] = Flag{0ull, 0ull};
+    for (uint32_t i = threadIdx.x; i < maxt; i += blockDim.x) flags[i] = Flag{0ull, 0ull};
     __threadfence();
+    __syncthreads();
   }
-  if (lane == 0) {
+  if (threadIdx.x == 0) {
     ws->max_tiles = maxt;
-    ws->ticket = 0;
     ws->exited = 0;
+    ws->hold_tile = 0;
     ws->epoch = (epoch == 0xFFFFFFFFu) ? 0u : epoch;
     __threadfence();
   }
 }
-
-__device__ __forceinline__ uint32_t draw_ticket(WsHeader* ws) {
-  uint32_t t = 0;
-  if (lane_id() == 0) t = atomicAdd(&ws->ticket, 1u);
-  return __shfl_sync(kFull, t, 0);
-}
-
 
 // After encode_tile: publish the tile's escape count, find its escape offset by
 // look-back, write the offset-table entry, the header parts this tile owns
@@ -633,8 +632,9 @@ __device__ __forceinline__ uint32_t draw_ticket(WsHeader* ws) {
 // whose first global tile is g - lt.  Warp-wide.
 __device__ __forceinline__ void publish_tile(Flag* flags, uint32_t g, uint32_t lt, uint32_t epoch, const TileEsc& te,
                                              uint32_t tb, uint8_t* main, uint64_t n, const uint8_t* cb,
-                                             uint8_t* esc, uint64_t esc_cap, int32_t* status) {
+                                             uint8_t* esc, uint64_t esc_cap, int32_t* status, uint32_t hold) {
   const uint32_t lane = lane_id();
+  if (hold == g + 1) return;  // test hook: this tile stays unpublished
   const uint64_t ntiles = num_tiles(n);
   const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
   uint64_t prefix = 0;

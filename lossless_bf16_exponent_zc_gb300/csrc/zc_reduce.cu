@@ -9,8 +9,8 @@
 // the 5632-byte tile, cp.async for its escape bytes, two stages in flight);
 // each copy is decoded from shared memory straight into the accumulators.
 // With re-encoding, the rounded tile goes to shared memory and through the
-// same encoder and look-back as zc_compress, so tiles are handed out by
-// ticket; without it they are assigned statically.
+// same encoder and look-back as zc_compress (cooperative launch: every tile
+// owner is resident).  Warp w owns tiles w, w + W, w + 2W, ...
 #include "zc_device.cuh"
 #include "zc_internal.h"
 
@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kRedWarps * 32, 1) reduce_kernel(const __grid_
   }
   __syncthreads();
   const uint32_t epoch = REENC ? launch_epoch(p.ws) : 0u;
+  const uint32_t hold = REENC ? launch_hold(p.ws) : 0u;
   const uint32_t total_warps = gridDim.x * kRedWarps;
   const bool skip = (*bad != 0) || !ok_out;
   if (REENC && !skip && p.ntiles == 0 && blockIdx.x == 0 && warp == 0) {
@@ -161,11 +162,10 @@ __global__ void __launch_bounds__(kRedWarps * 32, 1) reduce_kernel(const __grid_
     write_header_tail(p.out_main, 0, 0);
   }
 
-  // ---- tile sequence: tickets with re-encoding, static otherwise
+  // ---- tile sequence: warp w owns tiles w, w + W, w + 2W, ...
   uint32_t static_next = blockIdx.x * kRedWarps + warp;
   auto next_tile = [&]() -> uint32_t {
     if (skip) return 0xFFFFFFFFu;
-    if (REENC) return draw_ticket(p.ws);
     const uint32_t g = static_next;
     static_next += total_warps;
     return g;
@@ -294,14 +294,15 @@ __global__ void __launch_bounds__(kRedWarps * 32, 1) reduce_kernel(const __grid_
           __syncwarp();
           TileEsc te;
           encode_tile(ytile_s, n_tile, lut_s, tile_ptr(p.out_main, p.ntiles, g), te);
-          publish_tile(p.flags, g, g, epoch, te, ytile_s, p.out_main, p.n, p.out_cb, p.out_esc, p.out_cap, p.status);
+          publish_tile(p.flags, g, g, epoch, te, ytile_s, p.out_main, p.n, p.out_cb, p.out_esc, p.out_cap, p.status,
+                       hold);
         }
       }
       __syncwarp();
       issue_item(s);
     }
   }
-  if (REENC) ticket_exit(p.ws, p.flags, epoch, p.ntiles, total_warps);
+  if (REENC) cta_exit(p.ws, p.flags, epoch, p.ntiles);
 }
 
 cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out, const uint8_t* out_cb,
@@ -327,13 +328,18 @@ cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out,
   if (out_cb) {
     err = cudaFuncSetAttribute(reduce_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
     if (err != cudaSuccess) return err;
-    reduce_kernel<true><<<ctas, kRedWarps * 32, kRedSmem, stream>>>(p);
-  } else {
-    if (p.ntiles == 0) return cudaSuccess;
-    err = cudaFuncSetAttribute(reduce_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reduce_kernel<true>, kRedWarps * 32, kRedSmem);
     if (err != cudaSuccess) return err;
-    reduce_kernel<false><<<ctas, kRedWarps * 32, kRedSmem, stream>>>(p);
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    void* args[] = {&p};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(reduce_kernel<true>), dim3(ctas),
+                                       dim3(kRedWarps * 32), args, kRedSmem, stream);
   }
+  if (p.ntiles == 0) return cudaSuccess;
+  err = cudaFuncSetAttribute(reduce_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
+  if (err != cudaSuccess) return err;
+  reduce_kernel<false><<<ctas, kRedWarps * 32, kRedSmem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -117,15 +117,15 @@ def test_reduce_shard_size_mismatch(zc):
 
 
 def test_lookback_wait_is_bounded(zc):
-    """A workspace whose ticket counter is pre-advanced never produces tile 0, so tile 1's look-back has a
-    flag nobody sets: the wait gives up after about a second with ZC_ERR_TIMEOUT and the kernel returns.
-    The context stays usable and the workspace counters are reset."""
+    """The workspace's hold hook keeps the first look-back unit (a group of 12 tiles) from publishing its
+    flag, so the next group's look-back waits on a flag nobody sets: the wait gives up after about a second
+    with ZC_ERR_TIMEOUT and the kernel returns.  The context stays usable and the counters are reset."""
     import time
-    n = 3 * 4096
+    n = 40 * 4096
     x = workloads.gradient(n=n, seed=7)
     cb = oracle.codebook_from_sigma(1e-3)
     ws = zc.workspace(n)
-    ws[0:4] = torch.tensor([1, 0, 0, 0], dtype=torch.uint8, device="cuda")   # ticket = 1
+    ws[0:4] = torch.tensor([1, 0, 0, 0], dtype=torch.uint8, device="cuda")   # hold unit 0
     st = zc.new_status()
     t0 = time.time()
     zc.compress(dev(x), zc.codebook_to_device(cb), ws, st)
@@ -134,7 +134,7 @@ def test_lookback_wait_is_bounded(zc):
     assert zc.status_value(st) == zc.ERR_TIMEOUT
     assert 0.5 < dt < 30
     hdr = ws[:8].cpu().numpy().view(np.uint32)
-    assert hdr[0] == 0 and hdr[1] == 0          # ticket and exit counters reset by the last warp
+    assert hdr[0] == 0 and hdr[1] == 0          # hook and exit counter reset by the last CTA
     # the same workspace works again
     st2 = zc.new_status()
     main, esc = zc.compress(dev(x), zc.codebook_to_device(cb), ws, st2)
