@@ -350,6 +350,25 @@ __device__ __forceinline__ void write_escapes(uint32_t tb, const TileEsc& te, ui
   }
 }
 
+// Moves the tile's escapes (8-bit exponents read back from the tile at shared
+// address `tb`) into a shared staging buffer `buf` in escape order; the
+// caller guarantees te.total fits.  Escapes of a lane are consecutive.
+__device__ __forceinline__ void stage_tile_escapes(uint32_t tb, const TileEsc& te, uint8_t* buf) {
+  const uint32_t lane = lane_id();
+  const uint32_t lane_off = tb + 16 * lane;
+#pragma unroll
+  for (uint32_t blk = 0; blk < 4; blk++) {
+    uint32_t m = te.mask[blk];
+    uint8_t* dst = buf + te.base[blk];
+    const uint32_t src = lane_off + 2 * blk * kBlock;
+    while (m) {
+      const uint32_t p = __ffs(m) - 1;
+      m &= m - 1;
+      *dst++ = static_cast<uint8_t>(lds_u16(src + 512 * (p >> 3) + 2 * (p & 7)) >> 7);
+    }
+  }
+}
+
 // Decoupled look-back (single pass): returns the exclusive escape prefix of
 // tile g, whose tensor starts at global tile g0, by summing the aggregates of
 // preceding tiles until one carrying an inclusive prefix is found.  Each step
