@@ -257,24 +257,30 @@ __device__ __forceinline__ bool build_enc_lut(uint32_t* lut, const uint8_t* cb_d
 __device__ __forceinline__ uint32_t lut_lo(uint32_t w, uint32_t lut) { return lds32(((w >> 5) & 0x3FCu) | lut); }
 __device__ __forceinline__ uint32_t lut_hi(uint32_t w, uint32_t lut) { return lds32(((w >> 21) & 0x3FCu) | lut); }
 
-// Per-lane escape bookkeeping of one encoded tile.
-struct TileEsc {
-  uint32_t mask[4];  // bit 8k + j: block element 256k + 8*lane + j is an escape
-  uint32_t base[4];  // tile-local rank of this lane's first escape in each block
-  uint32_t total;    // escapes in the tile (same in every lane)
+// Per-lane escape bookkeeping of NB encoded blocks (a tile: NB = 4).
+template <int NB>
+struct EscBook {
+  uint32_t mask[NB];  // bit 8k + j: block element 256k + 8*lane + j is an escape
+  uint32_t base[NB];  // rank of this lane's first escape in each block, from the first block on
+  uint32_t total;     // escapes in the NB blocks (same in every lane)
 };
+using TileEsc = EscBook<4>;
 
-// Encodes one tile held in shared memory (shared address `tb`: 4096 bf16 bit
-// patterns, zero beyond n_tile) into its 5632-byte ZC1 tile at `out`
-// (global).  One warp.  Lane l of group k handles block elements
-// 256k + 8l .. 256k + 8l + 7 (one 16-byte vector); its 4 groups' code bits
-// form one plane word per plane, which is exactly the column-major plane
-// layout (byte 4l + k).
-__device__ __forceinline__ void encode_tile(uint32_t tb, uint32_t n_tile, uint32_t lut, uint8_t* out, TileEsc& te) {
+// Encodes NB consecutive blocks held in shared memory (shared address `tb`:
+// NB * 1024 bf16 bit patterns, zero beyond the valid ones) into their 1408-byte
+// ZC1 blocks at `out` (global).  `blk0` is the index of the first block in its
+// tile and `n_tile` the tile's valid elements (positions past it get code 0 and
+// are not escapes).  One warp.  Lane l of group k handles block elements
+// 256k + 8l .. 256k + 8l + 7 (one 16-byte vector); its 4 groups' code bits form
+// one plane word per plane, which is exactly the column-major plane layout
+// (byte 4l + k).  Escape ranks come from one packed warp scan over all blocks.
+template <int NB>
+__device__ __forceinline__ void encode_blocks(uint32_t tb, uint32_t blk0, uint32_t n_tile, uint32_t lut, uint8_t* out,
+                                              EscBook<NB>& te) {
   const uint32_t lane = lane_id();
-  uint32_t run = 0;
+  uint32_t cnt[NB];
 #pragma unroll
-  for (uint32_t blk = 0; blk < 4; blk++) {
+  for (uint32_t blk = 0; blk < NB; blk++) {
     uint32_t acc[4];
     uint2 smv[4];
 #pragma unroll
@@ -300,7 +306,7 @@ __device__ __forceinline__ void encode_tile(uint32_t tb, uint32_t n_tile, uint32
     uint32_t w2 = __byte_perm(u01, u23, 0x5410);
     uint32_t x = __byte_perm(u01, u23, 0x7632);
     if (n_tile < kTile) {
-      const uint32_t valid = lane_valid_mask(blk, n_tile, lane);
+      const uint32_t valid = lane_valid_mask(blk0 + blk, n_tile, lane);
       w0 &= valid;
       w1 &= valid;
       w2 &= valid;
@@ -309,26 +315,43 @@ __device__ __forceinline__ void encode_tile(uint32_t tb, uint32_t n_tile, uint32
     *reinterpret_cast<uint32_t*>(ob + 1024 + lane * 4) = w0;
     *reinterpret_cast<uint32_t*>(ob + 1152 + lane * 4) = w1;
     *reinterpret_cast<uint32_t*>(ob + 1280 + lane * 4) = w2;
-    const uint32_t c = __popc(x);
-    const uint32_t inc = warp_inclusive_scan(c);
     te.mask[blk] = x;
-    te.base[blk] = run + inc - c;
-    run += __shfl_sync(kFull, inc, 31);
+    cnt[blk] = __popc(x);
+  }
+  // packed scan: two blocks per 32-bit word, 16-bit fields (a block's total is at most 1024)
+  uint32_t run = 0;
+#pragma unroll
+  for (int b = 0; b < NB; b += 2) {
+    const uint32_t packed = cnt[b] | ((b + 1 < NB ? cnt[b + 1] : 0u) << 16);
+    const uint32_t inc = warp_inclusive_scan(packed);
+    const uint32_t tot = __shfl_sync(kFull, inc, 31);
+    const uint32_t exc = inc - packed;
+    te.base[b] = run + (exc & 0xFFFFu);
+    run += tot & 0xFFFFu;
+    if (b + 1 < NB) {
+      te.base[b + 1] = run + (exc >> 16);
+      run += tot >> 16;
+    }
   }
   te.total = run;
 }
 
-// Writes the tile's escapes (their 8-bit exponents, read back from the tile
-// in shared memory at shared address `tb`) at global positions prefix + rank,
-// skipping positions at or beyond `cap`.  Escapes of a lane are consecutive,
-// in bit order.
-__device__ __forceinline__ void write_escapes(uint32_t tb, const TileEsc& te, uint64_t prefix, uint8_t* esc,
+__device__ __forceinline__ void encode_tile(uint32_t tb, uint32_t n_tile, uint32_t lut, uint8_t* out, TileEsc& te) {
+  encode_blocks<4>(tb, 0, n_tile, lut, out, te);
+}
+
+// Writes the escapes of NB blocks (their 8-bit exponents, read back from the
+// blocks in shared memory at shared address `tb`) at global positions prefix +
+// rank, skipping positions at or beyond `cap`.  Escapes of a lane are
+// consecutive, in bit order.
+template <int NB>
+__device__ __forceinline__ void write_escapes(uint32_t tb, const EscBook<NB>& te, uint64_t prefix, uint8_t* esc,
                                               uint64_t cap) {
   const uint32_t lane = lane_id();
   const bool fits = prefix + te.total <= cap;
   const uint32_t lane_off = tb + 16 * lane;
 #pragma unroll
-  for (uint32_t blk = 0; blk < 4; blk++) {
+  for (uint32_t blk = 0; blk < NB; blk++) {
     uint32_t m = te.mask[blk];
     uint8_t* dst = esc + prefix + te.base[blk];
     const uint32_t src = lane_off + 2 * blk * kBlock;
@@ -350,51 +373,71 @@ __device__ __forceinline__ void write_escapes(uint32_t tb, const TileEsc& te, ui
   }
 }
 
-// Moves the tile's escapes (8-bit exponents read back from the tile at shared
-// address `tb`) into a shared staging buffer `buf` in escape order; the
-// caller guarantees te.total fits.  Escapes of a lane are consecutive.
-__device__ __forceinline__ void stage_tile_escapes(uint32_t tb, const TileEsc& te, uint8_t* buf) {
+// Moves the escapes of NB blocks (8-bit exponents read back from the blocks at
+// shared address `tb`) into a shared staging buffer `buf` in escape order; the
+// caller guarantees te.total fits.  Escapes of a lane are consecutive.  Up to
+// four escapes per iteration, so their shared loads overlap.
+template <int NB>
+__device__ __forceinline__ void stage_escapes_smem(uint32_t tb, const EscBook<NB>& te, uint8_t* buf) {
   const uint32_t lane = lane_id();
   const uint32_t lane_off = tb + 16 * lane;
 #pragma unroll
-  for (uint32_t blk = 0; blk < 4; blk++) {
+  for (uint32_t blk = 0; blk < NB; blk++) {
     uint32_t m = te.mask[blk];
     uint8_t* dst = buf + te.base[blk];
     const uint32_t src = lane_off + 2 * blk * kBlock;
     while (m) {
-      const uint32_t p = __ffs(m) - 1;
-      m &= m - 1;
-      *dst++ = static_cast<uint8_t>(lds_u16(src + 512 * (p >> 3) + 2 * (p & 7)) >> 7);
+      uint32_t p[4], v[4];
+      int k = 0;
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        p[u] = m ? static_cast<uint32_t>(__ffs(m) - 1) : 0u;
+        k += m != 0;
+        m &= m - 1;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; u++) v[u] = lds_u16(src + 512 * (p[u] >> 3) + 2 * (p[u] & 7));
+#pragma unroll
+      for (int u = 0; u < 4; u++)
+        if (u < k) dst[u] = static_cast<uint8_t>(v[u] >> 7);
+      dst += k;
     }
   }
 }
 
 // Decoupled look-back (single pass): returns the exclusive escape prefix of
-// tile g, whose tensor starts at global tile g0, by summing the aggregates of
-// preceding tiles until one carrying an inclusive prefix is found.  Each step
-// reads the flags of the 128 nearest unresolved predecessors (4 per lane) so
-// the resolved front moves quickly even with ~1,800 tiles in flight.  Every
-// warp owns a fixed set of tiles, visits them in increasing order, and all
-// warps are resident (cooperative launch), so predecessors always make
-// progress; the wait is still bounded (ZC_ERR_TIMEOUT, prefix then
-// meaningless).
-constexpr int kLookbackPerLane = 4;
+// unit g (a tile or a group of tiles), whose tensor starts at unit g0, by
+// summing the aggregates of preceding units until one carrying an inclusive
+// prefix is found.  A caller that already knows the inclusive prefix of an
+// earlier unit of the same tensor (its own previous unit) passes it as
+// (known_idx, known_val): the scan then needs only the aggregates in between,
+// which other units publish without waiting on anyone, so no chain of
+// look-backs forms.  Each step reads the flags of the 160 nearest unresolved
+// predecessors (5 per lane).  Every unit's owner visits its units in
+// increasing order and all owners are resident (cooperative launch), so
+// predecessors always make progress; the wait is still bounded
+// (ZC_ERR_TIMEOUT, prefix then meaningless).
+constexpr int kLookbackPerLane = 5;
 
 __device__ __forceinline__ uint64_t lookback(const Flag* flags, uint32_t g, uint32_t g0, uint32_t epoch,
-                                             int32_t* status, bool* timed_out) {
+                                             int32_t* status, bool* timed_out, int64_t known_idx = -1,
+                                             uint64_t known_val = 0) {
   const uint32_t lane = lane_id();
   uint64_t prefix = 0;
   int64_t end = g;  // exclusive end of the window
   unsigned long long t0 = 0;
   *timed_out = false;
   while (true) {
-    uint32_t st[kLookbackPerLane], val[kLookbackPerLane];
+    uint32_t st[kLookbackPerLane];
+    uint64_t val[kLookbackPerLane];
 #pragma unroll
     for (int q = 0; q < kLookbackPerLane; q++) {
       const int64_t idx = end - 1 - static_cast<int64_t>(lane + 32 * q);  // distance lane + 32q
       st[q] = 2;
       val[q] = 0;
-      if (idx >= static_cast<int64_t>(g0)) {
+      if (idx == known_idx) {
+        val[q] = known_val;
+      } else if (idx >= static_cast<int64_t>(g0)) {
         const ulonglong2 f = ld_relaxed_v2(flags + idx);
         if (static_cast<uint32_t>(f.y >> 32) == epoch) {
           val[q] = static_cast<uint32_t>(f.y);
@@ -434,10 +477,12 @@ __device__ __forceinline__ uint64_t lookback(const Flag* flags, uint32_t g, uint
       }
       continue;
     }
-    uint32_t part = 0;
+    uint64_t part = 0;
 #pragma unroll
     for (int q = 0; q < kLookbackPerLane; q++) part += (lane + 32 * q <= first) ? val[q] : 0u;
-    prefix += warp_sum(part);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) part += __shfl_xor_sync(kFull, part, d);
+    prefix += part;
     if (found) return prefix;
     end -= 32 * kLookbackPerLane;
   }
@@ -672,7 +717,7 @@ __device__ __forceinline__ void publish_tile(Flag* flags, uint32_t g, uint32_t l
     write_header_tail(main, ntiles, n_esc);
     if (lane == 0 && n_esc > esc_cap) set_status(status, ZC_ERR_ESCAPE_OVERFLOW);
   }
-  write_escapes(tb, te, prefix, esc, esc_cap);
+  write_escapes<4>(tb, te, prefix, esc, esc_cap);
 }
 
 // bfloat16 bits of f, rounded to nearest even (IEEE-754 definition: add half
