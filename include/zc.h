@@ -206,6 +206,30 @@ zc_status zc_decompress_reduce(int P, const void* const* h_mains, const void* co
                                int32_t* d_status, void* stream);
 
 /*
+ * zc_compress without a workspace argument, for callers that cannot allocate
+ * device memory: code running while a stream is captured into a CUDA graph,
+ * hooks of a communication or training framework that receive only the
+ * tensors to send, and latency-critical paths that must never call cudaMalloc
+ * (it can synchronise the device).  The method pages have no counterpart; it
+ * is a deployment convenience.  Output is identical to zc_compress.
+ *   - The scratch is a fixed 1 MiB + 4 KiB device array inside libzc
+ *     (every GPU that loads the library holds it until the process exits), so
+ *     n is limited to 2^28 values (512 MiB of bf16); larger n returns
+ *     ZC_ERR_WORKSPACE and enqueues nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the array and it keeps the last call's
+ *     contents; the call clears the counters that must start at zero with an
+ *     8-byte cudaMemsetAsync on `stream`.  Calls that overlap on the GPU (two
+ *     streams at once) race: order them on one stream.
+ *   - No cudaMalloc, cudaFree or allocating library routine is called.
+ * Arguments, alignment and device errors as in zc_compress.
+ */
+zc_status zc_compress_noalloc(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_main, void* d_esc,
+                              uint64_t esc_capacity, int32_t* d_status, void* stream);
+
+/*
  * One tensor of a batched call.  compress: bf16 = input (n values), main/esc =
  * outputs, esc_bytes = escape capacity, cb = device codebook.  decompress:
  * main/esc = inputs, esc_bytes = readable escape bytes, bf16 = output, cb unused.
