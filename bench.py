@@ -52,11 +52,13 @@ def parse_args(argv=None):
     p.add_argument("--ref-sample-log2", type=int, default=20, help="elements per reference-arm step")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-workloads", action="store_true", help="skip the per-workload section")
+    p.add_argument("--sweep-max-log2", type=int, default=29, help="largest reduce-scatter shard (elements)")
     p.add_argument("--profile", action="store_true",
-                   help="for profiler runs: no clock sampling, no soak, no e2e or CPU legs")
+                   help="for profiler runs: no clock sampling, no soak, no e2e, CPU or workload legs")
     a = p.parse_args(argv)
     if a.profile:
-        a.no_e2e = a.no_cpu_baseline = True
+        a.no_e2e = a.no_cpu_baseline = a.no_workloads = True
     return a
 
 
@@ -335,6 +337,11 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(x, args.cpu_sample_log2)
 
+    per_workload = None
+    if world == 1 and not args.no_workloads:
+        del main_a, main_b, esc_a, esc_b, y
+        per_workload = run_workloads(args, zc, torch, device, peak)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -355,6 +362,7 @@ def run_ours(args):
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "workloads": per_workload,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -420,6 +428,148 @@ def run_e2e(args, zc, torch, device, x, mb, eb, world):
     value = sum_over_ranks(4 * 2 * n, world, device) * steps / dt / 1e9
     return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": 2 * n + 7,
             "d2h_bytes_per_step": d2h[0], "steps": steps}
+
+
+# ------------------------------------------------------------------ per-workload section
+def _time_ms(torch, fn, reps, warmup=2):
+    for _ in range(warmup):
+        fn()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(reps):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / reps
+
+
+def run_workloads(args, zc, torch, device, peak):
+    """Per-kernel GB/s (uncompressed and algorithmic), HBM fraction, ratio and escape rate for the other
+    workloads: the 2^20 Gaussian (L2-resident), the 9-tensor Llama-3-8B bucket (batched), the MoE payload
+    (histogram codebook, 8 Zipf chunks batched), and the reduce-scatter local stage (P = 8) with its
+    shard-size sweep.  Inputs above L2 size are not flushed between repetitions of the same op."""
+    import math as _m
+    out = {}
+    st = zc.new_status(device=device)
+    dev = lambda a: torch.from_numpy(a.view(np.int16)).to(device)
+
+    def entry(ms, n_unc, alg):
+        return {"ms": round(ms, 4), "GB_per_s_uncompressed": round(n_unc / ms / 1e6, 1),
+                "alg_GB_per_s": round(alg / ms / 1e6, 1), "frac_of_hbm": round(alg / ms / 1e6 / peak, 4)}
+
+    # 1. gaussian 2^20, sigma codebook
+    x = workloads.gaussian()
+    n = x.size
+    xt = dev(x)
+    cb = zc.codebook_to_device(zc.codebook_from_sigma(workloads.GAUSSIAN_SIGMA), device)
+    ws = zc.workspace(n, device=device)
+    mb, eb = zc.compressed_size(n)
+    m_t = torch.empty(mb, dtype=torch.uint8, device=device)
+    e_t = torch.empty(eb, dtype=torch.uint8, device=device)
+    y = torch.empty(n, dtype=torch.int16, device=device)
+    tc = _time_ms(torch, lambda: zc.compress(xt, cb, ws, st, main=m_t, esc=e_t), 50)
+    k = zc.header_n_esc(m_t)
+    td = _time_ms(torch, lambda: zc.decompress(m_t, e_t, n, st, out=y), 50)
+    out["gaussian_2^20_L2_resident"] = {"compress": entry(tc, 2 * n, 2 * n + mb + k),
+                                        "decompress": entry(td, 2 * n, 2 * n + mb + k),
+                                        "ratio": round(2 * n / (mb + k), 4), "escape_rate": round(k / n, 5)}
+
+    # 2. Llama-3-8B layer bucket, one batched launch each way
+    bucket = workloads.llama_bucket()
+    items, outs, total_n = [], [], 0
+    for name, a, sigma in bucket:
+        mb_i, eb_i = zc.compressed_size(a.size)
+        items.append(zc.BatchItem(bf16=dev(a), main=torch.empty(mb_i, dtype=torch.uint8, device=device),
+                                  esc=torch.empty(eb_i, dtype=torch.uint8, device=device),
+                                  cb=zc.codebook_to_device(zc.codebook_from_sigma(sigma), device)))
+        total_n += a.size
+    del bucket
+    ws = zc.workspace([it.bf16.numel() for it in items], device=device)
+    tc = _time_ms(torch, lambda: zc.compress_batched(items, ws, st), 10)
+    mains = sum(it.main.numel() for it in items)
+    escs = sum(zc.header_n_esc(it.main) for it in items)
+    outs = [zc.BatchItem(bf16=torch.empty_like(it.bf16), main=it.main, esc=it.esc) for it in items]
+    td = _time_ms(torch, lambda: zc.decompress_batched(outs, st), 10)
+    ok = all(torch.equal(o.bf16, it.bf16) for o, it in zip(outs, items))
+    out["llama3_8b_layer_bucket_9_tensors"] = {
+        "elements": total_n, "compress_batched": entry(tc, 2 * total_n, 2 * total_n + mains + escs),
+        "decompress_batched": entry(td, 2 * total_n, 2 * total_n + mains + escs),
+        "ratio": round(2 * total_n / (mains + escs), 4), "escape_rate": round(escs / total_n, 5), "round_trip_ok": ok}
+    del items, outs
+
+    # 3. MoE all-to-all payload: histogram codebook over the payload, 8 destination chunks
+    x, counts = workloads.moe_payload()
+    n = x.size
+    xt = dev(x)
+    del x
+    ws = zc.workspace([c * 4096 for c in counts], device=device)
+    cbh = torch.empty(7, dtype=torch.uint8, device=device)
+    th = _time_ms(torch, lambda: zc.histogram_topk(xt, ws, st, cb_out=cbh), 10)
+    items, start = [], 0
+    for c in counts:
+        m_ = c * 4096
+        mb_i, eb_i = zc.compressed_size(m_)
+        items.append(zc.BatchItem(bf16=xt[start:start + m_], main=torch.empty(mb_i, dtype=torch.uint8, device=device),
+                                  esc=torch.empty(eb_i, dtype=torch.uint8, device=device), cb=cbh))
+        start += m_
+    tc = _time_ms(torch, lambda: zc.compress_batched(items, ws, st), 10)
+    mains = sum(it.main.numel() for it in items)
+    escs = sum(zc.header_n_esc(it.main) for it in items)
+    outs = [zc.BatchItem(bf16=torch.empty_like(it.bf16), main=it.main, esc=it.esc) for it in items]
+    td = _time_ms(torch, lambda: zc.decompress_batched(outs, st), 10)
+    ok = torch.equal(torch.cat([o.bf16 for o in outs]), xt)
+    out["moe_payload_16384x4096_8_chunks"] = {
+        "histogram": entry(th, 2 * n, 2 * n), "compress_batched": entry(tc, 2 * n, 2 * n + mains + escs),
+        "decompress_batched": entry(td, 2 * n, 2 * n + mains + escs), "ratio": round(2 * n / (mains + escs), 4),
+        "escape_rate": round(escs / n, 5), "round_trip_ok": bool(ok)}
+    del items, outs, xt
+
+    # 4. reduce-scatter local stage: P = 8 shards of 2^25, sigma codebook in, sigma*sqrt(8) out
+    P = 8
+    shards = workloads.rs_shards()
+    base = [dev(a) for a in shards]
+    del shards
+    cb_in = zc.codebook_to_device(zc.codebook_from_sigma(workloads.RS_SIGMA), device)
+    cb_out = zc.codebook_to_device(zc.codebook_from_sigma(workloads.RS_SIGMA * _m.sqrt(P)), device)
+
+    def reduce_case(m):
+        """Compress P shards of m elements (tiling the 2^25 base shards), time decompress_reduce."""
+        reps_src = -(-m // base[0].numel())
+        src = [b.repeat(reps_src)[:m] if reps_src > 1 else b[:m] for b in base]
+        ws_ = zc.workspace(m, device=device)
+        mains_, escs_ = [], []
+        for s_ in src:
+            a_, b_ = zc.compress(s_, cb_in, ws_, st)
+            mains_.append(a_)
+            escs_.append(b_)
+        del src
+        mb_, eb_ = zc.compressed_size(m)
+        y_ = torch.empty(m, dtype=torch.int16, device=device)
+        om_ = torch.empty(mb_, dtype=torch.uint8, device=device)
+        oe_ = torch.empty(eb_, dtype=torch.uint8, device=device)
+        reps = max(3, min(50, int(2e9 // (P * m * 2))))
+        t_ = _time_ms(torch, lambda: zc.decompress_reduce(mains_, escs_, m, st, out=y_, out_cb=cb_out, out_main=om_,
+                                                          out_esc=oe_, ws=ws_), reps)
+        in_bytes = sum(mb_ + zc.header_n_esc(a_) for a_ in mains_)
+        k_out = zc.header_n_esc(om_)
+        alg = in_bytes + 2 * m + mb_ + k_out
+        r = entry(t_, 2 * P * m, alg)
+        r.update({"shard_elements": m, "escape_rate_in": round((in_bytes - P * mb_) / (P * m), 5),
+                  "escape_rate_out": round(k_out / m, 5)})
+        return r
+
+    out["reduce_scatter_8x2^25"] = reduce_case(1 << 25)
+    sweep = []
+    for lg in range(15, args.sweep_max_log2 + 1):
+        sweep.append(reduce_case(1 << lg))
+        torch.cuda.empty_cache()
+    out["reduce_scatter_sweep_P8"] = [{"shard_bytes": r["shard_elements"] * 2, "ms": r["ms"],
+                                       "GB_per_s_uncompressed": r["GB_per_s_uncompressed"],
+                                       "frac_of_hbm": r["frac_of_hbm"]} for r in sweep]
+    if zc.status_value(st) != 0:
+        out["status"] = zc.status_string(zc.status_value(st))
+    return out
 
 
 def main(argv=None):
