@@ -603,6 +603,81 @@ __device__ __forceinline__ uint32_t decode_block(uint32_t tile, uint32_t blk, ui
   return c;
 }
 
+// Code-0 positions (escapes) of block `blk` of a staged tile, per lane
+// (bit 8k + j <-> block element 256k + 8*lane + j).
+__device__ __forceinline__ uint32_t block_zero_mask(uint32_t tile, uint32_t blk, uint32_t n_tile) {
+  const uint32_t lane = lane_id();
+  const uint32_t b = tile + blk * kBlockBytes;
+  uint32_t z = ~(lds32(b + 1024 + lane * 4) | lds32(b + 1152 + lane * 4) | lds32(b + 1280 + lane * 4));
+  if (n_tile < kTile) z &= lane_valid_mask(blk, n_tile, lane);
+  return z;
+}
+
+// Decodes block `blk` of a staged tile for this lane, like decode_block, when
+// the tile-local rank of the block's first escape (`first`) is already known:
+// out[k] receives 8 bf16 values of block elements 256k + 8*lane + 0..7.
+// Escapes are patched only in the lanes that have some (lane-private scratch).
+// Returns the block's number of escapes.
+__device__ __forceinline__ uint32_t decode_one_block(uint32_t tile, uint32_t blk, uint32_t n_tile, uint32_t spread,
+                                                     DecTable dt, const EscSource& es, uint32_t first,
+                                                     uint8_t* scratch, uint4 out[4]) {
+  const uint32_t lane = lane_id();
+  const uint32_t b = tile + blk * kBlockBytes;
+  const uint32_t w0 = lds32(b + 1024 + lane * 4);
+  const uint32_t w1 = lds32(b + 1152 + lane * 4);
+  const uint32_t w2 = lds32(b + 1280 + lane * 4);
+  uint32_t z = ~(w0 | w1 | w2);
+  if (n_tile < kTile) z &= lane_valid_mask(blk, n_tile, lane);
+  const uint32_t c = __popc(z);
+  const uint32_t inc = warp_inclusive_scan(c);
+  uint32_t rank = first + inc - c;
+  uint32_t ex[8];
+#pragma unroll
+  for (uint32_t k = 0; k < 4; k++) {
+    const uint32_t sel = spread_at(w0, k, spread) | spread_at(w1, k, spread + 1024) | spread_at(w2, k, spread + 2048);
+    ex[2 * k] = __byte_perm(dt.t0, dt.t1, sel & 0xFFFFu);
+    ex[2 * k + 1] = __byte_perm(dt.t0, dt.t1, sel >> 16);
+  }
+  if (z) {
+    uint4* sp = reinterpret_cast<uint4*>(scratch + lane * 32);
+    sp[0] = make_uint4(ex[0], ex[1], ex[2], ex[3]);
+    sp[1] = make_uint4(ex[4], ex[5], ex[6], ex[7]);
+    uint32_t m = z;
+    while (m) {
+      const uint32_t p = __ffs(m) - 1;
+      m &= m - 1;
+      scratch[lane * 32 + p] = static_cast<uint8_t>(esc_byte(es, rank));
+      rank++;
+    }
+    const uint4 a = sp[0], bq = sp[1];
+    ex[0] = a.x; ex[1] = a.y; ex[2] = a.z; ex[3] = a.w;
+    ex[4] = bq.x; ex[5] = bq.y; ex[6] = bq.z; ex[7] = bq.w;
+  }
+#pragma unroll
+  for (uint32_t k = 0; k < 4; k++) {
+    const uint2 sm = lds64(b + k * 256 + lane * 8);
+    out[k].x = join_pair(__byte_perm(sm.x, ex[2 * k], 0x5140));
+    out[k].y = join_pair(__byte_perm(sm.x, ex[2 * k], 0x7362));
+    out[k].z = join_pair(__byte_perm(sm.y, ex[2 * k + 1], 0x5140));
+    out[k].w = join_pair(__byte_perm(sm.y, ex[2 * k + 1], 0x7362));
+  }
+  return __shfl_sync(kFull, inc, 31);
+}
+
+// acc[i] += bf16 value i of the 8 packed in v (two fp32 adds per instruction,
+// IEEE round-to-nearest, subnormals kept).
+__device__ __forceinline__ void accumulate8(float (&acc)[8], uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    unsigned long long a, x;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(acc[2 * i]), "f"(acc[2 * i + 1]));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(w[i] << 16), "r"(w[i] & 0xFFFF0000u));
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(a) : "l"(x));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[2 * i]), "=f"(acc[2 * i + 1]) : "l"(a));
+  }
+}
+
 // Stores 8 bf16 values (one 16-byte vector) at element index `idx` of a tensor
 // of n elements, element by element past the end.
 __device__ __forceinline__ void store8_guarded(uint16_t* out, uint64_t idx, uint64_t n, uint4 v) {

@@ -3,32 +3,54 @@
 // bfloat16 (nearest even), optionally re-encode the result -- one launch, no
 // decoded intermediate ever touches global memory.
 //
-// Design on sm_103a: 8 warps per CTA, one CTA per SM.  A warp owns one output
-// tile at a time and keeps its 4096 fp32 partial sums in registers (128 per
-// lane).  Its pipeline streams the P compressed copies of that tile (TMA for
-// the 5632-byte tile, cp.async for its escape bytes, two stages in flight);
-// each copy is decoded from shared memory straight into the accumulators.
-// With re-encoding, the rounded tile goes to shared memory and through the
-// same encoder and look-back as zc_compress (cooperative launch: every tile
-// owner is resident).  Warp w owns tiles w, w + W, w + 2W, ...
+// Design on sm_103a: a persistent grid, one CTA of 18 warps per SM.
+//   * 16 consumer warps in 4 teams; team t owns tile 4G + t of each group G
+//     (G, G + C, ... for C CTAs) and warp b of the team owns block b of that
+//     tile, keeping its 1024 fp32 partial sums in registers (32 per lane).
+//   * 1 producer warp streams the P compressed copies of each team's tile
+//     through a 4-stage ring per team: one TMA bulk copy for the 5632-byte
+//     tile, 16-byte cp.async copies for its escape bytes, both completing on
+//     the stage's full barrier; the team's 4 warps release the stage on its
+//     empty barrier.  Offset-table entries are prefetched a round ahead.
+//   * Each consumer decodes its block straight into its sums (two fp32 adds
+//     per instruction), rounds, stores, and -- when re-encoding -- encodes its
+//     block of the result from shared memory.
+//   * With re-encoding, 1 scan warp runs the escape scan of the output exactly
+//     like the encoder: the last warp of a group publishes the group's count,
+//     the scan warp finds the group's offset by a decoupled look-back from its
+//     own previous group, and the consumers write their escapes one round
+//     later.  The cooperative launch keeps every group owner resident.
 #include "zc_device.cuh"
 #include "zc_internal.h"
 
 namespace zc {
 
-constexpr int kRedWarps = 8;
-constexpr int kRedStages = 2;
-constexpr uint32_t kRedEscCap = 512;
-constexpr uint32_t kRedStageBytes = kTileBytes + kRedEscCap;  // 6144
-// After 1 KB alignment: spread tables (3 KB), per-warp encoder LUTs (1 KB each,
-// 1 KB aligned), shard tables, a flag, then per warp: stages, y tile (8 KB),
-// exponent scratch (1 KB), barriers.
-constexpr uint32_t kRedLutOff = 3 * 1024;
-constexpr uint32_t kRedShardOff = kRedLutOff + kRedWarps * 1024;
-constexpr uint32_t kRedFlagOff = kRedShardOff + ZC_MAX_SHARDS * 16;
-constexpr uint32_t kRedWarpOff = kRedFlagOff + 16;
-constexpr uint32_t kRedWarpSmem = kRedStages * kRedStageBytes + 8192 + 1024 + 64;
-constexpr uint32_t kRedSmem = 1024 + kRedWarpOff + kRedWarps * kRedWarpSmem;
+constexpr int kRedTeams = 4;
+constexpr int kRedCons = kRedTeams * 4;           // consumer warps: team t, block b = warp 4t + b
+constexpr int kRedProd = kRedCons;                // producer warp
+constexpr int kRedScan = kRedCons + 1;            // scan warp (re-encoding only)
+constexpr int kRedThreads = (kRedCons + 2) * 32;  // 576
+constexpr int kRedStages = 4;                     // stage ring per team
+constexpr uint32_t kRedEscCap = 512;              // staged input escape bytes per tile copy
+constexpr uint32_t kRedStageBytes = kTileBytes + kRedEscCap;
+constexpr uint32_t kRedEbuf = 512;                // staged output escapes per block and round
+constexpr int kRedSlots = 2;                      // rounds in flight for the output offsets
+constexpr uint32_t kGroupTilesR = kRedTeams;      // tiles per look-back group
+// Shared-memory layout after 1 KB alignment.
+constexpr uint32_t kRSpread = 0;      // decode spread tables, 3 x 1 KB
+constexpr uint32_t kRLut = 3072;      // encoder LUT of the output codebook, 1 KB aligned
+constexpr uint32_t kRShard = 4096;    // per-shard tables, 64 x 16 B
+constexpr uint32_t kRRound = 5120;    // round bookkeeping (<= 512 B)
+constexpr uint32_t kRFlag = 5632;     // validity flags
+constexpr uint32_t kRBars = 5648;     // full / empty barriers, 2 x 4 teams x 4 stages
+constexpr uint32_t kRMeta = kRBars + 2 * kRedTeams * kRedStages * 8;  // stage metadata
+constexpr uint32_t kRScratch = 6272;  // per-consumer exponent scratch, 1 KB each
+constexpr uint32_t kREbuf = kRScratch + kRedCons * 1024;
+constexpr uint32_t kRYtile = kREbuf + kRedCons * kRedSlots * kRedEbuf;  // per-team rounded tile, 8 KB
+constexpr uint32_t kRStage = kRYtile + kRedTeams * 8192;
+constexpr uint32_t kRedSmem = 1024 + kRStage + kRedTeams * kRedStages * kRedStageBytes;
+static_assert(kRMeta + kRedTeams * kRedStages * 16 <= kRScratch, "reduce layout");
+static_assert(kRedSmem + 1024 <= 232448, "shared memory budget");
 
 struct RedParams {
   Shard s[ZC_MAX_SHARDS];
@@ -50,43 +72,30 @@ struct ShardInfo {
   unsigned long long n_esc;
 };
 
-// Offsets [a, b) of the current tile for shard `lane` (a0, b0) and `lane + 32` (a1, b1).
-struct TileOffs {
-  uint32_t a0, b0, a1, b1;
+// What the producer tells the consumers about a staged tile copy.
+struct StageMeta {
+  uint32_t a;       // first escape of the tile in the shard's escape stream
+  uint32_t cnt;     // escapes of the tile
+  uint32_t staged;  // how many of them sit in the stage
+  uint16_t shard;
+  uint16_t ok;      // offset table consistent
 };
 
-__device__ __forceinline__ TileOffs load_offs(const RedParams& p, const ShardInfo* si, uint32_t g) {
-  TileOffs o{0, 0, 0, 0};
-  if (g >= p.ntiles) return o;
-  const uint32_t lane = lane_id();
-#pragma unroll
-  for (int h = 0; h < 2; h++) {
-    const int r = static_cast<int>(lane) + 32 * h;
-    if (r < p.P) {
-      const uint32_t* tbl = reinterpret_cast<const uint32_t*>(p.s[r].main + kHeader);
-      const uint32_t a = __ldg(tbl + g);
-      const uint64_t b = (g + 1 < p.ntiles) ? static_cast<uint64_t>(__ldg(tbl + g + 1)) : si[r].n_esc;
-      const uint32_t bb = b > 0xFFFFFFFFull ? 0xFFFFFFFFu : static_cast<uint32_t>(b);
-      if (h == 0) {
-        o.a0 = a;
-        o.b0 = bb;
-      } else {
-        o.a1 = a;
-        o.b1 = bb;
-      }
-    }
-  }
-  return o;
-}
+struct RedRound {
+  uint32_t agg[kRedSlots];                    // arrivals << 16 | escape count so far
+  uint32_t cnt[kRedSlots][16];                // output escapes of each consumer's block
+  unsigned long long uprefix[kRedSlots][16];  // exclusive output escape offset of each block
+  uint64_t cnt_bar[kRedSlots];
+  uint64_t pre_bar[kRedSlots];
+};
+static_assert(sizeof(RedRound) <= 512, "round bookkeeping too large");
 
-__device__ __forceinline__ void accumulate(float (&acc)[8], uint4 v) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; i++) {
-    acc[2 * i] = __fadd_rn(acc[2 * i], __uint_as_float(w[i] << 16));
-    acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __uint_as_float(w[i] & 0xFFFF0000u));
-  }
-}
+// A consumer's output block of a round, kept until the round's offsets arrive.
+struct RedPending {
+  bool has, spilled, done;
+  uint32_t g;
+  EscBook<1> te;
+};
 
 __device__ __forceinline__ uint4 round_pack(const float (&acc)[8]) {
   uint32_t w[4];
@@ -96,25 +105,34 @@ __device__ __forceinline__ uint4 round_pack(const float (&acc)[8]) {
 }
 
 template <bool REENC>
-__global__ void __launch_bounds__(kRedWarps * 32, 1) reduce_kernel(const __grid_constant__ RedParams p) {
+__global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_constant__ RedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
   const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;
   uint8_t* gbase = smem + (sbase - smem_u32(smem));
-  uint32_t* spread = reinterpret_cast<uint32_t*>(gbase);
-  uint32_t* lut = reinterpret_cast<uint32_t*>(gbase + kRedLutOff + warp * 1024);
-  const uint32_t lut_s = sbase + kRedLutOff + warp * 1024;
-  ShardInfo* si = reinterpret_cast<ShardInfo*>(gbase + kRedShardOff);
-  int* bad = reinterpret_cast<int*>(gbase + kRedFlagOff);
-  uint8_t* wbase = gbase + kRedWarpOff + warp * kRedWarpSmem;
-  const uint32_t wbase_s = sbase + kRedWarpOff + warp * kRedWarpSmem;
-  uint16_t* ytile = reinterpret_cast<uint16_t*>(wbase + kRedStages * kRedStageBytes);
-  const uint32_t ytile_s = wbase_s + kRedStages * kRedStageBytes;
-  uint8_t* scratch = wbase + kRedStages * kRedStageBytes + 8192;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(scratch + 1024);
+  uint32_t* spread = reinterpret_cast<uint32_t*>(gbase + kRSpread);
+  uint32_t* lut = reinterpret_cast<uint32_t*>(gbase + kRLut);
+  ShardInfo* si = reinterpret_cast<ShardInfo*>(gbase + kRShard);
+  RedRound* rs = reinterpret_cast<RedRound*>(gbase + kRRound);
+  int* flags_s = reinterpret_cast<int*>(gbase + kRFlag);  // [0] bad input, [1] bad output codebook
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(gbase + kRBars);
+  uint64_t* empty_bar = full_bar + kRedTeams * kRedStages;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(gbase + kRMeta);
 
   build_spread_tables(spread);
-  if (threadIdx.x == 0) *bad = 0;
+  if (threadIdx.x == 0) {
+    flags_s[0] = flags_s[1] = 0;
+    for (int i = 0; i < kRedTeams * kRedStages; i++) {
+      mbar_init(&full_bar[i], 33);  // 1 TMA arrival + 32 cp.async arrivals
+      mbar_init(&empty_bar[i], 4);  // the team's 4 consumer warps
+    }
+    for (int r = 0; r < kRedSlots; r++) {
+      rs->agg[r] = 0;
+      mbar_init(&rs->cnt_bar[r], kRedCons);
+      mbar_init(&rs->pre_bar[r], 1);
+    }
+    fence_mbar_init();
+  }
   __syncthreads();
   // validate every shard header (each CTA reaches the same verdict)
   for (int r = threadIdx.x; r < p.P; r += blockDim.x) {
@@ -134,7 +152,7 @@ __global__ void __launch_bounds__(kRedWarps * 32, 1) reduce_kernel(const __grid_
       err = ZC_ERR_BAD_HEADER;
     if (n != p.n) err = ZC_ERR_SIZE_MISMATCH;
     if (err) {
-      atomicExch(bad, 1);
+      atomicExch(&flags_s[0], 1);
       set_status(p.status, err);
     }
     const DecTable dt = make_dec_table(cb);
@@ -142,167 +160,263 @@ __global__ void __launch_bounds__(kRedWarps * 32, 1) reduce_kernel(const __grid_
     si[r].t1 = dt.t1;
     si[r].n_esc = n_esc;
   }
-  if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < kRedStages; s++) mbar_init(&bar[s], 33);
-    fence_mbar_init();
-  }
-  bool ok_out = true;
-  if (REENC) {
-    ok_out = build_enc_lut(lut, p.out_cb);
-    if (!ok_out && lane == 0) set_status(p.status, ZC_ERR_DUP_CODEBOOK);
+  if (REENC && warp == 0) {
+    if (!build_enc_lut(lut, p.out_cb)) {
+      if (lane == 0) {
+        flags_s[1] = 1;
+        set_status(p.status, ZC_ERR_DUP_CODEBOOK);
+      }
+    }
   }
   __syncthreads();
+  const bool skip = flags_s[0] != 0 || flags_s[1] != 0;
   const uint32_t epoch = REENC ? launch_epoch(p.ws) : 0u;
   const uint32_t hold = REENC ? launch_hold(p.ws) : 0u;
-  const uint32_t total_warps = gridDim.x * kRedWarps;
-  const bool skip = (*bad != 0) || !ok_out;
+  const uint32_t ngroups = (p.ntiles + kGroupTilesR - 1) / kGroupTilesR;
+  const uint32_t step = gridDim.x;
   if (REENC && !skip && p.ntiles == 0 && blockIdx.x == 0 && warp == 0) {
     write_header_words(p.out_main, 0, p.out_cb);
     write_header_tail(p.out_main, 0, 0);
   }
 
-  // ---- tile sequence: warp w owns tiles w, w + W, w + 2W, ...
-  uint32_t static_next = blockIdx.x * kRedWarps + warp;
-  auto next_tile = [&]() -> uint32_t {
-    if (skip) return 0xFFFFFFFFu;
-    const uint32_t g = static_next;
-    static_next += total_warps;
-    return g;
-  };
-
-  // ---- producer state
-  uint32_t pg = next_tile();
-  TileOffs po = load_offs(p, si, pg);
-  uint32_t qg = next_tile();
-  TileOffs qo = load_offs(p, si, qg);
-  int pr = 0;
-
-  uint32_t st_g[kRedStages], st_r[kRedStages], st_a[kRedStages], st_cnt[kRedStages], st_staged[kRedStages];
-  bool st_ok[kRedStages];
-  auto stage_ptr = [&](int s) { return wbase + s * kRedStageBytes; };
-  auto issue_item = [&](int s) {
-    st_g[s] = pg;
-    if (pg >= p.ntiles) return;
-    const int r = pr;
-    const uint32_t src = static_cast<uint32_t>(r & 31);
-    const uint32_t a = __shfl_sync(kFull, r < 32 ? po.a0 : po.a1, src);
-    const uint32_t b = __shfl_sync(kFull, r < 32 ? po.b0 : po.b1, src);
-    const bool ok = a <= b && b <= si[r].n_esc && b - a <= kTile;
-    if (!ok && lane == 0) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
-    st_r[s] = static_cast<uint32_t>(r);
-    st_a[s] = ok ? a : 0;
-    st_cnt[s] = ok ? b - a : 0;
-    st_ok[s] = ok;
-    uint8_t* sp = stage_ptr(s);
-    // escape bytes (cp.async) -- same staging rule as the decoder
-    {
-      const uint32_t cnt = st_cnt[s], aa = st_a[s];
-      const uint32_t head = aa & 15u;
-      uint32_t region = head + cnt;
-      if (region > kRedEscCap) region = kRedEscCap;
-      st_staged[s] = cnt == 0 ? 0 : region - head;
-      if (cnt != 0)
-        for (uint32_t c = lane; c * 16 < region; c += 32) {
-          const uint32_t left = region - c * 16;
-          cp_async_16(sp + kTileBytes + c * 16, p.s[r].esc + (aa - head) + c * 16, left < 16 ? left : 16);
-        }
-      cp_async_arrive_noinc(&bar[s]);
-    }
-    if (lane == 0) {
-      fence_proxy_async();
-      mbar_arrive_expect_tx(&bar[s], kTileBytes);
-      tma_load_1d(sp, tile_ptr(p.s[r].main, p.ntiles, pg), kTileBytes, &bar[s]);
-    }
-    if (++pr == p.P) {
-      pr = 0;
-      pg = qg;
-      po = qo;
-      qg = next_tile();
-      qo = load_offs(p, si, qg);
-    }
-  };
-
+  if (skip) {
+    // nothing to do; the exit protocol below still runs
+  } else if (warp == kRedProd) {
+    // ---------------- producer: stage the P copies of every team tile
+    uint32_t uses[kRedTeams] = {0, 0, 0, 0};
+    // offsets [a, b) of tile 4G + t for shard `lane` (h = 0) and `lane + 32` (h = 1)
+    uint32_t cur_a[kRedTeams][2], cur_b[kRedTeams][2], nxt_a[kRedTeams][2], nxt_b[kRedTeams][2];
+    auto load_round = [&](uint32_t G, uint32_t (&oa)[kRedTeams][2], uint32_t (&ob)[kRedTeams][2]) {
 #pragma unroll
-  for (int s = 0; s < kRedStages; s++) issue_item(s);
-
-  float acc[4][4][8];
-  uint32_t phase = 0;
-  bool done = false;
-  while (!done) {
+      for (int t = 0; t < kRedTeams; t++)
 #pragma unroll
-    for (int s = 0; s < kRedStages; s++) {
-      const uint32_t g = st_g[s];
-      if (g >= p.ntiles) {
-        done = true;
-        break;
-      }
-      const uint32_t r = st_r[s];
-      const uint64_t rem = p.n - static_cast<uint64_t>(g) * kTile;
-      const uint32_t n_tile = rem >= kTile ? kTile : static_cast<uint32_t>(rem);
-      if (r == 0) {
-#pragma unroll
-        for (int b = 0; b < 4; b++)
-#pragma unroll
-          for (int k = 0; k < 4; k++)
-#pragma unroll
-            for (int j = 0; j < 8; j++) acc[b][k][j] = -0.0f;  // -0 + x == x for every x
-      }
-      const uint8_t* tile = stage_ptr(s);
-      const uint32_t tile_s = wbase_s + s * kRedStageBytes;
-      mbar_wait_bounded(&bar[s], (phase >> s) & 1u, p.status);
-      phase ^= 1u << s;
-      {
-        DecTable dt;
-        dt.t0 = si[r].t0;
-        dt.t1 = si[r].t1;
-        EscSource es;
-        es.smem = tile + kTileBytes + (st_a[s] & 15u);
-        es.glob = p.s[r].esc + st_a[s];
-        es.staged = st_staged[s];
-        es.count = st_cnt[s];
-        uint32_t run = 0;
-#pragma unroll
-        for (uint32_t blk = 0; blk < 4; blk++) {
-          uint4 v[4];
-          decode_block(tile_s, blk, n_tile, sbase, dt, es, run, scratch, v);
-#pragma unroll
-          for (int k = 0; k < 4; k++) accumulate(acc[blk][k], v[k]);
-        }
-        if (st_ok[s] && run != st_cnt[s] && lane == 0) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
-      }
-      if (r + 1 == static_cast<uint32_t>(p.P)) {
-        // finished tile g: round, store, re-encode
-#pragma unroll
-        for (uint32_t blk = 0; blk < 4; blk++) {
-#pragma unroll
-          for (uint32_t k = 0; k < 4; k++) {
-            const uint32_t idx = blk * kBlock + k * 256 + lane * 8;
-            uint4 v = round_pack(acc[blk][k]);
-            if (n_tile < kTile) {
-              uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (uint32_t j = 0; j < 8; j++)
-                if (idx + j >= n_tile) w[j >> 1] &= (j & 1) ? 0x0000FFFFu : 0xFFFF0000u;
-              v = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            if (p.out) store8_guarded(p.out + static_cast<uint64_t>(g) * kTile, idx, rem, v);
-            if (REENC) *reinterpret_cast<uint4*>(ytile + idx) = v;
+        for (int h = 0; h < 2; h++) {
+          oa[t][h] = ob[t][h] = 0;
+          const uint32_t g = G * kGroupTilesR + t;
+          const int r = static_cast<int>(lane) + 32 * h;
+          if (G < ngroups && g < p.ntiles && r < p.P) {
+            const uint32_t* tbl = reinterpret_cast<const uint32_t*>(p.s[r].main + kHeader);
+            oa[t][h] = __ldg(tbl + g);
+            const uint64_t bb = (g + 1 < p.ntiles) ? static_cast<uint64_t>(__ldg(tbl + g + 1)) : si[r].n_esc;
+            ob[t][h] = bb > 0xFFFFFFFFull ? 0xFFFFFFFFu : static_cast<uint32_t>(bb);
           }
         }
-        if (REENC) {
+    };
+    load_round(blockIdx.x, cur_a, cur_b);
+    for (uint32_t G = blockIdx.x; G < ngroups; G += step) {
+      load_round(G + step, nxt_a, nxt_b);  // consumed next round; the loads complete meanwhile
+      for (int r = 0; r < p.P; r++) {
+#pragma unroll
+        for (int t = 0; t < kRedTeams; t++) {
+          const uint32_t g = G * kGroupTilesR + t;
+          if (g >= p.ntiles) continue;
+          const uint32_t s = uses[t] % kRedStages;
+          const uint32_t bi = t * kRedStages + s;
+          if (uses[t] >= kRedStages) mbar_wait_bounded(&empty_bar[bi], (uses[t] / kRedStages - 1) & 1u, p.status);
+          const uint32_t src = static_cast<uint32_t>(r & 31);
+          const uint32_t a = __shfl_sync(kFull, r < 32 ? cur_a[t][0] : cur_a[t][1], src);
+          const uint32_t b = __shfl_sync(kFull, r < 32 ? cur_b[t][0] : cur_b[t][1], src);
+          const bool ok = a <= b && b <= si[r].n_esc && b - a <= kTile;
+          if (!ok && lane == 0) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
+          const uint32_t aa = ok ? a : 0, cnt = ok ? b - a : 0;
+          uint8_t* stage = gbase + kRStage + bi * kRedStageBytes;
+          // escape bytes by cp.async (16-byte chunks, the ragged end zero-filled)
+          const uint32_t head = aa & 15u;
+          uint32_t region = head + cnt;
+          if (region > kRedEscCap) region = kRedEscCap;
+          if (cnt != 0)
+            for (uint32_t c = lane; c * 16 < region; c += 32) {
+              const uint32_t left = region - c * 16;
+              cp_async_16(stage + kTileBytes + c * 16, p.s[r].esc + (aa - head) + c * 16, left < 16 ? left : 16);
+            }
+          cp_async_arrive_noinc(&full_bar[bi]);
+          if (lane == 0) {
+            StageMeta m;
+            m.a = aa;
+            m.cnt = cnt;
+            m.staged = cnt == 0 ? 0 : region - head;
+            m.shard = static_cast<uint16_t>(r);
+            m.ok = ok;
+            meta[bi] = m;
+            fence_proxy_async();
+            mbar_arrive_expect_tx(&full_bar[bi], kTileBytes);
+            tma_load_1d(stage, tile_ptr(p.s[r].main, p.ntiles, g), kTileBytes, &full_bar[bi]);
+          }
           __syncwarp();
-          TileEsc te;
-          encode_tile(ytile_s, n_tile, lut_s, tile_ptr(p.out_main, p.ntiles, g), te);
-          publish_tile(p.flags, g, g, epoch, te, ytile_s, p.out_main, p.n, p.out_cb, p.out_esc, p.out_cap, p.status,
-                       hold);
+          uses[t]++;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kRedTeams; t++)
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+          cur_a[t][h] = nxt_a[t][h];
+          cur_b[t][h] = nxt_b[t][h];
+        }
+    }
+  } else if (warp == kRedScan) {
+    // ---------------- scan warp (re-encoding): one look-back per group of output tiles
+    if (REENC) {
+      int64_t prev_G = -1;
+      uint64_t prev_incl = 0;
+      uint32_t j = 0;
+      for (uint32_t G = blockIdx.x; G < ngroups; G += step, j++) {
+        const int sl = static_cast<int>(j & 1u);
+        mbar_wait_bounded(&rs->cnt_bar[sl], (j >> 1) & 1u, p.status);
+        if (lane == 0) rs->agg[sl] = 0;
+        const uint32_t c = lane < kRedCons ? rs->cnt[sl][lane] : 0u;
+        const uint32_t inc = warp_inclusive_scan(c);
+        const uint32_t agg = __shfl_sync(kFull, inc, 31);
+        uint64_t prefix = 0;
+        if (hold != G + 1) {
+          const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
+          if (G != 0) {  // (the group's count is already published by its last consumer warp)
+            bool timed_out;
+            prefix = lookback(p.flags, G, 0, epoch, p.status, &timed_out, prev_G, prev_incl);
+            if (lane == 0) st_relaxed(&p.flags[G].incl, tag | static_cast<uint32_t>(prefix + agg));
+          }
+          prev_G = G;
+          prev_incl = prefix + agg;
+        }
+        if (lane < kRedCons) rs->uprefix[sl][lane] = prefix + (inc - c);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rs->pre_bar[sl]);
+      }
+    }
+  } else {
+    // ---------------- consumers: team t, block b
+    const uint32_t t = warp >> 2, b = warp & 3u;
+    uint8_t* scratch = gbase + kRScratch + warp * 1024;
+    uint8_t* ebuf = gbase + kREbuf + warp * kRedSlots * kRedEbuf;
+    const uint32_t ytile_s = sbase + kRYtile + t * 8192;  // shared address of the team's rounded tile
+    uint16_t* ytile = reinterpret_cast<uint16_t*>(gbase + kRYtile + t * 8192);
+    const uint32_t lut_s = sbase + kRLut;
+    uint32_t k_item = 0;
+
+    // output offsets posted for round j: write the table entry, header parts, escapes
+    auto finish = [&](uint32_t j, const RedPending& pd) {
+      const int sl = static_cast<int>(j & 1u);
+      mbar_wait_bounded(&rs->pre_bar[sl], (j >> 1) & 1u, p.status);
+      if (pd.has) {
+        const uint64_t prefix = rs->uprefix[sl][warp];
+        if (b == 0) {
+          if (lane == 0) *reinterpret_cast<uint32_t*>(p.out_main + kHeader + 4ull * pd.g) = static_cast<uint32_t>(prefix);
+          if (pd.g == 0) write_header_words(p.out_main, p.n, p.out_cb);
+        }
+        if (b == 3 && pd.g + 1 == p.ntiles) {
+          const uint64_t n_esc = prefix + pd.te.total;
+          write_header_tail(p.out_main, p.ntiles, n_esc);
+          if (lane == 0 && n_esc > p.out_cap) set_status(p.status, ZC_ERR_ESCAPE_OVERFLOW);
+        }
+        if (pd.spilled) {
+          write_escapes<1>(ytile_s + b * 2048, pd.te, prefix, p.out_esc, p.out_cap);
+        } else {
+          const uint8_t* src = ebuf + sl * kRedEbuf;
+          for (uint32_t i = lane; i < pd.te.total; i += 32)
+            if (prefix + i < p.out_cap) p.out_esc[prefix + i] = src[i];
         }
       }
       __syncwarp();
-      issue_item(s);
+    };
+
+    RedPending prev;
+    prev.has = prev.spilled = false;
+    prev.done = true;
+    uint32_t j = 0;
+    for (uint32_t G = blockIdx.x; G < ngroups; G += step, j++) {
+      const uint32_t g = G * kGroupTilesR + t;
+      const bool has = g < p.ntiles;
+      const uint64_t rem = has ? p.n - static_cast<uint64_t>(g) * kTile : 0;
+      const uint32_t n_tile = rem >= kTile ? kTile : static_cast<uint32_t>(rem);
+      float acc[4][8];
+#pragma unroll
+      for (int k = 0; k < 4; k++)
+#pragma unroll
+        for (int i = 0; i < 8; i++) acc[k][i] = -0.0f;  // -0 + x == x for every x
+      if (has) {
+        for (int r = 0; r < p.P; r++) {
+          const uint32_t s = k_item % kRedStages;
+          const uint32_t bi = t * kRedStages + s;
+          mbar_wait_bounded(&full_bar[bi], (k_item / kRedStages) & 1u, p.status);
+          const StageMeta m = meta[bi];
+          const uint32_t tile_s = sbase + kRStage + bi * kRedStageBytes;
+          uint32_t first = 0;
+          for (uint32_t bb = 0; bb < b; bb++) first += __reduce_add_sync(kFull, __popc(block_zero_mask(tile_s, bb, n_tile)));
+          DecTable dt;
+          dt.t0 = si[m.shard].t0;
+          dt.t1 = si[m.shard].t1;
+          EscSource es;
+          es.smem = gbase + kRStage + bi * kRedStageBytes + kTileBytes + (m.a & 15u);
+          es.glob = p.s[m.shard].esc + m.a;
+          es.staged = m.staged;
+          es.count = m.cnt;
+          uint4 v[4];
+          const uint32_t zb = decode_one_block(tile_s, b, n_tile, sbase + kRSpread, dt, es, first, scratch, v);
+          if (b == 3 && m.ok && first + zb != m.cnt && lane == 0) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
+#pragma unroll
+          for (int k = 0; k < 4; k++) accumulate8(acc[k], v[k]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty_bar[bi]);  // release the stage to the producer
+          k_item++;
+        }
+      }
+      RedPending cur;
+      cur.has = has;
+      cur.spilled = false;
+      cur.done = false;
+      cur.g = g;
+      cur.te.total = 0;
+      if (REENC && !prev.done && prev.spilled) {  // its escapes still sit in the rounded tile
+        finish(j - 1, prev);
+        prev.done = true;
+      }
+      if (has) {
+        uint16_t* out = p.out ? p.out + static_cast<uint64_t>(g) * kTile : nullptr;
+#pragma unroll
+        for (uint32_t k = 0; k < 4; k++) {
+          const uint32_t idx = b * kBlock + k * 256 + lane * 8;  // tile-local element index
+          uint4 v = round_pack(acc[k]);
+          if (n_tile < kTile) {
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (uint32_t jj = 0; jj < 8; jj++)
+              if (idx + jj >= n_tile) w[jj >> 1] &= (jj & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+            v = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          if (out) store8_guarded(out, idx, rem, v);
+          if (REENC) *reinterpret_cast<uint4*>(ytile + idx) = v;
+        }
+      }
+      if (REENC) {
+        if (has) {
+          __syncwarp();
+          encode_blocks<1>(ytile_s + b * 2048, b, n_tile, lut_s, tile_ptr(p.out_main, p.ntiles, g) + b * kBlockBytes,
+                           cur.te);
+          cur.spilled = cur.te.total > kRedEbuf;
+          if (!cur.spilled) stage_escapes_smem<1>(ytile_s + b * 2048, cur.te, ebuf + (j & 1u) * kRedEbuf);
+        }
+        const int sl = static_cast<int>(j & 1u);
+        if (lane == 0) {
+          rs->cnt[sl][warp] = cur.te.total;
+          const uint32_t old = atomicAdd(&rs->agg[sl], (1u << 16) | cur.te.total);
+          if ((old >> 16) == kRedCons - 1 && hold != G + 1) {
+            const uint32_t agg = (old & 0xFFFFu) + cur.te.total;
+            const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
+            if (G == 0)
+              st_relaxed(&p.flags[G].incl, tag | agg);
+            else
+              st_relaxed(&p.flags[G].agg, tag | agg);
+          }
+          mbar_arrive(&rs->cnt_bar[sl]);
+        }
+        __syncwarp();
+        if (!prev.done) finish(j - 1, prev);
+        prev = cur;
+      }
     }
+    if (REENC && j > 0 && !prev.done) finish(j - 1, prev);
   }
-  if (REENC) cta_exit(p.ws, p.flags, epoch, p.ntiles);
+  if (REENC) cta_exit(p.ws, p.flags, epoch, ngroups);
 }
 
 cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out, const uint8_t* out_cb,
@@ -321,7 +435,8 @@ cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out,
   p.ws = ws;
   p.flags = flags;
   p.status = status;
-  uint32_t ctas = (p.ntiles + kRedWarps - 1) / kRedWarps;
+  const uint32_t ngroups = (p.ntiles + kGroupTilesR - 1) / kGroupTilesR;
+  uint32_t ctas = ngroups;
   if (ctas > static_cast<uint32_t>(dev.sm_count)) ctas = dev.sm_count;
   if (ctas == 0) ctas = 1;
   cudaError_t err;
@@ -329,17 +444,17 @@ cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out,
     err = cudaFuncSetAttribute(reduce_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
     if (err != cudaSuccess) return err;
     int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reduce_kernel<true>, kRedWarps * 32, kRedSmem);
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reduce_kernel<true>, kRedThreads, kRedSmem);
     if (err != cudaSuccess) return err;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     void* args[] = {&p};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(reduce_kernel<true>), dim3(ctas),
-                                       dim3(kRedWarps * 32), args, kRedSmem, stream);
+                                       dim3(kRedThreads), args, kRedSmem, stream);
   }
   if (p.ntiles == 0) return cudaSuccess;
   err = cudaFuncSetAttribute(reduce_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
   if (err != cudaSuccess) return err;
-  reduce_kernel<false><<<ctas, kRedWarps * 32, kRedSmem, stream>>>(p);
+  reduce_kernel<false><<<ctas, kRedThreads, kRedSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
