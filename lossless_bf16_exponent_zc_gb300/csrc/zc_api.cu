@@ -73,11 +73,39 @@ double binade_mass(int e, double sigma) {
 }  // namespace
 
 namespace zc {
+namespace {
+std::atomic<int> g_sm_count[kMaxDevices];
+}
+
 cudaError_t device_info(DeviceInfo* info) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  return cudaDeviceGetAttribute(&info->sm_count, cudaDevAttrMultiProcessorCount, dev);
+  info->device = dev;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached) {
+    info->sm_count = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (info->sm_count > 0) return cudaSuccess;
+  }
+  e = cudaDeviceGetAttribute(&info->sm_count, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess && cached) g_sm_count[dev].store(info->sm_count, std::memory_order_relaxed);
+  return e;
+}
+
+cudaError_t prepare_kernel(KernelPrep& kp, const void* fn, int threads, int smem_bytes, const DeviceInfo& dev,
+                           int* per_sm) {
+  const bool cached = dev.device >= 0 && dev.device < kMaxDevices;
+  if (cached) {
+    *per_sm = kp.per_sm[dev.device].load(std::memory_order_acquire);
+    if (*per_sm > 0) return cudaSuccess;
+  }
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, fn, threads, static_cast<size_t>(smem_bytes));
+  if (e != cudaSuccess) return e;
+  if (*per_sm < 1) return cudaErrorInvalidConfiguration;
+  if (cached) kp.per_sm[dev.device].store(*per_sm, std::memory_order_release);
+  return cudaSuccess;
 }
 }  // namespace zc
 

@@ -230,7 +230,10 @@ static cudaError_t launch_decode_t(const DecTensor* ts, int count, int32_t* stat
   p.total_tiles = total;
   p.status = status;
   if (total == 0) return cudaSuccess;
-  cudaError_t err = cudaFuncSetAttribute(decode_kernel<MAXB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
+  static KernelPrep prep;
+  int per_sm = 0;
+  cudaError_t err =
+      prepare_kernel(prep, reinterpret_cast<const void*>(decode_kernel<MAXB>), kDecWarps * 32, kDecSmem, dev, &per_sm);
   if (err != cudaSuccess) return err;
   uint32_t ctas = (total + kDecWarps - 1) / kDecWarps;
   if (ctas > static_cast<uint32_t>(dev.sm_count)) ctas = dev.sm_count;

@@ -365,12 +365,11 @@ static cudaError_t launch_encode_t(const EncTensor* ts, int count, WsHeader* ws,
   static_assert(sizeof(EncParams<MAXB>) < 4000, "encode parameters too large");
   static_assert(sizeof(RoundShared) <= 1280, "round bookkeeping too large");
   static_assert(kEncSmem + 1024 <= 232448, "shared memory budget");
-  cudaError_t err = cudaFuncSetAttribute(encode_kernel<MAXB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEncSmem);
-  if (err != cudaSuccess) return err;
+  static KernelPrep prep;
   int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel<MAXB>, kEncThreads, kEncSmem);
+  cudaError_t err =
+      prepare_kernel(prep, reinterpret_cast<const void*>(encode_kernel<MAXB>), kEncThreads, kEncSmem, dev, &per_sm);
   if (err != cudaSuccess) return err;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
   uint32_t ctas = groups;
   const uint32_t cap = static_cast<uint32_t>(dev.sm_count) * static_cast<uint32_t>(per_sm);
   if (ctas > cap) ctas = cap;

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "zc.h"
 
 namespace zc {
@@ -38,11 +40,26 @@ struct Shard {
   uint64_t esc_bytes;
 };
 
+// Devices whose properties and kernel set-up are cached by the library.
+constexpr int kMaxDevices = 64;
+
 struct DeviceInfo {
+  int device;
   int sm_count;
 };
 
+// The current device and its SM count (looked up once per device).
 cudaError_t device_info(DeviceInfo* info);
+
+// Launch preparation of one kernel, done once per device: raise its dynamic
+// shared-memory limit and find how many CTAs fit on an SM.  Later calls on the
+// same device return the cached count without calling the runtime, so a
+// launch costs no extra driver calls.  Zero-initialised as a static object.
+struct KernelPrep {
+  std::atomic<int> per_sm[kMaxDevices];
+};
+cudaError_t prepare_kernel(KernelPrep& kp, const void* fn, int threads, int smem_bytes, const DeviceInfo& dev,
+                           int* per_sm);
 
 // count <= kMaxBatch; flags = workspace flag array (one per tile of the launch).
 cudaError_t launch_encode(const EncTensor* ts, int count, WsHeader* ws, Flag* flags, int32_t* status,

@@ -3,15 +3,16 @@
 // bfloat16 (nearest even), optionally re-encode the result -- one launch, no
 // decoded intermediate ever touches global memory.
 //
-// Design on sm_103a: a persistent grid, one CTA of 18 warps per SM.
+// Design on sm_103a: a persistent grid, one CTA of 19 warps per SM.
 //   * 16 consumer warps in 4 teams; team t owns tile 4G + t of each group G
 //     (G, G + C, ... for C CTAs) and warp b of the team owns block b of that
 //     tile, keeping its 1024 fp32 partial sums in registers (32 per lane).
-//   * 1 producer warp streams the P compressed copies of each team's tile
-//     through a 4-stage ring per team: one TMA bulk copy for the 5632-byte
-//     tile, 16-byte cp.async copies for its escape bytes, both completing on
-//     the stage's full barrier; the team's 4 warps release the stage on its
-//     empty barrier.  Offset-table entries are prefetched a round ahead.
+//   * 2 producer warps, each serving two teams, stream the P compressed copies
+//     of a team's tile through the team's 4-stage ring: one TMA bulk copy for
+//     the 5632-byte tile and one for the 16-byte-aligned span holding its
+//     escape bytes, both completing on the stage's full barrier; the team's
+//     4 warps release the stage on its empty barrier.  Offset-table entries
+//     are prefetched a round ahead.
 //   * Each consumer decodes its block straight into its sums (two fp32 adds
 //     per instruction), rounds, stores, and -- when re-encoding -- encodes its
 //     block of the result from shared memory.
@@ -27,9 +28,11 @@ namespace zc {
 
 constexpr int kRedTeams = 4;
 constexpr int kRedCons = kRedTeams * 4;           // consumer warps: team t, block b = warp 4t + b
-constexpr int kRedProd = kRedCons;                // producer warp
-constexpr int kRedScan = kRedCons + 1;            // scan warp (re-encoding only)
-constexpr int kRedThreads = (kRedCons + 2) * 32;  // 576
+constexpr int kRedProducers = 2;                    // producer warps kRedProd + q, each serving 2 teams
+constexpr int kRedProd = kRedCons;
+constexpr int kRedScan = kRedProd + kRedProducers;  // scan warp (re-encoding only)
+constexpr int kRedThreads = (kRedScan + 1) * 32;    // 608 (at most 5 warps per scheduler: 96 registers)
+constexpr int kTeamsPerProducer = kRedTeams / kRedProducers;
 constexpr int kRedStages = 4;                     // stage ring per team
 constexpr uint32_t kRedEscCap = 512;              // staged input escape bytes per tile copy
 constexpr uint32_t kRedStageBytes = kTileBytes + kRedEscCap;
@@ -123,7 +126,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
   if (threadIdx.x == 0) {
     flags_s[0] = flags_s[1] = 0;
     for (int i = 0; i < kRedTeams * kRedStages; i++) {
-      mbar_init(&full_bar[i], 33);  // 1 TMA arrival + 32 cp.async arrivals
+      mbar_init(&full_bar[i], 1);  // the producer's arrival with the expected bytes
       mbar_init(&empty_bar[i], 4);  // the team's 4 consumer warps
     }
     for (int r = 0; r < kRedSlots; r++) {
@@ -181,24 +184,26 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
 
   if (skip) {
     // nothing to do; the exit protocol below still runs
-  } else if (warp == kRedProd) {
-    // ---------------- producer: stage the P copies of every team tile
-    uint32_t uses[kRedTeams] = {0, 0, 0, 0};
-    // offsets [a, b) of tile 4G + t for shard `lane` (h = 0) and `lane + 32` (h = 1)
-    uint32_t cur_a[kRedTeams][2], cur_b[kRedTeams][2], nxt_a[kRedTeams][2], nxt_b[kRedTeams][2];
-    auto load_round = [&](uint32_t G, uint32_t (&oa)[kRedTeams][2], uint32_t (&ob)[kRedTeams][2]) {
+  } else if (warp >= kRedProd && warp < kRedScan) {
+    // ---------------- producer q: stage the P copies of the tiles of teams 2q, 2q + 1
+    const uint32_t t0 = (warp - kRedProd) * kTeamsPerProducer;
+    uint32_t uses[kTeamsPerProducer] = {};
+    // offsets [a, b) of tile 4G + t0 + u for shard `lane` (h = 0) and `lane + 32` (h = 1)
+    uint32_t cur_a[kTeamsPerProducer][2], cur_b[kTeamsPerProducer][2];
+    uint32_t nxt_a[kTeamsPerProducer][2], nxt_b[kTeamsPerProducer][2];
+    auto load_round = [&](uint32_t G, uint32_t (&oa)[kTeamsPerProducer][2], uint32_t (&ob)[kTeamsPerProducer][2]) {
 #pragma unroll
-      for (int t = 0; t < kRedTeams; t++)
+      for (int u = 0; u < kTeamsPerProducer; u++)
 #pragma unroll
         for (int h = 0; h < 2; h++) {
-          oa[t][h] = ob[t][h] = 0;
-          const uint32_t g = G * kGroupTilesR + t;
+          oa[u][h] = ob[u][h] = 0;
+          const uint32_t g = G * kGroupTilesR + t0 + u;
           const int r = static_cast<int>(lane) + 32 * h;
           if (G < ngroups && g < p.ntiles && r < p.P) {
             const uint32_t* tbl = reinterpret_cast<const uint32_t*>(p.s[r].main + kHeader);
-            oa[t][h] = __ldg(tbl + g);
+            oa[u][h] = __ldg(tbl + g);
             const uint64_t bb = (g + 1 < p.ntiles) ? static_cast<uint64_t>(__ldg(tbl + g + 1)) : si[r].n_esc;
-            ob[t][h] = bb > 0xFFFFFFFFull ? 0xFFFFFFFFu : static_cast<uint32_t>(bb);
+            ob[u][h] = bb > 0xFFFFFFFFull ? 0xFFFFFFFFu : static_cast<uint32_t>(bb);
           }
         }
     };
@@ -206,52 +211,58 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     for (uint32_t G = blockIdx.x; G < ngroups; G += step) {
       load_round(G + step, nxt_a, nxt_b);  // consumed next round; the loads complete meanwhile
       for (int r = 0; r < p.P; r++) {
+        const uint32_t src = static_cast<uint32_t>(r & 31);
+        uint32_t a[kTeamsPerProducer], b[kTeamsPerProducer];
 #pragma unroll
-        for (int t = 0; t < kRedTeams; t++) {
-          const uint32_t g = G * kGroupTilesR + t;
-          if (g >= p.ntiles) continue;
-          const uint32_t s = uses[t] % kRedStages;
-          const uint32_t bi = t * kRedStages + s;
-          if (uses[t] >= kRedStages) mbar_wait_bounded(&empty_bar[bi], (uses[t] / kRedStages - 1) & 1u, p.status);
-          const uint32_t src = static_cast<uint32_t>(r & 31);
-          const uint32_t a = __shfl_sync(kFull, r < 32 ? cur_a[t][0] : cur_a[t][1], src);
-          const uint32_t b = __shfl_sync(kFull, r < 32 ? cur_b[t][0] : cur_b[t][1], src);
-          const bool ok = a <= b && b <= si[r].n_esc && b - a <= kTile;
-          if (!ok && lane == 0) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
-          const uint32_t aa = ok ? a : 0, cnt = ok ? b - a : 0;
-          uint8_t* stage = gbase + kRStage + bi * kRedStageBytes;
-          // escape bytes by cp.async (16-byte chunks, the ragged end zero-filled)
-          const uint32_t head = aa & 15u;
-          uint32_t region = head + cnt;
-          if (region > kRedEscCap) region = kRedEscCap;
-          if (cnt != 0)
-            for (uint32_t c = lane; c * 16 < region; c += 32) {
-              const uint32_t left = region - c * 16;
-              cp_async_16(stage + kTileBytes + c * 16, p.s[r].esc + (aa - head) + c * 16, left < 16 ? left : 16);
-            }
-          cp_async_arrive_noinc(&full_bar[bi]);
-          if (lane == 0) {
+        for (int u = 0; u < kTeamsPerProducer; u++) {
+          a[u] = __shfl_sync(kFull, r < 32 ? cur_a[u][0] : cur_a[u][1], src);
+          b[u] = __shfl_sync(kFull, r < 32 ? cur_b[u][0] : cur_b[u][1], src);
+        }
+        if (lane == 0) {
+          const uint64_t n_esc = si[r].n_esc;
+          const uint64_t buf = p.s[r].esc_bytes;
+#pragma unroll
+          for (int u = 0; u < kTeamsPerProducer; u++) {
+            const uint32_t t = t0 + u;
+            const uint32_t g = G * kGroupTilesR + t;
+            if (g >= p.ntiles) continue;
+            const uint32_t bi = t * kRedStages + uses[u] % kRedStages;
+            if (uses[u] >= kRedStages)
+              mbar_wait_bounded(&empty_bar[bi], (uses[u] / kRedStages - 1) & 1u, p.status);
+            const bool ok = a[u] <= b[u] && b[u] <= n_esc && b[u] - a[u] <= kTile;
+            if (!ok) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
+            const uint32_t aa = ok ? a[u] : 0, cnt = ok ? b[u] - a[u] : 0;
+            // escape bytes: the 16-byte-aligned span [aa - head, ...) that holds
+            // them, at most kRedEscCap bytes and never past the end of the
+            // buffer; ranks beyond it are read from global memory by consumers
+            const uint32_t head = aa & 15u;
+            const uint64_t base = aa - head;
+            uint32_t span = cnt == 0 ? 0u : (head + cnt + 15u) & ~15u;
+            if (span > kRedEscCap) span = kRedEscCap;
+            if (base + span > buf) span = base >= buf ? 0u : static_cast<uint32_t>((buf - base) & ~15ull);
+            uint8_t* stage = gbase + kRStage + bi * kRedStageBytes;
             StageMeta m;
             m.a = aa;
             m.cnt = cnt;
-            m.staged = cnt == 0 ? 0 : region - head;
+            m.staged = span <= head ? 0u : (span - head < cnt ? span - head : cnt);
             m.shard = static_cast<uint16_t>(r);
             m.ok = ok;
             meta[bi] = m;
             fence_proxy_async();
-            mbar_arrive_expect_tx(&full_bar[bi], kTileBytes);
+            mbar_arrive_expect_tx(&full_bar[bi], kTileBytes + span);
             tma_load_1d(stage, tile_ptr(p.s[r].main, p.ntiles, g), kTileBytes, &full_bar[bi]);
+            if (span != 0) tma_load_1d(stage + kTileBytes, p.s[r].esc + base, span, &full_bar[bi]);
+            uses[u]++;
           }
-          __syncwarp();
-          uses[t]++;
         }
+        __syncwarp();
       }
 #pragma unroll
-      for (int t = 0; t < kRedTeams; t++)
+      for (int u = 0; u < kTeamsPerProducer; u++)
 #pragma unroll
         for (int h = 0; h < 2; h++) {
-          cur_a[t][h] = nxt_a[t][h];
-          cur_b[t][h] = nxt_b[t][h];
+          cur_a[u][h] = nxt_a[u][h];
+          cur_b[u][h] = nxt_b[u][h];
         }
     }
   } else if (warp == kRedScan) {
@@ -440,19 +451,19 @@ cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out,
   if (ctas > static_cast<uint32_t>(dev.sm_count)) ctas = dev.sm_count;
   if (ctas == 0) ctas = 1;
   cudaError_t err;
+  static KernelPrep prep_reenc, prep_plain;
+  int per_sm = 0;
   if (out_cb) {
-    err = cudaFuncSetAttribute(reduce_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
+    err = prepare_kernel(prep_reenc, reinterpret_cast<const void*>(reduce_kernel<true>), kRedThreads, kRedSmem, dev,
+                         &per_sm);
     if (err != cudaSuccess) return err;
-    int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reduce_kernel<true>, kRedThreads, kRedSmem);
-    if (err != cudaSuccess) return err;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
     void* args[] = {&p};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(reduce_kernel<true>), dim3(ctas),
                                        dim3(kRedThreads), args, kRedSmem, stream);
   }
   if (p.ntiles == 0) return cudaSuccess;
-  err = cudaFuncSetAttribute(reduce_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRedSmem);
+  err = prepare_kernel(prep_plain, reinterpret_cast<const void*>(reduce_kernel<false>), kRedThreads, kRedSmem, dev,
+                       &per_sm);
   if (err != cudaSuccess) return err;
   reduce_kernel<false><<<ctas, kRedThreads, kRedSmem, stream>>>(p);
   return cudaGetLastError();
