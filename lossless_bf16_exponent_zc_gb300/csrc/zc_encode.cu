@@ -12,10 +12,18 @@
 // unit of the escape scan: the warps' escape counts meet in shared memory,
 // the last encoding warp to finish a group publishes the group's count at
 // once, the 21st "scan" warp finds the group's escape offset with a single-pass
-// decoupled look-back, and the encoding warps write their
-// escapes at the final global positions two rounds later.  Meanwhile the
-// escapes wait in a small per-warp buffer, so a stage is refilled as soon as
-// its data is encoded.  The scan warp knows the inclusive offset of its own
+// decoupled look-back and posts the group's offsets in shared memory.
+//
+// CTAs drift apart by several rounds (the order in which HBM serves their
+// loads), and a group's offset is known only once every group before it is
+// encoded, so an encoding warp never waits for its offsets while it has
+// work: it keeps each unit's escapes in a per-warp shared-memory ring, with
+// a queue of up to 16 rounds in flight, and writes a round's offset-table
+// entry, header parts and escapes to global memory whenever it finds that
+// round's offsets posted.  It blocks only when the ring or the queue is full,
+// and at the end.  A stage is refilled as soon as its data is encoded; a unit
+// with more escapes than a ring share waits for its offsets and writes them
+// from the stage itself.  The scan warp knows the inclusive offset of its own
 // previous group, so a look-back needs only the aggregates of the C - 1 groups
 // in between, which are published without waiting on anyone.  The cooperative
 // launch guarantees every group owner is resident, which the waits rely on.
@@ -33,15 +41,20 @@ constexpr uint32_t kUnitsPerTile = kTile / kUnitElems;
 constexpr uint32_t kGroupUnits = kEncWarps;     // units per look-back group (one per encoding warp)
 constexpr uint32_t kGroupTiles = kGroupUnits / kUnitsPerTile;
 constexpr uint32_t kEncStageBytes = kUnitElems * 2;  // 4096
-constexpr uint32_t kEncEscBuf = 512;            // staged escapes per unit; more falls back to the stage itself
-constexpr int kEncSlots = 3;                    // rounds in flight: a round's escapes are written two rounds later
+constexpr int kEncSlots = 16;                   // rounds in flight per warp (round slot = round mod 16)
+constexpr uint32_t kEncRing = 1024;             // per-warp escape ring (bytes, a power of two)
+constexpr uint32_t kEncRingUnitMax = 512;       // a unit with more escapes bypasses the ring
+constexpr uint32_t kEncQEntry = 16;             // bytes per queued round
 // After 1 KB alignment: per-warp LUTs (1 KB each, 1 KB aligned), per-warp stage
-// barriers, CTA round bookkeeping, per-warp escape buffers, per-warp stages.
+// barriers, CTA round bookkeeping, per-warp round queues, per-warp escape
+// rings, per-warp stages.
 constexpr uint32_t kEncLutOff = 0;
 constexpr uint32_t kEncBarOff = kEncWarps * 1024;
 constexpr uint32_t kEncGrpOff = kEncBarOff + 512;
-constexpr uint32_t kEncEbufOff = kEncGrpOff + 1280;
-constexpr uint32_t kEncStageOff = kEncEbufOff + kEncWarps * kEncSlots * kEncEscBuf;
+constexpr uint32_t kEncGrpBytes = 4352;
+constexpr uint32_t kEncQueueOff = kEncGrpOff + kEncGrpBytes;
+constexpr uint32_t kEncRingOff = kEncQueueOff + kEncWarps * kEncSlots * kEncQEntry;
+constexpr uint32_t kEncStageOff = kEncRingOff + kEncWarps * kEncRing;
 constexpr uint32_t kEncSmem = 1024 + kEncStageOff + kEncWarps * kEncStages * kEncStageBytes;
 static_assert(kGroupUnits % kUnitsPerTile == 0, "a group holds whole tiles");
 
@@ -64,29 +77,34 @@ __device__ __forceinline__ uint32_t locate_group(const EncParams<MAXB>& p, uint3
   return ti;
 }
 
-// CTA bookkeeping of the rounds in flight (slot = round mod 3).  Round j's
-// escapes are written in round j + 2, so a slot is reused by round j + 3 only
-// after every warp is done with round j: the counts after the scan warp
-// consumed them (it posts round j's offsets before any warp can finish round
-// j, which happens before that warp writes round j + 3's count), the offsets
-// after every warp has arrived with its round j + 3 count.
+// CTA bookkeeping of the rounds in flight (slot = round mod 16).  A warp
+// finishes round j (after waiting for its offsets) before it starts round
+// j + 16, so a slot is reused only after every warp is done with round j: the
+// counts and the arrival word after the scan warp consumed them (it posts
+// round j's offsets only after that), the offsets after every warp has
+// arrived with its round j + 16 count.
 struct RoundShared {
-  uint32_t agg[kEncSlots];                    // arrivals << 16 | escape count so far (the last warp publishes)
-  uint32_t cnt[kEncSlots][32];                // escape count of each encoding warp's unit
-  unsigned long long uprefix[kEncSlots][32];  // exclusive escape offset of each warp's unit
-  uint64_t cnt_bar[kEncSlots];                // kEncWarps arrivals: all counts of the round are in
-  uint64_t pre_bar[kEncSlots];                // 1 arrival: the scan warp has posted the offsets
+  uint32_t agg[kEncSlots];                           // arrivals << 16 | escape count so far (the last warp publishes)
+  uint32_t cnt[kEncSlots][kEncWarps];                // escape count of each encoding warp's unit
+  unsigned long long uprefix[kEncSlots][kEncWarps];  // exclusive escape offset of each warp's unit
+  uint64_t cnt_bar[kEncSlots];                       // kEncWarps arrivals: all counts of the round are in
+  uint64_t pre_bar[kEncSlots];                       // 1 arrival: the scan warp has posted the offsets
 };
+static_assert(sizeof(RoundShared) <= kEncGrpBytes, "round bookkeeping too large");
 
-// What an encoding warp remembers about its unit of a round until the
-// round's offsets are known.
-struct Pending {
-  bool has;      // the warp had a unit this round
-  bool spilled;  // more escapes than the staging buffer: written from the stage itself
-  bool done;     // already finished (a spilled unit finishes early to free its stage)
-  uint32_t ti, lt;
-  EscBook<kUnitBlocks> te;
+// A round queued by an encoding warp until its offsets are known.  The
+// unit's escapes sit in the warp's ring at byte start % kEncRing (start is a
+// running byte count; an allocation never wraps around the ring's end).
+struct QEntry {
+  uint32_t lt;     // local tile of the unit
+  uint32_t start;  // ring position of its escapes
+  uint16_t ti;     // tensor
+  uint16_t cnt;    // escapes
+  uint32_t has;    // the warp had a unit this round
 };
+static_assert(sizeof(QEntry) == kEncQEntry, "queue entry size");
+static_assert(kEncRingUnitMax <= kEncRing, "a ring share fits the ring");
+static_assert((kEncRing & (kEncRing - 1)) == 0, "ring positions stay contiguous across 32-bit wrap-around");
 
 template <int MAXB>
 __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_constant__ EncParams<MAXB> p) {
@@ -111,7 +129,8 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   uint32_t* lut = reinterpret_cast<uint32_t*>(gbase + kEncLutOff + w * 1024);
   const uint32_t lut_s = sbase + kEncLutOff + w * 1024;
   uint64_t* bar = reinterpret_cast<uint64_t*>(gbase + kEncBarOff + w * 16);
-  uint8_t* ebuf = gbase + kEncEbufOff + w * kEncSlots * kEncEscBuf;
+  QEntry* queue = reinterpret_cast<QEntry*>(gbase + kEncQueueOff + w * kEncSlots * kEncQEntry);
+  uint8_t* ring = gbase + kEncRingOff + w * kEncRing;
   uint8_t* wstage = gbase + kEncStageOff + w * kEncStages * kEncStageBytes;
   const uint32_t wstage_s = sbase + kEncStageOff + w * kEncStages * kEncStageBytes;
   if (warp < kEncWarps && lane == 0) {
@@ -156,7 +175,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
           for (int b = a + 1; b < 7; b++) cb_ok &= __ldg(cb + a) != __ldg(cb + b);
       }
       mbar_wait_bounded(&rs->cnt_bar[r], ph, p.status);
-      if (lane == 0) rs->agg[r] = 0;  // every warp has added to it; ready for round j + 3
+      if (lane == 0) rs->agg[r] = 0;  // every warp has added to it; ready for round j + kEncSlots
       const uint32_t gl = G - p.group_start[ti];
       const uint32_t c = lane < kGroupUnits ? rs->cnt[r][lane] : 0u;
       const uint32_t inc = warp_inclusive_scan(c);
@@ -210,37 +229,42 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
         }
       }
     };
-    // Second half of round j: the group's offsets have been posted (slot r);
-    // write the offset-table entry, this unit's header parts and escapes.  A
-    // spilled unit's escapes come from its stage, which is refilled afterwards.
-    auto finish = [&](uint32_t j, uint32_t G, const Pending& pd) {
-      const int r = static_cast<int>(j % kEncSlots);
-      const int s = static_cast<int>(j & 1u);
-      mbar_wait_bounded(&rs->pre_bar[r], (j / kEncSlots) & 1u, p.status);
-      if (pd.has) {
-        const EncTensor& T = p.t[pd.ti];
-        const uint64_t ntiles = num_tiles(T.n);
-        const uint64_t prefix = rs->uprefix[r][warp];
-        if (half == 0) {
-          if (lane == 0) *reinterpret_cast<uint32_t*>(T.main + kHeader + 4ull * pd.lt) = static_cast<uint32_t>(prefix);
-          if (pd.lt == 0) write_header_words(T.main, T.n, T.cb);
-        }
-        if (half == kUnitsPerTile - 1 && pd.lt + 1 == ntiles) {
-          const uint64_t n_esc = prefix + pd.te.total;
-          write_header_tail(T.main, ntiles, n_esc);
-          if (lane == 0 && n_esc > T.esc_cap) set_status(p.status, ZC_ERR_ESCAPE_OVERFLOW);
-        }
-        if (pd.spilled) {
-          write_escapes<kUnitBlocks>(wstage_s + s * kEncStageBytes, pd.te, prefix, T.esc, T.esc_cap);
+    // Second half of round k, once its offsets are posted (slot k mod 16):
+    // the offset-table entry and header parts of unit (ti, lt); returns the
+    // unit's escape offset.
+    auto write_meta = [&](uint32_t k, uint32_t ti, uint32_t lt, uint32_t cnt) -> uint64_t {
+      const EncTensor& T = p.t[ti];
+      const uint64_t ntiles = num_tiles(T.n);
+      const uint64_t prefix = rs->uprefix[k % kEncSlots][warp];
+      if (half == 0) {
+        if (lane == 0) *reinterpret_cast<uint32_t*>(T.main + kHeader + 4ull * lt) = static_cast<uint32_t>(prefix);
+        if (lt == 0) write_header_words(T.main, T.n, T.cb);
+      }
+      if (half == kUnitsPerTile - 1 && lt + 1 == ntiles) {
+        const uint64_t n_esc = prefix + cnt;
+        write_header_tail(T.main, ntiles, n_esc);
+        if (lane == 0 && n_esc > T.esc_cap) set_status(p.status, ZC_ERR_ESCAPE_OVERFLOW);
+      }
+      return prefix;
+    };
+    // Finishes queued round k: waits for its offsets, then writes its meta
+    // data and moves its escapes from the ring to the escape stream.
+    auto finish = [&](uint32_t k) {
+      mbar_wait_bounded(&rs->pre_bar[k % kEncSlots], (k / kEncSlots) & 1u, p.status);
+      const QEntry e = queue[k % kEncSlots];
+      if (e.has) {
+        const uint64_t prefix = write_meta(k, e.ti, e.lt, e.cnt);
+        const EncTensor& T = p.t[e.ti];
+        const uint8_t* src = ring + e.start % kEncRing;
+        uint8_t* dst = T.esc + prefix;
+        if (prefix + e.cnt <= T.esc_cap) {
+          for (uint32_t i = lane; i < e.cnt; i += 32) dst[i] = src[i];
         } else {
-          const uint8_t* src = ebuf + r * kEncEscBuf;
-          const uint64_t cap = T.esc_cap;
-          for (uint32_t i = lane; i < pd.te.total; i += 32)
-            if (prefix + i < cap) T.esc[prefix + i] = src[i];
+          for (uint32_t i = lane; i < e.cnt; i += 32)
+            if (prefix + i < T.esc_cap) dst[i] = src[i];
         }
       }
       __syncwarp();
-      if (pd.spilled) issue(s, G + kEncStages * step);  // the stage was held for the escapes
     };
 
 #pragma unroll
@@ -249,98 +273,97 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
     uint32_t phase = 0;
     int cur_ti = -1;
     bool cb_ok = true;
-    Pending pend[kEncStages];  // rounds j - 2 and j - 1, indexed by round parity (= stage)
-#pragma unroll
-    for (int s = 0; s < kEncStages; s++) {
-      pend[s].has = pend[s].spilled = false;
-      pend[s].done = true;
-    }
+    uint32_t fin = 0;   // oldest round not finished; rounds fin .. j - 1 are queued
+    uint32_t head = 0;  // ring bytes allocated so far (running count)
     uint32_t j = 0;
-    bool more = true;
-    while (more) {
-#pragma unroll
-      for (int s = 0; s < kEncStages; s++) {  // rounds of stage 0, then stage 1
-        const uint32_t G = blockIdx.x + j * step;
-        if (G >= p.total_groups) {
-          more = false;
-          break;
+    for (uint32_t G = blockIdx.x; G < p.total_groups; G += step, j++) {
+      const int r = static_cast<int>(j % kEncSlots);
+      const int s = static_cast<int>(j & 1u);
+      if (j - fin == kEncSlots) finish(fin++);  // slot r is still held by round j - 16
+      uint32_t ti, lt;
+      bool has = my_unit(G, ti, lt);
+      EscBook<kUnitBlocks> te;
+      te.total = 0;
+      const EncTensor& T = p.t[ti];
+      if (static_cast<int>(ti) != cur_ti) {
+        cb_ok = build_enc_lut(lut, T.cb);  // every warp of the group reaches the same verdict
+        cur_ti = static_cast<int>(ti);
+        if (!cb_ok && lane == 0) set_status(p.status, ZC_ERR_DUP_CODEBOOK);
+      }
+      const uint32_t tb_s = wstage_s + s * kEncStageBytes;
+      if (has) {
+        const uint32_t nv = unit_valid(T, lt);
+        const uint64_t rem = T.n - static_cast<uint64_t>(lt) * kTile;
+        const uint32_t n_tile = rem >= kTile ? kTile : static_cast<uint32_t>(rem);
+        mbar_wait_bounded(&bar[s], (phase >> s) & 1u, p.status);
+        phase ^= 1u << s;
+        if (nv < kUnitElems) {
+          uint16_t* tb = stage_ptr(s);
+          const uint16_t* src = T.in + static_cast<uint64_t>(lt) * kTile + half * kUnitElems;
+          for (uint32_t i = lane; i < kUnitElems; i += 32) tb[i] = i < nv ? src[i] : static_cast<uint16_t>(0);
+          __syncwarp();
         }
-        const int r = static_cast<int>(j % kEncSlots);
-        // round j - 2 used this stage; if it spilled, finish it now to free the stage
-        if (!pend[s].done && pend[s].spilled) {
-          finish(j - 2, G - 2 * step, pend[s]);
-          pend[s].done = true;
+        if (cb_ok)
+          encode_blocks<kUnitBlocks>(tb_s, half * kUnitBlocks, n_tile, lut_s,
+                                     tile_ptr(T.main, num_tiles(T.n), lt) + half * kUnitBlocks * kBlockBytes, te);
+        else
+          has = false;
+      }
+      const uint32_t cnt = te.total;
+      if (lane == 0) {
+        rs->cnt[r][warp] = cnt;
+        // the last warp of the group publishes the group's escape count right away
+        const uint32_t old = atomicAdd(&rs->agg[r], (1u << 16) | cnt);
+        if ((old >> 16) == kEncWarps - 1 && cb_ok && hold != G + 1) {
+          const uint32_t agg = (old & 0xFFFFu) + cnt;
+          const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
+          if (G == p.group_start[ti])
+            st_relaxed(&p.flags[G].incl, tag | agg);  // first group of its tensor: nothing before it
+          else
+            st_relaxed(&p.flags[G].agg, tag | agg);
         }
-        Pending cur;
-        cur.has = my_unit(G, cur.ti, cur.lt);
-        cur.spilled = false;
-        cur.done = false;
-        cur.te.total = 0;
-        const EncTensor& T = p.t[cur.ti];
-        if (static_cast<int>(cur.ti) != cur_ti) {
-          cb_ok = build_enc_lut(lut, T.cb);  // every warp of the group reaches the same verdict
-          cur_ti = static_cast<int>(cur.ti);
-          if (!cb_ok && lane == 0) set_status(p.status, ZC_ERR_DUP_CODEBOOK);
+        mbar_arrive(&rs->cnt_bar[r]);  // release: the count is visible to the scan warp
+      }
+      __syncwarp();
+      if (cnt <= kEncRingUnitMax) {
+        // a contiguous ring share: skip the ring's tail if the share would
+        // cross its end; finish old rounds until the share is free
+        uint32_t pos;
+        for (;;) {
+          pos = head;
+          if (pos % kEncRing + cnt > kEncRing) pos += kEncRing - pos % kEncRing;
+          const uint32_t tail = fin == j ? pos : queue[fin % kEncSlots].start;
+          if (pos + cnt - tail <= kEncRing) break;
+          finish(fin++);
         }
-        if (cur.has) {
-          const uint32_t tb_s = wstage_s + s * kEncStageBytes;
-          const uint32_t nv = unit_valid(T, cur.lt);
-          const uint64_t rem = T.n - static_cast<uint64_t>(cur.lt) * kTile;
-          const uint32_t n_tile = rem >= kTile ? kTile : static_cast<uint32_t>(rem);
-          mbar_wait_bounded(&bar[s], (phase >> s) & 1u, p.status);
-          phase ^= 1u << s;
-          if (nv < kUnitElems) {
-            uint16_t* tb = stage_ptr(s);
-            const uint16_t* src = T.in + static_cast<uint64_t>(cur.lt) * kTile + half * kUnitElems;
-            for (uint32_t i = lane; i < kUnitElems; i += 32) tb[i] = i < nv ? src[i] : static_cast<uint16_t>(0);
-            __syncwarp();
-          }
-          if (cb_ok) {
-            encode_blocks<kUnitBlocks>(tb_s, half * kUnitBlocks, n_tile, lut_s,
-                                       tile_ptr(T.main, num_tiles(T.n), cur.lt) + half * kUnitBlocks * kBlockBytes,
-                                       cur.te);
-            cur.spilled = cur.te.total > kEncEscBuf;
-            if (!cur.spilled) stage_escapes_smem<kUnitBlocks>(tb_s, cur.te, ebuf + r * kEncEscBuf);
-          } else {
-            cur.has = false;
-          }
-        }
+        if (cnt != 0) stage_escapes_smem<kUnitBlocks>(tb_s, te, ring + pos % kEncRing);
+        head = pos + cnt;
         if (lane == 0) {
-          rs->cnt[r][warp] = cur.te.total;
-          // the last warp of the group publishes the group's escape count right away
-          const uint32_t old = atomicAdd(&rs->agg[r], (1u << 16) | cur.te.total);
-          if ((old >> 16) == kEncWarps - 1 && cb_ok && hold != G + 1) {
-            const uint32_t agg = (old & 0xFFFFu) + cur.te.total;
-            const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
-            if (G == p.group_start[cur.ti])
-              st_relaxed(&p.flags[G].incl, tag | agg);  // first group of its tensor: nothing before it
-            else
-              st_relaxed(&p.flags[G].agg, tag | agg);
-          }
-          mbar_arrive(&rs->cnt_bar[r]);  // release: the count is visible to the scan warp
+          QEntry e;
+          e.lt = lt;
+          e.start = pos;
+          e.ti = static_cast<uint16_t>(ti);
+          e.cnt = static_cast<uint16_t>(cnt);
+          e.has = has;
+          queue[r] = e;
         }
         __syncwarp();
-        if (!cur.spilled) issue(s, G + kEncStages * step);  // refill now; escapes are staged
-        if (!pend[s].done) finish(j - 2, G - 2 * step, pend[s]);  // round j - 2, oldest first
-        pend[s] = cur;
-        j++;
-      }
-    }
-    // drain the last two rounds, oldest first
-    auto drain = [&](uint32_t k, Pending& pd) {
-      if (!pd.done) finish(k, blockIdx.x + k * step, pd);
-    };
-    if (j >= 2) {
-      if (((j - 2) & 1u) == 0) {
-        drain(j - 2, pend[0]);
-        drain(j - 1, pend[1]);
+        issue(s, G + kEncStages * step);  // refill now; the escapes are in the ring
       } else {
-        drain(j - 2, pend[1]);
-        drain(j - 1, pend[0]);
+        // too many escapes for the ring: finish everything before, wait for
+        // this round's offsets and write the escapes from the stage
+        while (fin < j) finish(fin++);
+        mbar_wait_bounded(&rs->pre_bar[r], (j / kEncSlots) & 1u, p.status);
+        const uint64_t prefix = write_meta(j, ti, lt, cnt);
+        write_escapes<kUnitBlocks>(tb_s, te, prefix, T.esc, T.esc_cap);
+        __syncwarp();
+        fin = j + 1;
+        issue(s, G + kEncStages * step);
       }
-    } else if (j == 1) {
-      drain(0, pend[0]);
+      // finish whatever rounds already have their offsets
+      while (fin <= j && mbar_test_wait(&rs->pre_bar[fin % kEncSlots], (fin / kEncSlots) & 1u)) finish(fin++);
     }
+    while (fin < j) finish(fin++);  // drain
   }
   cta_exit(p.ws, p.flags, epoch, p.total_groups);
 }
@@ -363,7 +386,6 @@ static cudaError_t launch_encode_t(const EncTensor* ts, int count, WsHeader* ws,
   p.flags = flags;
   p.status = status;
   static_assert(sizeof(EncParams<MAXB>) < 4000, "encode parameters too large");
-  static_assert(sizeof(RoundShared) <= 1280, "round bookkeeping too large");
   static_assert(kEncSmem + 1024 <= 232448, "shared memory budget");
   static KernelPrep prep;
   int per_sm = 0;
