@@ -515,25 +515,35 @@ __device__ __forceinline__ void build_spread_tables(uint32_t* spread /* 3 x 256 
   }
 }
 
-// Code -> exponent table as two words for __byte_perm: byte c of (t0, t1) is
-// the exponent of code c (byte 0, code 0 = escape, is a placeholder 0).
+// An exponent rotated right by one bit: (e & 1) << 7 | e >> 1.  In this form
+// the exponent's low bit sits where a bf16's low byte wants it (bit 7) and its
+// other seven bits where the high byte wants them (bits 0..6), so a bf16 is
+// a bit-select between its sign-mantissa byte and this byte (see bf16_pair).
+__device__ __forceinline__ uint32_t rot_exp(uint32_t e) { return ((e >> 1) | (e << 7)) & 0xFFu; }
+
+// Code -> rotated exponent table as two words for __byte_perm: byte c of
+// (t0, t1) is rot_exp of the exponent of code c (byte 0, code 0 = escape, is
+// a placeholder 0).
 struct DecTable {
   uint32_t t0, t1;
 };
 
 __device__ __forceinline__ DecTable make_dec_table(const uint8_t cb[7]) {
   DecTable d;
-  d.t0 = (static_cast<uint32_t>(cb[0]) << 8) | (static_cast<uint32_t>(cb[1]) << 16) |
-         (static_cast<uint32_t>(cb[2]) << 24);
-  d.t1 = static_cast<uint32_t>(cb[3]) | (static_cast<uint32_t>(cb[4]) << 8) | (static_cast<uint32_t>(cb[5]) << 16) |
-         (static_cast<uint32_t>(cb[6]) << 24);
+  d.t0 = (rot_exp(cb[0]) << 8) | (rot_exp(cb[1]) << 16) | (rot_exp(cb[2]) << 24);
+  d.t1 = rot_exp(cb[3]) | (rot_exp(cb[4]) << 8) | (rot_exp(cb[5]) << 16) | (rot_exp(cb[6]) << 24);
   return d;
 }
 
-// Two packed bf16 values from bytes x = [sm0, e0, sm1, e1] (16-bit lanes e<<8 | sm):
-// value = sign << 15 | e << 7 | mantissa.
-__device__ __forceinline__ uint32_t join_pair(uint32_t x) {
-  return ((x >> 1) & 0x7F807F80u) | (x & 0x007F007Fu) | ((x << 8) & 0x80008000u);
+// Two packed bf16 values (elements 2h, 2h + 1 of a group of four) from the
+// group's sign-mantissa word `sm` (byte i = s << 7 | m of element i) and its
+// rotated-exponent word `rx` (byte i = rot_exp(e) of element i):
+// low byte = (e & 1) << 7 | m, high byte = s << 7 | e >> 1.
+template <int H>
+__device__ __forceinline__ uint32_t bf16_pair(uint32_t sm, uint32_t rx) {
+  const uint32_t a = __byte_perm(sm, rx, H ? 0x7362 : 0x5140);  // [sm, rx, sm, rx] per value
+  const uint32_t b = __byte_perm(sm, rx, H ? 0x3726 : 0x1504);  // [rx, sm, rx, sm] per value
+  return (a & 0x7F7F7F7Fu) | (b & 0x80808080u);
 }
 
 // Source of escape bytes for one (tile, stream): the first `staged` ranks sit
@@ -580,7 +590,7 @@ __device__ __forceinline__ uint32_t decode_block(uint32_t tile, uint32_t blk, ui
   uint32_t rank = run + inc - c;
   run += __shfl_sync(kFull, inc, 31);
 
-  // exponents of the 32 elements, 4 per word: ex[2k] = elements 0..3 of group k
+  // rotated exponents of the 32 elements, 4 per word: ex[2k] = elements 0..3 of group k
   uint32_t ex[8];
 #pragma unroll
   for (uint32_t k = 0; k < 4; k++) {
@@ -597,7 +607,7 @@ __device__ __forceinline__ uint32_t decode_block(uint32_t tile, uint32_t blk, ui
     while (m) {
       const uint32_t p = __ffs(m) - 1;
       m &= m - 1;
-      scratch[lane * 32 + p] = static_cast<uint8_t>(esc_byte(es, rank));
+      scratch[lane * 32 + p] = static_cast<uint8_t>(rot_exp(esc_byte(es, rank)));
       rank++;
     }
     const uint4 a = sp[0], bq = sp[1];
@@ -608,10 +618,10 @@ __device__ __forceinline__ uint32_t decode_block(uint32_t tile, uint32_t blk, ui
 #pragma unroll
   for (uint32_t k = 0; k < 4; k++) {
     const uint2 sm = lds64(b + k * 256 + lane * 8);
-    out[k].x = join_pair(__byte_perm(sm.x, ex[2 * k], 0x5140));
-    out[k].y = join_pair(__byte_perm(sm.x, ex[2 * k], 0x7362));
-    out[k].z = join_pair(__byte_perm(sm.y, ex[2 * k + 1], 0x5140));
-    out[k].w = join_pair(__byte_perm(sm.y, ex[2 * k + 1], 0x7362));
+    out[k].x = bf16_pair<0>(sm.x, ex[2 * k]);
+    out[k].y = bf16_pair<1>(sm.x, ex[2 * k]);
+    out[k].z = bf16_pair<0>(sm.y, ex[2 * k + 1]);
+    out[k].w = bf16_pair<1>(sm.y, ex[2 * k + 1]);
   }
   return c;
 }
@@ -651,16 +661,27 @@ __device__ __forceinline__ uint32_t decode_one_block(uint32_t tile, uint32_t blk
     ex[2 * k] = __byte_perm(dt.t0, dt.t1, sel & 0xFFFFu);
     ex[2 * k + 1] = __byte_perm(dt.t0, dt.t1, sel >> 16);
   }
+  const uint32_t total = __shfl_sync(kFull, inc, 31);
   if (z) {
     uint4* sp = reinterpret_cast<uint4*>(scratch + lane * 32);
     sp[0] = make_uint4(ex[0], ex[1], ex[2], ex[3]);
     sp[1] = make_uint4(ex[4], ex[5], ex[6], ex[7]);
     uint32_t m = z;
-    while (m) {
-      const uint32_t p = __ffs(m) - 1;
-      m &= m - 1;
-      scratch[lane * 32 + p] = static_cast<uint8_t>(esc_byte(es, rank));
-      rank++;
+    uint8_t* dst = scratch + lane * 32;
+    if (first + total <= es.staged) {  // (warp-uniform) every escape of the block is staged
+      const uint8_t* src = es.smem + rank;
+      do {
+        const uint32_t p = __ffs(m) - 1;
+        m &= m - 1;
+        dst[p] = static_cast<uint8_t>(rot_exp(*src++));
+      } while (m);
+    } else {
+      while (m) {
+        const uint32_t p = __ffs(m) - 1;
+        m &= m - 1;
+        dst[p] = static_cast<uint8_t>(rot_exp(esc_byte(es, rank)));
+        rank++;
+      }
     }
     const uint4 a = sp[0], bq = sp[1];
     ex[0] = a.x; ex[1] = a.y; ex[2] = a.z; ex[3] = a.w;
@@ -669,26 +690,27 @@ __device__ __forceinline__ uint32_t decode_one_block(uint32_t tile, uint32_t blk
 #pragma unroll
   for (uint32_t k = 0; k < 4; k++) {
     const uint2 sm = lds64(b + k * 256 + lane * 8);
-    out[k].x = join_pair(__byte_perm(sm.x, ex[2 * k], 0x5140));
-    out[k].y = join_pair(__byte_perm(sm.x, ex[2 * k], 0x7362));
-    out[k].z = join_pair(__byte_perm(sm.y, ex[2 * k + 1], 0x5140));
-    out[k].w = join_pair(__byte_perm(sm.y, ex[2 * k + 1], 0x7362));
+    out[k].x = bf16_pair<0>(sm.x, ex[2 * k]);
+    out[k].y = bf16_pair<1>(sm.x, ex[2 * k]);
+    out[k].z = bf16_pair<0>(sm.y, ex[2 * k + 1]);
+    out[k].w = bf16_pair<1>(sm.y, ex[2 * k + 1]);
   }
-  return __shfl_sync(kFull, inc, 31);
+  return total;
 }
 
-// acc[i] += bf16 value i of the 8 packed in v (two fp32 adds per instruction,
-// IEEE round-to-nearest, subnormals kept).
+// acc[i] += bf16 value i of the 8 packed in v: each add takes the bf16 operand
+// as it is (mixed-precision add, exact widening), IEEE round-to-nearest,
+// subnormals kept.
 __device__ __forceinline__ void accumulate8(float (&acc)[8], uint4 v) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int i = 0; i < 4; i++) {
-    unsigned long long a, x;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(acc[2 * i]), "f"(acc[2 * i + 1]));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(w[i] << 16), "r"(w[i] & 0xFFFF0000u));
-    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(a) : "l"(x));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[2 * i]), "=f"(acc[2 * i + 1]) : "l"(a));
-  }
+  for (int i = 0; i < 4; i++)
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\t"
+        "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(acc[2 * i]), "+f"(acc[2 * i + 1])
+        : "r"(w[i]));
 }
 
 // Stores 8 bf16 values (one 16-byte vector) at element index `idx` of a tensor

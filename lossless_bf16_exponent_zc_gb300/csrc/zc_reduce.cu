@@ -100,10 +100,21 @@ struct RedPending {
   EscBook<1> te;
 };
 
+// The 8 sums of a lane's 8-element run rounded to bf16 (nearest even) and
+// packed.  The hardware conversion rounds exactly as the IEEE definition
+// does but returns its own NaN pattern, so when a NaN may be among the sums
+// (their total is NaN; an inf - inf total only costs the slow path) the
+// run is rounded by the definition instead, which maps NaN to 0x7FC0.
 __device__ __forceinline__ uint4 round_pack(const float (&acc)[8]) {
   uint32_t w[4];
+  const float t = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+  if (t != t) {
 #pragma unroll
-  for (int i = 0; i < 4; i++) w[i] = f32_to_bf16_rne(acc[2 * i]) | (f32_to_bf16_rne(acc[2 * i + 1]) << 16);
+    for (int i = 0; i < 4; i++) w[i] = f32_to_bf16_rne(acc[2 * i]) | (f32_to_bf16_rne(acc[2 * i + 1]) << 16);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; i++) asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[i]) : "f"(acc[2 * i + 1]), "f"(acc[2 * i]));
+  }
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
@@ -351,8 +362,14 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
           mbar_wait_bounded(&full_bar[bi], (k_item / kRedStages) & 1u, p.status);
           const StageMeta m = meta[bi];
           const uint32_t tile_s = sbase + kRStage + bi * kRedStageBytes;
+          // escapes of the tile's earlier blocks: one warp reduction over their masks
           uint32_t first = 0;
-          for (uint32_t bb = 0; bb < b; bb++) first += __reduce_add_sync(kFull, __popc(block_zero_mask(tile_s, bb, n_tile)));
+          if (b != 0) {
+            uint32_t c = __popc(block_zero_mask(tile_s, 0, n_tile));
+            if (b > 1) c += __popc(block_zero_mask(tile_s, 1, n_tile));
+            if (b > 2) c += __popc(block_zero_mask(tile_s, 2, n_tile));
+            first = __reduce_add_sync(kFull, c);
+          }
           DecTable dt;
           dt.t0 = si[m.shard].t0;
           dt.t1 = si[m.shard].t1;
