@@ -1,8 +1,8 @@
 // zc_device.cuh -- device building blocks shared by the libzc kernels (sm_103a).
 //
-// Format constants, the per-warp TMA/mbarrier pipeline primitives, the bounded
-// decoupled look-back that gives every tile its escape offset, and the
-// per-tile encode and decode routines of ZC1 (layout in include/zc.h).
+// Format constants, the per-warp TMA/mbarrier pipeline primitives, the
+// bounded window sum that gives every scan unit its escape offset, and the
+// per-block encode and decode routines of ZC1 (layout in include/zc.h).
 // Method: [ZipCCL §2.B] field split, 3-bit codes, escape array; [ZipCCL §2.C]
 // three 1-bit code arrays, column-major, 128-byte blocks.
 #pragma once
@@ -20,17 +20,18 @@ constexpr uint32_t kTileBytes = ZC_TILE_BYTES;     // 5632
 constexpr uint32_t kBlockBytes = ZC_BLOCK_BYTES;   // 1408
 constexpr uint32_t kHeader = ZC_HEADER_BYTES;      // 128
 constexpr uint32_t kFull = 0xFFFFFFFFu;
-// Upper bound on any inter-block wait (look-back, TMA completion).  Normal
+// Upper bound on any inter-block wait (escape scan, TMA completion).  Normal
 // waits last microseconds; after this the kernel records ZC_ERR_TIMEOUT.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
 // ---------------------------------------------------------------- workspace
 // The caller zero-fills the workspace once.  Every kernel returns it to a
-// reusable state: the exit counter is reset by the last CTA to leave, look-back flags are tagged with a per-launch epoch so stale flags of
-// earlier launches never match, and histogram bins are cleared by the last CTA.
+// reusable state: the exit counter is reset by the last CTA to leave, escape
+// scan flags are tagged with a per-launch epoch so stale flags of earlier
+// launches never match, and histogram bins are cleared by the last CTA.
 struct WsHeader {
-  uint32_t hold_tile;  // test hook for the bounded waits: if non-zero, look-back unit hold_tile - 1
-                       // publishes no flag, so its successor's look-back must time out; the
+  uint32_t hold_tile;  // test hook for the bounded waits: if non-zero, scan unit hold_tile - 1
+                       // publishes no count, so the scans that need it must time out; the
                        // last CTA of the launch resets it to 0
   uint32_t exited;     // CTAs of the running encoding launch that have left
   uint32_t epoch;      // epoch tag of the last finished encoding launch
@@ -86,15 +87,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
 __device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
   uint16_t v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
-  return v;
-}
-
-__device__ __forceinline__ ulonglong2 ld_relaxed_v2(const Flag* f) {
-  ulonglong2 v;
-  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];"
-               : "=l"(v.x), "=l"(v.y)
-               : "l"(f)
-               : "memory");
   return v;
 }
 
@@ -277,7 +269,6 @@ struct EscBook {
   uint32_t base[NB];  // rank of this lane's first escape in each block, from the first block on
   uint32_t total;     // escapes in the NB blocks (same in every lane)
 };
-using TileEsc = EscBook<4>;
 
 // Encodes NB consecutive blocks held in shared memory (shared address `tb`:
 // NB * 1024 bf16 bit patterns, zero beyond the valid ones) into their 1408-byte
@@ -349,9 +340,6 @@ __device__ __forceinline__ void encode_blocks(uint32_t tb, uint32_t blk0, uint32
   te.total = run;
 }
 
-__device__ __forceinline__ void encode_tile(uint32_t tb, uint32_t n_tile, uint32_t lut, uint8_t* out, TileEsc& te) {
-  encode_blocks<4>(tb, 0, n_tile, lut, out, te);
-}
 
 // Writes the escapes of NB blocks (their 8-bit exponents, read back from the
 // blocks in shared memory at shared address `tb`) at global positions prefix +
@@ -418,67 +406,51 @@ __device__ __forceinline__ void stage_escapes_smem(uint32_t tb, const EscBook<NB
   }
 }
 
-// Decoupled look-back (single pass): returns the exclusive escape prefix of
-// unit g (a tile or a group of tiles), whose tensor starts at unit g0, by
-// summing the aggregates of preceding units until one carrying an inclusive
-// prefix is found.  A caller that already knows the inclusive prefix of an
-// earlier unit of the same tensor (its own previous unit) passes it as
-// (known_idx, known_val): the scan then needs only the aggregates in between,
-// which other units publish without waiting on anyone, so no chain of
-// look-backs forms.  Each step reads the flags of the 160 nearest unresolved
-// predecessors (5 per lane).  Every unit's owner visits its units in
-// increasing order and all owners are resident (cooperative launch), so
-// predecessors always make progress; the wait is still bounded
-// (ZC_ERR_TIMEOUT, prefix then meaningless).
-constexpr int kLookbackPerLane = 5;
+// Escape scan across scan units (a group of tiles; one flag per unit).  The
+// owner of a unit publishes the unit's escape count ("aggregate", tagged with
+// the launch epoch) in flags[u].agg as soon as the unit is encoded, without
+// waiting on anyone.  Each CTA visits its units in increasing order, so the
+// exclusive offset of its unit G is the inclusive offset of its previous unit
+// P of the same tensor plus the aggregates of the units in between (or, for
+// its first unit of a tensor, the aggregates from the tensor's first unit):
+// window_sum() adds the aggregates of units [lo, hi) with one warp.  This is
+// a decoupled look-back whose window is fixed in advance, so it never waits
+// for another unit's scan, only for aggregates.  Each pass reads up to 160
+// flags (5 per lane) and re-reads only those not yet published.  The wait is
+// bounded (ZC_ERR_TIMEOUT; the sum is then meaningless).  All lanes return
+// the sum.
+constexpr int kWindowPerLane = 5;
 
-__device__ __forceinline__ uint64_t lookback(const Flag* flags, uint32_t g, uint32_t g0, uint32_t epoch,
-                                             int32_t* status, bool* timed_out, int64_t known_idx = -1,
-                                             uint64_t known_val = 0) {
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint64_t window_sum(const Flag* flags, uint32_t lo, uint32_t hi, uint32_t epoch,
+                                               int32_t* status, bool* timed_out) {
   const uint32_t lane = lane_id();
-  uint64_t prefix = 0;
-  int64_t end = g;  // exclusive end of the window
-  unsigned long long t0 = 0;
+  uint64_t sum = 0;
   *timed_out = false;
-  while (true) {
-    uint32_t st[kLookbackPerLane];
-    uint64_t val[kLookbackPerLane];
+  for (uint32_t base = lo; base < hi; base += 32 * kWindowPerLane) {
+    uint32_t pending = 0;  // bit q: unit base + lane + 32q not yet counted
 #pragma unroll
-    for (int q = 0; q < kLookbackPerLane; q++) {
-      const int64_t idx = end - 1 - static_cast<int64_t>(lane + 32 * q);  // distance lane + 32q
-      st[q] = 2;
-      val[q] = 0;
-      if (idx == known_idx) {
-        val[q] = known_val;
-      } else if (idx >= static_cast<int64_t>(g0)) {
-        const ulonglong2 f = ld_relaxed_v2(flags + idx);
-        if (static_cast<uint32_t>(f.y >> 32) == epoch) {
-          val[q] = static_cast<uint32_t>(f.y);
-        } else if (static_cast<uint32_t>(f.x >> 32) == epoch) {
-          st[q] = 1;
-          val[q] = static_cast<uint32_t>(f.x);
-        } else {
-          st[q] = 0;
+    for (int q = 0; q < kWindowPerLane; q++)
+      if (base + lane + 32u * q < hi) pending |= 1u << q;
+    unsigned long long t0 = 0;
+    while (true) {
+      unsigned long long f[kWindowPerLane];
+#pragma unroll
+      for (int q = 0; q < kWindowPerLane; q++)
+        f[q] = (pending >> q) & 1u ? ld_relaxed_u64(&flags[base + lane + 32u * q].agg) : 0ull;
+#pragma unroll
+      for (int q = 0; q < kWindowPerLane; q++) {
+        if (((pending >> q) & 1u) && static_cast<uint32_t>(f[q] >> 32) == epoch) {
+          sum += static_cast<uint32_t>(f[q]);
+          pending &= ~(1u << q);
         }
       }
-    }
-    // nearest predecessor carrying an inclusive prefix: distance `first`
-    uint32_t first = 32 * kLookbackPerLane - 1;
-    bool found = false, missing = false;
-#pragma unroll
-    for (int q = 0; q < kLookbackPerLane; q++) {
-      const uint32_t inc = __ballot_sync(kFull, st[q] == 2);
-      const uint32_t mis = __ballot_sync(kFull, st[q] == 0);
-      if (!found) {
-        const uint32_t upto = inc ? ((2u << (__ffs(inc) - 1)) - 1u) : kFull;  // lanes up to the inclusive one
-        missing |= (mis & upto) != 0;
-        if (inc) {
-          found = true;
-          first = 32 * q + (__ffs(inc) - 1);
-        }
-      }
-    }
-    if (missing) {
+      if (!__any_sync(kFull, pending != 0)) break;
       unsigned long long now = 0;
       if (lane == 0) now = global_ns();
       now = __shfl_sync(kFull, now, 0);
@@ -486,19 +458,13 @@ __device__ __forceinline__ uint64_t lookback(const Flag* flags, uint32_t g, uint
       if (now - t0 > kWaitLimitNs) {
         if (lane == 0) set_status(status, ZC_ERR_TIMEOUT);
         *timed_out = true;
-        return prefix;
+        break;
       }
-      continue;
     }
-    uint64_t part = 0;
-#pragma unroll
-    for (int q = 0; q < kLookbackPerLane; q++) part += (lane + 32 * q <= first) ? val[q] : 0u;
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) part += __shfl_xor_sync(kFull, part, d);
-    prefix += part;
-    if (found) return prefix;
-    end -= 32 * kLookbackPerLane;
   }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) sum += __shfl_xor_sync(kFull, sum, d);
+  return sum;
 }
 
 // ---------------------------------------------------------------- decode side
@@ -590,19 +556,28 @@ __device__ __forceinline__ uint32_t decode_block(uint32_t tile, uint32_t blk, ui
   uint32_t rank = run + inc - c;
   run += __shfl_sync(kFull, inc, 31);
 
-  // rotated exponents of the 32 elements, 4 per word: ex[2k] = elements 0..3 of group k
-  uint32_t ex[8];
+  // rotated exponents of the 32 elements, 4 per word: word 2k = elements 0..3 of group k,
+  // word 2k + 1 = elements 4..7 (exa holds words 0..3, exb words 4..7)
+  uint4 exa, exb;  // ex words 0..3 and 4..7 (16-byte vectors: stored and reloaded without moves)
+  {
+    uint32_t sel[4];
 #pragma unroll
-  for (uint32_t k = 0; k < 4; k++) {
-    const uint32_t sel = spread_at(w0, k, spread) | spread_at(w1, k, spread + 1024) | spread_at(w2, k, spread + 2048);
-    ex[2 * k] = __byte_perm(dt.t0, dt.t1, sel & 0xFFFFu);
-    ex[2 * k + 1] = __byte_perm(dt.t0, dt.t1, sel >> 16);
+    for (uint32_t k = 0; k < 4; k++)
+      sel[k] = spread_at(w0, k, spread) | spread_at(w1, k, spread + 1024) | spread_at(w2, k, spread + 2048);
+    exa.x = __byte_perm(dt.t0, dt.t1, sel[0] & 0xFFFFu);
+    exa.y = __byte_perm(dt.t0, dt.t1, sel[0] >> 16);
+    exa.z = __byte_perm(dt.t0, dt.t1, sel[1] & 0xFFFFu);
+    exa.w = __byte_perm(dt.t0, dt.t1, sel[1] >> 16);
+    exb.x = __byte_perm(dt.t0, dt.t1, sel[2] & 0xFFFFu);
+    exb.y = __byte_perm(dt.t0, dt.t1, sel[2] >> 16);
+    exb.z = __byte_perm(dt.t0, dt.t1, sel[3] & 0xFFFFu);
+    exb.w = __byte_perm(dt.t0, dt.t1, sel[3] >> 16);
   }
   if (__any_sync(kFull, z != 0)) {
     // patch escapes through shared memory (bit p of z <-> byte p of ex)
     uint4* sp = reinterpret_cast<uint4*>(scratch + lane * 32);
-    sp[0] = make_uint4(ex[0], ex[1], ex[2], ex[3]);
-    sp[1] = make_uint4(ex[4], ex[5], ex[6], ex[7]);
+    sp[0] = exa;
+    sp[1] = exb;
     uint32_t m = z;
     while (m) {
       const uint32_t p = __ffs(m) - 1;
@@ -610,18 +585,19 @@ __device__ __forceinline__ uint32_t decode_block(uint32_t tile, uint32_t blk, ui
       scratch[lane * 32 + p] = static_cast<uint8_t>(rot_exp(esc_byte(es, rank)));
       rank++;
     }
-    const uint4 a = sp[0], bq = sp[1];
-    ex[0] = a.x; ex[1] = a.y; ex[2] = a.z; ex[3] = a.w;
-    ex[4] = bq.x; ex[5] = bq.y; ex[6] = bq.z; ex[7] = bq.w;
+    exa = sp[0];
+    exb = sp[1];
     __syncwarp();
   }
 #pragma unroll
   for (uint32_t k = 0; k < 4; k++) {
     const uint2 sm = lds64(b + k * 256 + lane * 8);
-    out[k].x = bf16_pair<0>(sm.x, ex[2 * k]);
-    out[k].y = bf16_pair<1>(sm.x, ex[2 * k]);
-    out[k].z = bf16_pair<0>(sm.y, ex[2 * k + 1]);
-    out[k].w = bf16_pair<1>(sm.y, ex[2 * k + 1]);
+    const uint32_t r0 = k == 0 ? exa.x : k == 1 ? exa.z : k == 2 ? exb.x : exb.z;
+    const uint32_t r1 = k == 0 ? exa.y : k == 1 ? exa.w : k == 2 ? exb.y : exb.w;
+    out[k].x = bf16_pair<0>(sm.x, r0);
+    out[k].y = bf16_pair<1>(sm.x, r0);
+    out[k].z = bf16_pair<0>(sm.y, r1);
+    out[k].w = bf16_pair<1>(sm.y, r1);
   }
   return c;
 }
@@ -654,18 +630,26 @@ __device__ __forceinline__ uint32_t decode_one_block(uint32_t tile, uint32_t blk
   const uint32_t c = __popc(z);
   const uint32_t inc = warp_inclusive_scan(c);
   uint32_t rank = first + inc - c;
-  uint32_t ex[8];
+  uint4 exa, exb;  // ex words 0..3 and 4..7 (16-byte vectors: stored and reloaded without moves)
+  {
+    uint32_t sel[4];
 #pragma unroll
-  for (uint32_t k = 0; k < 4; k++) {
-    const uint32_t sel = spread_at(w0, k, spread) | spread_at(w1, k, spread + 1024) | spread_at(w2, k, spread + 2048);
-    ex[2 * k] = __byte_perm(dt.t0, dt.t1, sel & 0xFFFFu);
-    ex[2 * k + 1] = __byte_perm(dt.t0, dt.t1, sel >> 16);
+    for (uint32_t k = 0; k < 4; k++)
+      sel[k] = spread_at(w0, k, spread) | spread_at(w1, k, spread + 1024) | spread_at(w2, k, spread + 2048);
+    exa.x = __byte_perm(dt.t0, dt.t1, sel[0] & 0xFFFFu);
+    exa.y = __byte_perm(dt.t0, dt.t1, sel[0] >> 16);
+    exa.z = __byte_perm(dt.t0, dt.t1, sel[1] & 0xFFFFu);
+    exa.w = __byte_perm(dt.t0, dt.t1, sel[1] >> 16);
+    exb.x = __byte_perm(dt.t0, dt.t1, sel[2] & 0xFFFFu);
+    exb.y = __byte_perm(dt.t0, dt.t1, sel[2] >> 16);
+    exb.z = __byte_perm(dt.t0, dt.t1, sel[3] & 0xFFFFu);
+    exb.w = __byte_perm(dt.t0, dt.t1, sel[3] >> 16);
   }
   const uint32_t total = __shfl_sync(kFull, inc, 31);
   if (z) {
     uint4* sp = reinterpret_cast<uint4*>(scratch + lane * 32);
-    sp[0] = make_uint4(ex[0], ex[1], ex[2], ex[3]);
-    sp[1] = make_uint4(ex[4], ex[5], ex[6], ex[7]);
+    sp[0] = exa;
+    sp[1] = exb;
     uint32_t m = z;
     uint8_t* dst = scratch + lane * 32;
     if (first + total <= es.staged) {  // (warp-uniform) every escape of the block is staged
@@ -683,17 +667,18 @@ __device__ __forceinline__ uint32_t decode_one_block(uint32_t tile, uint32_t blk
         rank++;
       }
     }
-    const uint4 a = sp[0], bq = sp[1];
-    ex[0] = a.x; ex[1] = a.y; ex[2] = a.z; ex[3] = a.w;
-    ex[4] = bq.x; ex[5] = bq.y; ex[6] = bq.z; ex[7] = bq.w;
+    exa = sp[0];
+    exb = sp[1];
   }
 #pragma unroll
   for (uint32_t k = 0; k < 4; k++) {
     const uint2 sm = lds64(b + k * 256 + lane * 8);
-    out[k].x = bf16_pair<0>(sm.x, ex[2 * k]);
-    out[k].y = bf16_pair<1>(sm.x, ex[2 * k]);
-    out[k].z = bf16_pair<0>(sm.y, ex[2 * k + 1]);
-    out[k].w = bf16_pair<1>(sm.y, ex[2 * k + 1]);
+    const uint32_t r0 = k == 0 ? exa.x : k == 1 ? exa.z : k == 2 ? exb.x : exb.z;
+    const uint32_t r1 = k == 0 ? exa.y : k == 1 ? exa.w : k == 2 ? exb.y : exb.w;
+    out[k].x = bf16_pair<0>(sm.x, r0);
+    out[k].y = bf16_pair<1>(sm.x, r0);
+    out[k].z = bf16_pair<0>(sm.y, r1);
+    out[k].w = bf16_pair<1>(sm.y, r1);
   }
   return total;
 }
@@ -769,7 +754,7 @@ __device__ __forceinline__ uint32_t launch_epoch(const WsHeader* ws) {
   return e == 0 ? 1u : e;
 }
 
-// Exit protocol of a launch that uses look-back flags: every thread of every
+// Exit protocol of a launch that uses escape-scan flags: every thread of every
 // CTA calls this once, after its last flag access.  The last CTA to leave
 // resets the exit counter and publishes the epoch; when the epoch wraps it
 // clears every flag first, so a flag written 2^32 launches earlier can never
@@ -797,37 +782,6 @@ __device__ __forceinline__ void cta_exit(WsHeader* ws, Flag* flags, uint32_t epo
     ws->epoch = (epoch == 0xFFFFFFFFu) ? 0u : epoch;
     __threadfence();
   }
-}
-
-// After encode_tile: publish the tile's escape count, find its escape offset by
-// look-back, write the offset-table entry, the header parts this tile owns
-// (tile 0: everything but n_esc; last tile: n_esc and table padding) and the
-// escapes themselves.  Tile g of the launch is local tile lt of its tensor,
-// whose first global tile is g - lt.  Warp-wide.
-__device__ __forceinline__ void publish_tile(Flag* flags, uint32_t g, uint32_t lt, uint32_t epoch, const TileEsc& te,
-                                             uint32_t tb, uint8_t* main, uint64_t n, const uint8_t* cb,
-                                             uint8_t* esc, uint64_t esc_cap, int32_t* status, uint32_t hold) {
-  const uint32_t lane = lane_id();
-  if (hold == g + 1) return;  // test hook: this tile stays unpublished
-  const uint64_t ntiles = num_tiles(n);
-  const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
-  uint64_t prefix = 0;
-  if (lt == 0) {
-    if (lane == 0) st_relaxed(&flags[g].incl, tag | te.total);
-  } else {
-    if (lane == 0) st_relaxed(&flags[g].agg, tag | te.total);
-    bool timed_out;
-    prefix = lookback(flags, g, g - lt, epoch, status, &timed_out);
-    if (lane == 0) st_relaxed(&flags[g].incl, tag | static_cast<uint32_t>(prefix + te.total));
-  }
-  if (lane == 0) *reinterpret_cast<uint32_t*>(main + kHeader + 4ull * lt) = static_cast<uint32_t>(prefix);
-  if (lt == 0) write_header_words(main, n, cb);
-  if (lt + 1 == ntiles) {
-    const uint64_t n_esc = prefix + te.total;
-    write_header_tail(main, ntiles, n_esc);
-    if (lane == 0 && n_esc > esc_cap) set_status(status, ZC_ERR_ESCAPE_OVERFLOW);
-  }
-  write_escapes<4>(tb, te, prefix, esc, esc_cap);
 }
 
 // bfloat16 bits of f, rounded to nearest even (IEEE-754 definition: add half

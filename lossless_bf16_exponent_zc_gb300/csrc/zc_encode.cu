@@ -11,8 +11,8 @@
 // CTAs); encoding warp w takes half-tile w of each group.  The group is the
 // unit of the escape scan: the warps' escape counts meet in shared memory,
 // the last encoding warp to finish a group publishes the group's count at
-// once, the 21st "scan" warp finds the group's escape offset with a single-pass
-// decoupled look-back and posts the group's offsets in shared memory.
+// once, the 21st "scan" warp finds the group's escape offset and posts the
+// group's offsets in shared memory.
 //
 // CTAs drift apart by several rounds (the order in which HBM serves their
 // loads), and a group's offset is known only once every group before it is
@@ -24,9 +24,10 @@
 // and at the end.  A stage is refilled as soon as its data is encoded; a unit
 // with more escapes than a ring share waits for its offsets and writes them
 // from the stage itself.  The scan warp knows the inclusive offset of its own
-// previous group, so a look-back needs only the aggregates of the C - 1 groups
-// in between, which are published without waiting on anyone.  The cooperative
-// launch guarantees every group owner is resident, which the waits rely on.
+// previous group, so it needs only the counts of the C - 1 groups in between,
+// which their encoders publish without waiting on anyone; it adds them up
+// while its own CTA is still encoding the group.  The cooperative launch
+// guarantees every group owner is resident, which the waits rely on.
 #include "zc_device.cuh"
 #include "zc_internal.h"
 
@@ -38,7 +39,7 @@ constexpr int kEncStages = 2;
 constexpr uint32_t kUnitBlocks = 2;             // blocks per warp unit (half a tile)
 constexpr uint32_t kUnitElems = kUnitBlocks * kBlock;
 constexpr uint32_t kUnitsPerTile = kTile / kUnitElems;
-constexpr uint32_t kGroupUnits = kEncWarps;     // units per look-back group (one per encoding warp)
+constexpr uint32_t kGroupUnits = kEncWarps;     // units per scan group (one per encoding warp)
 constexpr uint32_t kGroupTiles = kGroupUnits / kUnitsPerTile;
 constexpr uint32_t kEncStageBytes = kUnitElems * 2;  // 4096
 constexpr int kEncSlots = 16;                   // rounds in flight per warp (round slot = round mod 16)
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   }
 
   if (warp == kEncWarps) {
-    // ---------------- scan warp: one decoupled look-back per group
+    // ---------------- scan warp: the escape offsets of each group
     int cur_ti = -1;
     bool cb_ok = true;
     int64_t prev_G = -1;     // this CTA's previous group ...
@@ -174,25 +175,22 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
 #pragma unroll
           for (int b = a + 1; b < 7; b++) cb_ok &= __ldg(cb + a) != __ldg(cb + b);
       }
+      // the groups between this CTA's previous group and G: their counts are
+      // published by their encoders, so this overlaps the CTA's own encoding
+      const uint32_t g0 = p.group_start[ti];
+      const bool own = prev_G >= static_cast<int64_t>(g0);  // previous group of this CTA, same tensor
+      uint64_t prefix = 0;
+      if (cb_ok) {
+        bool timed_out;
+        prefix = (own ? prev_incl : 0) +
+                 window_sum(p.flags, own ? static_cast<uint32_t>(prev_G) + 1 : g0, G, epoch, p.status, &timed_out);
+      }
       mbar_wait_bounded(&rs->cnt_bar[r], ph, p.status);
       if (lane == 0) rs->agg[r] = 0;  // every warp has added to it; ready for round j + kEncSlots
-      const uint32_t gl = G - p.group_start[ti];
       const uint32_t c = lane < kGroupUnits ? rs->cnt[r][lane] : 0u;
       const uint32_t inc = warp_inclusive_scan(c);
-      const uint32_t agg = __shfl_sync(kFull, inc, 31);
-      uint64_t prefix = 0;
-      if (cb_ok && hold != G + 1) {
-        const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
-        if (gl != 0) {  // (the group's count is already published by its last encoding warp)
-          bool timed_out;
-          const uint32_t g0 = G - gl;
-          const bool own = prev_G >= static_cast<int64_t>(g0);  // previous group of this CTA, same tensor
-          prefix = lookback(p.flags, G, g0, epoch, p.status, &timed_out, own ? prev_G : -1, own ? prev_incl : 0);
-          if (lane == 0) st_relaxed(&p.flags[G].incl, tag | static_cast<uint32_t>(prefix + agg));
-        }
-        prev_G = G;
-        prev_incl = prefix + agg;
-      }
+      prev_G = G;
+      prev_incl = prefix + __shfl_sync(kFull, inc, 31);
       if (lane < kGroupUnits) rs->uprefix[r][lane] = prefix + (inc - c);
       __syncwarp();
       if (lane == 0) mbar_arrive(&rs->pre_bar[r]);  // release: the offsets are visible to waiters
@@ -317,10 +315,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
         if ((old >> 16) == kEncWarps - 1 && cb_ok && hold != G + 1) {
           const uint32_t agg = (old & 0xFFFFu) + cnt;
           const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
-          if (G == p.group_start[ti])
-            st_relaxed(&p.flags[G].incl, tag | agg);  // first group of its tensor: nothing before it
-          else
-            st_relaxed(&p.flags[G].agg, tag | agg);
+          st_relaxed(&p.flags[G].agg, tag | agg);
         }
         mbar_arrive(&rs->cnt_bar[r]);  // release: the count is visible to the scan warp
       }

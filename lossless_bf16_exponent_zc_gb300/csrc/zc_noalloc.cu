@@ -64,7 +64,7 @@ extern "C" zc_status zc_compress_noalloc(const void* d_in, uint64_t n, const uin
   zc::DeviceInfo dev;
   if (zc::device_info(&dev) != cudaSuccess) return ZC_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The scratch keeps whatever the previous call left.  The look-back flags
+  // The scratch keeps whatever the previous call left.  The escape-scan flags
   // are tagged with a launch epoch kept in the scratch itself, so stale flags
   // never match; the two counters that must start at zero (the test hook and
   // the exit count) are cleared here.  A call that overlaps another on the GPU

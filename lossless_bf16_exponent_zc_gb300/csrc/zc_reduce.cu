@@ -18,9 +18,9 @@
 //     block of the result from shared memory.
 //   * With re-encoding, 1 scan warp runs the escape scan of the output exactly
 //     like the encoder: the last warp of a group publishes the group's count,
-//     the scan warp finds the group's offset by a decoupled look-back from its
-//     own previous group, and the consumers write their escapes one round
-//     later.  The cooperative launch keeps every group owner resident.
+//     the scan warp adds the counts of the groups since its own previous
+//     group to that group's inclusive offset, and the consumers write their
+//     escapes one round later.  The cooperative launch keeps every group owner resident.
 #include "zc_device.cuh"
 #include "zc_internal.h"
 
@@ -38,7 +38,7 @@ constexpr uint32_t kRedEscCap = 512;              // staged input escape bytes p
 constexpr uint32_t kRedStageBytes = kTileBytes + kRedEscCap;
 constexpr uint32_t kRedEbuf = 512;                // staged output escapes per block and round
 constexpr int kRedSlots = 2;                      // rounds in flight for the output offsets
-constexpr uint32_t kGroupTilesR = kRedTeams;      // tiles per look-back group
+constexpr uint32_t kGroupTilesR = kRedTeams;      // tiles per escape-scan group
 // Shared-memory layout after 1 KB alignment.
 constexpr uint32_t kRSpread = 0;      // decode spread tables, 3 x 1 KB
 constexpr uint32_t kRLut = 3072;      // encoder LUT of the output codebook, 1 KB aligned
@@ -277,29 +277,24 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
         }
     }
   } else if (warp == kRedScan) {
-    // ---------------- scan warp (re-encoding): one look-back per group of output tiles
+    // ---------------- scan warp (re-encoding): the escape offsets of each group of output tiles
     if (REENC) {
       int64_t prev_G = -1;
       uint64_t prev_incl = 0;
       uint32_t j = 0;
       for (uint32_t G = blockIdx.x; G < ngroups; G += step, j++) {
         const int sl = static_cast<int>(j & 1u);
+        // the groups between this CTA's previous group and G (their counts are
+        // published by their consumers), added while this CTA still works on G
+        bool timed_out;
+        const uint64_t prefix =
+            prev_incl + window_sum(p.flags, static_cast<uint32_t>(prev_G + 1), G, epoch, p.status, &timed_out);
         mbar_wait_bounded(&rs->cnt_bar[sl], (j >> 1) & 1u, p.status);
         if (lane == 0) rs->agg[sl] = 0;
         const uint32_t c = lane < kRedCons ? rs->cnt[sl][lane] : 0u;
         const uint32_t inc = warp_inclusive_scan(c);
-        const uint32_t agg = __shfl_sync(kFull, inc, 31);
-        uint64_t prefix = 0;
-        if (hold != G + 1) {
-          const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
-          if (G != 0) {  // (the group's count is already published by its last consumer warp)
-            bool timed_out;
-            prefix = lookback(p.flags, G, 0, epoch, p.status, &timed_out, prev_G, prev_incl);
-            if (lane == 0) st_relaxed(&p.flags[G].incl, tag | static_cast<uint32_t>(prefix + agg));
-          }
-          prev_G = G;
-          prev_incl = prefix + agg;
-        }
+        prev_G = G;
+        prev_incl = prefix + __shfl_sync(kFull, inc, 31);
         if (lane < kRedCons) rs->uprefix[sl][lane] = prefix + (inc - c);
         __syncwarp();
         if (lane == 0) mbar_arrive(&rs->pre_bar[sl]);
@@ -430,10 +425,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
           if ((old >> 16) == kRedCons - 1 && hold != G + 1) {
             const uint32_t agg = (old & 0xFFFFu) + cur.te.total;
             const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
-            if (G == 0)
-              st_relaxed(&p.flags[G].incl, tag | agg);
-            else
-              st_relaxed(&p.flags[G].agg, tag | agg);
+            st_relaxed(&p.flags[G].agg, tag | agg);
           }
           mbar_arrive(&rs->cnt_bar[sl]);
         }
