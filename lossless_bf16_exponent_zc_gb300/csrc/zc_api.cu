@@ -175,7 +175,7 @@ zc_status zc_histogram_topk(const void* d_in, uint64_t n, uint8_t* d_cb_out, uin
   DeviceInfo dev;
   if (device_info(&dev) != cudaSuccess) return ZC_ERR_CUDA;
   return cuda_status(launch_histogram(static_cast<const uint16_t*>(d_in), n, d_cb_out, d_hist_out, ws_header(d_ws),
-                                      as_stream(stream), dev));
+                                      d_status, as_stream(stream), dev));
 }
 
 static zc_status validate_encode_tensor(const void* in, uint64_t n, const uint8_t* cb, const void* main,

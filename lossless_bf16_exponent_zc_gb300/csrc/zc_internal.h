@@ -73,6 +73,6 @@ cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out,
                           int32_t* status, cudaStream_t stream, const DeviceInfo& dev);
 
 cudaError_t launch_histogram(const uint16_t* in, uint64_t n, uint8_t* cb_out, uint32_t* hist_out, WsHeader* ws,
-                             cudaStream_t stream, const DeviceInfo& dev);
+                             int32_t* status, cudaStream_t stream, const DeviceInfo& dev);
 
 }  // namespace zc
