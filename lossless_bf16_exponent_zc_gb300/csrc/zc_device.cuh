@@ -754,28 +754,30 @@ __device__ __forceinline__ uint32_t launch_epoch(const WsHeader* ws) {
   return e == 0 ? 1u : e;
 }
 
-// Exit protocol of a launch that uses escape-scan flags: every thread of every
-// CTA calls this once, after its last flag access.  The last CTA to leave
-// resets the exit counter and publishes the epoch; when the epoch wraps it
-// clears every flag first, so a flag written 2^32 launches earlier can never
-// pass for a current one.  One atomic per CTA.
-__device__ __forceinline__ void cta_exit(WsHeader* ws, Flag* flags, uint32_t epoch, uint32_t total_tiles) {
-  __shared__ int last;
-  __syncthreads();
-  if (threadIdx.x == 0) {
+// Exit protocol of a launch that uses escape-scan flags, run by each CTA's
+// scan warp once the CTA's last escape offsets are posted: from then on the
+// CTA neither reads nor writes a flag (its units' counts were published
+// before they reached the scan warp) and has read the epoch and the test hook
+// long ago, so the rest of the CTA may still be writing escapes.  The last
+// CTA to get here resets the exit counter and the test hook and publishes the
+// epoch; when the epoch wraps it clears every flag first, so a flag written
+// 2^32 launches earlier can never pass for a current one.  One atomic per CTA.
+__device__ __forceinline__ void scan_exit(WsHeader* ws, Flag* flags, uint32_t epoch, uint32_t total_units) {
+  const uint32_t lane = lane_id();
+  int last = 0;
+  if (lane == 0) {
     __threadfence();
     last = atomicAdd(&ws->exited, 1u) == gridDim.x - 1;
   }
-  __syncthreads();
-  if (!last) return;
+  if (!__shfl_sync(kFull, last, 0)) return;
   __threadfence();
-  const uint32_t maxt = max(*reinterpret_cast<volatile uint32_t*>(&ws->max_tiles), total_tiles);
+  const uint32_t maxt = max(*reinterpret_cast<volatile uint32_t*>(&ws->max_tiles), total_units);
   if (epoch == 0xFFFFFFFFu) {
-    for (uint32_t i = threadIdx.x; i < maxt; i += blockDim.x) flags[i] = Flag{0ull, 0ull};
+    for (uint32_t i = lane; i < maxt; i += 32) flags[i] = Flag{0ull, 0ull};
     __threadfence();
-    __syncthreads();
+    __syncwarp();
   }
-  if (threadIdx.x == 0) {
+  if (lane == 0) {
     ws->max_tiles = maxt;
     ws->exited = 0;
     ws->hold_tile = 0;

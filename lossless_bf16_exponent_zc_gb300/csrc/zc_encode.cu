@@ -114,8 +114,6 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;  // 1 KB aligned shared address
   uint8_t* gbase = smem + (sbase - smem_u32(smem));           // its generic pointer
   RoundShared* rs = reinterpret_cast<RoundShared*>(gbase + kEncGrpOff);
-  const uint32_t epoch = launch_epoch(p.ws);
-  const uint32_t hold = launch_hold(p.ws);
   const uint32_t step = gridDim.x;
 
   if (threadIdx.x == 0) {
@@ -134,12 +132,53 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   uint8_t* ring = gbase + kEncRingOff + w * kEncRing;
   uint8_t* wstage = gbase + kEncStageOff + w * kEncStages * kEncStageBytes;
   const uint32_t wstage_s = sbase + kEncStageOff + w * kEncStages * kEncStageBytes;
-  if (warp < kEncWarps && lane == 0) {
+  auto stage_ptr = [&](int s) { return reinterpret_cast<uint16_t*>(wstage + s * kEncStageBytes); };
+  // This warp's unit of group G: tensor ti, local tile lt, half (warp & 1);
+  // false if the group (the last of its tensor) has fewer tiles.
+  auto my_unit = [&](uint32_t G, uint32_t& ti, uint32_t& lt) {
+    ti = locate_group(p, G);
+    lt = (G - p.group_start[ti]) * kGroupTiles + warp / kUnitsPerTile;
+    return static_cast<uint64_t>(lt) < num_tiles(p.t[ti].n);
+  };
+  const uint32_t half = warp % kUnitsPerTile;
+  // valid elements of this warp's unit in tile lt
+  auto unit_valid = [&](const EncTensor& T, uint32_t lt) -> uint32_t {
+    const uint64_t start = static_cast<uint64_t>(lt) * kTile + half * kUnitElems;
+    return T.n <= start ? 0u : (T.n - start >= kUnitElems ? kUnitElems : static_cast<uint32_t>(T.n - start));
+  };
+  auto issue = [&](int s, uint32_t G) {
+    if (G >= p.total_groups) return;
+    uint32_t ti, lt;
+    if (!my_unit(G, ti, lt)) return;
+    const EncTensor& T = p.t[ti];
+    if (lane == 0) {
+      if (unit_valid(T, lt) == kUnitElems) {
+        fence_proxy_async();
+        mbar_arrive_expect_tx(&bar[s], kEncStageBytes);
+        tma_load_1d(stage_ptr(s), T.in + static_cast<uint64_t>(lt) * kTile + half * kUnitElems, kEncStageBytes,
+                    &bar[s]);
+      } else {
+        mbar_arrive(&bar[s]);  // ragged end of the tensor: filled by plain loads when consumed
+      }
+    }
+  };
+  // Each encoding warp starts its first two loads before anything reads global
+  // memory (the epoch, the test hook, codebooks), so HBM is busy from the start.
+  if (warp < kEncWarps) {
+    if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < kEncStages; s++) mbar_init(&bar[s], 1);
+      for (int s = 0; s < kEncStages; s++) mbar_init(&bar[s], 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+#pragma unroll
+    for (int s = 0; s < kEncStages; s++) issue(s, blockIdx.x + s * step);
   }
-  if (lane == 0) fence_mbar_init();
+  // (thread 0's round barriers were initialised before its fence above; no
+  // fence after the copies: a release fence would wait for them)
   __syncthreads();
+  const uint32_t epoch = launch_epoch(p.ws);
+  const uint32_t hold = launch_hold(p.ws);
 
   // Tensors without tiles still get a header.
   if (blockIdx.x == 0 && warp == 0) {
@@ -195,38 +234,9 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(&rs->pre_bar[r]);  // release: the offsets are visible to waiters
     }
+    scan_exit(p.ws, p.flags, epoch, p.total_groups);
   } else {
     // ---------------- encoding warps: unit `warp` of every group
-    auto stage_ptr = [&](int s) { return reinterpret_cast<uint16_t*>(wstage + s * kEncStageBytes); };
-    // This warp's unit of group G: tensor ti, local tile lt, half (warp & 1);
-    // false if the group (the last of its tensor) has fewer tiles.
-    auto my_unit = [&](uint32_t G, uint32_t& ti, uint32_t& lt) {
-      ti = locate_group(p, G);
-      lt = (G - p.group_start[ti]) * kGroupTiles + warp / kUnitsPerTile;
-      return static_cast<uint64_t>(lt) < num_tiles(p.t[ti].n);
-    };
-    const uint32_t half = warp % kUnitsPerTile;
-    // valid elements of this warp's unit in tile lt
-    auto unit_valid = [&](const EncTensor& T, uint32_t lt) -> uint32_t {
-      const uint64_t start = static_cast<uint64_t>(lt) * kTile + half * kUnitElems;
-      return T.n <= start ? 0u : (T.n - start >= kUnitElems ? kUnitElems : static_cast<uint32_t>(T.n - start));
-    };
-    auto issue = [&](int s, uint32_t G) {
-      if (G >= p.total_groups) return;
-      uint32_t ti, lt;
-      if (!my_unit(G, ti, lt)) return;
-      const EncTensor& T = p.t[ti];
-      if (lane == 0) {
-        if (unit_valid(T, lt) == kUnitElems) {
-          fence_proxy_async();
-          mbar_arrive_expect_tx(&bar[s], kEncStageBytes);
-          tma_load_1d(stage_ptr(s), T.in + static_cast<uint64_t>(lt) * kTile + half * kUnitElems, kEncStageBytes,
-                      &bar[s]);
-        } else {
-          mbar_arrive(&bar[s]);  // ragged end of the tensor: filled by plain loads when consumed
-        }
-      }
-    };
     // Second half of round k, once its offsets are posted (slot k mod 16):
     // the offset-table entry and header parts of unit (ti, lt); returns the
     // unit's escape offset.
@@ -264,9 +274,6 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
       }
       __syncwarp();
     };
-
-#pragma unroll
-    for (int s = 0; s < kEncStages; s++) issue(s, blockIdx.x + s * step);
 
     uint32_t phase = 0;
     int cur_ti = -1;
@@ -360,7 +367,6 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
     }
     while (fin < j) finish(fin++);  // drain
   }
-  cta_exit(p.ws, p.flags, epoch, p.total_groups);
 }
 
 template <int MAXB>

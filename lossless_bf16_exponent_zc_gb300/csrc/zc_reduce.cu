@@ -299,6 +299,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
         __syncwarp();
         if (lane == 0) mbar_arrive(&rs->pre_bar[sl]);
       }
+      scan_exit(p.ws, p.flags, epoch, ngroups);
     }
   } else {
     // ---------------- consumers: team t, block b
@@ -436,7 +437,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     }
     if (REENC && j > 0 && !prev.done) finish(j - 1, prev);
   }
-  if (REENC) cta_exit(p.ws, p.flags, epoch, ngroups);
+  if (REENC && skip && warp == kRedScan) scan_exit(p.ws, p.flags, epoch, ngroups);  // (nothing was run)
 }
 
 cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out, const uint8_t* out_cb,
