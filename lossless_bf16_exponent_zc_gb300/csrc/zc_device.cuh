@@ -555,6 +555,7 @@ __device__ __forceinline__ uint32_t decode_block(uint32_t tile, uint32_t blk, ui
   const uint32_t inc = warp_inclusive_scan(c);
   uint32_t rank = run + inc - c;
   run += __shfl_sync(kFull, inc, 31);
+  const uint32_t run_end = run;  // the tile-local rank just past the block's escapes
 
   // rotated exponents of the 32 elements, 4 per word: word 2k = elements 0..3 of group k,
   // word 2k + 1 = elements 4..7 (exa holds words 0..3, exb words 4..7)
@@ -573,21 +574,30 @@ __device__ __forceinline__ uint32_t decode_block(uint32_t tile, uint32_t blk, ui
     exb.z = __byte_perm(dt.t0, dt.t1, sel[3] & 0xFFFFu);
     exb.w = __byte_perm(dt.t0, dt.t1, sel[3] >> 16);
   }
-  if (__any_sync(kFull, z != 0)) {
+  if (z) {
     // patch escapes through shared memory (bit p of z <-> byte p of ex)
     uint4* sp = reinterpret_cast<uint4*>(scratch + lane * 32);
     sp[0] = exa;
     sp[1] = exb;
     uint32_t m = z;
-    while (m) {
-      const uint32_t p = __ffs(m) - 1;
-      m &= m - 1;
-      scratch[lane * 32 + p] = static_cast<uint8_t>(rot_exp(esc_byte(es, rank)));
-      rank++;
+    uint8_t* dst = scratch + lane * 32;
+    if (run_end <= es.staged) {  // (warp-uniform) every escape of the block is staged
+      const uint8_t* src = es.smem + rank;
+      do {
+        const uint32_t p = __ffs(m) - 1;
+        m &= m - 1;
+        dst[p] = static_cast<uint8_t>(rot_exp(*src++));
+      } while (m);
+    } else {
+      while (m) {
+        const uint32_t p = __ffs(m) - 1;
+        m &= m - 1;
+        dst[p] = static_cast<uint8_t>(rot_exp(esc_byte(es, rank)));
+        rank++;
+      }
     }
     exa = sp[0];
     exb = sp[1];
-    __syncwarp();
   }
 #pragma unroll
   for (uint32_t k = 0; k < 4; k++) {
