@@ -75,12 +75,13 @@ __device__ __forceinline__ HdrInfo read_header(const DecTensor& T, int ti, int32
   return h;
 }
 
+// Tensor of global tile g.  Every caller visits tiles in increasing order, so
+// it keeps a running index (`ti`, starting at 0) and only moves it forward.
 template <int MAXB>
-__device__ __forceinline__ uint32_t dec_locate(const DecParams<MAXB>& p, uint32_t g) {
-  uint32_t ti = 0;
+__device__ __forceinline__ uint32_t dec_locate(const DecParams<MAXB>& p, uint32_t g, uint32_t& ti) {
   if (MAXB > 1)
     while (static_cast<int>(ti) + 1 < p.count && g >= p.tile_start[ti + 1]) ti++;
-  return ti;
+  return MAXB > 1 ? ti : 0u;
 }
 
 // Escape range [a, b) of local tile lt, or ok = false when the table is corrupt.
@@ -144,8 +145,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   issue_hdr.ti = -1;
   uint32_t st_a[kDecStages], st_cnt[kDecStages], st_staged[kDecStages];
   bool st_ok[kDecStages];
+  uint32_t issue_ti = 0;  // running tensor index of issue()
   auto issue = [&](int s, uint32_t g) {
-    const uint32_t ti = dec_locate(p, g);
+    const uint32_t ti = dec_locate(p, g, issue_ti);
     const DecTensor& T = p.t[ti];
     if (issue_hdr.ti != static_cast<int>(ti)) issue_hdr = read_header(T, ti, p.status);
     const uint32_t lt = g - p.tile_start[ti];
@@ -173,13 +175,14 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
 
   HdrInfo hdr;
   hdr.ti = -1;
+  uint32_t run_ti = 0;
   uint32_t phase = 0;
   for (uint32_t g0 = gw; g0 < p.total_tiles; g0 += kDecStages * total_warps) {
 #pragma unroll
     for (int s = 0; s < kDecStages; s++) {
       const uint32_t g = g0 + s * total_warps;
       if (g >= p.total_tiles) break;
-      const uint32_t ti = dec_locate(p, g);
+      const uint32_t ti = dec_locate(p, g, run_ti);
       const DecTensor& T = p.t[ti];
       if (hdr.ti != static_cast<int>(ti)) hdr = read_header(T, ti, p.status);
       const uint32_t lt = g - p.tile_start[ti];

@@ -70,12 +70,13 @@ struct EncParams {
   int32_t* status;
 };
 
+// Tensor of global group G.  Every caller visits groups in increasing order,
+// so it keeps a running index (`ti`, starting at 0) and only moves it forward.
 template <int MAXB>
-__device__ __forceinline__ uint32_t locate_group(const EncParams<MAXB>& p, uint32_t G) {
-  uint32_t ti = 0;
+__device__ __forceinline__ uint32_t locate_group(const EncParams<MAXB>& p, uint32_t G, uint32_t& ti) {
   if (MAXB > 1)
     while (static_cast<int>(ti) + 1 < p.count && G >= p.group_start[ti + 1]) ti++;
-  return ti;
+  return MAXB > 1 ? ti : 0u;
 }
 
 // CTA bookkeeping of the rounds in flight (slot = round mod 16).  A warp
@@ -135,8 +136,8 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   auto stage_ptr = [&](int s) { return reinterpret_cast<uint16_t*>(wstage + s * kEncStageBytes); };
   // This warp's unit of group G: tensor ti, local tile lt, half (warp & 1);
   // false if the group (the last of its tensor) has fewer tiles.
-  auto my_unit = [&](uint32_t G, uint32_t& ti, uint32_t& lt) {
-    ti = locate_group(p, G);
+  auto my_unit = [&](uint32_t G, uint32_t& ti, uint32_t& lt, uint32_t& run_ti) {
+    ti = locate_group(p, G, run_ti);
     lt = (G - p.group_start[ti]) * kGroupTiles + warp / kUnitsPerTile;
     return static_cast<uint64_t>(lt) < num_tiles(p.t[ti].n);
   };
@@ -146,10 +147,11 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
     const uint64_t start = static_cast<uint64_t>(lt) * kTile + half * kUnitElems;
     return T.n <= start ? 0u : (T.n - start >= kUnitElems ? kUnitElems : static_cast<uint32_t>(T.n - start));
   };
+  uint32_t issue_ti = 0;  // running tensor index of issue()
   auto issue = [&](int s, uint32_t G) {
     if (G >= p.total_groups) return;
     uint32_t ti, lt;
-    if (!my_unit(G, ti, lt)) return;
+    if (!my_unit(G, ti, lt, issue_ti)) return;
     const EncTensor& T = p.t[ti];
     if (lane == 0) {
       if (unit_valid(T, lt) == kUnitElems) {
@@ -198,13 +200,14 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
     // ---------------- scan warp: the escape offsets of each group
     int cur_ti = -1;
     bool cb_ok = true;
+    uint32_t run_ti = 0;
     int64_t prev_G = -1;     // this CTA's previous group ...
     uint64_t prev_incl = 0;  // ... and its inclusive escape offset
     uint32_t j = 0;
     for (uint32_t G = blockIdx.x; G < p.total_groups; G += step, j++) {
       const int r = static_cast<int>(j % kEncSlots);  // round slot
       const uint32_t ph = (j / kEncSlots) & 1u;       // its barrier phase
-      const uint32_t ti = locate_group(p, G);
+      const uint32_t ti = locate_group(p, G, run_ti);
       if (static_cast<int>(ti) != cur_ti) {
         cur_ti = static_cast<int>(ti);
         const uint8_t* cb = p.t[ti].cb;
@@ -278,6 +281,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
     uint32_t phase = 0;
     int cur_ti = -1;
     bool cb_ok = true;
+    uint32_t run_ti = 0;
     uint32_t fin = 0;   // oldest round not finished; rounds fin .. j - 1 are queued
     uint32_t head = 0;  // ring bytes allocated so far (running count)
     uint32_t j = 0;
@@ -286,7 +290,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
       const int s = static_cast<int>(j & 1u);
       if (j - fin == kEncSlots) finish(fin++);  // slot r is still held by round j - 16
       uint32_t ti, lt;
-      bool has = my_unit(G, ti, lt);
+      bool has = my_unit(G, ti, lt, run_ti);
       EscBook<kUnitBlocks> te;
       te.total = 0;
       const EncTensor& T = p.t[ti];
