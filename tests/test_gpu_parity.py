@@ -252,10 +252,10 @@ def test_config_moe_payload_chunks(zc):
     assert np.array_equal(np.concatenate([host_u16(o.bf16) for o in outs]), x)
 
 
-def _reduce_case(zc, P, m, sigma=1e-3, reencode=True, seed=5):
+def _reduce_case(zc, P, m, sigma=1e-3, reencode=True, seed=5, cb_in=None, cb_out=None):
     shards = workloads.rs_shards(P=P, m=m, sigma=sigma, seed=seed)
-    cb_in = oracle.codebook_from_sigma(sigma)
-    cb_out = oracle.codebook_from_sigma(sigma * math.sqrt(P))
+    cb_in = oracle.codebook_from_sigma(sigma) if cb_in is None else cb_in
+    cb_out = oracle.codebook_from_sigma(sigma * math.sqrt(P)) if cb_out is None else cb_out
     st = zc.new_status()
     ws = zc.workspace(m)
     mains, escs, omains, oescs = [], [], [], []
@@ -283,6 +283,18 @@ def _reduce_case(zc, P, m, sigma=1e-3, reencode=True, seed=5):
 @pytest.mark.parametrize("reencode", [True, False])
 def test_decompress_reduce_small(zc, P, m, reencode):
     _reduce_case(zc, P, m, reencode=reencode, seed=P * 7 + m % 13)
+
+
+FAR_CODEBOOK = np.array([1, 2, 3, 4, 5, 6, 7], dtype=np.uint8)  # no N(0, 1e-3) value has these exponents
+
+
+@pytest.mark.parametrize("far_in,far_out", [(True, False), (False, True), (True, True)])
+def test_decompress_reduce_all_escape(zc, far_in, far_out):
+    """Every input and/or every output value an escape: input tiles carry 4096 escape bytes, more than a
+    stage holds (the rest is read from global memory), and every re-encoded block has more escapes than its
+    staging buffer (written from the rounded tile instead)."""
+    _reduce_case(zc, 3, 5 * 4096 + 123, seed=91, cb_in=FAR_CODEBOOK if far_in else None,
+                 cb_out=FAR_CODEBOOK if far_out else None)
 
 
 def test_decompress_reduce_special_values(zc):
