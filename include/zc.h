@@ -167,9 +167,10 @@ zc_status zc_histogram_topk(const void* d_in, uint64_t n, uint8_t* d_cb_out, uin
  * over).  The escape count is the header's n_esc; if it exceeds esc_capacity,
  * only the first esc_capacity escapes are stored and *d_status gets
  * ZC_ERR_ESCAPE_OVERFLOW.  A codebook with repeated entries sets
- * ZC_ERR_DUP_CODEBOOK and writes nothing else.  One kernel launch: per-tile
- * escape offsets come from a single-pass decoupled look-back scan whose waits
- * are bounded (ZC_ERR_TIMEOUT).
+ * ZC_ERR_DUP_CODEBOOK and writes nothing else.  One kernel launch: the escape
+ * offsets come from a single-pass scan inside it (each group of tiles adds the
+ * counts published since its block's previous group), whose waits are
+ * bounded (ZC_ERR_TIMEOUT).
  */
 zc_status zc_compress(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_main, void* d_esc,
                       uint64_t esc_capacity, void* d_ws, uint64_t ws_bytes, int32_t* d_status,
@@ -207,10 +208,9 @@ zc_status zc_decompress_reduce(int P, const void* const* h_mains, const void* co
 
 /*
  * zc_compress without a workspace argument, for callers that cannot allocate
- * device memory: code running while a stream is captured into a CUDA graph,
- * hooks of a communication or training framework that receive only the
- * tensors to send, and latency-critical paths that must never call cudaMalloc
- * (it can synchronise the device).  The method pages have no counterpart; it
+ * device memory: hooks of a communication or training framework that receive
+ * only the tensors to send, and latency-critical paths that must never call
+ * cudaMalloc (it can synchronise the device).  The method pages have no counterpart; it
  * is a deployment convenience.  Output is identical to zc_compress.
  *   - The scratch is a fixed 1 MiB + 4 KiB device array inside libzc
  *     (every GPU that loads the library holds it until the process exits), so

@@ -1,8 +1,6 @@
 // zc_noalloc.cu -- zc_compress for callers that cannot allocate device memory.
 //
-// Some callers have no way to provide a workspace: code that runs while a
-// stream is being captured into a CUDA graph (allocation there is either
-// forbidden or would be baked into the graph), hooks invoked by a
+// Some callers have no way to provide a workspace: hooks invoked by a
 // communication or training framework that hands over only the tensors to
 // send, and latency-critical paths that must never call cudaMalloc (it can
 // synchronise the whole device).  For them this file keeps the encoder's

@@ -1,7 +1,7 @@
 """zc_compress_noalloc: the encoder for callers that cannot allocate device memory.
 
-Such callers (code inside a CUDA graph capture, framework hooks that only hand
-over the tensors to send, paths that must never call cudaMalloc) pass no
+Such callers (framework hooks that only hand over the tensors to send, paths
+that must never call cudaMalloc) pass no
 workspace; the library keeps the scratch in a fixed device array of its own.
 This file is collected last so that a run stopping at its first failure has
 already run everything else, and it passes both alone in a fresh process and
