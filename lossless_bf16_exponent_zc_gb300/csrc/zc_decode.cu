@@ -45,7 +45,8 @@ struct HdrInfo {
   DecTable dt;
 };
 
-// Reads and validates a ZC1 header (every lane reads the same bytes).
+// Reads and validates a ZC1 header (one thread; it records a bad header in
+// *status).
 __device__ __forceinline__ HdrInfo read_header(const DecTensor& T, int ti, int32_t* status) {
   HdrInfo h;
   h.ti = ti;
@@ -70,7 +71,7 @@ __device__ __forceinline__ HdrInfo read_header(const DecTensor& T, int ti, int32
     err = ZC_ERR_BAD_HEADER;
   if (n != T.n) err = ZC_ERR_SIZE_MISMATCH;
   h.ok = err == 0;
-  if (!h.ok && lane_id() == 0) set_status(status, err);
+  if (!h.ok) set_status(status, err);
   h.dt = make_dec_table(cb);
   return h;
 }
@@ -129,6 +130,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   uint8_t* wstage = gbase + kDecStageOff + warp * kDecStages * kDecStageBytes;
   const uint32_t wstage_s = sbase + kDecStageOff + warp * kDecStages * kDecStageBytes;
 
+  // every tensor's header, read once per CTA (a warp's tiles cross many tensors)
+  __shared__ HdrInfo hdr_cache[MAXB];
+  for (int i = threadIdx.x; i < p.count; i += blockDim.x) hdr_cache[i] = read_header(p.t[i], i, p.status);
   build_spread_tables(spread);
   if (lane == 0) {
 #pragma unroll
@@ -145,17 +149,19 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   issue_hdr.ti = -1;
   uint32_t st_a[kDecStages], st_cnt[kDecStages], st_staged[kDecStages];
   bool st_ok[kDecStages];
+  DecTable st_dt[kDecStages];  // code table of the staged tile's tensor (read when it was issued)
   uint32_t issue_ti = 0;  // running tensor index of issue()
   auto issue = [&](int s, uint32_t g) {
     const uint32_t ti = dec_locate(p, g, issue_ti);
     const DecTensor& T = p.t[ti];
-    if (issue_hdr.ti != static_cast<int>(ti)) issue_hdr = read_header(T, ti, p.status);
+    if (issue_hdr.ti != static_cast<int>(ti)) issue_hdr = hdr_cache[ti];
     const uint32_t lt = g - p.tile_start[ti];
     uint32_t a, cnt;
     bool ok;
     tile_escape_range(T, issue_hdr, lt, a, cnt, ok);
     if (!ok && issue_hdr.ok && lane == 0) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
     uint8_t* sp = stage_ptr(s);
+    st_dt[s] = issue_hdr.dt;
     st_a[s] = a;
     st_cnt[s] = cnt;
     st_ok[s] = ok;
@@ -173,8 +179,6 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     if (g < p.total_tiles) issue(s, g);
   }
 
-  HdrInfo hdr;
-  hdr.ti = -1;
   uint32_t run_ti = 0;
   uint32_t phase = 0;
   for (uint32_t g0 = gw; g0 < p.total_tiles; g0 += kDecStages * total_warps) {
@@ -184,7 +188,6 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
       if (g >= p.total_tiles) break;
       const uint32_t ti = dec_locate(p, g, run_ti);
       const DecTensor& T = p.t[ti];
-      if (hdr.ti != static_cast<int>(ti)) hdr = read_header(T, ti, p.status);
       const uint32_t lt = g - p.tile_start[ti];
       const uint64_t rem = T.n - static_cast<uint64_t>(lt) * kTile;
       const uint32_t n_tile = rem >= kTile ? kTile : static_cast<uint32_t>(rem);
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
 #pragma unroll 1
         for (uint32_t blk = 0; blk < 4; blk++) {
           uint4 v[4];
-          decode_block(tile_s, blk, n_tile, sbase, hdr.dt, es, run, scratch, v);
+          decode_block(tile_s, blk, n_tile, sbase, st_dt[s], es, run, scratch, v);
 #pragma unroll
           for (uint32_t k = 0; k < 4; k++) store8_guarded(out, blk * kBlock + k * 256 + lane * 8, n_left, v[k]);
         }

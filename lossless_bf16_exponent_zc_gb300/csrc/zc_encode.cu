@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   if (warp == kEncWarps) {
     // ---------------- scan warp: the escape offsets of each group
     int cur_ti = -1;
+    const uint8_t* cur_cb = nullptr;
     bool cb_ok = true;
     uint32_t run_ti = 0;
     int64_t prev_G = -1;     // this CTA's previous group ...
@@ -211,11 +212,14 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
       if (static_cast<int>(ti) != cur_ti) {
         cur_ti = static_cast<int>(ti);
         const uint8_t* cb = p.t[ti].cb;
-        cb_ok = true;
+        if (cb != cur_cb) {  // tensors that share a codebook share the verdict
+          cur_cb = cb;
+          cb_ok = true;
 #pragma unroll
-        for (int a = 0; a < 7; a++)
+          for (int a = 0; a < 7; a++)
 #pragma unroll
-          for (int b = a + 1; b < 7; b++) cb_ok &= __ldg(cb + a) != __ldg(cb + b);
+            for (int b = a + 1; b < 7; b++) cb_ok &= __ldg(cb + a) != __ldg(cb + b);
+        }
       }
       // the groups between this CTA's previous group and G: their counts are
       // published by their encoders, so this overlaps the CTA's own encoding
@@ -280,6 +284,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
 
     uint32_t phase = 0;
     int cur_ti = -1;
+    const uint8_t* cur_cb = nullptr;
     bool cb_ok = true;
     uint32_t run_ti = 0;
     uint32_t fin = 0;   // oldest round not finished; rounds fin .. j - 1 are queued
@@ -295,9 +300,12 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
       te.total = 0;
       const EncTensor& T = p.t[ti];
       if (static_cast<int>(ti) != cur_ti) {
-        cb_ok = build_enc_lut(lut, T.cb);  // every warp of the group reaches the same verdict
         cur_ti = static_cast<int>(ti);
-        if (!cb_ok && lane == 0) set_status(p.status, ZC_ERR_DUP_CODEBOOK);
+        if (T.cb != cur_cb) {  // tensors that share a codebook (same pointer) share the table
+          cb_ok = build_enc_lut(lut, T.cb);  // every warp of the group reaches the same verdict
+          cur_cb = T.cb;
+          if (!cb_ok && lane == 0) set_status(p.status, ZC_ERR_DUP_CODEBOOK);
+        }
       }
       const uint32_t tb_s = wstage_s + s * kEncStageBytes;
       if (has) {
