@@ -285,6 +285,10 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
     uint32_t phase = 0;
     int cur_ti = -1;
     const uint8_t* cur_cb = nullptr;
+    uint64_t cur_n = 0;            // the current tensor's size ...
+    uint32_t cur_ntiles = 0;       // ... tiles ...
+    uint8_t* cur_tiles = nullptr;  // ... first tile ...
+    uint32_t cur_g0 = 0;           // ... and first group
     bool cb_ok = true;
     uint32_t run_ti = 0;
     uint32_t fin = 0;   // oldest round not finished; rounds fin .. j - 1 are queued
@@ -294,23 +298,30 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
       const int r = static_cast<int>(j % kEncSlots);
       const int s = static_cast<int>(j & 1u);
       if (j - fin == kEncSlots) finish(fin++);  // slot r is still held by round j - 16
-      uint32_t ti, lt;
-      bool has = my_unit(G, ti, lt, run_ti);
-      EscBook<kUnitBlocks> te;
-      te.total = 0;
+      const uint32_t ti = locate_group(p, G, run_ti);
       const EncTensor& T = p.t[ti];
-      if (static_cast<int>(ti) != cur_ti) {
+      if (static_cast<int>(ti) != cur_ti) {  // per-tensor values, kept while the tensor lasts
         cur_ti = static_cast<int>(ti);
+        cur_n = T.n;
+        cur_ntiles = static_cast<uint32_t>(num_tiles(cur_n));
+        cur_tiles = T.main + kHeader + table_bytes(cur_ntiles);
+        cur_g0 = p.group_start[ti];
         if (T.cb != cur_cb) {  // tensors that share a codebook (same pointer) share the table
           cb_ok = build_enc_lut(lut, T.cb);  // every warp of the group reaches the same verdict
           cur_cb = T.cb;
           if (!cb_ok && lane == 0) set_status(p.status, ZC_ERR_DUP_CODEBOOK);
         }
       }
+      const uint32_t lt = (G - cur_g0) * kGroupTiles + warp / kUnitsPerTile;
+      bool has = lt < cur_ntiles;
+      EscBook<kUnitBlocks> te;
+      te.total = 0;
       const uint32_t tb_s = wstage_s + s * kEncStageBytes;
       if (has) {
-        const uint32_t nv = unit_valid(T, lt);
-        const uint64_t rem = T.n - static_cast<uint64_t>(lt) * kTile;
+        const uint64_t start = static_cast<uint64_t>(lt) * kTile + half * kUnitElems;
+        const uint32_t nv =
+            cur_n <= start ? 0u : (cur_n - start >= kUnitElems ? kUnitElems : static_cast<uint32_t>(cur_n - start));
+        const uint64_t rem = cur_n - static_cast<uint64_t>(lt) * kTile;
         const uint32_t n_tile = rem >= kTile ? kTile : static_cast<uint32_t>(rem);
         mbar_wait_bounded(&bar[s], (phase >> s) & 1u, p.status);
         phase ^= 1u << s;
@@ -322,7 +333,8 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
         }
         if (cb_ok)
           encode_blocks<kUnitBlocks>(tb_s, half * kUnitBlocks, n_tile, lut_s,
-                                     tile_ptr(T.main, num_tiles(T.n), lt) + half * kUnitBlocks * kBlockBytes, te);
+                                     cur_tiles + static_cast<uint64_t>(lt) * kTileBytes + half * kUnitBlocks * kBlockBytes,
+                                     te);
         else
           has = false;
       }
