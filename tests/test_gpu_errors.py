@@ -1,5 +1,5 @@
 """Device-side error reporting: corrupt or inconsistent streams, escape overflow, bad codebooks and the
-bounded inter-block wait.  Every failure is produced on the host (corrupted bytes, a pre-advanced ticket);
+bounded inter-block wait.  Every failure is produced on the host (corrupted bytes, the workspace's hold hook);
 nothing here faults or hangs the GPU: kernels finish and report through the status word."""
 import numpy as np
 import pytest
@@ -116,9 +116,9 @@ def test_reduce_shard_size_mismatch(zc):
     assert zc.status_value(st) in (zc.ERR_SIZE_MISMATCH, zc.ERR_BAD_HEADER)
 
 
-def test_lookback_wait_is_bounded(zc):
-    """The workspace's hold hook keeps the first look-back unit (a group of 12 tiles) from publishing its
-    flag, so the next group's look-back waits on a flag nobody sets: the wait gives up after about a second
+def test_escape_scan_wait_is_bounded(zc):
+    """The workspace's hold hook keeps the first scan unit (a group of 10 tiles) from publishing its escape
+    count, so the scans that need it wait on a count nobody publishes: the wait gives up after about a second
     with ZC_ERR_TIMEOUT and the kernel returns.  The context stays usable and the counters are reset."""
     import time
     n = 40 * 4096

@@ -350,11 +350,11 @@ def test_workspace_reused_without_rezeroing(zc):
         om, oe = oracle.compress(x, cb)
         assert_stream_equal(gm, ge, om, oe)
     hdr = host_u8(ws[:16]).view(np.uint32)
-    assert hdr[0] == 0 and hdr[1] == 0 and hdr[2] == 5   # ticket, exit count reset; epoch = launches
+    assert hdr[0] == 0 and hdr[1] == 0 and hdr[2] == 5   # test hook, exit count reset; epoch = launches
 
 
 def test_epoch_wraparound(zc):
-    """The look-back epoch tag wraps after 2^32 - 1 launches; the wrap clears every flag first.
+    """The escape-scan epoch tag wraps after 2^32 - 1 launches; the wrap clears every flag first.
 
     The first launch leaves flags tagged with epoch 1 holding other escape
     counts; if the wrap did not clear them, the launch tagged 1 after the wrap
