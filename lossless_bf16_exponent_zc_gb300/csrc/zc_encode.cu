@@ -134,31 +134,31 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   uint8_t* wstage = gbase + kEncStageOff + w * kEncStages * kEncStageBytes;
   const uint32_t wstage_s = sbase + kEncStageOff + w * kEncStages * kEncStageBytes;
   auto stage_ptr = [&](int s) { return reinterpret_cast<uint16_t*>(wstage + s * kEncStageBytes); };
-  // This warp's unit of group G: tensor ti, local tile lt, half (warp & 1);
-  // false if the group (the last of its tensor) has fewer tiles.
-  auto my_unit = [&](uint32_t G, uint32_t& ti, uint32_t& lt, uint32_t& run_ti) {
-    ti = locate_group(p, G, run_ti);
-    lt = (G - p.group_start[ti]) * kGroupTiles + warp / kUnitsPerTile;
-    return static_cast<uint64_t>(lt) < num_tiles(p.t[ti].n);
-  };
-  const uint32_t half = warp % kUnitsPerTile;
-  // valid elements of this warp's unit in tile lt
-  auto unit_valid = [&](const EncTensor& T, uint32_t lt) -> uint32_t {
-    const uint64_t start = static_cast<uint64_t>(lt) * kTile + half * kUnitElems;
-    return T.n <= start ? 0u : (T.n - start >= kUnitElems ? kUnitElems : static_cast<uint32_t>(T.n - start));
-  };
+  const uint32_t half = warp % kUnitsPerTile;  // this warp's half of each tile of a group
   uint32_t issue_ti = 0;  // running tensor index of issue()
+  // issue()'s view of its current tensor, kept while the tensor lasts
+  int issue_cur = -1;
+  uint64_t issue_n = 0;
+  const uint16_t* issue_in = nullptr;
+  uint32_t issue_ntiles = 0, issue_g0 = 0;
   auto issue = [&](int s, uint32_t G) {
     if (G >= p.total_groups) return;
-    uint32_t ti, lt;
-    if (!my_unit(G, ti, lt, issue_ti)) return;
-    const EncTensor& T = p.t[ti];
+    const uint32_t ti = locate_group(p, G, issue_ti);
+    if (static_cast<int>(ti) != issue_cur) {
+      issue_cur = static_cast<int>(ti);
+      issue_n = p.t[ti].n;
+      issue_in = p.t[ti].in;
+      issue_ntiles = static_cast<uint32_t>(num_tiles(issue_n));
+      issue_g0 = p.group_start[ti];
+    }
+    const uint32_t lt = (G - issue_g0) * kGroupTiles + warp / kUnitsPerTile;
+    if (lt >= issue_ntiles) return;
     if (lane == 0) {
-      if (unit_valid(T, lt) == kUnitElems) {
+      const uint64_t start = static_cast<uint64_t>(lt) * kTile + half * kUnitElems;
+      if (issue_n >= start + kUnitElems) {
         fence_proxy_async();
         mbar_arrive_expect_tx(&bar[s], kEncStageBytes);
-        tma_load_1d(stage_ptr(s), T.in + static_cast<uint64_t>(lt) * kTile + half * kUnitElems, kEncStageBytes,
-                    &bar[s]);
+        tma_load_1d(stage_ptr(s), issue_in + start, kEncStageBytes, &bar[s]);
       } else {
         mbar_arrive(&bar[s]);  // ragged end of the tensor: filled by plain loads when consumed
       }
