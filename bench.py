@@ -381,7 +381,7 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "u16 bits in, u8 streams (integer path)",
+            "scaling": "weak", "vs_baseline": None, "dtype": "u32",
             "data": "synthetic (seeded)",
             "config": {"workload": WORKLOAD, "elements": n, "codebooks": "exact histogram top-7 and sigma=1e-3",
                        "l2": "inputs (134 MB bf16) larger than the 129 MB L2; no flush",
