@@ -238,7 +238,7 @@ def run_reference(args):
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16 bits / u8 streams",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
         "data": "synthetic (seeded)",
         "config": {"workload": WORKLOAD, "sample": f"first 2^{args.ref_sample_log2} elements per step",
                    "parallelism": "rank 0 only (CPU oracle)"},
