@@ -79,6 +79,11 @@ def _load():
     lib.zo_topk_from_histogram.restype = None
     lib.zo_compress.argtypes = [u16p, ctypes.c_uint64, u8p, u8p, u8p, ctypes.c_uint64, u64p]
     lib.zo_compress.restype = ctypes.c_int
+    lib.zo_raw_spill.argtypes = [ctypes.c_uint64]
+    lib.zo_raw_spill.restype = ctypes.c_uint64
+    lib.zo_compress_adaptive.argtypes = [u16p, ctypes.c_uint64, u8p, u8p, u8p, ctypes.c_uint64, u64p,
+                                         ctypes.POINTER(ctypes.c_int)]
+    lib.zo_compress_adaptive.restype = ctypes.c_int
     lib.zo_decompress.argtypes = [u8p, u8p, ctypes.c_uint64, ctypes.c_uint64, u16p]
     lib.zo_decompress.restype = ctypes.c_int
     lib.zo_float_to_bf16_rne.argtypes = [ctypes.c_float]
@@ -172,6 +177,35 @@ def compress(x, cb, esc_capacity: int | None = None, allow_overflow: bool = Fals
     if rc != OK:
         raise OracleError(rc, "compress")
     return main, esc[: n_esc.value].copy()
+
+
+def raw_spill(n: int) -> int:
+    """Bytes of a RAW stream of n values that go to the escape stream (reading R8)."""
+    return int(_load().zo_raw_spill(n))
+
+
+def compress_adaptive(x, cb, esc_capacity: int | None = None, allow_overflow: bool = False):
+    """Encode, then store RAW when that is strictly smaller (reading R8).
+
+    Returns (main, escapes, raw) with raw = True for a RAW stream, or
+    (main, escapes, raw, rc) with ``allow_overflow`` when neither form fits.
+    """
+    x = _u16(x)
+    cb = _cb(cb)
+    n = x.size
+    cap = n if esc_capacity is None else int(esc_capacity)
+    main = np.zeros(main_bytes(n), np.uint8)
+    esc = np.zeros(max(cap, 1), np.uint8)
+    n_esc = ctypes.c_uint64(0)
+    raw = ctypes.c_int(0)
+    rc = _load().zo_compress_adaptive(_ptr(x, ctypes.c_uint16), n, _ptr(cb, ctypes.c_uint8),
+                                      _ptr(main, ctypes.c_uint8), _ptr(esc, ctypes.c_uint8), cap,
+                                      ctypes.byref(n_esc), ctypes.byref(raw))
+    if rc == ERR_ESCAPE_OVERFLOW and allow_overflow:
+        return main, esc[:min(cap, n_esc.value)].copy(), bool(raw.value), rc
+    if rc != OK:
+        raise OracleError(rc, "compress_adaptive")
+    return main, esc[: n_esc.value].copy(), bool(raw.value)
 
 
 def decompress_status(main, esc, n: int):

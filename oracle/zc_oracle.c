@@ -43,6 +43,16 @@
  *   R7  local reduction = sum (not mean), fp32, rank order 0..P-1, IEEE
  *       round-to-nearest with subnormals kept, then RNE to bf16; a NaN sum
  *       becomes 0x7FC0.
+ *   R8  raw bypass ([CCCL §3.3] tiny tensors are not worth compressing;
+ *       [CCCL §5.2] a ratio near or above 1 means fall back to sending the
+ *       data uncompressed): header flags bit 0 marks a RAW stream.  It holds
+ *       the 2n little-endian bytes of the n values in order: the first
+ *       min(2n, 5632 ntiles) fill the tile region (the rest of it is zero),
+ *       the remaining 2n - 5632 ntiles bytes (the "spill", if any) form the
+ *       escape stream, n_esc = spill, and the offset table is zero.  The main
+ *       stream keeps its size.  The adaptive encoder stores RAW exactly when
+ *       the coded form's escape count exceeds the spill, i.e. when RAW is
+ *       strictly smaller in total.
  *
  * Compile: plain C11, -O2 -ffp-contract=off, no -ffast-math.
  */
@@ -271,11 +281,55 @@ int zo_compress(const uint16_t *x, uint64_t n, const uint8_t cb[7], uint8_t *mai
   return overflow ? O_ERR_ESCAPE_OVERFLOW : O_OK;
 }
 
+/* ---- raw bypass, reading R8 ---------------------------------------------- */
+/* bytes of a RAW stream that do not fit in the tile region */
+uint64_t zo_raw_spill(uint64_t n) {
+  uint64_t region = (uint64_t)O_TILE_BYTES * zo_num_tiles(n);
+  return 2 * n > region ? 2 * n - region : 0;
+}
+
+/* byte k of the raw little-endian image of x */
+static uint8_t raw_byte(const uint16_t *x, uint64_t k) {
+  uint16_t u = x[k / 2];
+  return (uint8_t)(k % 2 == 0 ? u & 0xFFu : u >> 8);
+}
+
+/* Encode like zo_compress, then switch to RAW when that is strictly smaller
+ * (coded escapes > spill) and the spill fits in esc_capacity.  *raw_out = 1
+ * for a RAW stream.  An overflowing coded form that RAW rescues is not an
+ * error; when neither fits, the coded output and ESCAPE_OVERFLOW stand. */
+int zo_compress_adaptive(const uint16_t *x, uint64_t n, const uint8_t cb[7], uint8_t *main_out,
+                         uint8_t *esc_out, uint64_t esc_capacity, uint64_t *n_esc_out,
+                         int *raw_out) {
+  *raw_out = 0;
+  int rc = zo_compress(x, n, cb, main_out, esc_out, esc_capacity, n_esc_out);
+  if (rc != O_OK && rc != O_ERR_ESCAPE_OVERFLOW) return rc;
+  uint64_t spill = zo_raw_spill(n);
+  if (*n_esc_out <= spill || spill > esc_capacity) return rc;
+  uint64_t ntiles = zo_num_tiles(n);
+  uint64_t tbl = table_bytes(ntiles);
+  uint64_t region = (uint64_t)O_TILE_BYTES * ntiles;
+  uint8_t *tiles = main_out + O_HEADER + tbl;
+  memset(main_out + O_HEADER, 0, tbl + region); /* offset table and tile region */
+  for (uint64_t k = 0; k < 2 * n; k++) {
+    if (k < region)
+      tiles[k] = raw_byte(x, k);
+    else
+      esc_out[k - region] = raw_byte(x, k);
+  }
+  put_u16(main_out + 6, 1); /* flags: RAW */
+  put_u64(main_out + 24, spill);
+  *n_esc_out = spill;
+  *raw_out = 1;
+  return O_OK;
+}
+
 /* ---- decode: the inverse of zo_compress, bit for bit --------------------- */
 int zo_decompress(const uint8_t *main_in, const uint8_t *esc_in, uint64_t esc_bytes, uint64_t n,
                   uint16_t *out) {
-  if (get_u32(main_in + 0) != 0x3142435Au || get_u16(main_in + 4) != 1 ||
-      get_u16(main_in + 6) != 0 || get_u32(main_in + 16) != O_TILE)
+  unsigned flags = get_u16(main_in + 6);
+  if (get_u32(main_in + 0) != 0x3142435Au || get_u16(main_in + 4) != 1 || flags > 1 ||
+      get_u32(main_in + 16) != O_TILE)
     return O_ERR_HEADER;
   if (get_u64(main_in + 8) != n) return O_ERR_SIZE;
   uint64_t ntiles = zo_num_tiles(n);
@@ -286,6 +340,19 @@ int zo_decompress(const uint8_t *main_in, const uint8_t *esc_in, uint64_t esc_by
   for (int k = 0; k < 7; k++) cb[k] = main_in[32 + k];
   if (!codebook_is_valid(cb)) return O_ERR_HEADER;
   uint64_t tbl = table_bytes(ntiles);
+
+  if (flags == 1) { /* RAW, reading R8: the bytes in order, tile region then escapes */
+    if (n_esc != zo_raw_spill(n)) return O_ERR_HEADER;
+    uint64_t region = (uint64_t)O_TILE_BYTES * ntiles;
+    const uint8_t *tiles = main_in + O_HEADER + tbl;
+    for (uint64_t i = 0; i < n; i++) {
+      uint64_t k = 2 * i;
+      uint8_t lo = k < region ? tiles[k] : esc_in[k - region];
+      uint8_t hi = k + 1 < region ? tiles[k + 1] : esc_in[k + 1 - region];
+      out[i] = (uint16_t)(lo | hi << 8);
+    }
+    return O_OK;
+  }
 
   for (uint64_t t = 0; t < ntiles; t++) {
     uint64_t start = get_u32(main_in + O_HEADER + 4 * t);
