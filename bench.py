@@ -483,8 +483,9 @@ def _time_ms(torch, fn, reps, warmup=2):
 def run_workloads(args, zc, torch, device, peak):
     """Per-kernel GB/s (uncompressed and algorithmic), HBM fraction, ratio and escape rate for the other
     workloads: the 2^20 Gaussian (L2-resident), the 9-tensor Llama-3-8B bucket (batched), the MoE payload
-    (histogram codebook, 8 Zipf chunks batched), and the reduce-scatter local stage (P = 8) with its
-    shard-size sweep.  Inputs above L2 size are not flushed between repetitions of the same op."""
+    (histogram codebook, 8 Zipf chunks batched), the reduce-scatter local stage (P = 8) with its
+    shard-size sweep, and the raw bypass (adaptive compression of coded and incompressible 2^26 tensors).
+    Inputs above L2 size are not flushed between repetitions of the same op."""
     import math as _m
     out = {}
     st = zc.new_status(device=device)
@@ -603,6 +604,37 @@ def run_workloads(args, zc, torch, device, peak):
     out["reduce_scatter_sweep_P8"] = [{"shard_bytes": r["shard_elements"] * 2, "ms": r["ms"],
                                        "GB_per_s_uncompressed": r["GB_per_s_uncompressed"],
                                        "frac_of_hbm": r["frac_of_hbm"]} for r in sweep]
+    del base
+
+    # 5. raw bypass [CCCL §3.3, §5.2]: adaptive compression of a 2^26 N(0, 1e-3) tensor (stays coded: the cost
+    #    is the device-side decision) and of 2^26 uniformly random bit patterns (stored RAW; its algorithmic
+    #    bytes are those of a copy: read 2n, write the 2n-byte RAW image)
+    n = 1 << 26
+    mb, _ = zc.compressed_size(n)
+    spill = zc.raw_spill(n)
+    ws = zc.workspace(n, device=device)
+    m_t = torch.empty(mb, dtype=torch.uint8, device=device)
+    e_t = torch.empty(n, dtype=torch.uint8, device=device)
+    y = torch.empty(n, dtype=torch.int16, device=device)
+    xt = dev(workloads.gaussian(n, sigma=workloads.RS_SIGMA, seed=6))
+    cbg = zc.codebook_to_device(zc.codebook_from_sigma(workloads.RS_SIGMA), device)
+    tp = _time_ms(torch, lambda: zc.compress(xt, cbg, ws, st, main=m_t, esc=e_t), 20)
+    ta = _time_ms(torch, lambda: zc.compress_adaptive(xt, cbg, ws, st, main=m_t, esc=e_t), 20)
+    k = zc.header_n_esc(m_t)
+    coded = {"compress": entry(tp, 2 * n, 2 * n + mb + k), "compress_adaptive": entry(ta, 2 * n, 2 * n + mb + k),
+             "stored_raw": zc.header_is_raw(m_t), "decision_cost_us": round(1e3 * (ta - tp), 2)}
+    xt = dev(workloads.random_bits(n))
+    ta = _time_ms(torch, lambda: zc.compress_adaptive(xt, cbg, ws, st, main=m_t, esc=e_t), 20)
+    is_raw = zc.header_is_raw(m_t)
+    td = _time_ms(torch, lambda: zc.decompress(m_t, e_t, n, st, out=y), 20)
+    ok = torch.equal(y, xt)
+    out["raw_bypass_2^26"] = {
+        "coded_gaussian": coded,
+        "random_bits": {"compress_adaptive": entry(ta, 2 * n, 4 * n), "decompress": entry(td, 2 * n, 4 * n),
+                        "stored_raw": is_raw, "bytes_sent": mb + spill, "ratio": round(2 * n / (mb + spill), 4),
+                        "round_trip_ok": bool(ok)}}
+    del xt, m_t, e_t, y
+
     if zc.status_value(st) != 0:
         out["status"] = zc.status_string(zc.status_value(st))
     return out

@@ -18,6 +18,9 @@
  *   §2.D  a zipped reduce-scatter is an all-to-all of compressed shards plus a
  *         local reduction; MoE all-to-all sends a fixed-size part first and a
  *         variable-size part after it.
+ * and [CCCL §x] cites the jsqmd.com article on CCCL, an in-GPU
+ * compression-coupled collective communication library: §3.3 (adaptive
+ * choice of whether to compress), §5.2 (falling back to uncompressed data).
  *
  * ------------------------------------------------------------------------
  * Stream format "ZC1" (all integers little-endian)
@@ -50,6 +53,16 @@
  *   a block in ascending plane-bit position (q, j).
  * CODEBOOK: 7 distinct exponent bytes in rank order; codebook[k] <-> code k+1,
  *   code 0 <-> escape.  It travels in the header, so decoding needs no codebook.
+ * RAW streams (header flags bit 0 = ZC_FLAG_RAW): the raw bypass for data the
+ *   coding does not shrink ([CCCL §3.3]: tiny tensors are left uncompressed;
+ *   [CCCL §5.2]: a ratio near or above 1 falls back to the data as is).  The
+ *   main stream keeps its size and header; its offset table is zero; the
+ *   2n little-endian bytes of the values fill the tile region in order
+ *   (5632 * ntiles bytes, zero beyond 2n) and the rest, the "spill"
+ *   max(0, 2n - 5632 * ntiles) bytes, forms the escape stream (n_esc = spill).
+ *   Only the adaptive encoders write RAW streams, exactly when the coded
+ *   form's escape count exceeds the spill (RAW is then strictly smaller);
+ *   every decoder reads both kinds.
  *
  * ------------------------------------------------------------------------
  * Conventions for every entry point
@@ -91,6 +104,7 @@ extern "C" {
 #define ZC_HEADER_BYTES 128
 #define ZC_MAGIC 0x3142435Au
 #define ZC_VERSION 1
+#define ZC_FLAG_RAW 1u
 #define ZC_MAX_SHARDS 64
 #define ZC_WORKSPACE_HEADER_BYTES 4096
 #define ZC_WORKSPACE_BYTES_PER_TILE 16
@@ -177,11 +191,35 @@ zc_status zc_compress(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d
                       void* stream);
 
 /*
+ * Escape bytes of a RAW stream of n values, max(0, 2n - 5632 * ceil(n/4096))
+ * (about 0.625 n).  An adaptive compression never needs a larger escape
+ * capacity: with esc_capacity >= this bound it cannot overflow.
+ * n >= 2^32 -> ZC_ERR_TOO_LARGE.
+ */
+zc_status zc_raw_spill(uint64_t n, uint64_t* bytes);
+
+/*
+ * zc_compress with the raw bypass ([CCCL §3.3], [CCCL §5.2]): encodes like
+ * zc_compress, then a second launch on the same stream reads the escape count
+ * on the device and rewrites the tensor as a RAW stream (format above) when
+ * that is strictly smaller, i.e. when n_esc > zc_raw_spill(n) -- no host
+ * synchronisation.  The header's flags tell which form was stored and n_esc
+ * the escape bytes to send.  A coded form that overflows esc_capacity is not
+ * an error when the RAW form fits; ZC_ERR_ESCAPE_OVERFLOW is reported only
+ * when neither fits (then the coded output stands, as in zc_compress).
+ * Arguments, alignment, workspace and other errors as in zc_compress.
+ */
+zc_status zc_compress_adaptive(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_main, void* d_esc,
+                               uint64_t esc_capacity, void* d_ws, uint64_t ws_bytes, int32_t* d_status,
+                               void* stream);
+
+/*
  * Decode a ZC1 stream back to n bf16 values, bit for bit (the inverse of
- * zc_compress).  esc_bytes: the readable size of d_esc (at least the header's
- * n_esc).  The header and every tile's escape range are validated on the
- * device before use; a bad header writes nothing, a corrupt tile skips that
- * tile; errors go to *d_status.  No workspace.
+ * zc_compress and zc_compress_adaptive; coded and RAW streams alike).
+ * esc_bytes: the readable size of d_esc (at least the header's n_esc).  The
+ * header and every tile's escape range are validated on the device before
+ * use; a bad header writes nothing, a corrupt tile skips that tile; errors go
+ * to *d_status.  No workspace.
  */
 zc_status zc_decompress(const void* d_main, const void* d_esc, uint64_t esc_bytes, uint64_t n,
                         void* d_out, int32_t* d_status, void* stream);
@@ -198,7 +236,8 @@ zc_status zc_decompress(const void* d_main, const void* d_esc, uint64_t esc_byte
  *     d_out must be non-NULL and d_out_main/d_out_esc/d_ws may be NULL).
  *   d_out_main / d_out_esc / out_esc_capacity: as in zc_compress.
  * 1 <= P <= ZC_MAX_SHARDS.  Every shard's header must carry n
- * (ZC_ERR_SIZE_MISMATCH otherwise).  One fused kernel launch.
+ * (ZC_ERR_SIZE_MISMATCH otherwise); shards may be coded or RAW.  The
+ * re-encoded output is always coded.  One fused kernel launch.
  */
 zc_status zc_decompress_reduce(int P, const void* const* h_mains, const void* const* h_escs,
                                const uint64_t* h_esc_bytes, uint64_t n, void* d_out,
@@ -253,6 +292,9 @@ typedef struct zc_tensor {
  */
 zc_status zc_compress_batched(int count, const zc_tensor* h_tensors, void* d_ws, uint64_t ws_bytes,
                               int32_t* d_status, void* stream);
+/* zc_compress_batched with the raw bypass of zc_compress_adaptive, decided per tensor. */
+zc_status zc_compress_batched_adaptive(int count, const zc_tensor* h_tensors, void* d_ws, uint64_t ws_bytes,
+                                       int32_t* d_status, void* stream);
 zc_status zc_decompress_batched(int count, const zc_tensor* h_tensors, int32_t* d_status, void* stream);
 
 #ifdef __cplusplus

@@ -186,8 +186,9 @@ static zc_status validate_encode_tensor(const void* in, uint64_t n, const uint8_
   return ZC_OK;
 }
 
-zc_status zc_compress(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_main, void* d_esc,
-                      uint64_t esc_capacity, void* d_ws, uint64_t ws_bytes, int32_t* d_status, void* stream) {
+static zc_status compress_one(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_main, void* d_esc,
+                              uint64_t esc_capacity, void* d_ws, uint64_t ws_bytes, int32_t* d_status, void* stream,
+                              bool adaptive) {
   if (!d_status) return ZC_ERR_INVALID_ARG;
   if (!aligned(d_status, 4)) return ZC_ERR_ALIGNMENT;
   if (zc_status s = validate_encode_tensor(d_in, n, d_cb, d_main, d_esc, esc_capacity)) return s;
@@ -196,7 +197,26 @@ zc_status zc_compress(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d
   if (device_info(&dev) != cudaSuccess) return ZC_ERR_CUDA;
   EncTensor t{static_cast<const uint16_t*>(d_in), static_cast<uint8_t*>(d_main), static_cast<uint8_t*>(d_esc),
               d_cb, n, esc_capacity};
-  return cuda_status(launch_encode(&t, 1, ws_header(d_ws), ws_flags(d_ws), d_status, as_stream(stream), dev));
+  if (launch_encode(&t, 1, ws_header(d_ws), ws_flags(d_ws), d_status, as_stream(stream), dev, adaptive) !=
+      cudaSuccess)
+    return ZC_ERR_CUDA;
+  if (adaptive) return cuda_status(launch_raw_switch(&t, 1, ws_header(d_ws), d_status, as_stream(stream), dev));
+  return ZC_OK;
+}
+zc_status zc_compress(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_main, void* d_esc,
+                      uint64_t esc_capacity, void* d_ws, uint64_t ws_bytes, int32_t* d_status, void* stream) {
+  return compress_one(d_in, n, d_cb, d_main, d_esc, esc_capacity, d_ws, ws_bytes, d_status, stream, false);
+}
+zc_status zc_compress_adaptive(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_main, void* d_esc,
+                               uint64_t esc_capacity, void* d_ws, uint64_t ws_bytes, int32_t* d_status,
+                               void* stream) {
+  return compress_one(d_in, n, d_cb, d_main, d_esc, esc_capacity, d_ws, ws_bytes, d_status, stream, true);
+}
+zc_status zc_raw_spill(uint64_t n, uint64_t* bytes) {
+  if (!bytes) return ZC_ERR_INVALID_ARG;
+  if (n > kMaxN) return ZC_ERR_TOO_LARGE;
+  *bytes = raw_spill(n);
+  return ZC_OK;
 }
 
 static zc_status validate_decode_tensor(const void* main, const void* esc, uint64_t esc_bytes, uint64_t n,
@@ -251,8 +271,8 @@ zc_status zc_decompress_reduce(int P, const void* const* h_mains, const void* co
                                    out_esc_capacity, ws, flags, d_status, as_stream(stream), dev));
 }
 
-zc_status zc_compress_batched(int count, const zc_tensor* h_tensors, void* d_ws, uint64_t ws_bytes,
-                              int32_t* d_status, void* stream) {
+static zc_status compress_batched(int count, const zc_tensor* h_tensors, void* d_ws, uint64_t ws_bytes,
+                                  int32_t* d_status, void* stream, bool adaptive) {
   if (count < 1 || !h_tensors || !d_status) return ZC_ERR_INVALID_ARG;
   if (!aligned(d_status, 4)) return ZC_ERR_ALIGNMENT;
   uint64_t tiles = 0;
@@ -274,10 +294,19 @@ zc_status zc_compress_batched(int count, const zc_tensor* h_tensors, void* d_ws,
       ts[i] = EncTensor{static_cast<const uint16_t*>(t.bf16), static_cast<uint8_t*>(t.main),
                         static_cast<uint8_t*>(t.esc), t.cb, t.n, t.esc_bytes};
     }
-    cudaError_t e = launch_encode(ts, m, ws_header(d_ws), ws_flags(d_ws), d_status, as_stream(stream), dev);
+    cudaError_t e = launch_encode(ts, m, ws_header(d_ws), ws_flags(d_ws), d_status, as_stream(stream), dev, adaptive);
+    if (e == cudaSuccess && adaptive) e = launch_raw_switch(ts, m, ws_header(d_ws), d_status, as_stream(stream), dev);
     if (e != cudaSuccess) return ZC_ERR_CUDA;
   }
   return ZC_OK;
+}
+zc_status zc_compress_batched(int count, const zc_tensor* h_tensors, void* d_ws, uint64_t ws_bytes,
+                              int32_t* d_status, void* stream) {
+  return compress_batched(count, h_tensors, d_ws, ws_bytes, d_status, stream, false);
+}
+zc_status zc_compress_batched_adaptive(int count, const zc_tensor* h_tensors, void* d_ws, uint64_t ws_bytes,
+                                       int32_t* d_status, void* stream) {
+  return compress_batched(count, h_tensors, d_ws, ws_bytes, d_status, stream, true);
 }
 
 zc_status zc_decompress_batched(int count, const zc_tensor* h_tensors, int32_t* d_status, void* stream) {

@@ -12,7 +12,9 @@
 // mbarrier; two stages are in flight per warp.  Code -> exponent goes
 // through byte permutes on an 8-byte table held in registers, with a 3 x 256
 // spread table in shared memory turning the three plane bytes into a permute
-// selector.  Output is written with 16-byte vector stores.
+// selector.  Output is written with 16-byte vector stores.  A RAW stream
+// (the raw bypass: the values' own bytes) skips the staging: each warp
+// copies its tiles' 8192 bytes with 16-byte loads and stores.
 #include "zc_device.cuh"
 #include "zc_internal.h"
 
@@ -41,6 +43,7 @@ struct DecParams {
 struct HdrInfo {
   int ti;
   bool ok;
+  bool raw;  // RAW stream
   uint64_t n_esc;
   DecTable dt;
 };
@@ -66,8 +69,9 @@ __device__ __forceinline__ HdrInfo read_header(const DecTensor& T, int ti, int32
 #pragma unroll
     for (int b = a + 1; b < 7; b++) dup |= cb[a] == cb[b];
   int err = 0;
-  if (magic != ZC_MAGIC || vf != ZC_VERSION || tile_elems != kTile || ntiles != num_tiles(T.n) || dup ||
-      h.n_esc > T.esc_bytes || h.n_esc > T.n)
+  h.raw = vf == (ZC_VERSION | (kFlagRaw << 16));
+  if (magic != ZC_MAGIC || (vf != ZC_VERSION && !h.raw) || tile_elems != kTile || ntiles != num_tiles(T.n) ||
+      dup || h.n_esc > T.esc_bytes || h.n_esc > T.n || (h.raw && h.n_esc != raw_spill(T.n)))
     err = ZC_ERR_BAD_HEADER;
   if (n != T.n) err = ZC_ERR_SIZE_MISMATCH;
   h.ok = err == 0;
@@ -148,7 +152,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   HdrInfo issue_hdr;
   issue_hdr.ti = -1;
   uint32_t st_a[kDecStages], st_cnt[kDecStages], st_staged[kDecStages];
-  bool st_ok[kDecStages];
+  bool st_ok[kDecStages], st_raw[kDecStages];
   DecTable st_dt[kDecStages];  // code table of the staged tile's tensor (read when it was issued)
   uint32_t issue_ti = 0;  // running tensor index of issue()
   auto issue = [&](int s, uint32_t g) {
@@ -156,10 +160,13 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     const DecTensor& T = p.t[ti];
     if (issue_hdr.ti != static_cast<int>(ti)) issue_hdr = hdr_cache[ti];
     const uint32_t lt = g - p.tile_start[ti];
-    uint32_t a, cnt;
-    bool ok;
-    tile_escape_range(T, issue_hdr, lt, a, cnt, ok);
-    if (!ok && issue_hdr.ok && lane == 0) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
+    uint32_t a = 0, cnt = 0;
+    bool ok = issue_hdr.ok;
+    st_raw[s] = issue_hdr.raw;
+    if (!issue_hdr.raw) {
+      tile_escape_range(T, issue_hdr, lt, a, cnt, ok);
+      if (!ok && issue_hdr.ok && lane == 0) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
+    }
     uint8_t* sp = stage_ptr(s);
     st_dt[s] = issue_hdr.dt;
     st_a[s] = a;
@@ -167,9 +174,13 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     st_ok[s] = ok;
     st_staged[s] = stage_escapes(sp + kTileBytes, T.esc, a, ok ? cnt : 0, &bar[s]);
     if (lane == 0) {
-      fence_proxy_async();
-      mbar_arrive_expect_tx(&bar[s], kTileBytes);
-      tma_load_1d(sp, tile_ptr(T.main, num_tiles(T.n), lt), kTileBytes, &bar[s]);
+      if (issue_hdr.raw) {
+        mbar_arrive(&bar[s]);  // nothing to stage: the tile is copied from global memory
+      } else {
+        fence_proxy_async();
+        mbar_arrive_expect_tx(&bar[s], kTileBytes);
+        tma_load_1d(sp, tile_ptr(T.main, num_tiles(T.n), lt), kTileBytes, &bar[s]);
+      }
     }
   };
 
@@ -196,7 +207,23 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
 
       mbar_wait_bounded(&bar[s], (phase >> s) & 1u, p.status);
       phase ^= 1u << s;
-      if (st_ok[s]) {
+      if (st_ok[s] && st_raw[s]) {
+        // RAW: bytes [8192 lt, 8192 lt + 2 n_tile) of the image, 16 per lane and step
+        const uint64_t ntiles = num_tiles(T.n);
+        const uint8_t* tiles = tile_ptr(T.main, ntiles, 0);
+        const uint64_t region = static_cast<uint64_t>(kTileBytes) * ntiles;
+        uint16_t* out = T.out + static_cast<uint64_t>(lt) * kTile;
+#pragma unroll 1
+        for (uint32_t q = 0; q < 4; q++) {
+          uint4 v[4];
+#pragma unroll
+          for (uint32_t k = 0; k < 4; k++)
+            v[k] = raw_load16(tiles, T.esc, region, 2 * T.n,
+                              2 * (static_cast<uint64_t>(lt) * kTile + q * kBlock + k * 256 + lane * 8));
+#pragma unroll
+          for (uint32_t k = 0; k < 4; k++) store8_guarded(out, q * kBlock + k * 256 + lane * 8, rem, v[k]);
+        }
+      } else if (st_ok[s]) {
         EscSource es;
         es.smem = tile + kTileBytes + (st_a[s] & 15u);
         es.glob = T.esc + st_a[s];

@@ -37,7 +37,8 @@ struct WsHeader {
   uint32_t epoch;      // epoch tag of the last finished encoding launch
   uint32_t max_tiles;  // largest flag range ever used (cleared when the epoch wraps)
   uint32_t hist_done;  // CTAs of the running histogram launch that have finished
-  uint32_t pad[27];
+  uint32_t raw_done;   // CTAs of the running raw-bypass launch that have finished
+  uint32_t pad[26];
   uint32_t hist[256];  // global exponent bins, all zero between calls
 };
 static_assert(sizeof(WsHeader) <= ZC_WORKSPACE_HEADER_BYTES, "workspace header too large");
@@ -224,6 +225,32 @@ __device__ __forceinline__ uint8_t* tile_ptr(uint8_t* main, uint64_t ntiles, uin
 }
 __device__ __forceinline__ const uint8_t* tile_ptr(const uint8_t* main, uint64_t ntiles, uint64_t t) {
   return main + kHeader + table_bytes(ntiles) + static_cast<uint64_t>(kTileBytes) * t;
+}
+
+// ---------------------------------------------------------------- RAW streams
+// Header flags bit 0 marks a RAW stream: the values' 2n little-endian bytes
+// fill the tile region (5632 ntiles bytes) and the rest, the spill, is the
+// escape stream.
+constexpr uint32_t kFlagRaw = ZC_FLAG_RAW;
+__host__ __device__ __forceinline__ uint64_t raw_spill(uint64_t n) {
+  const uint64_t region = static_cast<uint64_t>(kTileBytes) * num_tiles(n);
+  return 2 * n > region ? 2 * n - region : 0;
+}
+
+// 16 bytes of a RAW image at byte offset `b` (a multiple of 16): from the
+// tile region below `region`, from the escape stream above it; bytes at or
+// past `two_n` read as zero and are never loaded.  Both sources are
+// 16-byte aligned and `region` is a multiple of 16, so a 16-byte piece never
+// straddles the two.
+__device__ __forceinline__ uint4 raw_load16(const uint8_t* tiles, const uint8_t* esc, uint64_t region,
+                                            uint64_t two_n, uint64_t b) {
+  if (b >= two_n) return make_uint4(0u, 0u, 0u, 0u);
+  const uint8_t* src = b < region ? tiles + b : esc + (b - region);
+  if (b + 16 <= two_n) return __ldg(reinterpret_cast<const uint4*>(src));
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  const uint16_t* h = reinterpret_cast<const uint16_t*>(src);
+  for (uint32_t j = 0; b + 2 * j < two_n; j++) w[j >> 1] |= static_cast<uint32_t>(__ldg(h + j)) << (16 * (j & 1));
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Valid-element mask of this lane in block `blk` of a tile holding `n_tile`

@@ -68,6 +68,7 @@ struct EncParams {
   WsHeader* ws;
   Flag* flags;  // one per group
   int32_t* status;
+  int adaptive;  // an escape overflow is left to the raw-bypass launch that follows
 };
 
 // Tensor of global group G.  Every caller visits groups in increasing order,
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
       if (half == kUnitsPerTile - 1 && lt + 1 == ntiles) {
         const uint64_t n_esc = prefix + cnt;
         write_header_tail(T.main, ntiles, n_esc);
-        if (lane == 0 && n_esc > T.esc_cap) set_status(p.status, ZC_ERR_ESCAPE_OVERFLOW);
+        if (lane == 0 && n_esc > T.esc_cap && !p.adaptive) set_status(p.status, ZC_ERR_ESCAPE_OVERFLOW);
       }
       return prefix;
     };
@@ -395,8 +396,9 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
 
 template <int MAXB>
 static cudaError_t launch_encode_t(const EncTensor* ts, int count, WsHeader* ws, Flag* flags, int32_t* status,
-                                   cudaStream_t stream, const DeviceInfo& dev) {
+                                   cudaStream_t stream, const DeviceInfo& dev, bool adaptive) {
   EncParams<MAXB> p;
+  p.adaptive = adaptive ? 1 : 0;
   uint32_t groups = 0;
   for (int i = 0; i < count; i++) {
     p.t[i] = ts[i];
@@ -427,9 +429,9 @@ static cudaError_t launch_encode_t(const EncTensor* ts, int count, WsHeader* ws,
 }
 
 cudaError_t launch_encode(const EncTensor* ts, int count, WsHeader* ws, Flag* flags, int32_t* status,
-                          cudaStream_t stream, const DeviceInfo& dev) {
-  if (count == 1) return launch_encode_t<1>(ts, count, ws, flags, status, stream, dev);
-  return launch_encode_t<kMaxBatch>(ts, count, ws, flags, status, stream, dev);
+                          cudaStream_t stream, const DeviceInfo& dev, bool adaptive) {
+  if (count == 1) return launch_encode_t<1>(ts, count, ws, flags, status, stream, dev, adaptive);
+  return launch_encode_t<kMaxBatch>(ts, count, ws, flags, status, stream, dev, adaptive);
 }
 
 }  // namespace zc

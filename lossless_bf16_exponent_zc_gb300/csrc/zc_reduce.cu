@@ -16,6 +16,9 @@
 //   * Each consumer decodes its block straight into its sums (two fp32 adds
 //     per instruction), rounds, stores, and -- when re-encoding -- encodes its
 //     block of the result from shared memory.
+//   * A RAW shard (the raw bypass: the values' own bytes) stages nothing: the
+//     producer only signals the stage, and each consumer reads its block's
+//     values of that shard straight from global memory.
 //   * With re-encoding, 1 scan warp runs the escape scan of the output exactly
 //     like the encoder: the last warp of a group publishes the group's count,
 //     the scan warp adds the counts of the groups since its own previous
@@ -44,7 +47,7 @@ constexpr uint32_t kRSpread = 0;      // decode spread tables, 3 x 1 KB
 constexpr uint32_t kRLut = 3072;      // encoder LUT of the output codebook, 1 KB aligned
 constexpr uint32_t kRShard = 4096;    // per-shard tables, 64 x 16 B
 constexpr uint32_t kRRound = 5120;    // round bookkeeping (<= 512 B)
-constexpr uint32_t kRFlag = 5632;     // validity flags
+constexpr uint32_t kRFlag = 5632;     // validity flags, then the RAW shard mask (u64)
 constexpr uint32_t kRBars = 5648;     // full / empty barriers, 2 x 4 teams x 4 stages
 constexpr uint32_t kRMeta = kRBars + 2 * kRedTeams * kRedStages * 8;  // stage metadata
 constexpr uint32_t kRScratch = 6272;  // per-consumer exponent scratch, 1 KB each
@@ -81,8 +84,9 @@ struct StageMeta {
   uint32_t cnt;     // escapes of the tile
   uint32_t staged;  // how many of them sit in the stage
   uint16_t shard;
-  uint16_t ok;      // offset table consistent
+  uint16_t ok;      // kMetaOk: offset table consistent; kMetaRaw: RAW shard, nothing staged
 };
+constexpr uint16_t kMetaOk = 1, kMetaRaw = 2;
 
 struct RedRound {
   uint32_t agg[kRedSlots];                    // arrivals << 16 | escape count so far
@@ -118,7 +122,11 @@ __device__ __forceinline__ uint4 round_pack(const float (&acc)[8]) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-template <bool REENC>
+// RAW = false: the launch for all-coded inputs; it leaves at once when a shard
+// is RAW.  RAW = true: the launch that follows it and does the work only when
+// some shard is RAW (its shard loop tests every copy for RAW; keeping that
+// test out of the all-coded kernel keeps its code as lean as before).
+template <bool REENC, bool RAW>
 __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_constant__ RedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
@@ -129,13 +137,21 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
   ShardInfo* si = reinterpret_cast<ShardInfo*>(gbase + kRShard);
   RedRound* rs = reinterpret_cast<RedRound*>(gbase + kRRound);
   int* flags_s = reinterpret_cast<int*>(gbase + kRFlag);  // [0] bad input, [1] bad output codebook
+  unsigned long long* raw_s = reinterpret_cast<unsigned long long*>(gbase + kRFlag + 8);  // RAW shards (bit r)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(gbase + kRBars);
   uint64_t* empty_bar = full_bar + kRedTeams * kRedStages;
   StageMeta* meta = reinterpret_cast<StageMeta*>(gbase + kRMeta);
+  if (RAW) {  // nothing to do unless a shard is RAW: leave before touching anything
+    bool any = false;
+    for (int r = threadIdx.x; r < p.P; r += blockDim.x)
+      any |= __ldg(reinterpret_cast<const uint32_t*>(p.s[r].main) + 1) == (ZC_VERSION | (kFlagRaw << 16));
+    if (!__syncthreads_or(any)) return;
+  }
 
   build_spread_tables(spread);
   if (threadIdx.x == 0) {
     flags_s[0] = flags_s[1] = 0;
+    *raw_s = 0ull;
     for (int i = 0; i < kRedTeams * kRedStages; i++) {
       mbar_init(&full_bar[i], 1);  // the producer's arrival with the expected bytes
       mbar_init(&empty_bar[i], 4);  // the team's 4 consumer warps
@@ -161,9 +177,12 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     for (int a = 0; a < 7; a++)
       for (int b = a + 1; b < 7; b++) dup |= cb[a] == cb[b];
     int err = 0;
-    if (__ldg(w) != ZC_MAGIC || __ldg(w + 1) != ZC_VERSION || __ldg(w + 4) != kTile ||
-        __ldg(w + 5) != p.ntiles || dup || n_esc > p.s[r].esc_bytes || n_esc > p.n)
+    const uint32_t vf = __ldg(w + 1);
+    const bool raw = vf == (ZC_VERSION | (kFlagRaw << 16));
+    if (__ldg(w) != ZC_MAGIC || (vf != ZC_VERSION && !raw) || __ldg(w + 4) != kTile || __ldg(w + 5) != p.ntiles ||
+        dup || n_esc > p.s[r].esc_bytes || n_esc > p.n || (raw && n_esc != raw_spill(p.n)))
       err = ZC_ERR_BAD_HEADER;
+    if (raw) atomicOr(raw_s, 1ull << r);
     if (n != p.n) err = ZC_ERR_SIZE_MISMATCH;
     if (err) {
       atomicExch(&flags_s[0], 1);
@@ -183,6 +202,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     }
   }
   __syncthreads();
+  if (!RAW && *raw_s != 0ull) return;  // the RAW-capable launch that follows does the work
   const bool skip = flags_s[0] != 0 || flags_s[1] != 0;
   const uint32_t epoch = REENC ? launch_epoch(p.ws) : 0u;
   const uint32_t hold = REENC ? launch_hold(p.ws) : 0u;
@@ -240,6 +260,16 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
             const uint32_t bi = t * kRedStages + uses[u] % kRedStages;
             if (uses[u] >= kRedStages)
               mbar_wait_bounded(&empty_bar[bi], (uses[u] / kRedStages - 1) & 1u, p.status);
+            if (RAW && ((*raw_s >> r) & 1ull)) {  // RAW shard: the consumers read global memory
+              StageMeta m;
+              m.a = m.cnt = m.staged = 0;
+              m.shard = static_cast<uint16_t>(r);
+              m.ok = kMetaOk | kMetaRaw;
+              meta[bi] = m;
+              mbar_arrive(&full_bar[bi]);
+              uses[u]++;
+              continue;
+            }
             const bool ok = a[u] <= b[u] && b[u] <= n_esc && b[u] - a[u] <= kTile;
             if (!ok) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
             const uint32_t aa = ok ? a[u] : 0, cnt = ok ? b[u] - a[u] : 0;
@@ -352,11 +382,27 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
 #pragma unroll
         for (int i = 0; i < 8; i++) acc[k][i] = -0.0f;  // -0 + x == x for every x
       if (has) {
+        // the P copies of this block, added in rank order
         for (int r = 0; r < p.P; r++) {
           const uint32_t s = k_item % kRedStages;
           const uint32_t bi = t * kRedStages + s;
           mbar_wait_bounded(&full_bar[bi], (k_item / kRedStages) & 1u, p.status);
           const StageMeta m = meta[bi];
+          if (RAW && (m.ok & kMetaRaw)) {
+            // RAW shard: this block's values, 16 bytes per lane and chunk
+            const uint8_t* tiles = tile_ptr(p.s[m.shard].main, p.ntiles, 0);
+            const uint64_t region = static_cast<uint64_t>(kTileBytes) * p.ntiles;
+            const uint64_t b0 = 2 * (static_cast<uint64_t>(g) * kTile + b * kBlock + lane * 8);
+            uint4 v[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++) v[k] = raw_load16(tiles, p.s[m.shard].esc, region, 2 * p.n, b0 + 512 * k);
+#pragma unroll
+            for (int k = 0; k < 4; k++) accumulate8(acc[k], v[k]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[bi]);
+            k_item++;
+            continue;
+          }
           const uint32_t tile_s = sbase + kRStage + bi * kRedStageBytes;
           // escapes of the tile's earlier blocks: one warp reduction over their masks
           uint32_t first = 0;
@@ -460,23 +506,33 @@ cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out,
   uint32_t ctas = ngroups;
   if (ctas > static_cast<uint32_t>(dev.sm_count)) ctas = dev.sm_count;
   if (ctas == 0) ctas = 1;
-  cudaError_t err;
-  static KernelPrep prep_reenc, prep_plain;
-  int per_sm = 0;
-  if (out_cb) {
-    err = prepare_kernel(prep_reenc, reinterpret_cast<const void*>(reduce_kernel<true>), kRedThreads, kRedSmem, dev,
-                         &per_sm);
+  // The all-coded launch, then the RAW-capable one; exactly one of them works.
+  static KernelPrep prep[2][2];
+  for (int raw = 0; raw < 2; raw++) {
+    int per_sm = 0;
+    cudaError_t err;
+    if (out_cb) {
+      const void* fn = raw ? reinterpret_cast<const void*>(reduce_kernel<true, true>)
+                           : reinterpret_cast<const void*>(reduce_kernel<true, false>);
+      err = prepare_kernel(prep[1][raw], fn, kRedThreads, kRedSmem, dev, &per_sm);
+      if (err != cudaSuccess) return err;
+      void* args[] = {&p};
+      err = cudaLaunchCooperativeKernel(fn, dim3(ctas), dim3(kRedThreads), args, kRedSmem, stream);
+    } else {
+      if (p.ntiles == 0) return cudaSuccess;
+      const void* fn = raw ? reinterpret_cast<const void*>(reduce_kernel<false, true>)
+                           : reinterpret_cast<const void*>(reduce_kernel<false, false>);
+      err = prepare_kernel(prep[0][raw], fn, kRedThreads, kRedSmem, dev, &per_sm);
+      if (err != cudaSuccess) return err;
+      if (raw)
+        reduce_kernel<false, true><<<ctas, kRedThreads, kRedSmem, stream>>>(p);
+      else
+        reduce_kernel<false, false><<<ctas, kRedThreads, kRedSmem, stream>>>(p);
+      err = cudaGetLastError();
+    }
     if (err != cudaSuccess) return err;
-    void* args[] = {&p};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(reduce_kernel<true>), dim3(ctas),
-                                       dim3(kRedThreads), args, kRedSmem, stream);
   }
-  if (p.ntiles == 0) return cudaSuccess;
-  err = prepare_kernel(prep_plain, reinterpret_cast<const void*>(reduce_kernel<false>), kRedThreads, kRedSmem, dev,
-                       &per_sm);
-  if (err != cudaSuccess) return err;
-  reduce_kernel<false><<<ctas, kRedThreads, kRedSmem, stream>>>(p);
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace zc

@@ -71,14 +71,17 @@ def load() -> ctypes.CDLL:
     lib.zc_workspace_size.argtypes = [u64p, i32, u64p]
     lib.zc_histogram_topk.argtypes = [vp, u64, vp, vp, vp, u64, vp, vp]
     lib.zc_compress.argtypes = [vp, u64, vp, vp, vp, u64, vp, u64, vp, vp]
+    lib.zc_compress_adaptive.argtypes = [vp, u64, vp, vp, vp, u64, vp, u64, vp, vp]
+    lib.zc_raw_spill.argtypes = [u64, u64p]
     lib.zc_decompress.argtypes = [vp, vp, u64, u64, vp, vp, vp]
     lib.zc_decompress_reduce.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), u64p, u64, vp, vp, vp, vp,
                                          u64, vp, u64, vp, vp]
     lib.zc_compress_batched.argtypes = [i32, ctypes.POINTER(ZcTensor), vp, u64, vp, vp]
+    lib.zc_compress_batched_adaptive.argtypes = [i32, ctypes.POINTER(ZcTensor), vp, u64, vp, vp]
     lib.zc_decompress_batched.argtypes = [i32, ctypes.POINTER(ZcTensor), vp, vp]
     for name in ("zc_codebook_from_sigma", "zc_compressed_size", "zc_workspace_size", "zc_histogram_topk",
-                 "zc_compress", "zc_decompress", "zc_decompress_reduce", "zc_compress_batched",
-                 "zc_decompress_batched"):
+                 "zc_compress", "zc_compress_adaptive", "zc_raw_spill", "zc_decompress", "zc_decompress_reduce",
+                 "zc_compress_batched", "zc_compress_batched_adaptive", "zc_decompress_batched"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -130,6 +133,13 @@ def compressed_size(n: int) -> tuple[int, int]:
     return m.value, e.value
 
 
+def raw_spill(n: int) -> int:
+    """Escape bytes of a RAW stream of n values (the most an adaptive compression needs)."""
+    out = ctypes.c_uint64()
+    _check(load().zc_raw_spill(int(n), ctypes.byref(out)), "zc_raw_spill")
+    return out.value
+
+
 def workspace_size(ns: Sequence[int] | int) -> int:
     ns = [int(ns)] if isinstance(ns, (int, np.integer)) else [int(v) for v in ns]
     arr = (ctypes.c_uint64 * len(ns))(*ns)
@@ -176,6 +186,24 @@ def compress(x: torch.Tensor, cb: torch.Tensor, ws: torch.Tensor, status: torch.
     rc = load().zc_compress(_ptr(x), n, _ptr(cb), _ptr(main), _ptr(esc), esc.numel(), _ptr(ws), ws.numel(),
                             _ptr(status), _stream(stream))
     _check(rc, "zc_compress")
+    return main, esc
+
+
+def compress_adaptive(x: torch.Tensor, cb: torch.Tensor, ws: torch.Tensor, status: torch.Tensor,
+                      main: torch.Tensor | None = None, esc: torch.Tensor | None = None, stream=None):
+    """compress with the raw bypass: the stream is stored RAW (header flags bit 0) when that is smaller.
+
+    The default escape buffer is raw_spill(n) bytes, which never overflows.
+    """
+    n = _nelem16(x)
+    mb, _ = compressed_size(n)
+    if main is None:
+        main = torch.empty(mb, dtype=torch.uint8, device=x.device)
+    if esc is None:
+        esc = torch.empty(max(raw_spill(n), 16), dtype=torch.uint8, device=x.device)
+    rc = load().zc_compress_adaptive(_ptr(x), n, _ptr(cb), _ptr(main), _ptr(esc), esc.numel(), _ptr(ws),
+                                     ws.numel(), _ptr(status), _stream(stream))
+    _check(rc, "zc_compress_adaptive")
     return main, esc
 
 
@@ -243,6 +271,13 @@ def compress_batched(items: Sequence[BatchItem], ws: torch.Tensor, status: torch
            "zc_compress_batched")
 
 
+def compress_batched_adaptive(items: Sequence[BatchItem], ws: torch.Tensor, status: torch.Tensor,
+                              stream=None) -> None:
+    arr = _descs(items)
+    _check(load().zc_compress_batched_adaptive(len(items), arr, _ptr(ws), ws.numel(), _ptr(status),
+                                               _stream(stream)), "zc_compress_batched_adaptive")
+
+
 def decompress_batched(items: Sequence[BatchItem], status: torch.Tensor, stream=None) -> None:
     arr = _descs(items)
     _check(load().zc_decompress_batched(len(items), arr, _ptr(status), _stream(stream)), "zc_decompress_batched")
@@ -252,6 +287,11 @@ def decompress_batched(items: Sequence[BatchItem], status: torch.Tensor, stream=
 def header_n_esc(main: torch.Tensor) -> int:
     """Escape count from a main stream's header (a device-to-host read of 8 bytes)."""
     return int.from_bytes(main[24:32].cpu().numpy().tobytes(), "little")
+
+
+def header_is_raw(main: torch.Tensor) -> bool:
+    """Whether a main stream holds a RAW stream (header flags bit 0; a device-to-host read)."""
+    return bool(int.from_bytes(main[6:8].cpu().numpy().tobytes(), "little") & 1)
 
 
 def status_value(status: torch.Tensor) -> int:

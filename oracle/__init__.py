@@ -180,12 +180,12 @@ def compress(x, cb, esc_capacity: int | None = None, allow_overflow: bool = Fals
 
 
 def raw_spill(n: int) -> int:
-    """Bytes of a RAW stream of n values that go to the escape stream (reading R8)."""
+    """Bytes of a RAW stream of n values that go to the escape stream (reading R12)."""
     return int(_load().zo_raw_spill(n))
 
 
 def compress_adaptive(x, cb, esc_capacity: int | None = None, allow_overflow: bool = False):
-    """Encode, then store RAW when that is strictly smaller (reading R8).
+    """Encode, then store RAW when that is strictly smaller (reading R12).
 
     Returns (main, escapes, raw) with raw = True for a RAW stream, or
     (main, escapes, raw, rc) with ``allow_overflow`` when neither form fits.

@@ -43,7 +43,7 @@
  *   R7  local reduction = sum (not mean), fp32, rank order 0..P-1, IEEE
  *       round-to-nearest with subnormals kept, then RNE to bf16; a NaN sum
  *       becomes 0x7FC0.
- *   R8  raw bypass ([CCCL §3.3] tiny tensors are not worth compressing;
+ *   R12 raw bypass ([CCCL §3.3] tiny tensors are not worth compressing;
  *       [CCCL §5.2] a ratio near or above 1 means fall back to sending the
  *       data uncompressed): header flags bit 0 marks a RAW stream.  It holds
  *       the 2n little-endian bytes of the n values in order: the first
@@ -281,7 +281,7 @@ int zo_compress(const uint16_t *x, uint64_t n, const uint8_t cb[7], uint8_t *mai
   return overflow ? O_ERR_ESCAPE_OVERFLOW : O_OK;
 }
 
-/* ---- raw bypass, reading R8 ---------------------------------------------- */
+/* ---- raw bypass, reading R12 ---------------------------------------------- */
 /* bytes of a RAW stream that do not fit in the tile region */
 uint64_t zo_raw_spill(uint64_t n) {
   uint64_t region = (uint64_t)O_TILE_BYTES * zo_num_tiles(n);
@@ -341,7 +341,7 @@ int zo_decompress(const uint8_t *main_in, const uint8_t *esc_in, uint64_t esc_by
   if (!codebook_is_valid(cb)) return O_ERR_HEADER;
   uint64_t tbl = table_bytes(ntiles);
 
-  if (flags == 1) { /* RAW, reading R8: the bytes in order, tile region then escapes */
+  if (flags == 1) { /* RAW, reading R12: the bytes in order, tile region then escapes */
     if (n_esc != zo_raw_spill(n)) return O_ERR_HEADER;
     uint64_t region = (uint64_t)O_TILE_BYTES * ntiles;
     const uint8_t *tiles = main_in + O_HEADER + tbl;

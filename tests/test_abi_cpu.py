@@ -24,7 +24,8 @@ def test_library_exports_every_declared_symbol():
     names = declared_functions()
     assert {"zc_codebook_from_sigma", "zc_histogram_topk", "zc_compress", "zc_decompress", "zc_decompress_reduce",
             "zc_compressed_size", "zc_workspace_size", "zc_compress_batched", "zc_decompress_batched",
-            "zc_status_string", "zc_version"} <= set(names)
+            "zc_status_string", "zc_version", "zc_compress_adaptive", "zc_compress_batched_adaptive",
+            "zc_raw_spill"} <= set(names)
     for name in names:
         assert hasattr(lib, name), name
 
@@ -99,3 +100,21 @@ def test_argument_errors_are_synchronous():
                 None) == E.ERR_INVALID_ARG
     # batched: empty batch
     assert _raw("zc_compress_batched", 0, None, None, 0, status, None) == E.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("n", [0, 1, 2816, 2817, 4096, 65536, (1 << 26) + 5])
+def test_raw_spill_matches_oracle(n):
+    assert zc.raw_spill(n) == oracle.raw_spill(n)
+
+
+def test_adaptive_argument_errors_are_synchronous():
+    E = zc
+    assert _raw("zc_compress_adaptive", None, 10, None, None, None, 0, None, 0, None, None) == E.ERR_INVALID_ARG
+    fake, status = 1 << 20, 1 << 21
+    assert _raw("zc_compress_adaptive", fake + 2, 10, fake, fake, fake, 10, fake, 1 << 20, status,
+                None) == E.ERR_ALIGNMENT
+    assert _raw("zc_compress_adaptive", fake, 1 << 20, fake, fake, fake, 10, fake, 4096, status,
+                None) == E.ERR_WORKSPACE
+    assert _raw("zc_compress_batched_adaptive", 0, None, None, 0, status, None) == E.ERR_INVALID_ARG
+    with pytest.raises(zc.ZcError):
+        zc.raw_spill(1 << 32)

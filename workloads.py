@@ -22,6 +22,9 @@ Workloads (n = elements):
   moe_payload   16384 x 4096, 0.5 * Student-t(4); destination token counts
                 Zipf(1.2) over 8 ranks (largest-remainder rounding); seed 4
   rs_shards     P = 8 shards of m = 2^25 elements, N(0, 1e-3); seed 5 + rank
+  random_bits   n = 2^26 uniformly random 16-bit patterns, seed 6 -- data the
+                exponent coding cannot shrink (exponents spread over all 256
+                values), the case of the raw bypass
 """
 from __future__ import annotations
 
@@ -129,6 +132,11 @@ def rs_shards(P: int = 8, m: int = 1 << 25, sigma: float = RS_SIGMA, seed: int =
         rng = np.random.default_rng(seed + r)
         shards.append(to_bf16_bits(rng.standard_normal(m, dtype=np.float32) * np.float32(sigma)))
     return shards
+
+
+def random_bits(n: int = 1 << 26, seed: int = 6) -> np.ndarray:
+    """Uniformly random bf16 bit patterns (NaNs and infinities included)."""
+    return np.random.default_rng(seed).integers(0, 65536, n, dtype=np.uint16)
 
 
 def all_bf16_patterns() -> np.ndarray:
