@@ -624,13 +624,16 @@ def run_workloads(args, zc, torch, device, peak):
     coded = {"compress": entry(tp, 2 * n, 2 * n + mb + k), "compress_adaptive": entry(ta, 2 * n, 2 * n + mb + k),
              "stored_raw": zc.header_is_raw(m_t), "decision_cost_us": round(1e3 * (ta - tp), 2)}
     xt = dev(workloads.random_bits(n))
+    tp = _time_ms(torch, lambda: zc.compress(xt, cbg, ws, st, main=m_t, esc=e_t), 5)
+    k = zc.header_n_esc(m_t)
     ta = _time_ms(torch, lambda: zc.compress_adaptive(xt, cbg, ws, st, main=m_t, esc=e_t), 20)
     is_raw = zc.header_is_raw(m_t)
     td = _time_ms(torch, lambda: zc.decompress(m_t, e_t, n, st, out=y), 20)
     ok = torch.equal(y, xt)
     out["raw_bypass_2^26"] = {
         "coded_gaussian": coded,
-        "random_bits": {"compress_adaptive": entry(ta, 2 * n, 4 * n), "decompress": entry(td, 2 * n, 4 * n),
+        "random_bits": {"compress_coded": entry(tp, 2 * n, 2 * n + mb + k), "coded_escape_rate": round(k / n, 5),
+                        "compress_adaptive": entry(ta, 2 * n, 4 * n), "decompress": entry(td, 2 * n, 4 * n),
                         "stored_raw": is_raw, "bytes_sent": mb + spill, "ratio": round(2 * n / (mb + spill), 4),
                         "round_trip_ok": bool(ok)}}
     del xt, m_t, e_t, y

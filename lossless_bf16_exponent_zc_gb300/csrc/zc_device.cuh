@@ -416,6 +416,35 @@ __device__ __forceinline__ void write_escapes(uint32_t tb, const EscBook<NB>& te
   }
 }
 
+// write_escapes for a warp that has a free 1 KB shared buffer `buf`: one
+// block at a time, the block's escapes (at most 1024) are gathered in `buf`
+// and then stored with consecutive lanes on consecutive bytes, so each store
+// instruction fills one 32-byte sector instead of touching 32 of them.
+template <int NB>
+__device__ __forceinline__ void write_escapes_coalesced(uint32_t tb, const EscBook<NB>& te, uint64_t prefix,
+                                                        uint8_t* esc, uint64_t cap, uint8_t* buf) {
+  const uint32_t lane = lane_id();
+  const uint32_t lane_off = tb + 16 * lane;
+#pragma unroll
+  for (uint32_t blk = 0; blk < NB; blk++) {
+    const uint32_t first = __shfl_sync(kFull, te.base[blk], 0);  // escapes before this block
+    const uint32_t end = blk + 1 < NB ? __shfl_sync(kFull, te.base[blk + 1], 0) : te.total;
+    uint32_t m = te.mask[blk];
+    uint8_t* dst = buf + (te.base[blk] - first);
+    const uint32_t src = lane_off + 2 * blk * kBlock;
+    while (m) {
+      const uint32_t p = __ffs(m) - 1;
+      m &= m - 1;
+      *dst++ = static_cast<uint8_t>(lds_u16(src + 512 * (p >> 3) + 2 * (p & 7)) >> 7);
+    }
+    __syncwarp();
+    const uint64_t g0 = prefix + first;
+    for (uint32_t i = lane; i < end - first; i += 32)
+      if (g0 + i < cap) esc[g0 + i] = buf[i];
+    __syncwarp();
+  }
+}
+
 // Moves the escapes of NB blocks (8-bit exponents read back from the blocks at
 // shared address `tb`) into a shared staging buffer `buf` in escape order; the
 // caller guarantees te.total fits.  Escapes of a lane are consecutive.  Up to

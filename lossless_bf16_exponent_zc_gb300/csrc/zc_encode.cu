@@ -116,6 +116,9 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;  // 1 KB aligned shared address
   uint8_t* gbase = smem + (sbase - smem_u32(smem));           // its generic pointer
   RoundShared* rs = reinterpret_cast<RoundShared*>(gbase + kEncGrpOff);
+  // A launch that follows as a programmatic dependent (the raw-bypass
+  // decision) may be scheduled now; it waits for this grid's completion.
+  asm volatile("griddepcontrol.launch_dependents;");
   const uint32_t step = gridDim.x;
 
   if (threadIdx.x == 0) {
@@ -378,11 +381,12 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
         issue(s, G + kEncStages * step);  // refill now; the escapes are in the ring
       } else {
         // too many escapes for the ring: finish everything before, wait for
-        // this round's offsets and write the escapes from the stage
+        // this round's offsets and write the escapes from the stage, a block
+        // at a time through the ring (empty now)
         while (fin < j) finish(fin++);
         mbar_wait_bounded(&rs->pre_bar[r], (j / kEncSlots) & 1u, p.status);
         const uint64_t prefix = write_meta(j, ti, lt, cnt);
-        write_escapes<kUnitBlocks>(tb_s, te, prefix, T.esc, T.esc_cap);
+        write_escapes_coalesced<kUnitBlocks>(tb_s, te, prefix, T.esc, T.esc_cap, ring);
         __syncwarp();
         fin = j + 1;
         issue(s, G + kEncStages * step);

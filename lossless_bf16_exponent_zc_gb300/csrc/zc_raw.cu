@@ -10,18 +10,25 @@
 //
 // Design on sm_103a: one launch right after the encoder on the same stream,
 // so the decision reads the header's n_esc on the device and the host never
-// waits.  Every CTA reads the escape counts and reaches the same verdict; the
-// RAW tensors are rewritten by a grid-stride loop of 16-byte copies (offset
-// table zeroed, tile region and spill filled from the input); the last CTA to
+// waits.  It is a programmatic dependent launch: the encoder releases it as
+// soon as it starts, its small CTAs settle beside the encoder's and wait in
+// griddepcontrol.wait, and they read the headers the moment the encoder's
+// writes are visible -- no launch gap.  Every CTA reads the escape counts and
+// reaches the same verdict; when nothing goes RAW it leaves at once.  The RAW
+// tensors are rewritten by a grid-stride loop of 16-byte copies (offset table
+// zeroed, tile region and spill filled from the input); the last CTA to
 // finish -- after every CTA has read the counts -- writes the RAW headers
-// (flags and n_esc) and resets its counter in the workspace.  When nothing
-// goes RAW, each CTA only reads a few header words.
+// (flags and n_esc) and resets its counter in the workspace.
 #include "zc_device.cuh"
 #include "zc_internal.h"
 
 namespace zc {
 
-constexpr int kRawThreads = 512;
+// 256 threads at <= 40 registers (6 CTAs per SM) fit in what an encoder CTA
+// leaves free of an SM (21 warps at 80 registers), so the dependent launch can
+// be resident before the encoder ends.
+constexpr int kRawThreads = 256;
+constexpr int kRawUnroll = 4;     // 16-byte copies in flight per thread
 
 template <int MAXB>
 struct RawParams {
@@ -48,10 +55,11 @@ __device__ __forceinline__ bool goes_raw(const EncTensor& T, bool* overflow) {
 }
 
 template <int MAXB>
-__global__ void __launch_bounds__(kRawThreads) raw_switch_kernel(const __grid_constant__ RawParams<MAXB> p) {
+__global__ void __launch_bounds__(kRawThreads, 6) raw_switch_kernel(const __grid_constant__ RawParams<MAXB> p) {
   static_assert(MAXB <= 32, "one mask bit per tensor");
   __shared__ uint32_t raw_mask;
   if (threadIdx.x == 0) raw_mask = 0;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the encoder has finished and its writes are visible
   __syncthreads();
   for (int i = threadIdx.x; i < p.count; i += blockDim.x) {
     bool overflow;
@@ -60,6 +68,7 @@ __global__ void __launch_bounds__(kRawThreads) raw_switch_kernel(const __grid_co
   }
   __syncthreads();
   const uint32_t mask = raw_mask;
+  if (mask == 0) return;  // every CTA reached the same verdict: nothing to rewrite, no counter to touch
   const uint64_t tid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const uint64_t nthreads = static_cast<uint64_t>(gridDim.x) * blockDim.x;
   for (int i = 0; i < p.count; i++) {
@@ -72,33 +81,43 @@ __global__ void __launch_bounds__(kRawThreads) raw_switch_kernel(const __grid_co
     uint8_t* tiles = T.main + kHeader + tbl;
     const uint64_t table_chunks = tbl / 16;
     const uint64_t chunks = table_chunks + (region + spill + 15) / 16;
-    for (uint64_t c = tid; c < chunks; c += nthreads) {
-      if (c < table_chunks) {
-        *reinterpret_cast<uint4*>(T.main + kHeader + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
-        continue;
-      }
-      const uint64_t b = 16 * (c - table_chunks);  // byte of the RAW image
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (b + 16 <= two_n) {
-        v = __ldg(reinterpret_cast<const uint4*>(T.in + b / 2));
-      } else if (b < two_n) {
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        for (uint32_t j = 0; b + 2 * j < two_n; j++)
-          w[j >> 1] |= static_cast<uint32_t>(__ldg(T.in + b / 2 + j)) << (16 * (j & 1));
-        v = make_uint4(w[0], w[1], w[2], w[3]);
-      }
+    // 16 bytes of the RAW image at byte b (a multiple of 16), zero past 2n
+    auto load = [&](uint64_t b) -> uint4 {
+      if (b + 16 <= two_n) return __ldg(reinterpret_cast<const uint4*>(T.in + b / 2));
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      for (uint32_t j = 0; b + 2 * j < two_n; j++)
+        w[j >> 1] |= static_cast<uint32_t>(__ldg(T.in + b / 2 + j)) << (16 * (j & 1));
+      return make_uint4(w[0], w[1], w[2], w[3]);
+    };
+    auto store = [&](uint64_t b, uint4 v) {
       if (b < region) {
         *reinterpret_cast<uint4*>(tiles + b) = v;  // zero past 2n: the tile region's tail
+        return;
+      }
+      uint8_t* dst = T.esc + (b - region);
+      const uint64_t left = spill - (b - region);  // spill bytes from here, even
+      if (left >= 16) {
+        *reinterpret_cast<uint4*>(dst) = v;
       } else {
-        uint8_t* dst = T.esc + (b - region);
-        const uint64_t left = spill - (b - region);  // spill bytes from here, even
-        if (left >= 16) {
-          *reinterpret_cast<uint4*>(dst) = v;
-        } else {
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-          for (uint32_t j = 0; 2 * j < left; j++)
-            reinterpret_cast<uint16_t*>(dst)[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
-        }
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        for (uint32_t j = 0; 2 * j < left; j++)
+          reinterpret_cast<uint16_t*>(dst)[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+      }
+    };
+    for (uint64_t c = tid; c < table_chunks; c += nthreads)
+      *reinterpret_cast<uint4*>(T.main + kHeader + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
+    const uint64_t image_chunks = chunks - table_chunks;
+    for (uint64_t c0 = tid; c0 < image_chunks; c0 += kRawUnroll * nthreads) {
+      uint4 v[kRawUnroll];
+#pragma unroll
+      for (int u = 0; u < kRawUnroll; u++) {
+        const uint64_t c = c0 + u * nthreads;
+        v[u] = c < image_chunks ? load(16 * c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kRawUnroll; u++) {
+        const uint64_t c = c0 + u * nthreads;
+        if (c < image_chunks) store(16 * c, v[u]);
       }
     }
   }
@@ -133,12 +152,23 @@ static cudaError_t launch_raw_switch_t(const EncTensor* ts, int count, WsHeader*
   p.count = count;
   p.ws = ws;
   p.status = status;
-  uint64_t ctas = (chunks + kRawThreads - 1) / kRawThreads;
-  const uint64_t cap = 4ull * static_cast<uint64_t>(dev.sm_count);
+  uint64_t ctas = (chunks + kRawThreads * kRawUnroll - 1) / (kRawThreads * kRawUnroll);
+  const uint64_t cap = 6ull * static_cast<uint64_t>(dev.sm_count);  // a full SM of them keeps ~96 KB of copies in flight
   if (ctas > cap) ctas = cap;
   if (ctas == 0) ctas = 1;
-  raw_switch_kernel<MAXB><<<static_cast<unsigned>(ctas), kRawThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  // programmatic dependent launch: it may start while the encoder runs and
+  // waits for it in griddepcontrol.wait
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(kRawThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, raw_switch_kernel<MAXB>, p);
 }
 
 cudaError_t launch_raw_switch(const EncTensor* ts, int count, WsHeader* ws, int32_t* status, cudaStream_t stream,

@@ -13,9 +13,9 @@
 //     escape bytes, both completing on the stage's full barrier; the team's
 //     4 warps release the stage on its empty barrier.  Offset-table entries
 //     are prefetched a round ahead.
-//   * Each consumer decodes its block straight into its sums (two fp32 adds
-//     per instruction), rounds, stores, and -- when re-encoding -- encodes its
-//     block of the result from shared memory.
+//   * Each consumer decodes its block straight into its sums (one fp32 += bf16
+//     add per value, the decoded half-word as the addend), rounds, stores, and
+//     -- when re-encoding -- encodes its block of the result from shared memory.
 //   * A RAW shard (the raw bypass: the values' own bytes) stages nothing: the
 //     producer only signals the stage, and each consumer reads its block's
 //     values of that shard straight from global memory.
