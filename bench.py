@@ -484,7 +484,8 @@ def run_workloads(args, zc, torch, device, peak):
     """Per-kernel GB/s (uncompressed and algorithmic), HBM fraction, ratio and escape rate for the other
     workloads: the 2^20 Gaussian (L2-resident), the 9-tensor Llama-3-8B bucket (batched), the MoE payload
     (histogram codebook, 8 Zipf chunks batched), the reduce-scatter local stage (P = 8) with its
-    shard-size sweep, and the raw bypass (adaptive compression of coded and incompressible 2^26 tensors).
+    shard-size sweep, the raw bypass (adaptive compression of coded and incompressible 2^26 tensors), and the
+    zipped transfer pipeline (16 or 4 chunks on three streams against one stream and a plain copy).
     Inputs above L2 size are not flushed between repetitions of the same op."""
     import math as _m
     out = {}
@@ -637,6 +638,32 @@ def run_workloads(args, zc, torch, device, peak):
                         "stored_raw": is_raw, "bytes_sent": mb + spill, "ratio": round(2 * n / (mb + spill), 4),
                         "round_trip_ok": bool(ok)}}
     del xt, m_t, e_t, y
+
+    # 6. zipped transfer pipeline [CCCL §3.2, ZipCCL §2.D]: 2^26 N(0, 1e-3) values in chunks of 2^22 and 2^24,
+    #    compress / link (device-to-device copy standing in for the network) / decompress on three streams,
+    #    against the same calls on one stream and a plain copy of the uncompressed tensor
+    xt = dev(workloads.gaussian(n, sigma=workloads.RS_SIGMA, seed=6))
+    y = torch.empty(n, dtype=torch.int16, device=device)
+    yc = torch.empty_like(xt)
+    tcopy = _time_ms(torch, lambda: yc.copy_(xt), 10)
+    cur = torch.cuda.current_stream()
+    s3 = (cur, torch.cuda.Stream(device=device), torch.cuda.Stream(device=device))
+    pipe = {"uncompressed_device_copy_ms": round(tcopy, 4)}
+    for lg in (22, 24):
+        chunk = 1 << lg
+        pws = zc.pipeline_workspace(chunk, device=device)
+        t3 = _time_ms(torch, lambda: zc.pipelined_transfer(xt, cbg, chunk, pws, st, out=y, streams=s3), 10)
+        ok = torch.equal(y, xt)
+        t1 = _time_ms(torch, lambda: zc.pipelined_transfer(xt, cbg, chunk, pws, st, out=y, streams=(cur, cur, cur)),
+                      10)
+        pipe[f"chunks_2^{lg}"] = {
+            "chunks": n // chunk,
+            "three_streams": {"ms": round(t3, 4), "GB_per_s_uncompressed": round(2 * n / t3 / 1e6, 1)},
+            "one_stream": {"ms": round(t1, 4), "GB_per_s_uncompressed": round(2 * n / t1 / 1e6, 1)},
+            "overlap_speedup": round(t1 / t3, 3), "round_trip_ok": bool(ok)}
+        del pws
+    out["pipelined_transfer_2^26"] = pipe
+    del xt, y, yc
 
     if zc.status_value(st) != 0:
         out["status"] = zc.status_string(zc.status_value(st))

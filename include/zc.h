@@ -19,7 +19,8 @@
  *         local reduction; MoE all-to-all sends a fixed-size part first and a
  *         variable-size part after it.
  * and [CCCL §x] cites the jsqmd.com article on CCCL, an in-GPU
- * compression-coupled collective communication library: §3.3 (adaptive
+ * compression-coupled collective communication library: §3.2 (chunked
+ * compress / transfer / decompress on separate streams), §3.3 (adaptive
  * choice of whether to compress), §5.2 (falling back to uncompressed data).
  *
  * ------------------------------------------------------------------------
@@ -292,6 +293,42 @@ typedef struct zc_tensor {
  */
 zc_status zc_compress_batched(int count, const zc_tensor* h_tensors, void* d_ws, uint64_t ws_bytes,
                               int32_t* d_status, void* stream);
+/*
+ * Zipped transfer pipeline ([CCCL §3.2]; the static/dynamic split of
+ * [ZipCCL §2.D]): moves n bf16 values from d_in to d_out the way a compressed
+ * collective moves them over a link -- in chunks of chunk_elems values, with
+ * three stages overlapped on three streams:
+ *   stream_compress    chunk k      zc_compress_adaptive into send slot k % 2
+ *   stream_link        chunk k - 1  the fixed-size main stream (one
+ *                                   device-to-device copy: the static part),
+ *                                   then exactly n_esc escape bytes, n_esc
+ *                                   read on the device from the header that
+ *                                   just arrived (the dynamic part)
+ *   stream_decompress  chunk k - 2  zc_decompress from receive slot k % 2
+ *                                   into d_out
+ * On one GPU the receive slots (in the workspace) stand in for the peer's
+ * buffers and the copy for the link.  Send and receive slots are double
+ * buffered: compressing chunk k waits until the link has taken chunk k - 2
+ * out of the send slot, and the link waits until chunk k - 2 has been decoded
+ * out of the receive slot.  Each chunk is compressed adaptively (a chunk the
+ * coding does not shrink travels RAW), so its escape slot (5/8 of a chunk's
+ * values in bytes) never overflows.
+ *   - The stages start after all work already enqueued on stream_compress;
+ *     when the call's work on stream_decompress is done, d_out holds the
+ *     values, and stream_compress and stream_link also wait for that point.
+ *     The three streams may be the same stream (then nothing overlaps).
+ *   - chunk_elems: a positive multiple of 8; d_in, d_out 16-byte aligned.
+ *   - d_ws: zc_pipeline_workspace_size(chunk_elems) bytes, 256-byte aligned,
+ *     zero-filled before its first use (like every workspace).  Calls that
+ *     share it must be ordered.
+ *   - The call creates and releases seven CUDA events (no device memory).
+ *   - Device errors of any stage go to *d_status.
+ */
+zc_status zc_pipeline_workspace_size(uint64_t chunk_elems, uint64_t* bytes);
+zc_status zc_pipelined_transfer(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_out,
+                                uint64_t chunk_elems, void* d_ws, uint64_t ws_bytes, int32_t* d_status,
+                                void* stream_compress, void* stream_link, void* stream_decompress);
+
 /* zc_compress_batched with the raw bypass of zc_compress_adaptive, decided per tensor. */
 zc_status zc_compress_batched_adaptive(int count, const zc_tensor* h_tensors, void* d_ws, uint64_t ws_bytes,
                                        int32_t* d_status, void* stream);

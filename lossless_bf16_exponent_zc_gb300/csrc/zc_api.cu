@@ -309,6 +309,27 @@ zc_status zc_compress_batched_adaptive(int count, const zc_tensor* h_tensors, vo
   return compress_batched(count, h_tensors, d_ws, ws_bytes, d_status, stream, true);
 }
 
+zc_status zc_pipeline_workspace_size(uint64_t chunk_elems, uint64_t* bytes) {
+  if (!bytes || chunk_elems == 0 || chunk_elems % 8 != 0) return ZC_ERR_INVALID_ARG;
+  if (chunk_elems > kMaxN) return ZC_ERR_TOO_LARGE;
+  *bytes = pipeline_workspace_bytes(chunk_elems);
+  return ZC_OK;
+}
+zc_status zc_pipelined_transfer(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_out,
+                                uint64_t chunk_elems, void* d_ws, uint64_t ws_bytes, int32_t* d_status,
+                                void* stream_compress, void* stream_link, void* stream_decompress) {
+  if (!d_status || !d_cb || !d_ws || ((!d_in || !d_out) && n) || chunk_elems == 0 || chunk_elems % 8 != 0)
+    return ZC_ERR_INVALID_ARG;
+  if (chunk_elems > kMaxN) return ZC_ERR_TOO_LARGE;
+  if (!aligned(d_in, 16) || !aligned(d_out, 16) || !aligned(d_ws, 256) || !aligned(d_status, 4))
+    return ZC_ERR_ALIGNMENT;
+  if (ws_bytes < pipeline_workspace_bytes(chunk_elems)) return ZC_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return ZC_ERR_CUDA;
+  return cuda_status(launch_pipeline(static_cast<const uint16_t*>(d_in), n, d_cb, static_cast<uint16_t*>(d_out),
+                                     chunk_elems, static_cast<uint8_t*>(d_ws), d_status, as_stream(stream_compress),
+                                     as_stream(stream_link), as_stream(stream_decompress), dev));
+}
 zc_status zc_decompress_batched(int count, const zc_tensor* h_tensors, int32_t* d_status, void* stream) {
   if (count < 1 || !h_tensors || !d_status) return ZC_ERR_INVALID_ARG;
   if (!aligned(d_status, 4)) return ZC_ERR_ALIGNMENT;

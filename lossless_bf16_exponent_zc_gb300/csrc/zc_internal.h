@@ -76,6 +76,14 @@ cudaError_t launch_raw_switch(const EncTensor* ts, int count, WsHeader* ws, int3
 cudaError_t launch_decode(const DecTensor* ts, int count, int32_t* status, cudaStream_t stream,
                           const DeviceInfo& dev);
 
+// Zipped transfer pipeline of n values in chunks of c (a multiple of 8):
+// compress on sc, link on sl, decompress on sd; ws holds
+// pipeline_workspace_bytes(c) bytes (zero-filled before first use).
+uint64_t pipeline_workspace_bytes(uint64_t c);
+cudaError_t launch_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, uint16_t* out, uint64_t c,
+                            uint8_t* ws, int32_t* status, cudaStream_t sc, cudaStream_t sl, cudaStream_t sd,
+                            const DeviceInfo& dev);
+
 cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out, const uint8_t* out_cb,
                           uint8_t* out_main, uint8_t* out_esc, uint64_t out_cap, WsHeader* ws, Flag* flags,
                           int32_t* status, cudaStream_t stream, const DeviceInfo& dev);

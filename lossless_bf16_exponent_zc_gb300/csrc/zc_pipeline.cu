@@ -1,0 +1,149 @@
+// zc_pipeline.cu -- the zipped transfer pipeline: compress, link and decompress
+// overlapped chunk by chunk on three streams.
+//
+// [CCCL §3.2] cuts a tensor into chunks and runs three stages concurrently on
+// separate streams: compress chunk k, transfer chunk k - 1, decompress chunk
+// k - 2, with double-buffered send and receive buffers.  [ZipCCL §2.D] sends
+// each compressed tensor in two parts: a fixed-size part first (here the main
+// stream, whose size depends on n alone) and a variable-size part after it
+// (the escape stream, n_esc bytes).
+//
+// On one GPU the link is a device-to-device copy into receive slots that stand
+// in for the peer's buffers.  The static part is one cudaMemcpyAsync of the
+// main stream (its size is known on the host); the dynamic part is sized on the
+// device: a small kernel reads n_esc from the header that just arrived and
+// copies exactly that many escape bytes -- the host never waits for a count.
+// Chunks are compressed adaptively, so an incompressible chunk travels RAW and
+// an escape slot of 5/8 of the chunk's values never overflows.
+#include "zc_device.cuh"
+#include "zc_internal.h"
+
+namespace zc {
+
+constexpr int kLinkThreads = 256;
+
+// Copies the dynamic part of a chunk: n_esc escape bytes, n_esc read from the
+// main stream's header (clamped to the slot's capacity; a bad count is then
+// caught by the decoder's header check).  Both buffers are 16-byte aligned.
+__global__ void __launch_bounds__(kLinkThreads) link_escapes_kernel(const uint8_t* __restrict__ main,
+                                                                    const uint8_t* __restrict__ src,
+                                                                    uint8_t* __restrict__ dst, uint64_t cap) {
+  uint64_t n_esc = __ldcg(reinterpret_cast<const unsigned long long*>(main + 24));
+  if (n_esc > cap) n_esc = cap;
+  const uint64_t tid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const uint64_t nthreads = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  const uint64_t vecs = n_esc / 16;
+  for (uint64_t i = tid; i < vecs; i += nthreads)
+    reinterpret_cast<uint4*>(dst)[i] = __ldcg(reinterpret_cast<const uint4*>(src) + i);
+  for (uint64_t i = 16 * vecs + tid; i < n_esc; i += nthreads) dst[i] = src[i];
+}
+
+// Workspace of a pipeline with chunks of c values: the encoder's workspace,
+// then two send and two receive slots of (main stream, escape buffer).
+struct PipeLayout {
+  uint64_t enc_bytes, main_bytes, esc_bytes, slot_bytes, total;
+};
+
+static uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+static PipeLayout pipeline_layout(uint64_t c) {
+  PipeLayout L;
+  L.enc_bytes = round_up(ZC_WORKSPACE_HEADER_BYTES + ZC_WORKSPACE_BYTES_PER_TILE * num_tiles(c), 256);
+  L.main_bytes = round_up(main_bytes(c), 256);
+  // 5m/8 bounds the RAW spill of every chunk of m <= c values (the last one
+  // may be shorter and spill more than a full chunk would when c is not a
+  // multiple of 4096), so an adaptive chunk never overflows its slot
+  L.esc_bytes = round_up((5 * c + 7) / 8 + 16, 256);
+  L.slot_bytes = L.main_bytes + L.esc_bytes;
+  L.total = L.enc_bytes + 4 * L.slot_bytes;
+  return L;
+}
+
+uint64_t pipeline_workspace_bytes(uint64_t c) { return pipeline_layout(c).total; }
+
+namespace {
+
+// Events of one call, destroyed (after their last use is enqueued) on return.
+struct Events {
+  cudaEvent_t fork = nullptr, comp[2] = {nullptr, nullptr}, link[2] = {nullptr, nullptr},
+              dec[2] = {nullptr, nullptr};
+  cudaError_t create() {
+    cudaError_t e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+    for (int s = 0; s < 2 && e == cudaSuccess; s++) {
+      e = cudaEventCreateWithFlags(&comp[s], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&link[s], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&dec[s], cudaEventDisableTiming);
+    }
+    return e;
+  }
+  ~Events() {
+    for (cudaEvent_t ev : {fork, comp[0], comp[1], link[0], link[1], dec[0], dec[1]})
+      if (ev) cudaEventDestroy(ev);
+  }
+};
+
+#define ZC_TRY(x)                              \
+  do {                                         \
+    cudaError_t e_ = (x);                      \
+    if (e_ != cudaSuccess) return e_;          \
+  } while (0)
+
+}  // namespace
+
+cudaError_t launch_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, uint16_t* out, uint64_t c,
+                            uint8_t* ws, int32_t* status, cudaStream_t sc, cudaStream_t sl, cudaStream_t sd,
+                            const DeviceInfo& dev) {
+  if (n == 0) return cudaSuccess;
+  const PipeLayout L = pipeline_layout(c);
+  WsHeader* enc_ws = reinterpret_cast<WsHeader*>(ws);
+  Flag* enc_flags = reinterpret_cast<Flag*>(ws + ZC_WORKSPACE_HEADER_BYTES);
+  uint8_t* slots = ws + L.enc_bytes;
+  auto send_main = [&](int s) { return slots + s * L.slot_bytes; };
+  auto send_esc = [&](int s) { return slots + s * L.slot_bytes + L.main_bytes; };
+  auto recv_main = [&](int s) { return slots + (2 + s) * L.slot_bytes; };
+  auto recv_esc = [&](int s) { return slots + (2 + s) * L.slot_bytes + L.main_bytes; };
+  const uint64_t esc_cap = L.esc_bytes;
+
+  Events ev;
+  ZC_TRY(ev.create());
+  // the other two streams start after everything already enqueued on the compress stream
+  ZC_TRY(cudaEventRecord(ev.fork, sc));
+  ZC_TRY(cudaStreamWaitEvent(sl, ev.fork, 0));
+  ZC_TRY(cudaStreamWaitEvent(sd, ev.fork, 0));
+  const uint64_t chunks = (n + c - 1) / c;
+  int last = 0;
+  for (uint64_t k = 0; k < chunks; k++) {
+    const int s = static_cast<int>(k & 1u);
+    last = s;
+    const uint64_t m = n - k * c < c ? n - k * c : c;
+    // compress chunk k into send slot s once the link has taken chunk k - 2 out of it
+    if (k >= 2) ZC_TRY(cudaStreamWaitEvent(sc, ev.link[s], 0));
+    EncTensor t{in + k * c, send_main(s), send_esc(s), cb, m, esc_cap};
+    ZC_TRY(launch_encode(&t, 1, enc_ws, enc_flags, status, sc, dev, true));
+    ZC_TRY(launch_raw_switch(&t, 1, enc_ws, status, sc, dev));
+    ZC_TRY(cudaEventRecord(ev.comp[s], sc));
+    // link: the static part (fixed-size main stream), then the dynamic part
+    // (n_esc escape bytes, counted on the device), once receive slot s is free
+    ZC_TRY(cudaStreamWaitEvent(sl, ev.comp[s], 0));
+    if (k >= 2) ZC_TRY(cudaStreamWaitEvent(sl, ev.dec[s], 0));
+    ZC_TRY(cudaMemcpyAsync(recv_main(s), send_main(s), main_bytes(m), cudaMemcpyDeviceToDevice, sl));
+    uint64_t blocks = (raw_spill(m) + kLinkThreads * 16 - 1) / (kLinkThreads * 16);
+    if (blocks > static_cast<uint64_t>(dev.sm_count)) blocks = dev.sm_count;
+    if (blocks == 0) blocks = 1;
+    link_escapes_kernel<<<static_cast<unsigned>(blocks), kLinkThreads, 0, sl>>>(recv_main(s), send_esc(s),
+                                                                                 recv_esc(s), esc_cap);
+    ZC_TRY(cudaGetLastError());
+    ZC_TRY(cudaEventRecord(ev.link[s], sl));
+    // decompress chunk k from receive slot s
+    ZC_TRY(cudaStreamWaitEvent(sd, ev.link[s], 0));
+    DecTensor d{recv_main(s), recv_esc(s), out + k * c, m, esc_cap};
+    ZC_TRY(launch_decode(&d, 1, status, sd, dev));
+    ZC_TRY(cudaEventRecord(ev.dec[s], sd));
+  }
+  // join: the compress and link streams continue after the last chunk is decoded
+  ZC_TRY(cudaStreamWaitEvent(sc, ev.dec[last], 0));
+  ZC_TRY(cudaStreamWaitEvent(sl, ev.dec[last], 0));
+  return cudaSuccess;
+}
+
+}  // namespace zc

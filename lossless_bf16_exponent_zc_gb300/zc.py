@@ -79,9 +79,12 @@ def load() -> ctypes.CDLL:
     lib.zc_compress_batched.argtypes = [i32, ctypes.POINTER(ZcTensor), vp, u64, vp, vp]
     lib.zc_compress_batched_adaptive.argtypes = [i32, ctypes.POINTER(ZcTensor), vp, u64, vp, vp]
     lib.zc_decompress_batched.argtypes = [i32, ctypes.POINTER(ZcTensor), vp, vp]
+    lib.zc_pipeline_workspace_size.argtypes = [u64, u64p]
+    lib.zc_pipelined_transfer.argtypes = [vp, u64, vp, vp, u64, vp, u64, vp, vp, vp, vp]
     for name in ("zc_codebook_from_sigma", "zc_compressed_size", "zc_workspace_size", "zc_histogram_topk",
                  "zc_compress", "zc_compress_adaptive", "zc_raw_spill", "zc_decompress", "zc_decompress_reduce",
-                 "zc_compress_batched", "zc_compress_batched_adaptive", "zc_decompress_batched"):
+                 "zc_compress_batched", "zc_compress_batched_adaptive", "zc_decompress_batched",
+                 "zc_pipeline_workspace_size", "zc_pipelined_transfer"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -281,6 +284,38 @@ def compress_batched_adaptive(items: Sequence[BatchItem], ws: torch.Tensor, stat
 def decompress_batched(items: Sequence[BatchItem], status: torch.Tensor, stream=None) -> None:
     arr = _descs(items)
     _check(load().zc_decompress_batched(len(items), arr, _ptr(status), _stream(stream)), "zc_decompress_batched")
+
+
+def pipeline_workspace_size(chunk_elems: int) -> int:
+    out = ctypes.c_uint64()
+    _check(load().zc_pipeline_workspace_size(int(chunk_elems), ctypes.byref(out)), "zc_pipeline_workspace_size")
+    return out.value
+
+
+def pipeline_workspace(chunk_elems: int, device="cuda") -> torch.Tensor:
+    """A zero-filled pipeline workspace (256-byte aligned, as the caching allocator returns)."""
+    return torch.zeros(pipeline_workspace_size(chunk_elems), dtype=torch.uint8, device=device)
+
+
+def pipelined_transfer(x: torch.Tensor, cb: torch.Tensor, chunk_elems: int, ws: torch.Tensor, status: torch.Tensor,
+                       out: torch.Tensor | None = None, streams=None) -> torch.Tensor:
+    """Zipped transfer of x into out through the compress / link / decompress pipeline.
+
+    streams: (compress, link, decompress) torch streams; default: the current
+    stream and two new ones.  out is ready once the current (compress) stream
+    reaches this point.
+    """
+    n = _nelem16(x)
+    if out is None:
+        out = torch.empty(n, dtype=torch.int16, device=x.device)
+    if streams is None:
+        cur = torch.cuda.current_stream()
+        streams = (cur, torch.cuda.Stream(device=x.device), torch.cuda.Stream(device=x.device))
+    sc, sl, sd = (s.cuda_stream for s in streams)
+    rc = load().zc_pipelined_transfer(_ptr(x), n, _ptr(cb), _ptr(out), int(chunk_elems), _ptr(ws), ws.numel(),
+                                      _ptr(status), sc, sl, sd)
+    _check(rc, "zc_pipelined_transfer")
+    return out
 
 
 # ------------------------------------------------------------------ small host helpers

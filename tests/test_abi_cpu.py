@@ -25,7 +25,7 @@ def test_library_exports_every_declared_symbol():
     assert {"zc_codebook_from_sigma", "zc_histogram_topk", "zc_compress", "zc_decompress", "zc_decompress_reduce",
             "zc_compressed_size", "zc_workspace_size", "zc_compress_batched", "zc_decompress_batched",
             "zc_status_string", "zc_version", "zc_compress_adaptive", "zc_compress_batched_adaptive",
-            "zc_raw_spill"} <= set(names)
+            "zc_raw_spill", "zc_pipeline_workspace_size", "zc_pipelined_transfer"} <= set(names)
     for name in names:
         assert hasattr(lib, name), name
 
@@ -118,3 +118,21 @@ def test_adaptive_argument_errors_are_synchronous():
     assert _raw("zc_compress_batched_adaptive", 0, None, None, 0, status, None) == E.ERR_INVALID_ARG
     with pytest.raises(zc.ZcError):
         zc.raw_spill(1 << 32)
+
+
+def test_pipeline_workspace_size():
+    for c in (8, 4096, 4104, 1 << 20):
+        ws = zc.pipeline_workspace_size(c)
+        # the encoder's workspace plus two send and two receive slots of a main stream and escape bytes
+        assert ws >= zc.workspace_size(c) + 4 * (oracle.main_bytes(c) + oracle.raw_spill(c))
+    for bad in (0, 4, 4100):
+        with pytest.raises(zc.ZcError) as e:
+            zc.pipeline_workspace_size(bad)
+        assert e.value.code == zc.ERR_INVALID_ARG
+    fake, status = 1 << 20, 1 << 21
+    assert _raw("zc_pipelined_transfer", fake, 10, fake, fake, 4100, fake, 1 << 30, status, None, None,
+                None) == zc.ERR_INVALID_ARG
+    assert _raw("zc_pipelined_transfer", fake + 2, 10, fake, fake, 4096, fake, 1 << 30, status, None, None,
+                None) == zc.ERR_ALIGNMENT
+    assert _raw("zc_pipelined_transfer", fake, 10, fake, fake, 4096, fake, 100, status, None, None,
+                None) == zc.ERR_WORKSPACE
