@@ -598,6 +598,34 @@ def run_workloads(args, zc, torch, device, peak):
         return r
 
     out["reduce_scatter_8x2^25"] = reduce_case(1 << 25)
+    # the senders' side of the same workload: compress and decompress of 2^25-element shards, cycling
+    # through the 8 shards (and 8 output buffers) so that consecutive calls miss L2
+    m = 1 << 25
+    ws_ = zc.workspace(m, device=device)
+    mb_, eb_ = zc.compressed_size(m)
+    sm_ = [torch.empty(mb_, dtype=torch.uint8, device=device) for _ in range(P)]
+    se_ = [torch.empty(eb_, dtype=torch.uint8, device=device) for _ in range(P)]
+    sy_ = [torch.empty(m, dtype=torch.int16, device=device) for _ in range(P)]
+    it = [0]
+
+    def shard_compress():
+        i = it[0] % P
+        it[0] += 1
+        zc.compress(base[i], cb_in, ws_, st, main=sm_[i], esc=se_[i])
+
+    def shard_decompress():
+        i = it[0] % P
+        it[0] += 1
+        zc.decompress(sm_[i], se_[i], m, st, out=sy_[i])
+
+    tc_ = _time_ms(torch, shard_compress, 4 * P)
+    k_ = sum(zc.header_n_esc(t) for t in sm_) / P
+    td_ = _time_ms(torch, shard_decompress, 4 * P)
+    out["reduce_scatter_shard_2^25"] = {"compress": entry(tc_, 2 * m, 2 * m + mb_ + k_),
+                                        "decompress": entry(td_, 2 * m, 2 * m + mb_ + k_),
+                                        "ratio": round(2 * m / (mb_ + k_), 4), "escape_rate": round(k_ / m, 5),
+                                        "l2": "8 shards and 8 output sets in rotation (512 MB of inputs)"}
+    del ws_, sm_, se_, sy_
     sweep = []
     for lg in range(15, args.sweep_max_log2 + 1):
         sweep.append(reduce_case(1 << lg))
