@@ -24,6 +24,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "zc_oracle.c")
+_QSRC = os.path.join(_HERE, "qlc_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -45,11 +46,12 @@ class OracleError(RuntimeError):
 def build(force: bool = False) -> str:
     """Compile zc_oracle.c into liboracle.so (plain C11, no fast-math, no FMA contraction)."""
     with _lock:
-        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        newest = max(os.path.getmtime(_SRC), os.path.getmtime(_QSRC))
+        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
             tmp = _LIB + f".tmp{os.getpid()}"
             subprocess.check_call([
                 "gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
-                "-fno-fast-math", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm",
+                "-fno-fast-math", "-Wall", "-Wextra", "-o", tmp, _SRC, _QSRC, "-lm",
             ])
             os.replace(tmp, _LIB)
     return _LIB
@@ -85,6 +87,18 @@ def _load():
                                          ctypes.POINTER(ctypes.c_int)]
     lib.zo_compress_adaptive.restype = ctypes.c_int
     lib.zo_decompress.argtypes = [u8p, u8p, ctypes.c_uint64, ctypes.c_uint64, u16p]
+    lib.zqo_table_is_valid.argtypes = [u8p, u8p]
+    lib.zqo_table_is_valid.restype = ctypes.c_int
+    lib.zqo_table_from_histogram.argtypes = [u64p, u8p]
+    lib.zqo_table_from_histogram.restype = None
+    lib.zqo_code_length.argtypes = [u8p, u8p, ctypes.c_uint]
+    lib.zqo_code_length.restype = ctypes.c_int
+    lib.zqo_max_bytes.argtypes = [ctypes.c_uint64]
+    lib.zqo_max_bytes.restype = ctypes.c_uint64
+    lib.zqo_compress.argtypes = [u8p, ctypes.c_uint64, u8p, u8p, u8p, ctypes.c_uint64, u64p]
+    lib.zqo_compress.restype = ctypes.c_int
+    lib.zqo_decompress.argtypes = [u8p, ctypes.c_uint64, ctypes.c_uint64, u8p]
+    lib.zqo_decompress.restype = ctypes.c_int
     lib.zo_decompress.restype = ctypes.c_int
     lib.zo_float_to_bf16_rne.argtypes = [ctypes.c_float]
     lib.zo_float_to_bf16_rne.restype = ctypes.c_uint16
@@ -284,3 +298,67 @@ def header_fields(main) -> dict:
         "n_esc": int.from_bytes(b[24:32], "little"),
         "codebook": list(b[32:39]),
     }
+
+
+# ---------------------------------------------------------------- QLC (FP8 e4m3), qlc_oracle.c
+QLC_DEFAULT_WIDTHS = (3, 3, 3, 3, 3, 4, 5, 8)  # reading Q2: code lengths 6/7/8/11
+Q_OK, Q_ERR_ARG, Q_ERR_TABLE, Q_ERR_HEADER, Q_ERR_CORRUPT, Q_ERR_SIZE, Q_ERR_ROOM = range(7)
+
+
+def _u8(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.uint8))
+
+
+def qlc_table_from_histogram(hist) -> np.ndarray:
+    """rank -> symbol, ordered by (count desc, symbol asc) (reading Q2)."""
+    h = np.ascontiguousarray(np.asarray(hist, dtype=np.uint64).reshape(256))
+    sym = np.zeros(256, np.uint8)
+    _load().zqo_table_from_histogram(_ptr(h, ctypes.c_uint64), _ptr(sym, ctypes.c_uint8))
+    return sym
+
+
+def qlc_table_for(x) -> np.ndarray:
+    return qlc_table_from_histogram(np.bincount(_u8(x), minlength=256))
+
+
+def qlc_table_is_valid(widths, sym) -> bool:
+    w, s = _u8(widths), _u8(sym)
+    return bool(_load().zqo_table_is_valid(_ptr(w, ctypes.c_uint8), _ptr(s, ctypes.c_uint8)))
+
+
+def qlc_code_length(widths, sym, symbol: int) -> int:
+    w, s = _u8(widths), _u8(sym)
+    return int(_load().zqo_code_length(_ptr(w, ctypes.c_uint8), _ptr(s, ctypes.c_uint8), int(symbol)))
+
+
+def qlc_max_bytes(n: int) -> int:
+    return int(_load().zqo_max_bytes(n))
+
+
+def qlc_compress(x, widths, sym) -> np.ndarray:
+    """Encode bytes x into a ZQ1 stream (reading Q3); returns the stream bytes."""
+    x, w, s = _u8(x), _u8(widths), _u8(sym)
+    cap = qlc_max_bytes(x.size)
+    out = np.zeros(cap, np.uint8)
+    nbytes = ctypes.c_uint64(0)
+    xb = x if x.size else np.zeros(1, np.uint8)
+    rc = _load().zqo_compress(_ptr(xb, ctypes.c_uint8), x.size, _ptr(w, ctypes.c_uint8), _ptr(s, ctypes.c_uint8),
+                              _ptr(out, ctypes.c_uint8), cap, ctypes.byref(nbytes))
+    if rc != Q_OK:
+        raise OracleError(rc, "qlc_compress")
+    return out[: nbytes.value].copy()
+
+
+def qlc_decompress_status(stream, n: int):
+    st = _u8(stream)
+    sb = st if st.size else np.zeros(1, np.uint8)
+    out = np.zeros(max(n, 1), np.uint8)
+    rc = _load().zqo_decompress(_ptr(sb, ctypes.c_uint8), st.size, n, _ptr(out, ctypes.c_uint8))
+    return rc, out[:n]
+
+
+def qlc_decompress(stream, n: int) -> np.ndarray:
+    rc, out = qlc_decompress_status(stream, n)
+    if rc != Q_OK:
+        raise OracleError(rc, "qlc_decompress")
+    return out

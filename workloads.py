@@ -25,6 +25,11 @@ Workloads (n = elements):
   random_bits   n = 2^26 uniformly random 16-bit patterns, seed 6 -- data the
                 exponent coding cannot shrink (exponents spread over all 256
                 values), the case of the raw bypass
+  fp8_ffn1      n = 2^26 FP8 e4m3 bytes: GELU(z), z ~ N(0, 1), scaled so the
+                largest magnitude maps to 448 (the e4m3 maximum) and rounded to
+                e4m3 by torch (round to nearest even); seed 7 -- a stand-in for
+                the FFN1 activations of the QLC article's Gemma 2B layers
+  fp8_gradient  n = 2^26 e4m3 bytes of N(0, 1) scaled the same way; seed 8
 """
 from __future__ import annotations
 
@@ -137,6 +142,23 @@ def rs_shards(P: int = 8, m: int = 1 << 25, sigma: float = RS_SIGMA, seed: int =
 def random_bits(n: int = 1 << 26, seed: int = 6) -> np.ndarray:
     """Uniformly random bf16 bit patterns (NaNs and infinities included)."""
     return np.random.default_rng(seed).integers(0, 65536, n, dtype=np.uint16)
+
+
+def to_e4m3_bits(values: np.ndarray) -> np.ndarray:
+    """Scale so that max |value| becomes 448, round to float8 e4m3 (torch, nearest even); return the bytes."""
+    v = torch.from_numpy(np.ascontiguousarray(values, dtype=np.float32))
+    amax = float(v.abs().max()) if v.numel() else 1.0
+    v = v * (448.0 / amax if amax > 0 else 1.0)
+    return v.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+
+
+def fp8_ffn1(n: int = 1 << 26, seed: int = 7) -> np.ndarray:
+    z = torch.from_numpy(np.random.default_rng(seed).standard_normal(n, dtype=np.float32))
+    return to_e4m3_bits(torch.nn.functional.gelu(z).numpy())
+
+
+def fp8_gradient(n: int = 1 << 26, seed: int = 8) -> np.ndarray:
+    return to_e4m3_bits(np.random.default_rng(seed).standard_normal(n, dtype=np.float32))
 
 
 def all_bf16_patterns() -> np.ndarray:
