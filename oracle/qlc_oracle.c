@@ -39,9 +39,10 @@
  *       128); u32 word offset of each block in the payload (zero-padded to a
  *       multiple of 128 bytes); the payload.  Block b (symbols 4096 b ...)
  *       is 8 words of lane word counts (byte l = words of lane l) followed
- *       by the words of lanes 0..31.  Lane l codes the block's symbols
- *       l, l + 32, l + 64, ... (those below n) into little-endian u32 words,
- *       first code at bit 31 of its first word, the last word zero-padded.
+ *       by the words of lanes 0..31.  The block's 4096 symbols form 256 runs
+ *       of 16; lane l codes runs l, l + 32, ..., l + 224 in that order (the
+ *       symbols below n) into little-endian u32 words, first code at bit 31 of
+ *       its first word, the last word zero-padded.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -71,6 +72,9 @@ static uint64_t q_get_u64(const uint8_t *p) {
 }
 
 uint64_t zqo_num_blocks(uint64_t n) { return (n + Q_BLOCK - 1) / Q_BLOCK; }
+
+/* the j-th symbol (0..127) of lane l within its block: run l + 32 (j / 16), position j % 16 */
+static uint64_t q_lane_symbol(unsigned l, unsigned j) { return 16u * (l + 32u * (j / 16u)) + j % 16u; }
 static uint64_t q_table_bytes(uint64_t nblocks) { return (4 * nblocks + 127) / 128 * 128; }
 
 /* ---- the table, readings Q1 and Q2 --------------------------------------- */
@@ -169,7 +173,7 @@ int zqo_compress(const uint8_t *x, uint64_t n, const uint8_t w[8], const uint8_t
     for (unsigned l = 0; l < Q_LANES; l++) {
       BitWriter bw = {lane_words[l], 44, 0};
       for (unsigned j = 0; j < Q_BLOCK / Q_LANES; j++) {
-        uint64_t i = b * Q_BLOCK + l + (uint64_t)Q_LANES * j;
+        uint64_t i = b * Q_BLOCK + q_lane_symbol(l, j);
         if (i >= n) break;
         unsigned k = rank_of[x[i]], start = 0;
         int r = q_region(w, k, &start);
@@ -228,7 +232,7 @@ int zqo_decompress(const uint8_t *in, uint64_t in_bytes, uint64_t n, uint8_t *x)
       if (limit > end - off) return Q_ERR_CORRUPT;
       uint64_t bit = 0; /* bits read from this lane's words */
       for (unsigned j = 0; j < Q_BLOCK / Q_LANES; j++) {
-        uint64_t i = b * Q_BLOCK + l + (uint64_t)Q_LANES * j;
+        uint64_t i = b * Q_BLOCK + q_lane_symbol(l, j);
         if (i >= n) break;
         uint32_t v[2] = {0, 0};
         unsigned need[2] = {3, 0};

@@ -63,8 +63,8 @@ def test_article_lookup_example_codes():
     for symbol in (113, 24):
         assert oracle.qlc_code_length(DEFAULT, sym, symbol) == 6
     s = oracle.qlc_compress(np.array([113, 24], np.uint8), DEFAULT, sym)
-    lane0, lane1 = s[512 + 32:512 + 40].view("<u4")
-    assert lane0 >> 26 == 0b000000 and lane1 >> 26 == 0b000001
+    (word,) = s[512 + 32:512 + 36].view("<u4")  # lane 0 codes both: 000000 000001, then padding
+    assert word >> 20 == 0b000000_000001
 
 
 @pytest.mark.parametrize("widths", [DEFAULT, DYNAMIC, (8, 0, 0, 0, 0, 0, 0, 0), (0, 1, 2, 3, 4, 5, 6, 8)])
