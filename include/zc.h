@@ -125,7 +125,8 @@ typedef enum zc_status {
   ZC_ERR_CORRUPT_STREAM = 9,  /* offset table inconsistent with the code planes or the escape stream */
   ZC_ERR_SIZE_MISMATCH = 10,  /* header n differs from the n passed in */
   ZC_ERR_TIMEOUT = 11,        /* an inter-block wait gave up (about one second); output invalid */
-  ZC_ERR_DUP_CODEBOOK = 12    /* a device codebook holds a repeated exponent; nothing was encoded */
+  ZC_ERR_DUP_CODEBOOK = 12,   /* a device codebook holds a repeated exponent; nothing was encoded */
+  ZC_ERR_OUT_OF_ROOM = 13     /* the output buffer is smaller than the stream (QLC) */
 } zc_status;
 
 /* Human-readable name of a status value (static string, never NULL). */
@@ -333,6 +334,71 @@ zc_status zc_pipelined_transfer(const void* d_in, uint64_t n, const uint8_t* d_c
 zc_status zc_compress_batched_adaptive(int count, const zc_tensor* h_tensors, void* d_ws, uint64_t ws_bytes,
                                        int32_t* d_status, void* stream);
 zc_status zc_decompress_batched(int count, const zc_tensor* h_tensors, int32_t* d_status, void* stream);
+
+/*
+ * ------------------------------------------------------------------------
+ * Quad Length Codes for FP8 (e4m3) bytes -- [QLC §x] cites the ijyty.com
+ * article on QLC for lossless compression of e4m3 tensors in LLM training:
+ * §3.1 a 3-bit prefix splits the frequency-ranked symbol space into 8
+ * regions with only four code lengths, §3.2 the static table (6/7/8/11-bit
+ * codes), §3.3 dynamic tables per layer, §4.1-§4.2 one lookup per symbol.
+ * ------------------------------------------------------------------------
+ * TABLE: width[r] (r = 0..7) = bits after the prefix in region r; sym[k] = the
+ *   byte value of frequency rank k (a permutation of 0..255).  Region r holds
+ *   ranks [s_r, s_r + 2^width[r]), s_0 = 0, s_(r+1) = s_r + 2^width[r]; rank k
+ *   in region r is coded as r (3 bits) then k - s_r (width[r] bits), most
+ *   significant bit first.  Valid when every width <= 8 and
+ *   sum 2^width[r] >= 256.  Every byte value (NaN, Inf included) has a code.
+ * STREAM "ZQ1" of n bytes (one buffer, little-endian):
+ *   [0, 384)   header: u32 magic 0x3142515A ("ZQB1") @0, u16 version 1 @4,
+ *              u16 flags 0 @6, u64 n @8, u32 4096 @16, u32 nblocks @20,
+ *              u64 payload_words @24, u8 width[8] @64, u8 sym[256] @128.
+ *   [384, 384+R)  u32 word offset of each block in the payload, zero padding
+ *              to R = roundup(4 * nblocks, 128).
+ *   payload    payload_words u32 words; block b = 8 words of lane word counts
+ *              (byte l = words of lane l) then the words of lanes 0..31.  The
+ *              block's symbols [4096 b, 4096 b + 4096) form 256 runs of 16;
+ *              lane l codes runs l, l + 32, ..., l + 224 in that order (the
+ *              symbols below n), first code at bit 31 of its first word, the
+ *              last word zero-padded.
+ *   Stream bytes = 384 + R + 4 * payload_words, at most zq_max_bytes(n).
+ */
+#define ZQ_BLOCK_SYMBOLS 4096
+#define ZQ_HEADER_BYTES 384
+
+typedef struct zq_table {
+  uint8_t width[8];
+  uint8_t sym[256];
+} zq_table;
+
+/* The static widths {3,3,3,3,3,4,5,8}: regions of 8,8,8,8,8,16,32 ranks and the
+ * rest (ranks 88-255), code lengths 6/7/8/11 ([QLC §3.2]).  Host. */
+zc_status zq_default_widths(uint8_t widths[8]);
+
+/* A table from a 256-bin byte histogram (host): ranks by (count desc, byte
+ * asc) ([QLC §4.1]); widths NULL = the static widths.  An invalid widths set
+ * returns ZC_ERR_CODEBOOK. */
+zc_status zq_table_from_histogram(const uint64_t* h_hist, const uint8_t* widths, zq_table* out);
+
+/* Largest stream of n bytes: 384 + R + 5664 * nblocks. */
+zc_status zq_max_bytes(uint64_t n, uint64_t* bytes);
+
+/* Encode n bytes (d_in, 16-byte aligned) into the ZQ1 stream d_out (16-byte
+ * aligned, out_capacity bytes; zq_max_bytes(n) always suffices).  h_table:
+ * host table (validated: ZC_ERR_CODEBOOK), embedded in the stream.  One
+ * cooperative launch with the single-pass block-offset scan of zc_compress;
+ * workspace zc_workspace_size(&n, 1) bytes, zeroed before first use.  A
+ * stream larger than out_capacity sets ZC_ERR_OUT_OF_ROOM (the header's
+ * payload_words is still exact); other device errors as in zc_compress. */
+zc_status zq_compress(const void* d_in, uint64_t n, const zq_table* h_table, void* d_out, uint64_t out_capacity,
+                      void* d_ws, uint64_t ws_bytes, int32_t* d_status, void* stream);
+
+/* Decode a ZQ1 stream of in_bytes readable bytes back to n bytes (d_out,
+ * 16-byte aligned).  The header (magic, sizes, table) is validated on the
+ * device: a bad header writes nothing; a block whose words do not add up sets
+ * ZC_ERR_CORRUPT_STREAM.  No workspace. */
+zc_status zq_decompress(const void* d_in, uint64_t in_bytes, uint64_t n, void* d_out, int32_t* d_status,
+                        void* stream);
 
 #ifdef __cplusplus
 }

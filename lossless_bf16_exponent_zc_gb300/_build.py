@@ -14,7 +14,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libzc.so")
-SOURCES = ["zc_api.cu", "zc_encode.cu", "zc_decode.cu", "zc_reduce.cu", "zc_hist.cu", "zc_noalloc.cu", "zc_raw.cu", "zc_pipeline.cu"]
+SOURCES = ["zc_api.cu", "zc_encode.cu", "zc_decode.cu", "zc_reduce.cu", "zc_hist.cu", "zc_noalloc.cu", "zc_raw.cu", "zc_pipeline.cu", "zq.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -126,6 +126,7 @@ const char* zc_status_string(int status) {
     case ZC_ERR_SIZE_MISMATCH: return "ZC_ERR_SIZE_MISMATCH";
     case ZC_ERR_TIMEOUT: return "ZC_ERR_TIMEOUT";
     case ZC_ERR_DUP_CODEBOOK: return "ZC_ERR_DUP_CODEBOOK";
+    case ZC_ERR_OUT_OF_ROOM: return "ZC_ERR_OUT_OF_ROOM";
     default: return "ZC_ERR_UNKNOWN";
   }
 }
@@ -329,6 +330,76 @@ zc_status zc_pipelined_transfer(const void* d_in, uint64_t n, const uint8_t* d_c
   return cuda_status(launch_pipeline(static_cast<const uint16_t*>(d_in), n, d_cb, static_cast<uint16_t*>(d_out),
                                      chunk_elems, static_cast<uint8_t*>(d_ws), d_status, as_stream(stream_compress),
                                      as_stream(stream_link), as_stream(stream_decompress), dev));
+}
+static const uint8_t kZqDefaultWidths[8] = {3, 3, 3, 3, 3, 4, 5, 8};
+static bool zq_widths_valid(const uint8_t* w) {
+  uint32_t cap = 0;
+  for (int r = 0; r < 8; r++) {
+    if (w[r] > 8) return false;
+    cap += 1u << w[r];
+  }
+  return cap >= 256;
+}
+static bool zq_table_valid(const zq_table* t) {
+  if (!zq_widths_valid(t->width)) return false;
+  bool seen[256] = {false};
+  for (int k = 0; k < 256; k++) {
+    if (seen[t->sym[k]]) return false;
+    seen[t->sym[k]] = true;
+  }
+  return true;
+}
+zc_status zq_default_widths(uint8_t widths[8]) {
+  if (!widths) return ZC_ERR_INVALID_ARG;
+  std::memcpy(widths, kZqDefaultWidths, 8);
+  return ZC_OK;
+}
+zc_status zq_table_from_histogram(const uint64_t* h_hist, const uint8_t* widths, zq_table* out) {
+  if (!h_hist || !out) return ZC_ERR_INVALID_ARG;
+  const uint8_t* w = widths ? widths : kZqDefaultWidths;
+  if (!zq_widths_valid(w)) return ZC_ERR_CODEBOOK;
+  std::memcpy(out->width, w, 8);
+  bool taken[256] = {false};
+  for (int k = 0; k < 256; k++) {
+    int best = -1;
+    for (int s = 0; s < 256; s++)
+      if (!taken[s] && (best < 0 || h_hist[s] > h_hist[best])) best = s;  // ties keep the smaller byte
+    taken[best] = true;
+    out->sym[k] = static_cast<uint8_t>(best);
+  }
+  return ZC_OK;
+}
+zc_status zq_max_bytes(uint64_t n, uint64_t* bytes) {
+  if (!bytes) return ZC_ERR_INVALID_ARG;
+  if (n > kMaxN) return ZC_ERR_TOO_LARGE;
+  *bytes = zq_stream_max_bytes(n);
+  return ZC_OK;
+}
+zc_status zq_compress(const void* d_in, uint64_t n, const zq_table* h_table, void* d_out, uint64_t out_capacity,
+                      void* d_ws, uint64_t ws_bytes, int32_t* d_status, void* stream) {
+  if (!d_status || !h_table || !d_out || (!d_in && n)) return ZC_ERR_INVALID_ARG;
+  if (n > kMaxN) return ZC_ERR_TOO_LARGE;
+  if (!aligned(d_in, 16) || !aligned(d_out, 16) || !aligned(d_status, 4)) return ZC_ERR_ALIGNMENT;
+  if (!zq_table_valid(h_table)) return ZC_ERR_CODEBOOK;
+  if (out_capacity < ZQ_HEADER_BYTES + (4 * ((n + ZQ_BLOCK_SYMBOLS - 1) / ZQ_BLOCK_SYMBOLS) + 127) / 128 * 128)
+    return ZC_ERR_INVALID_ARG;  // not even the header and offset table fit
+  if (zc_status s = check_ws(d_ws, ws_bytes, num_tiles(n))) return s;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return ZC_ERR_CUDA;
+  return cuda_status(launch_zq_encode(static_cast<const uint8_t*>(d_in), n, h_table->width, h_table->sym,
+                                      static_cast<uint8_t*>(d_out), out_capacity, ws_header(d_ws), ws_flags(d_ws),
+                                      d_status, as_stream(stream), dev));
+}
+zc_status zq_decompress(const void* d_in, uint64_t in_bytes, uint64_t n, void* d_out, int32_t* d_status,
+                        void* stream) {
+  if (!d_status || !d_in || (!d_out && n)) return ZC_ERR_INVALID_ARG;
+  if (n > kMaxN) return ZC_ERR_TOO_LARGE;
+  if (!aligned(d_in, 16) || !aligned(d_out, 16) || !aligned(d_status, 4)) return ZC_ERR_ALIGNMENT;
+  if (in_bytes < ZQ_HEADER_BYTES) return ZC_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return ZC_ERR_CUDA;
+  return cuda_status(launch_zq_decode(static_cast<const uint8_t*>(d_in), in_bytes, n, static_cast<uint8_t*>(d_out),
+                                      d_status, as_stream(stream), dev));
 }
 zc_status zc_decompress_batched(int count, const zc_tensor* h_tensors, int32_t* d_status, void* stream) {
   if (count < 1 || !h_tensors || !d_status) return ZC_ERR_INVALID_ARG;

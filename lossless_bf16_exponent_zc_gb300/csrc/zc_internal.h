@@ -88,6 +88,14 @@ cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out,
                           uint8_t* out_main, uint8_t* out_esc, uint64_t out_cap, WsHeader* ws, Flag* flags,
                           int32_t* status, cudaStream_t stream, const DeviceInfo& dev);
 
+// QLC (zq.cu): widths and sym validated by the caller.
+uint64_t zq_stream_max_bytes(uint64_t n);
+cudaError_t launch_zq_encode(const uint8_t* in, uint64_t n, const uint8_t width[8], const uint8_t sym[256],
+                             uint8_t* out, uint64_t out_bytes, WsHeader* ws, Flag* flags, int32_t* status,
+                             cudaStream_t stream, const DeviceInfo& dev);
+cudaError_t launch_zq_decode(const uint8_t* in, uint64_t in_bytes, uint64_t n, uint8_t* out, int32_t* status,
+                             cudaStream_t stream, const DeviceInfo& dev);
+
 cudaError_t launch_histogram(const uint16_t* in, uint64_t n, uint8_t* cb_out, uint32_t* hist_out, WsHeader* ws,
                              int32_t* status, cudaStream_t stream, const DeviceInfo& dev);
 

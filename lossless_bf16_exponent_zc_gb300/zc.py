@@ -28,6 +28,7 @@ STATUS_NAMES = [
     "ZC_OK", "ZC_ERR_INVALID_ARG", "ZC_ERR_ALIGNMENT", "ZC_ERR_TOO_LARGE", "ZC_ERR_WORKSPACE",
     "ZC_ERR_CODEBOOK", "ZC_ERR_CUDA", "ZC_ERR_ESCAPE_OVERFLOW", "ZC_ERR_BAD_HEADER",
     "ZC_ERR_CORRUPT_STREAM", "ZC_ERR_SIZE_MISMATCH", "ZC_ERR_TIMEOUT", "ZC_ERR_DUP_CODEBOOK",
+    "ZC_ERR_OUT_OF_ROOM",
 ]
 for _i, _name in enumerate(STATUS_NAMES):
     globals()[_name[3:]] = _i   # OK, ERR_INVALID_ARG, ...
@@ -37,6 +38,10 @@ class ZcError(RuntimeError):
     def __init__(self, code: int, where: str):
         super().__init__(f"{where}: {status_string(code)} ({code})")
         self.code = code
+
+
+class ZqTable(ctypes.Structure):
+    _fields_ = [("width", ctypes.c_uint8 * 8), ("sym", ctypes.c_uint8 * 256)]
 
 
 class ZcTensor(ctypes.Structure):
@@ -79,12 +84,18 @@ def load() -> ctypes.CDLL:
     lib.zc_compress_batched.argtypes = [i32, ctypes.POINTER(ZcTensor), vp, u64, vp, vp]
     lib.zc_compress_batched_adaptive.argtypes = [i32, ctypes.POINTER(ZcTensor), vp, u64, vp, vp]
     lib.zc_decompress_batched.argtypes = [i32, ctypes.POINTER(ZcTensor), vp, vp]
+    lib.zq_default_widths.argtypes = [ctypes.POINTER(ctypes.c_uint8)]
+    lib.zq_table_from_histogram.argtypes = [u64p, ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(ZqTable)]
+    lib.zq_max_bytes.argtypes = [u64, u64p]
+    lib.zq_compress.argtypes = [vp, u64, ctypes.POINTER(ZqTable), vp, u64, vp, u64, vp, vp]
+    lib.zq_decompress.argtypes = [vp, u64, u64, vp, vp, vp]
     lib.zc_pipeline_workspace_size.argtypes = [u64, u64p]
     lib.zc_pipelined_transfer.argtypes = [vp, u64, vp, vp, u64, vp, u64, vp, vp, vp, vp]
     for name in ("zc_codebook_from_sigma", "zc_compressed_size", "zc_workspace_size", "zc_histogram_topk",
                  "zc_compress", "zc_compress_adaptive", "zc_raw_spill", "zc_decompress", "zc_decompress_reduce",
                  "zc_compress_batched", "zc_compress_batched_adaptive", "zc_decompress_batched",
-                 "zc_pipeline_workspace_size", "zc_pipelined_transfer"):
+                 "zc_pipeline_workspace_size", "zc_pipelined_transfer", "zq_default_widths",
+                 "zq_table_from_histogram", "zq_max_bytes", "zq_compress", "zq_decompress"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -315,6 +326,69 @@ def pipelined_transfer(x: torch.Tensor, cb: torch.Tensor, chunk_elems: int, ws: 
     rc = load().zc_pipelined_transfer(_ptr(x), n, _ptr(cb), _ptr(out), int(chunk_elems), _ptr(ws), ws.numel(),
                                       _ptr(status), sc, sl, sd)
     _check(rc, "zc_pipelined_transfer")
+    return out
+
+
+# ------------------------------------------------------------------ QLC for FP8 (e4m3) bytes
+def zq_default_widths() -> np.ndarray:
+    w = (ctypes.c_uint8 * 8)()
+    _check(load().zq_default_widths(w), "zq_default_widths")
+    return np.frombuffer(bytes(w), np.uint8).copy()
+
+
+def zq_table_from_histogram(hist, widths=None) -> ZqTable:
+    h = np.ascontiguousarray(np.asarray(hist, dtype=np.uint64).reshape(256))
+    hp = h.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64))
+    wp = None
+    if widths is not None:
+        wp = (ctypes.c_uint8 * 8)(*[int(v) for v in widths])
+    t = ZqTable()
+    _check(load().zq_table_from_histogram(hp, wp, ctypes.byref(t)), "zq_table_from_histogram")
+    return t
+
+
+def zq_table(widths, sym) -> ZqTable:
+    t = ZqTable()
+    t.width[:] = [int(v) for v in widths]
+    t.sym[:] = [int(v) for v in sym]
+    return t
+
+
+def zq_max_bytes(n: int) -> int:
+    out = ctypes.c_uint64()
+    _check(load().zq_max_bytes(int(n), ctypes.byref(out)), "zq_max_bytes")
+    return out.value
+
+
+def zq_compress(x: torch.Tensor, table: ZqTable, ws: torch.Tensor, status: torch.Tensor,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """QLC-encode the bytes of x (uint8 / float8 tensor) into a ZQ1 stream buffer (zq_max_bytes(n) bytes)."""
+    if x.element_size() != 1:
+        raise ValueError("QLC codes 1-byte symbols (uint8 or float8 tensors)")
+    n = x.numel()
+    if out is None:
+        out = torch.empty(zq_max_bytes(n), dtype=torch.uint8, device=x.device)
+    rc = load().zq_compress(_ptr(x), n, ctypes.byref(table), _ptr(out), out.numel(), _ptr(ws), ws.numel(),
+                            _ptr(status), _stream(stream))
+    _check(rc, "zq_compress")
+    return out
+
+
+def zq_stream_bytes(stream_buf: torch.Tensor) -> int:
+    """Bytes of the ZQ1 stream in stream_buf, from its header (a device-to-host read)."""
+    h = stream_buf[:32].cpu().numpy()
+    nblocks = int.from_bytes(h[20:24].tobytes(), "little")
+    words = int.from_bytes(h[24:32].tobytes(), "little")
+    return 384 + -(-4 * nblocks // 128) * 128 + 4 * words
+
+
+def zq_decompress(stream_buf: torch.Tensor, n: int, status: torch.Tensor, out: torch.Tensor | None = None,
+                  in_bytes: int | None = None, stream=None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty(n, dtype=torch.uint8, device=stream_buf.device)
+    nb = stream_buf.numel() if in_bytes is None else int(in_bytes)
+    rc = load().zq_decompress(_ptr(stream_buf), nb, int(n), _ptr(out), _ptr(status), _stream(stream))
+    _check(rc, "zq_decompress")
     return out
 
 

@@ -16,7 +16,7 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(zc_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(z[cq]_[a-z_]+)\s*\(", text)))
 
 
 def test_library_exports_every_declared_symbol():
@@ -25,7 +25,8 @@ def test_library_exports_every_declared_symbol():
     assert {"zc_codebook_from_sigma", "zc_histogram_topk", "zc_compress", "zc_decompress", "zc_decompress_reduce",
             "zc_compressed_size", "zc_workspace_size", "zc_compress_batched", "zc_decompress_batched",
             "zc_status_string", "zc_version", "zc_compress_adaptive", "zc_compress_batched_adaptive",
-            "zc_raw_spill", "zc_pipeline_workspace_size", "zc_pipelined_transfer"} <= set(names)
+            "zc_raw_spill", "zc_pipeline_workspace_size", "zc_pipelined_transfer", "zq_default_widths",
+            "zq_table_from_histogram", "zq_max_bytes", "zq_compress", "zq_decompress"} <= set(names)
     for name in names:
         assert hasattr(lib, name), name
 
@@ -136,3 +137,21 @@ def test_pipeline_workspace_size():
                 None) == zc.ERR_ALIGNMENT
     assert _raw("zc_pipelined_transfer", fake, 10, fake, fake, 4096, fake, 100, status, None, None,
                 None) == zc.ERR_WORKSPACE
+
+
+def test_qlc_host_functions_match_oracle():
+    assert tuple(zc.zq_default_widths()) == tuple(oracle.QLC_DEFAULT_WIDTHS)
+    rng = np.random.default_rng(7)
+    for _ in range(5):
+        h = rng.integers(0, 50, 256)
+        t = zc.zq_table_from_histogram(h)
+        assert np.array_equal(np.frombuffer(bytes(t.sym), np.uint8), oracle.qlc_table_from_histogram(h))
+    for n in (0, 1, 4096, 4097, 10 ** 6):
+        assert zc.zq_max_bytes(n) == oracle.qlc_max_bytes(n)
+    with pytest.raises(zc.ZcError) as e:
+        zc.zq_table_from_histogram(np.ones(256), widths=(3, 3, 3, 3, 3, 3, 3, 3))
+    assert e.value.code == zc.ERR_CODEBOOK
+    fake, status = 1 << 20, 1 << 21
+    bad = zc.zq_table((3, 3, 3, 3, 3, 3, 3, 3), range(256))
+    assert zc.load().zq_compress(fake, 100, ctypes.byref(bad), fake, 1 << 20, fake, 1 << 20, status,
+                                 None) == zc.ERR_CODEBOOK
