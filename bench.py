@@ -485,7 +485,8 @@ def run_workloads(args, zc, torch, device, peak):
     workloads: the 2^20 Gaussian (L2-resident), the 9-tensor Llama-3-8B bucket (batched), the MoE payload
     (histogram codebook, 8 Zipf chunks batched), the reduce-scatter local stage (P = 8) with its
     shard-size sweep, the raw bypass (adaptive compression of coded and incompressible 2^26 tensors), and the
-    zipped transfer pipeline (16 or 4 chunks on three streams against one stream and a plain copy).
+    zipped transfer pipeline (16 or 4 chunks on three streams against one stream and a plain copy), and
+    Quad Length Codes on 2^26 FP8 e4m3 bytes.
     Inputs above L2 size are not flushed between repetitions of the same op."""
     import math as _m
     out = {}
@@ -692,6 +693,27 @@ def run_workloads(args, zc, torch, device, peak):
         del pws
     out["pipelined_transfer_2^26"] = pipe
     del xt, y, yc
+
+    # 7. Quad Length Codes on 2^26 FP8 e4m3 bytes [QLC §3-§4]: FFN1-activation and gradient stand-ins, the
+    #    table from each tensor's histogram, static widths; algorithmic bytes = read n + write the stream
+    #    (compress) and the reverse (decompress)
+    qlc = {}
+    wsq = zc.workspace(n, device=device)
+    for name, gen in (("fp8_ffn1", workloads.fp8_ffn1), ("fp8_gradient", workloads.fp8_gradient)):
+        xb = gen(n)
+        table = zc.zq_table_from_histogram(np.bincount(xb, minlength=256))
+        xq = torch.from_numpy(xb).to(device)
+        del xb
+        sq = torch.empty(zc.zq_max_bytes(n), dtype=torch.uint8, device=device)
+        yq = torch.empty(n, dtype=torch.uint8, device=device)
+        tq = _time_ms(torch, lambda: zc.zq_compress(xq, table, wsq, st, out=sq), 20)
+        nbytes = zc.zq_stream_bytes(sq)
+        tdq = _time_ms(torch, lambda: zc.zq_decompress(sq, n, st, out=yq, in_bytes=nbytes), 20)
+        ok = torch.equal(yq, xq)
+        qlc[name] = {"compress": entry(tq, n, n + nbytes), "decompress": entry(tdq, n, n + nbytes),
+                     "ratio": round(n / nbytes, 4), "saving": round(1 - nbytes / n, 4), "round_trip_ok": bool(ok)}
+        del xq, sq, yq
+    out["qlc_fp8_2^26"] = qlc
 
     if zc.status_value(st) != 0:
         out["status"] = zc.status_string(zc.status_value(st))

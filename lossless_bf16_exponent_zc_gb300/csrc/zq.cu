@@ -14,15 +14,17 @@
 //     packed most-significant-bit first into a 64-bit accumulator and leave
 //     as 32-bit words into the lane's shared-memory buffer.  The warp packs
 //     its 32 lanes' words behind the 8 words of lane counts and stores the
-//     block with consecutive lanes on consecutive words.  Block offsets come
-//     from the same single-pass scan as the bf16 encoder: a CTA's 8 warps form
-//     a group, the group's size is published at once, and the CTA's offset is
-//     its previous group's end plus the sizes published in between
-//     (cooperative launch, bounded waits, launch epochs in the workspace).
-//   * Decoder: the block's words are copied to shared memory with coalesced
-//     loads; each lane decodes its runs with a 64-bit bit buffer and a
-//     2048-entry table indexed by the next 11 bits, which gives the symbol
-//     and its code length in one shared load.
+//     block with consecutive lanes on consecutive words.  Each CTA owns a
+//     contiguous range of blocks: it sizes them first (lengths only),
+//     publishes its total and adds the totals of the CTAs before it (one
+//     bounded wait per launch, the workspace's epoch protocol, cooperative
+//     launch), then codes them again from L2 and stores them at their
+//     offsets.
+//   * Decoder: the block's words are copied to shared memory with batches of
+//     independent coalesced loads; each lane decodes its runs with a 32-bit
+//     funnel-shift window over two words and a 2048-entry table indexed by
+//     the next 11 bits, which gives the symbol and its code length in one
+//     shared load.
 #include "zc_device.cuh"
 #include "zc_internal.h"
 
@@ -59,12 +61,34 @@ struct QEncParams {
 // Shared memory of the encoder, per CTA.
 struct QEncShared {
   uint32_t lut[256];
-  uint32_t total[kQEncWarps];   // words of each warp's block this round
-  uint64_t offset[kQEncWarps];  // payload word offset of each warp's block this round
   uint32_t lanebuf[kQEncWarps][32 * kQLaneStride];
   uint32_t packed[kQEncWarps][kQBlockWordsMax];
 };
 
+// Run j of lane `lane` in block b (zero past n); *valid = its symbols below n.
+__device__ __forceinline__ uint4 zq_load_run(const uint8_t* in, uint64_t n, uint64_t b, uint32_t lane, uint32_t j,
+                                            uint32_t* valid) {
+  const uint64_t i0 = b * kQBlock + zq_run_offset(lane, j);
+  *valid = i0 >= n ? 0u : (n - i0 >= 16 ? 16u : static_cast<uint32_t>(n - i0));
+  if (*valid == 16) return __ldg(reinterpret_cast<const uint4*>(in + i0));
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  for (uint32_t t = 0; t < *valid; t++) w[t >> 2] |= uint32_t(__ldg(in + i0 + t)) << (8 * (t & 3));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// The 16 table entries of a run (0 past the valid symbols).
+__device__ __forceinline__ void zq_lookup_run(const uint32_t* lut, uint4 v, uint32_t valid, uint32_t (&e)[16]) {
+  const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (uint32_t t = 0; t < 16; t++) e[t] = t < valid ? lut[(w4[t >> 2] >> (8 * (t & 3))) & 0xFFu] : 0u;
+}
+
+// Design of the launch: CTA c owns the contiguous blocks [c B, c B + B).
+// Pass 1 sizes them (code lengths only) and leaves each block's word count in
+// its offset-table entry; the CTA publishes its total at once and learns its
+// base offset from the totals of the CTAs before it (one bounded wait, not one
+// per round).  Pass 2 codes the blocks again -- their input is mostly still in
+// L2 -- and stores each at its offset.
 __global__ void __launch_bounds__(kQEncWarps * 32, 1) zq_encode_kernel(const __grid_constant__ QEncParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   QEncShared& S = *reinterpret_cast<QEncShared*>(smem_raw);
@@ -72,8 +96,9 @@ __global__ void __launch_bounds__(kQEncWarps * 32, 1) zq_encode_kernel(const __g
   for (uint32_t i = threadIdx.x; i < 256; i += blockDim.x) S.lut[i] = p.code[i];
   const uint64_t nb = zq_blocks(p.n);
   const uint64_t tbl = zq_table_bytes(nb);
+  uint32_t* table = reinterpret_cast<uint32_t*>(p.out + kQHeader);
   uint8_t* payload = p.out + kQHeader + tbl;
-  // fixed header fields and the table (payload words come with the last block)
+  // fixed header fields and the rank table (payload words come with the last block)
   if (blockIdx.x == 0 && warp == 0) {
     uint32_t* h = reinterpret_cast<uint32_t*>(p.out);
     for (uint32_t i = lane; i < kQHeader / 4; i += 32) {
@@ -98,97 +123,119 @@ __global__ void __launch_bounds__(kQEncWarps * 32, 1) zq_encode_kernel(const __g
   }
   __syncthreads();
   const uint32_t epoch = launch_epoch(p.ws);
-  const uint32_t ngroups = static_cast<uint32_t>((nb + kQEncWarps - 1) / kQEncWarps);
-  uint32_t* lb = &S.lanebuf[warp][lane * kQLaneStride];
-  uint32_t* packed = S.packed[warp];
-  int64_t prev_G = -1;
-  uint64_t prev_incl = 0;
-  for (uint32_t G = blockIdx.x; G < ngroups; G += gridDim.x) {
-    const uint64_t b = static_cast<uint64_t>(G) * kQEncWarps + warp;
-    uint32_t T = 0;
-    if (b < nb) {
-      // ---- load this lane's 8 runs and code them
-      const uint64_t base = b * kQBlock;
-      uint4 v[8];
-#pragma unroll
-      for (uint32_t j = 0; j < 8; j++) {
-        const uint64_t i0 = base + zq_run_offset(lane, j);
-        if (i0 + 16 <= p.n) {
-          v[j] = __ldg(reinterpret_cast<const uint4*>(p.in + i0));
-        } else {
-          uint32_t w[4] = {0u, 0u, 0u, 0u};
-          for (uint32_t t = 0; i0 + t < p.n && t < 16; t++) w[t >> 2] |= uint32_t(__ldg(p.in + i0 + t)) << (8 * (t & 3));
-          v[j] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
-      unsigned long long acc = 0;
-      uint32_t nacc = 0, wc = 0;
-#pragma unroll
-      for (uint32_t j = 0; j < 8; j++) {
-        const uint64_t i0 = base + zq_run_offset(lane, j);
-        const uint32_t valid = i0 >= p.n ? 0u : (p.n - i0 >= 16 ? 16u : static_cast<uint32_t>(p.n - i0));
-        const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-        for (uint32_t t = 0; t < 16; t++) {
-          if (t < valid) {
-            const uint32_t e = S.lut[(w4[t >> 2] >> (8 * (t & 3))) & 0xFFu];
-            const uint32_t len = e >> 16;
-            acc |= static_cast<unsigned long long>(e & 0xFFFFu) << (64 - nacc - len);
-            nacc += len;
-            if (nacc >= 32) {
-              lb[wc++] = static_cast<uint32_t>(acc >> 32);
-              acc <<= 32;
-              nacc -= 32;
-            }
-          }
-        }
-      }
-      if (nacc > 0) lb[wc++] = static_cast<uint32_t>(acc >> 32);
-      // ---- pack: lane counts, then the lanes' words in lane order
-      const uint32_t inc = warp_inclusive_scan(wc);
-      const uint32_t pre = inc - wc;
-      T = 8 + __shfl_sync(kFull, inc, 31);
-      reinterpret_cast<uint8_t*>(packed)[lane] = static_cast<uint8_t>(wc);
-      for (uint32_t k = 0; k < wc; k++) packed[8 + pre + k] = lb[k];
+  const uint64_t per = (nb + gridDim.x - 1) / gridDim.x;  // blocks per CTA
+  const uint64_t b0 = static_cast<uint64_t>(blockIdx.x) * per;
+  const uint64_t b1 = b0 + per < nb ? b0 + per : nb;
+
+  // A warp's runs in coding order: run k is run k % 8 of its (k / 8)-th block.
+  // Four runs are loaded ahead (64 bytes per lane in flight).
+  const uint64_t first_b = b0 + warp;
+  const uint32_t nruns = first_b < b1 ? static_cast<uint32_t>(8 * ((b1 - first_b + kQEncWarps - 1) / kQEncWarps)) : 0u;
+  auto block_of = [&](uint32_t k) { return first_b + static_cast<uint64_t>(k >> 3) * kQEncWarps; };
+  auto load_k = [&](uint32_t k, uint32_t* valid) -> uint4 {
+    if (k >= nruns) {
+      *valid = 0;
+      return make_uint4(0u, 0u, 0u, 0u);
     }
-    if (lane == 0) S.total[warp] = T;
-    __syncthreads();
-    // ---- the group's offset: warp 0 publishes the group's size and adds the
-    // sizes published since this CTA's previous group
-    if (warp == 0) {
-      const uint32_t t = lane < kQEncWarps ? S.total[lane] : 0u;
-      const uint32_t tinc = warp_inclusive_scan(t);
-      const uint32_t gsum = __shfl_sync(kFull, tinc, 31);
-      if (lane == 0) {
-        const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
-        st_relaxed(&p.flags[G].agg, tag | gsum);
-      }
-      bool timed_out;
-      const uint64_t prefix = prev_incl + window_sum(p.flags, static_cast<uint32_t>(prev_G + 1), G, epoch, p.status,
-                                                     &timed_out);
-      if (lane < kQEncWarps) S.offset[lane] = prefix + (tinc - t);
-      prev_G = G;
-      prev_incl = prefix + gsum;
-    }
-    __syncthreads();
-    if (b < nb) {
-      const uint64_t off = S.offset[warp];
-      if (lane == 0) *reinterpret_cast<uint32_t*>(p.out + kQHeader + 4 * b) = static_cast<uint32_t>(off);
-      if (off + T <= p.out_words) {
-        uint32_t* dst = reinterpret_cast<uint32_t*>(payload) + off;
-        for (uint32_t k = lane; k < T; k += 32) dst[k] = packed[k];
-      } else if (lane == 0) {
-        set_status(p.status, ZC_ERR_OUT_OF_ROOM);
-      }
-      if (b + 1 == nb) {
-        // the last block: total payload words and the offset table's padding
-        if (lane == 0) *reinterpret_cast<unsigned long long*>(p.out + 24) = off + T;
-        for (uint64_t o = kQHeader + 4 * nb + 4 * lane; o < kQHeader + tbl; o += 128)
-          *reinterpret_cast<uint32_t*>(p.out + o) = 0u;
+    return zq_load_run(p.in, p.n, block_of(k), lane, k & 7u, valid);
+  };
+
+  // ---- pass 1: words of each block of this CTA (into its offset-table entry)
+  uint32_t cta_words = 0;  // lane 0 of each warp: this warp's blocks
+  {
+    uint32_t v0, v1, v2, v3, bits = 0;
+    uint4 q0 = load_k(0, &v0), q1 = load_k(1, &v1), q2 = load_k(2, &v2), q3 = load_k(3, &v3);
+#pragma unroll 1
+    for (uint32_t k = 0; k < nruns; k++) {
+      uint32_t e[16];
+      zq_lookup_run(S.lut, q0, v0, e);
+      q0 = q1, v0 = v1, q1 = q2, v1 = v2, q2 = q3, v2 = v3;
+      q3 = load_k(k + 4, &v3);
+#pragma unroll
+      for (uint32_t t = 0; t < 16; t++) bits += e[t] >> 16;
+      if ((k & 7u) == 7u) {
+        const uint32_t T = 8 + warp_sum((bits + 31) / 32);
+        bits = 0;
+        if (lane == 0) {
+          table[block_of(k)] = T;
+          cta_words += T;
+        }
       }
     }
   }
-  if (warp == 0) scan_exit(p.ws, p.flags, epoch, ngroups);
+  __shared__ uint32_t warp_words[kQEncWarps];
+  if (lane == 0) warp_words[warp] = cta_words;
+  __syncthreads();
+  // ---- the CTA's base: publish its total, add the totals of the CTAs before it
+  if (warp == 0) {
+    const uint32_t t = lane < kQEncWarps ? warp_words[lane] : 0u;
+    const uint32_t total = warp_sum(t);
+    if (lane == 0) st_relaxed(&p.flags[blockIdx.x].agg, (static_cast<unsigned long long>(epoch) << 32) | total);
+    bool timed_out;
+    const uint64_t base = window_sum(p.flags, 0u, blockIdx.x, epoch, p.status, &timed_out);
+    // block offsets: a running sum over this CTA's blocks, in order
+    uint64_t run = base;
+    for (uint64_t c = b0; c < b1; c += 32) {
+      const uint32_t w = c + lane < b1 ? table[c + lane] : 0u;
+      const uint32_t inc = warp_inclusive_scan(w);
+      if (c + lane < b1) table[c + lane] = static_cast<uint32_t>(run + inc - w);
+      run += __shfl_sync(kFull, inc, 31);
+    }
+    if (b1 == nb && b0 < b1 && lane == 0) *reinterpret_cast<unsigned long long*>(p.out + 24) = run;
+    if (b1 == nb)  // the offset table's padding
+      for (uint64_t o = kQHeader + 4 * nb + 4 * lane; o < kQHeader + tbl; o += 128)
+        *reinterpret_cast<uint32_t*>(p.out + o) = 0u;
+    scan_exit(p.ws, p.flags, epoch, gridDim.x);
+  }
+  __syncthreads();
+
+  // ---- pass 2: code each block and store it at its offset
+  uint32_t* lb = &S.lanebuf[warp][lane * kQLaneStride];
+  uint32_t* packed = S.packed[warp];
+  uint32_t v0, v1, v2, v3, nacc = 0, wc = 0;
+  unsigned long long acc = 0;  // codes most significant bit first; nacc bits used
+  uint4 q0 = load_k(0, &v0), q1 = load_k(1, &v1), q2 = load_k(2, &v2), q3 = load_k(3, &v3);
+#pragma unroll 1
+  for (uint32_t k = 0; k < nruns; k++) {
+    // the run's 16 lookups first, all in flight at once (the word stores
+    // below would otherwise keep each lookup behind the previous store)
+    uint32_t e[16];
+    zq_lookup_run(S.lut, q0, v0, e);
+    q0 = q1, v0 = v1, q1 = q2, v1 = v2, q2 = q3, v2 = v3;
+    q3 = load_k(k + 4, &v3);
+#pragma unroll
+    for (uint32_t t = 0; t < 16; t++) {
+      const uint32_t len = e[t] >> 16;  // 0 past n
+      acc |= static_cast<unsigned long long>(e[t] & 0xFFFFu) << ((64 - nacc - len) & 63);
+      nacc += len;
+      if (nacc >= 32) {
+        lb[wc++] = static_cast<uint32_t>(acc >> 32);
+        acc <<= 32;
+        nacc -= 32;
+      }
+    }
+    if ((k & 7u) != 7u) continue;
+    const uint64_t b = block_of(k);
+    if (nacc > 0) lb[wc++] = static_cast<uint32_t>(acc >> 32);
+    // pack: lane counts, then the lanes' words in lane order
+    const uint32_t inc = warp_inclusive_scan(wc);
+    const uint32_t pre = inc - wc;
+    const uint32_t T = 8 + __shfl_sync(kFull, inc, 31);
+    reinterpret_cast<uint8_t*>(packed)[lane] = static_cast<uint8_t>(wc);
+    for (uint32_t i = 0; i < wc; i++) packed[8 + pre + i] = lb[i];
+    __syncwarp();
+    const uint64_t off = table[b];
+    if (off + T <= p.out_words) {
+      uint32_t* dst = reinterpret_cast<uint32_t*>(payload) + off;
+      for (uint32_t i = lane; i < T; i += 32) dst[i] = packed[i];
+    } else if (lane == 0) {
+      set_status(p.status, ZC_ERR_OUT_OF_ROOM);
+    }
+    __syncwarp();
+    acc = 0;
+    nacc = 0;
+    wc = 0;
+  }
 }
 
 // ---------------------------------------------------------------- decoder
@@ -201,10 +248,15 @@ struct QDecParams {
 };
 
 struct QDecShared {
-  uint16_t lut[2048];  // next 11 bits -> (code length << 8) | symbol; 0 = no valid code
+  uint16_t lut[2048];  // next 11 bits -> (code length << 8) | symbol; bit 15 set: no valid code
+  uint32_t seen[8];    // byte values met in the rank table
+  uint32_t start[9];   // first rank of each region
   int bad;
-  uint32_t words[kQDecWarps][kQBlockWordsMax];
+  // + 48 words: a lane's window start advances at most 44 times (1408 bits)
+  // plus 2 words of look-ahead, from at most word 1416
+  uint32_t words[kQDecWarps][kQBlockWordsMax + 48];
 };
+constexpr uint16_t kQBadCode = 0x8000u | (11u << 8);
 
 __global__ void __launch_bounds__(kQDecWarps * 32) zq_decode_kernel(const __grid_constant__ QDecParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -213,6 +265,7 @@ __global__ void __launch_bounds__(kQDecWarps * 32) zq_decode_kernel(const __grid
   const uint64_t nb = zq_blocks(p.n);
   const uint64_t tbl = zq_table_bytes(nb);
   // header checks (every CTA reaches the same verdict) and the 11-bit table
+  if (threadIdx.x < 8) S.seen[threadIdx.x] = 0u;
   if (threadIdx.x == 0) {
     const uint32_t* h = reinterpret_cast<const uint32_t*>(p.in);
     int err = 0;
@@ -223,31 +276,37 @@ __global__ void __launch_bounds__(kQDecWarps * 32) zq_decode_kernel(const __grid
       err = ZC_ERR_SIZE_MISMATCH;
     if (!err) {
       const uint64_t words = static_cast<uint64_t>(__ldg(h + 6)) | (static_cast<uint64_t>(__ldg(h + 7)) << 32);
-      uint32_t cap = 0, seen[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      uint32_t cap = 0;
+      S.start[0] = 0;
       for (int r = 0; r < 8; r++) {
         const uint32_t w = __ldg(p.in + 64 + r);
         if (w > 8) err = ZC_ERR_BAD_HEADER;
-        else cap += 1u << w;
-      }
-      for (int k = 0; k < 256; k++) {
-        const uint32_t s = __ldg(p.in + 128 + k);
-        if (seen[s >> 5] & (1u << (s & 31))) err = ZC_ERR_BAD_HEADER;
-        seen[s >> 5] |= 1u << (s & 31);
+        cap += 1u << (w & 15u);
+        S.start[r + 1] = cap;
       }
       if (cap < 256 || kQHeader + tbl + 4 * words > p.in_bytes) err = ZC_ERR_BAD_HEADER;
     }
     S.bad = err;
-    if (err) set_status(p.status, err);
+  }
+  __syncthreads();
+  if (S.bad == 0 && threadIdx.x < 256) {  // the rank table is a permutation: every byte value once
+    const uint32_t v = __ldg(p.in + 128 + threadIdx.x);
+    atomicOr(&S.seen[v >> 5], 1u << (v & 31u));
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (S.bad == 0)
+      for (int i = 0; i < 8; i++)
+        if (S.seen[i] != 0xFFFFFFFFu) S.bad = ZC_ERR_BAD_HEADER;
+    if (S.bad) set_status(p.status, S.bad);
   }
   __syncthreads();
   if (S.bad) return;
   for (uint32_t q = threadIdx.x; q < 2048; q += blockDim.x) {
     const uint32_t r = q >> 8;
-    uint32_t start = 0;
-    for (uint32_t i = 0; i < r; i++) start += 1u << __ldg(p.in + 64 + i);
     const uint32_t w = __ldg(p.in + 64 + r);
-    const uint32_t rank = start + (w == 0 ? 0u : ((q & 0xFFu) >> (8 - w)));
-    S.lut[q] = rank > 255 ? uint16_t(0) : static_cast<uint16_t>(((3 + w) << 8) | __ldg(p.in + 128 + rank));
+    const uint32_t rank = S.start[r] + (w == 0 ? 0u : ((q & 0xFFu) >> (8 - w)));
+    S.lut[q] = rank > 255 ? kQBadCode : static_cast<uint16_t>(((3 + w) << 8) | __ldg(p.in + 128 + rank));
   }
   __syncthreads();
   const uint64_t words = static_cast<uint64_t>(reinterpret_cast<const uint32_t*>(p.in)[6]) |
@@ -264,52 +323,63 @@ __global__ void __launch_bounds__(kQDecWarps * 32) zq_decode_kernel(const __grid
       continue;
     }
     const uint32_t T = static_cast<uint32_t>(end - off);
-    for (uint32_t k = lane; k < T; k += 32) wbuf[k] = __ldg(payload + off + k);
+    for (uint32_t k0 = 0; k0 < T; k0 += 8 * 32) {  // 8 independent loads in flight per lane
+      uint32_t t[8];
+#pragma unroll
+      for (uint32_t u = 0; u < 8; u++) {
+        const uint32_t k = k0 + 32 * u + lane;
+        t[u] = k < T ? __ldg(payload + off + k) : 0u;
+      }
+#pragma unroll
+      for (uint32_t u = 0; u < 8; u++) {
+        const uint32_t k = k0 + 32 * u + lane;
+        if (k < T) wbuf[k] = t[u];
+      }
+    }
     __syncwarp();
     const uint32_t wc = reinterpret_cast<const uint8_t*>(wbuf)[lane];
     const uint32_t inc = warp_inclusive_scan(wc);
-    const uint32_t first = 8 + inc - wc;
     bool ok = 8 + __shfl_sync(kFull, inc, 31) == T;
-    const uint32_t limit = ok ? first + wc : first;  // this lane's words are [first, limit)
-    uint32_t next = first;
-    unsigned long long buf = 0;
-    uint32_t nbits = 0;
-    auto refill = [&]() {
-      while (nbits <= 32) {
-        const uint32_t w = next < limit ? wbuf[next] : 0u;
-        buf |= static_cast<unsigned long long>(w) << (32 - nbits);
-        nbits += 32;
-        next++;
-      }
-    };
-    refill();
-    uint64_t bits_used = 0;
+    const uint32_t first = ok ? 8 + inc - wc : 8u;  // lane counts that do not add up: read anything in range
+    // window: bits [pos, pos + 32) of the lane's stream are the funnel shift
+    // of (w0, w1); w2 is the word after them, loaded ahead.  The window may run
+    // past the lane's words into the next lane's (or the slack words): those
+    // bits only ever fill the unused tail of the last peek.
+    uint32_t idx = first + 2;
+    uint32_t w0 = wbuf[first], w1 = wbuf[first + 1], w2 = wbuf[idx];
+    uint32_t pos = 0, badcode = 0;
     const uint64_t base = b * kQBlock;
+    auto decode_one = [&]() -> uint32_t {  // returns the lookup entry, advances the window
+      const uint32_t e = S.lut[__funnelshift_l(w1, w0, pos) >> 21];
+      badcode |= e;
+      pos += (e >> 8) & 15u;
+      const bool adv = pos >= 32;
+      pos &= 31u;
+      w0 = adv ? w1 : w0;
+      w1 = adv ? w2 : w1;
+      idx += adv ? 1u : 0u;
+      w2 = wbuf[idx];
+      return e;
+    };
 #pragma unroll 1
     for (uint32_t j = 0; j < 8; j++) {
       const uint64_t i0 = base + zq_run_offset(lane, j);
       const uint32_t valid = i0 >= p.n ? 0u : (p.n - i0 >= 16 ? 16u : static_cast<uint32_t>(p.n - i0));
-      uint32_t o[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-      for (uint32_t t = 0; t < 16; t++) {
-        if (t < valid) {
-          const uint32_t e = S.lut[buf >> 53];
-          const uint32_t len = e >> 8;
-          ok &= len != 0;
-          const uint32_t use = len != 0 ? len : 11u;
-          o[t >> 2] |= (e & 0xFFu) << (8 * (t & 3));
-          buf <<= use;
-          nbits -= use;
-          bits_used += use;
-          if (nbits <= 32) refill();
-        }
-      }
       if (valid == 16) {
+        uint32_t o[4];
+#pragma unroll
+        for (uint32_t q = 0; q < 4; q++) {
+          const uint32_t e0 = decode_one(), e1 = decode_one(), e2 = decode_one(), e3 = decode_one();
+          o[q] = __byte_perm(__byte_perm(e0, e1, 0x0040), __byte_perm(e2, e3, 0x0040), 0x5410);
+        }
         *reinterpret_cast<uint4*>(p.out + i0) = make_uint4(o[0], o[1], o[2], o[3]);
       } else {
-        for (uint32_t t = 0; t < valid; t++) p.out[i0 + t] = static_cast<uint8_t>(o[t >> 2] >> (8 * (t & 3)));
+        for (uint32_t t = 0; t < valid; t++) p.out[i0 + t] = static_cast<uint8_t>(decode_one());
       }
     }
+    // words consumed: the window started at word `first`, advanced idx - first - 2 times
+    const uint32_t bits_used = 32u * (idx - first - 2u) + pos;
+    ok &= (badcode & 0x8000u) == 0;
     ok &= (bits_used + 31) / 32 == wc;
     if (!__all_sync(kFull, ok) && lane == 0) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
     __syncwarp();
@@ -355,7 +425,7 @@ cudaError_t launch_zq_encode(const uint8_t* in, uint64_t n, const uint8_t width[
                                    &per_sm);
   if (err != cudaSuccess) return err;
   const uint32_t groups = static_cast<uint32_t>((nb + kQEncWarps - 1) / kQEncWarps);
-  uint32_t ctas = groups;
+  uint32_t ctas = groups;  // at least 8 blocks per CTA, at most all resident CTAs
   const uint32_t cap = static_cast<uint32_t>(dev.sm_count) * static_cast<uint32_t>(per_sm);
   if (ctas > cap) ctas = cap;
   if (ctas == 0) ctas = 1;
