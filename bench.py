@@ -626,7 +626,18 @@ def run_workloads(args, zc, torch, device, peak):
                                         "decompress": entry(td_, 2 * m, 2 * m + mb_ + k_),
                                         "ratio": round(2 * m / (mb_ + k_), 4), "escape_rate": round(k_ / m, 5),
                                         "l2": "8 shards and 8 output sets in rotation (512 MB of inputs)"}
-    del ws_, sm_, se_, sy_
+    # a sender compresses its 8 destination shards in one batched launch; a receiver decodes them likewise
+    wsb = zc.workspace([m] * P, device=device)
+    items = [zc.BatchItem(bf16=base[i], main=sm_[i], esc=se_[i], cb=cb_in) for i in range(P)]
+    tcb = _time_ms(torch, lambda: zc.compress_batched(items, wsb, st), 10)
+    kb = sum(zc.header_n_esc(t) for t in sm_)
+    outs_b = [zc.BatchItem(bf16=sy_[i], main=sm_[i], esc=se_[i]) for i in range(P)]
+    tdb = _time_ms(torch, lambda: zc.decompress_batched(outs_b, st), 10)
+    okb = all(torch.equal(sy_[i], base[i]) for i in range(P))
+    out["reduce_scatter_8_shards_batched"] = {
+        "compress_batched": entry(tcb, 2 * m * P, P * (2 * m + mb_) + kb),
+        "decompress_batched": entry(tdb, 2 * m * P, P * (2 * m + mb_) + kb), "round_trip_ok": bool(okb)}
+    del ws_, sm_, se_, sy_, wsb, items, outs_b
     sweep = []
     for lg in range(15, args.sweep_max_log2 + 1):
         sweep.append(reduce_case(1 << lg))
