@@ -203,10 +203,14 @@ __global__ void __launch_bounds__(kQEncWarps * 32, 1) zq_encode_kernel(const __g
     zq_lookup_run(S.lut, q0, v0, e);
     q0 = q1, v0 = v1, q1 = q2, v1 = v2, q2 = q3, v2 = v3;
     q3 = load_k(k + 4, &v3);
+    // two codes at a time (at most 22 bits): one insertion and at most one
+    // full word per pair
 #pragma unroll
-    for (uint32_t t = 0; t < 16; t++) {
-      const uint32_t len = e[t] >> 16;  // 0 past n
-      acc |= static_cast<unsigned long long>(e[t] & 0xFFFFu) << ((64 - nacc - len) & 63);
+    for (uint32_t t = 0; t < 16; t += 2) {
+      const uint32_t l1 = e[t + 1] >> 16;  // 0 past n
+      const uint32_t len = (e[t] >> 16) + l1;
+      const uint32_t code = ((e[t] & 0xFFFFu) << l1) | (e[t + 1] & 0xFFFFu);
+      acc |= static_cast<unsigned long long>(code) << ((64 - nacc - len) & 63);
       nacc += len;
       if (nacc >= 32) {
         lb[wc++] = static_cast<uint32_t>(acc >> 32);
