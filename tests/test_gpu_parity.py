@@ -340,6 +340,48 @@ def test_config_reduce_scatter_8x32M(zc):
     _reduce_case(zc, 8, 1 << 25)
 
 
+@pytest.mark.slow
+def test_config_reduce_scatter_sweep_largest(zc):
+    """The largest point of the shard-size sweep, as the benchmark runs it: P = 8 shards of 2^29 elements
+    (1 GiB each), each the 2^25-element base shard repeated 16 times.  Checked on a seeded sample of tiles
+    (the format is tile-local given the offset table): the reduced values against the oracle's reduction of
+    the same input slices, each re-encoded tile's bytes and escapes against the oracle's encoding of that
+    tile alone, and the escape offsets against each other."""
+    P, m_base, reps = 8, 1 << 25, 16
+    m = m_base * reps
+    base = workloads.rs_shards(P=P, m=m_base)
+    cb_in = oracle.codebook_from_sigma(workloads.RS_SIGMA)
+    cb_out = oracle.codebook_from_sigma(workloads.RS_SIGMA * math.sqrt(P))
+    st = zc.new_status()
+    ws = zc.workspace(m)
+    mains, escs = [], []
+    for b in base:
+        main, esc = zc.compress(dev(b).repeat(reps), zc.codebook_to_device(cb_in), ws, st)
+        mains.append(main)
+        escs.append(esc)
+    y, om_t, oe_t = zc.decompress_reduce(mains, escs, m, st, out_cb=zc.codebook_to_device(cb_out), ws=ws)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0, zc.status_string(zc.status_value(st))
+    ntiles = m // 4096
+    R = -(-4 * ntiles // 128) * 128
+    n_esc = zc.header_n_esc(om_t)
+    rng = np.random.default_rng(29)
+    tiles = sorted({0, 1, 8191, 8192, ntiles - 2, ntiles - 1, *rng.integers(0, ntiles, 58).tolist()})
+    table = om_t[128:128 + 4 * ntiles].view(torch.int32)
+    for t in tiles:
+        tt = t % (m_base // 4096)
+        xs = [b[4096 * tt:4096 * (tt + 1)] for b in base]
+        want_y = oracle.reduce(xs)
+        assert np.array_equal(host_u16(y[4096 * t:4096 * (t + 1)]), want_y), f"tile {t}"
+        tm, te = oracle.compress(want_y, cb_out)
+        got_tile = host_u8(om_t[128 + R + 5632 * t:128 + R + 5632 * (t + 1)])
+        assert np.array_equal(got_tile, tm[256:256 + 5632]), f"re-encoded tile {t}"
+        a = int(table[t].item()) & 0xFFFFFFFF
+        b = int(table[t + 1].item()) & 0xFFFFFFFF if t + 1 < ntiles else n_esc
+        assert b - a == te.size, f"escape count of tile {t}"
+        assert np.array_equal(host_u8(oe_t[a:b]), te), f"escapes of tile {t}"
+
+
 # ------------------------------------------------------------------ workspace reuse
 def test_workspace_reused_without_rezeroing(zc):
     ws = zc.workspace(1 << 18)
