@@ -330,6 +330,44 @@ zc_status zc_pipelined_transfer(const void* d_in, uint64_t n, const uint8_t* d_c
                                 uint64_t chunk_elems, void* d_ws, uint64_t ws_bytes, int32_t* d_status,
                                 void* stream_compress, void* stream_link, void* stream_decompress);
 
+/*
+ * Cost models for deciding, on the host, whether compressing pays
+ * ([CCCL §2.2]: compression pays only while the time to compress plus the
+ * time to send the compressed data stays below the time to send the raw
+ * data; [ZipCCL §2.D]: the reduce-scatter switcher profiles bandwidth,
+ * latency and ratio once and picks the native reduce-scatter or the zipped
+ * all-to-all with a local reduction).  Plain arithmetic, no device work.
+ *   link:  bandwidth (GB/s per rank and direction) and latency (us) of a message.
+ *   codec: compress / decompress throughput in GB/s of uncompressed data (the
+ *          decompress figure stands for decompress-reduce in the
+ *          reduce-scatter model, per byte of its P inputs) and the expected
+ *          ratio (uncompressed / compressed bytes, e.g. from a sample).
+ * zc_transfer_pays: one message of `bytes`:
+ *   t_raw = latency + bytes / bandwidth
+ *   t_zipped = bytes / compress + latency + bytes / ratio / bandwidth + bytes / decompress
+ * zc_reduce_scatter_choose: P ranks, `bytes` per rank before the reduction:
+ *   native ring: (P - 1) steps of latency + bytes / P / bandwidth
+ *   zipped: compress bytes, one all-to-all step of latency +
+ *           (P - 1) / P * bytes / ratio / bandwidth, decompress-reduce of the
+ *           P received shards (P * bytes / P = bytes of inputs)
+ * Outputs (any may be NULL): the decision (1 = compress) and both times (us).
+ * Non-positive bandwidth, throughputs or ratio, negative latency, P < 1 ->
+ * ZC_ERR_INVALID_ARG.
+ */
+typedef struct zc_link_model {
+  double bandwidth_gbps;
+  double latency_us;
+} zc_link_model;
+typedef struct zc_codec_model {
+  double compress_gbps;
+  double decompress_gbps;
+  double ratio;
+} zc_codec_model;
+zc_status zc_transfer_pays(uint64_t bytes, const zc_link_model* link, const zc_codec_model* codec, int* pays,
+                           double* t_raw_us, double* t_zipped_us);
+zc_status zc_reduce_scatter_choose(uint64_t bytes, int P, const zc_link_model* link, const zc_codec_model* codec,
+                                   int* use_zipped, double* t_native_us, double* t_zipped_us);
+
 /* zc_compress_batched with the raw bypass of zc_compress_adaptive, decided per tensor. */
 zc_status zc_compress_batched_adaptive(int count, const zc_tensor* h_tensors, void* d_ws, uint64_t ws_bytes,
                                        int32_t* d_status, void* stream);

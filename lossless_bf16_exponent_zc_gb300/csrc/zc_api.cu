@@ -331,6 +331,38 @@ zc_status zc_pipelined_transfer(const void* d_in, uint64_t n, const uint8_t* d_c
                                      chunk_elems, static_cast<uint8_t*>(d_ws), d_status, as_stream(stream_compress),
                                      as_stream(stream_link), as_stream(stream_decompress), dev));
 }
+static bool models_valid(const zc_link_model* link, const zc_codec_model* codec) {
+  return link && codec && link->bandwidth_gbps > 0 && link->latency_us >= 0 && codec->compress_gbps > 0 &&
+         codec->decompress_gbps > 0 && codec->ratio > 0 && std::isfinite(link->bandwidth_gbps) &&
+         std::isfinite(link->latency_us) && std::isfinite(codec->compress_gbps) &&
+         std::isfinite(codec->decompress_gbps) && std::isfinite(codec->ratio);
+}
+// microseconds to move `bytes` at `gbps` (1 GB/s = 1e3 bytes per microsecond)
+static double us_at(double bytes, double gbps) { return bytes / (gbps * 1e3); }
+zc_status zc_transfer_pays(uint64_t bytes, const zc_link_model* link, const zc_codec_model* codec, int* pays,
+                           double* t_raw_us, double* t_zipped_us) {
+  if (!models_valid(link, codec)) return ZC_ERR_INVALID_ARG;
+  const double b = static_cast<double>(bytes);
+  const double raw = link->latency_us + us_at(b, link->bandwidth_gbps);
+  const double zipped = us_at(b, codec->compress_gbps) + link->latency_us +
+                        us_at(b / codec->ratio, link->bandwidth_gbps) + us_at(b, codec->decompress_gbps);
+  if (pays) *pays = zipped < raw ? 1 : 0;
+  if (t_raw_us) *t_raw_us = raw;
+  if (t_zipped_us) *t_zipped_us = zipped;
+  return ZC_OK;
+}
+zc_status zc_reduce_scatter_choose(uint64_t bytes, int P, const zc_link_model* link, const zc_codec_model* codec,
+                                   int* use_zipped, double* t_native_us, double* t_zipped_us) {
+  if (!models_valid(link, codec) || P < 1) return ZC_ERR_INVALID_ARG;
+  const double b = static_cast<double>(bytes), p = static_cast<double>(P);
+  const double native = (p - 1.0) * (link->latency_us + us_at(b / p, link->bandwidth_gbps));
+  const double exchange = P > 1 ? link->latency_us + us_at((p - 1.0) / p * b / codec->ratio, link->bandwidth_gbps) : 0.0;
+  const double zipped = us_at(b, codec->compress_gbps) + exchange + us_at(b, codec->decompress_gbps);
+  if (use_zipped) *use_zipped = zipped < native ? 1 : 0;
+  if (t_native_us) *t_native_us = native;
+  if (t_zipped_us) *t_zipped_us = zipped;
+  return ZC_OK;
+}
 static const uint8_t kZqDefaultWidths[8] = {3, 3, 3, 3, 3, 4, 5, 8};
 static bool zq_widths_valid(const uint8_t* w) {
   uint32_t cap = 0;

@@ -44,6 +44,14 @@ class ZqTable(ctypes.Structure):
     _fields_ = [("width", ctypes.c_uint8 * 8), ("sym", ctypes.c_uint8 * 256)]
 
 
+class LinkModel(ctypes.Structure):
+    _fields_ = [("bandwidth_gbps", ctypes.c_double), ("latency_us", ctypes.c_double)]
+
+
+class CodecModel(ctypes.Structure):
+    _fields_ = [("compress_gbps", ctypes.c_double), ("decompress_gbps", ctypes.c_double), ("ratio", ctypes.c_double)]
+
+
 class ZcTensor(ctypes.Structure):
     _fields_ = [("bf16", ctypes.c_void_p), ("main", ctypes.c_void_p), ("esc", ctypes.c_void_p),
                 ("cb", ctypes.c_void_p), ("n", ctypes.c_uint64), ("esc_bytes", ctypes.c_uint64)]
@@ -89,13 +97,19 @@ def load() -> ctypes.CDLL:
     lib.zq_max_bytes.argtypes = [u64, u64p]
     lib.zq_compress.argtypes = [vp, u64, ctypes.POINTER(ZqTable), vp, u64, vp, u64, vp, vp]
     lib.zq_decompress.argtypes = [vp, u64, u64, vp, vp, vp]
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.zc_transfer_pays.argtypes = [u64, ctypes.POINTER(LinkModel), ctypes.POINTER(CodecModel),
+                                     ctypes.POINTER(i32), dp, dp]
+    lib.zc_reduce_scatter_choose.argtypes = [u64, i32, ctypes.POINTER(LinkModel), ctypes.POINTER(CodecModel),
+                                             ctypes.POINTER(i32), dp, dp]
     lib.zc_pipeline_workspace_size.argtypes = [u64, u64p]
     lib.zc_pipelined_transfer.argtypes = [vp, u64, vp, vp, u64, vp, u64, vp, vp, vp, vp]
     for name in ("zc_codebook_from_sigma", "zc_compressed_size", "zc_workspace_size", "zc_histogram_topk",
                  "zc_compress", "zc_compress_adaptive", "zc_raw_spill", "zc_decompress", "zc_decompress_reduce",
                  "zc_compress_batched", "zc_compress_batched_adaptive", "zc_decompress_batched",
                  "zc_pipeline_workspace_size", "zc_pipelined_transfer", "zq_default_widths",
-                 "zq_table_from_histogram", "zq_max_bytes", "zq_compress", "zq_decompress"):
+                 "zq_table_from_histogram", "zq_max_bytes", "zq_compress", "zq_decompress", "zc_transfer_pays",
+                 "zc_reduce_scatter_choose"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -295,6 +309,27 @@ def compress_batched_adaptive(items: Sequence[BatchItem], ws: torch.Tensor, stat
 def decompress_batched(items: Sequence[BatchItem], status: torch.Tensor, stream=None) -> None:
     arr = _descs(items)
     _check(load().zc_decompress_batched(len(items), arr, _ptr(status), _stream(stream)), "zc_decompress_batched")
+
+
+def transfer_pays(nbytes: int, bandwidth_gbps: float, latency_us: float, compress_gbps: float,
+                  decompress_gbps: float, ratio: float) -> tuple[bool, float, float]:
+    """(compress?, t_raw_us, t_zipped_us) for one message (zc_transfer_pays)."""
+    link, codec = LinkModel(bandwidth_gbps, latency_us), CodecModel(compress_gbps, decompress_gbps, ratio)
+    pays, tr, tz = ctypes.c_int(), ctypes.c_double(), ctypes.c_double()
+    _check(load().zc_transfer_pays(int(nbytes), ctypes.byref(link), ctypes.byref(codec), ctypes.byref(pays),
+                                   ctypes.byref(tr), ctypes.byref(tz)), "zc_transfer_pays")
+    return bool(pays.value), tr.value, tz.value
+
+
+def reduce_scatter_choose(nbytes: int, P: int, bandwidth_gbps: float, latency_us: float, compress_gbps: float,
+                          decompress_gbps: float, ratio: float) -> tuple[bool, float, float]:
+    """(zipped?, t_native_us, t_zipped_us) for a reduce-scatter of nbytes per rank over P ranks."""
+    link, codec = LinkModel(bandwidth_gbps, latency_us), CodecModel(compress_gbps, decompress_gbps, ratio)
+    z, tn, tz = ctypes.c_int(), ctypes.c_double(), ctypes.c_double()
+    _check(load().zc_reduce_scatter_choose(int(nbytes), int(P), ctypes.byref(link), ctypes.byref(codec),
+                                           ctypes.byref(z), ctypes.byref(tn), ctypes.byref(tz)),
+           "zc_reduce_scatter_choose")
+    return bool(z.value), tn.value, tz.value
 
 
 def pipeline_workspace_size(chunk_elems: int) -> int:

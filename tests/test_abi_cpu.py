@@ -26,7 +26,8 @@ def test_library_exports_every_declared_symbol():
             "zc_compressed_size", "zc_workspace_size", "zc_compress_batched", "zc_decompress_batched",
             "zc_status_string", "zc_version", "zc_compress_adaptive", "zc_compress_batched_adaptive",
             "zc_raw_spill", "zc_pipeline_workspace_size", "zc_pipelined_transfer", "zq_default_widths",
-            "zq_table_from_histogram", "zq_max_bytes", "zq_compress", "zq_decompress"} <= set(names)
+            "zq_table_from_histogram", "zq_max_bytes", "zq_compress", "zq_decompress", "zc_transfer_pays",
+            "zc_reduce_scatter_choose"} <= set(names)
     for name in names:
         assert hasattr(lib, name), name
 
@@ -155,3 +156,45 @@ def test_qlc_host_functions_match_oracle():
     bad = zc.zq_table((3, 3, 3, 3, 3, 3, 3, 3), range(256))
     assert zc.load().zq_compress(fake, 100, ctypes.byref(bad), fake, 1 << 20, fake, 1 << 20, status,
                                  None) == zc.ERR_CODEBOOK
+
+
+# ------------------------------------------------------------------ cost models (host arithmetic)
+def test_transfer_cost_model_break_even():
+    """[CCCL §2.2]: compressing pays while compress + decompress + sending the smaller data beats sending the
+    raw data.  Latency appears on both sides, so the break-even link bandwidth is (1 - 1/ratio) / (1/c + 1/d)."""
+    c, d, r = 2800.0, 2900.0, 1.43
+    bw_star = (1 - 1 / r) / (1 / c + 1 / d)
+    assert zc.transfer_pays(1 << 28, bw_star * 0.99, 7.0, c, d, r)[0]
+    assert not zc.transfer_pays(1 << 28, bw_star * 1.01, 7.0, c, d, r)[0]
+    # a ratio of 1 or less never pays, however fast the codec
+    for ratio in (1.0, 0.9):
+        assert not zc.transfer_pays(1 << 30, 0.001, 0.0, 1e12, 1e12, ratio)[0]
+    # times in microseconds: 1 MB over 1 GB/s is 1000 us
+    pays, t_raw, t_zip = zc.transfer_pays(10 ** 6, 1.0, 2.0, 1000.0, 500.0, 2.0)
+    assert t_raw == pytest.approx(1002.0) and t_zip == pytest.approx(1.0 + 2.0 + 500.0 + 2.0) and pays
+
+
+def test_reduce_scatter_switcher():
+    """[ZipCCL §2.D] switcher: native ring (P - 1 steps of bytes / P) against compress + one all-to-all of the
+    compressed shards + decompress-reduce.  With no latency the break-even bandwidth is
+    (P - 1) / P * (1 - 1/ratio) / (1/c + 1/d)."""
+    c, d, r, P = 2800.0, 1300.0, 1.43, 8
+    bw_star = (P - 1) / P * (1 - 1 / r) / (1 / c + 1 / d)
+    assert zc.reduce_scatter_choose(1 << 28, P, bw_star * 0.99, 0.0, c, d, r)[0]
+    assert not zc.reduce_scatter_choose(1 << 28, P, bw_star * 1.01, 0.0, c, d, r)[0]
+    # one rank: nothing to send, the native path costs nothing
+    use, t_native, t_zip = zc.reduce_scatter_choose(1 << 20, 1, 10.0, 5.0, c, d, r)
+    assert not use and t_native == 0.0 and t_zip > 0
+    # many small messages: the ring pays P - 1 latencies, the all-to-all one
+    use, t_native, t_zip = zc.reduce_scatter_choose(1 << 10, 64, 100.0, 20.0, c, d, r)
+    assert use and t_native == pytest.approx(63 * (20.0 + (1 << 10) / 64 / 100e3))
+
+
+def test_cost_model_argument_errors():
+    for args in ((1, -1.0, 1.0, 1.0, 1.0, 1.0), (1, 1.0, -1.0, 1.0, 1.0, 1.0), (1, 1.0, 1.0, 0.0, 1.0, 1.0),
+                 (1, 1.0, 1.0, 1.0, 1.0, 0.0), (1, float("nan"), 1.0, 1.0, 1.0, 1.0)):
+        with pytest.raises(zc.ZcError) as e:
+            zc.transfer_pays(*args)
+        assert e.value.code == zc.ERR_INVALID_ARG
+    with pytest.raises(zc.ZcError):
+        zc.reduce_scatter_choose(1, 0, 1.0, 1.0, 1.0, 1.0, 1.0)
