@@ -399,12 +399,34 @@ def run_ours(args):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "workloads": per_workload,
+            "cost_model": cost_model_context(zc, ops_report, per_workload, n, 2 * n / (mb + n_esc_b)),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def cost_model_context(zc, ops_report, per_workload, n, ratio):
+    """The host cost models fed with this run's measured codec throughput and ratio, for two example links
+    (a 400 Gb/s network port, 50 GB/s, 5 us; an NVLink-class link, 900 GB/s, 2 us): does compressing a
+    2^26-value tensor pay, and which reduce-scatter would the switcher pick at P = 8 (with the measured
+    decode-reduce throughput when the workload section ran).  Context only: no link is measured on one GPU."""
+    c = ops_report["compress_sigma_cb"]["GB_per_s_uncompressed"]
+    d = ops_report["decompress_sigma_cb"]["GB_per_s_uncompressed"]
+    dr = d
+    if per_workload and "reduce_scatter_8x2^25" in per_workload:
+        dr = per_workload["reduce_scatter_8x2^25"]["GB_per_s_uncompressed"]
+    out = {"compress_gbps": c, "decompress_gbps": d, "decompress_reduce_gbps": dr, "ratio": round(ratio, 4),
+           "links": {}}
+    for name, bw, lat in (("network_50GBps_5us", 50.0, 5.0), ("nvlink_900GBps_2us", 900.0, 2.0)):
+        pays, t_raw, t_zip = zc.transfer_pays(2 * n, bw, lat, c, d, ratio)
+        use, t_nat, t_rs = zc.reduce_scatter_choose(2 * n, 8, bw, lat, c, dr, ratio)
+        out["links"][name] = {"transfer_pays": pays, "t_raw_us": round(t_raw, 1), "t_zipped_us": round(t_zip, 1),
+                              "reduce_scatter_zipped": use, "t_native_rs_us": round(t_nat, 1),
+                              "t_zipped_rs_us": round(t_rs, 1)}
+    return out
 
 
 def run_e2e(args, zc, torch, device, x, mb, eb, world):
