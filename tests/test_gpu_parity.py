@@ -382,6 +382,39 @@ def test_config_reduce_scatter_sweep_largest(zc):
         assert np.array_equal(host_u8(oe_t[a:b]), te), f"escapes of tile {t}"
 
 
+@pytest.mark.slow
+def test_huge_tensor_byte_offsets_beyond_2pow31(zc):
+    """2^31 + 12345 values (4 GiB of bf16, a 2.8 GiB main stream): every byte offset past 2^31 goes through
+    64-bit address arithmetic.  The input is drawn on the device (seeded, workloads.gaussian_on_device); the round trip is compared in
+    full on the device, and 24 seeded tiles of the main and escape streams against the oracle's encoding of
+    those tiles alone (the format is tile-local given the offset table)."""
+    n = (1 << 31) + 12345
+    xt = workloads.gaussian_on_device(n, 1e-3, seed=31)
+    cb = oracle.codebook_from_sigma(1e-3)
+    st = zc.new_status()
+    ws = zc.workspace(n)
+    main, esc = zc.compress(xt, zc.codebook_to_device(cb), ws, st)
+    y = zc.decompress(main, esc, n, st)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0, zc.status_string(zc.status_value(st))
+    assert torch.equal(y, xt)
+    del y
+    ntiles = -(-n // 4096)
+    R = -(-4 * ntiles // 128) * 128
+    n_esc = zc.header_n_esc(main)
+    table = main[128:128 + 4 * ntiles].view(torch.int32)
+    rng = np.random.default_rng(31)
+    tiles = sorted({0, (1 << 31) // 4096 // 2, ntiles - 2, ntiles - 1, *rng.integers(0, ntiles, 20).tolist()})
+    for t in tiles:
+        x_tile = host_u16(xt[4096 * t:min(n, 4096 * (t + 1))])
+        tm, te = oracle.compress(x_tile, cb)
+        got = host_u8(main[128 + R + 5632 * t:128 + R + 5632 * (t + 1)])
+        assert np.array_equal(got, tm[256:256 + 5632]), f"tile {t}"
+        a = int(table[t].item()) & 0xFFFFFFFF
+        b = int(table[t + 1].item()) & 0xFFFFFFFF if t + 1 < ntiles else n_esc
+        assert b - a == te.size and np.array_equal(host_u8(esc[a:b]), te), f"escapes of tile {t}"
+
+
 # ------------------------------------------------------------------ workspace reuse
 def test_workspace_reused_without_rezeroing(zc):
     ws = zc.workspace(1 << 18)

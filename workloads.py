@@ -139,6 +139,14 @@ def rs_shards(P: int = 8, m: int = 1 << 25, sigma: float = RS_SIGMA, seed: int =
     return shards
 
 
+def gaussian_on_device(n: int, sigma: float, seed: int, device="cuda") -> torch.Tensor:
+    """N(0, sigma^2) rounded to bfloat16, drawn on the device with torch's seeded generator (for tensors too
+    large to draw and copy from the host); returned as the int16 bit patterns."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return (torch.randn(n, device=device, generator=g) * sigma).to(torch.bfloat16).view(torch.int16)
+
+
 def random_bits(n: int = 1 << 26, seed: int = 6) -> np.ndarray:
     """Uniformly random bf16 bit patterns (NaNs and infinities included)."""
     return np.random.default_rng(seed).integers(0, 65536, n, dtype=np.uint16)
