@@ -415,6 +415,41 @@ def test_huge_tensor_byte_offsets_beyond_2pow31(zc):
         assert b - a == te.size and np.array_equal(host_u8(esc[a:b]), te), f"escapes of tile {t}"
 
 
+@pytest.mark.slow
+def test_huge_reduce_byte_offsets_beyond_2pow31(zc):
+    """Decode-reduce-re-encode of P = 2 shards of 2^31 + 777 values (2.8 GiB main streams, a 4 GiB result):
+    24 seeded tiles of the result and of the re-encoded stream against the oracle's reduction of the same
+    input slices and its encoding of each tile alone."""
+    n = (1 << 31) + 777
+    xs = [workloads.gaussian_on_device(n, 1e-3, seed=40 + r) for r in range(2)]
+    cb_in = oracle.codebook_from_sigma(1e-3)
+    cb_out = oracle.codebook_from_sigma(1e-3 * math.sqrt(2))
+    st = zc.new_status()
+    ws = zc.workspace(n)
+    streams = [zc.compress(x, zc.codebook_to_device(cb_in), ws, st) for x in xs]
+    y, om_t, oe_t = zc.decompress_reduce([m for m, _ in streams], [e for _, e in streams], n, st,
+                                         out_cb=zc.codebook_to_device(cb_out), ws=ws)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0, zc.status_string(zc.status_value(st))
+    del streams
+    ntiles = -(-n // 4096)
+    R = -(-4 * ntiles // 128) * 128
+    n_esc = zc.header_n_esc(om_t)
+    table = om_t[128:128 + 4 * ntiles].view(torch.int32)
+    rng = np.random.default_rng(41)
+    tiles = sorted({0, (1 << 31) // 4096 // 2, ntiles - 2, ntiles - 1, *rng.integers(0, ntiles, 20).tolist()})
+    for t in tiles:
+        lo, hi = 4096 * t, min(n, 4096 * (t + 1))
+        want_y = oracle.reduce([host_u16(x[lo:hi]) for x in xs])
+        assert np.array_equal(host_u16(y[lo:hi]), want_y), f"tile {t}"
+        tm, te = oracle.compress(want_y, cb_out)
+        got = host_u8(om_t[128 + R + 5632 * t:128 + R + 5632 * (t + 1)])
+        assert np.array_equal(got, tm[256:256 + 5632]), f"re-encoded tile {t}"
+        a = int(table[t].item()) & 0xFFFFFFFF
+        b = int(table[t + 1].item()) & 0xFFFFFFFF if t + 1 < ntiles else n_esc
+        assert b - a == te.size and np.array_equal(host_u8(oe_t[a:b]), te), f"escapes of tile {t}"
+
+
 # ------------------------------------------------------------------ workspace reuse
 def test_workspace_reused_without_rezeroing(zc):
     ws = zc.workspace(1 << 18)
