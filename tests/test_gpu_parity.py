@@ -383,12 +383,14 @@ def test_config_reduce_scatter_sweep_largest(zc):
 
 
 @pytest.mark.slow
-def test_huge_tensor_byte_offsets_beyond_2pow31(zc):
-    """2^31 + 12345 values (4 GiB of bf16, a 2.8 GiB main stream): every byte offset past 2^31 goes through
-    64-bit address arithmetic.  The input is drawn on the device (seeded, workloads.gaussian_on_device); the round trip is compared in
-    full on the device, and 24 seeded tiles of the main and escape streams against the oracle's encoding of
-    those tiles alone (the format is tile-local given the offset table)."""
-    n = (1 << 31) + 12345
+def test_largest_tensor(zc):
+    """The largest tensor the format allows, n = 2^32 - 1 values (8 GiB of bf16, a 5.6 GiB main stream, a
+    ragged last tile): byte offsets far past 2^31 and 2^32 go through 64-bit address arithmetic, tile and
+    group counts reach their u32 limits.  The input is drawn on the device (seeded,
+    workloads.gaussian_on_device); the round trip is compared in full on the device, and 24 seeded tiles of
+    the main and escape streams against the oracle's encoding of those tiles alone (the format is
+    tile-local given the offset table)."""
+    n = (1 << 32) - 1
     xt = workloads.gaussian_on_device(n, 1e-3, seed=31)
     cb = oracle.codebook_from_sigma(1e-3)
     st = zc.new_status()
@@ -404,7 +406,7 @@ def test_huge_tensor_byte_offsets_beyond_2pow31(zc):
     n_esc = zc.header_n_esc(main)
     table = main[128:128 + 4 * ntiles].view(torch.int32)
     rng = np.random.default_rng(31)
-    tiles = sorted({0, (1 << 31) // 4096 // 2, ntiles - 2, ntiles - 1, *rng.integers(0, ntiles, 20).tolist()})
+    tiles = sorted({0, (1 << 31) // 4096, ntiles - 2, ntiles - 1, *rng.integers(0, ntiles, 20).tolist()})
     for t in tiles:
         x_tile = host_u16(xt[4096 * t:min(n, 4096 * (t + 1))])
         tm, te = oracle.compress(x_tile, cb)

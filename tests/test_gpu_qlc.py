@@ -141,3 +141,36 @@ def test_full_size_ffn1(zc):
     n = 1 << 26
     x = workloads.fp8_ffn1(n)
     check(zc, x, DEFAULT, oracle.qlc_table_for(x))
+
+
+@pytest.mark.slow
+def test_largest_stream(zc):
+    """The largest QLC input, n = 2^32 - 1 bytes (payload word offsets past 2^30, byte offsets past 2^32):
+    full round trip on the device and 16 seeded blocks against the oracle's coding of each block alone."""
+    n = (1 << 32) - 1
+    g = torch.Generator(device="cuda")
+    g.manual_seed(77)
+    xt = torch.randint(0, 256, (n,), dtype=torch.uint8, device="cuda", generator=g)
+    xt = torch.where(xt < 192, torch.full_like(xt, 56) + (xt & 7), xt)  # a skewed byte distribution
+    hist = sum(torch.bincount(xt[i:i + (1 << 28)], minlength=256) for i in range(0, n, 1 << 28)).cpu().numpy()
+    sym = oracle.qlc_table_from_histogram(hist)
+    st = zc.new_status()
+    ws = zc.workspace(n)
+    out = zc.zq_compress(xt, zc.zq_table(DEFAULT, sym), ws, st)
+    y = zc.zq_decompress(out, n, st, in_bytes=zc.zq_stream_bytes(out))
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0, zc.status_string(zc.status_value(st))
+    assert torch.equal(y, xt)
+    del y
+    nb = -(-n // 4096)
+    tbl = -(-4 * nb // 128) * 128
+    offs = out[384:384 + 4 * nb].view(torch.int32)
+    words = int.from_bytes(out[24:32].cpu().numpy().tobytes(), "little")
+    rng = np.random.default_rng(78)
+    for b in sorted({0, nb // 2, nb - 1, *rng.integers(0, nb, 13).tolist()}):
+        x_blk = xt[4096 * b:min(n, 4096 * (b + 1))].cpu().numpy()
+        want = oracle.qlc_compress(x_blk, DEFAULT, sym)  # one block: its words start at byte 512
+        a = int(offs[b].item()) & 0xFFFFFFFF
+        e = int(offs[b + 1].item()) & 0xFFFFFFFF if b + 1 < nb else words
+        got = out[384 + tbl + 4 * a:384 + tbl + 4 * e].cpu().numpy()
+        assert np.array_equal(got, want[512:]), f"block {b}"
