@@ -72,6 +72,15 @@
  *   tensors allocated by PyTorch); h_* are host pointers.  libzc never
  *   allocates, never frees and never synchronises the host.  All device work
  *   is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ * - Launches: every kernel is launched as a programmatic dependent launch
+ *   (CUDA's programmatic stream serialization), so it may be scheduled while
+ *   the kernel before it on the stream finishes; it reads and writes global
+ *   memory only after that kernel has completed and its writes are visible,
+ *   so stream order holds for all data.  Each kernel also lets the launch
+ *   after it start early: a caller's kernel that follows on the same stream
+ *   with the programmatic attribute must wait for its prerequisites
+ *   (cudaGridDependencySynchronize) before it reads libzc's outputs, as that
+ *   attribute always requires; launches without it see plain stream order.
  * - Alignment: bfloat16 buffers, main streams and escape streams must be
  *   16-byte aligned; the workspace 16-byte aligned; d_status 4-byte aligned.
  * - Argument errors are returned synchronously and enqueue nothing.  A failed

@@ -107,6 +107,23 @@ cudaError_t prepare_kernel(KernelPrep& kp, const void* fn, int threads, int smem
   if (cached) kp.per_sm[dev.device].store(*per_sm, std::memory_order_release);
   return cudaSuccess;
 }
+
+cudaError_t launch_kernel(const void* fn, dim3 grid, dim3 block, int smem_bytes, cudaStream_t stream, void** args,
+                          bool cooperative) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cooperative ? 2u : 1u;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
 }  // namespace zc
 
 extern "C" {

@@ -125,6 +125,7 @@ __device__ __forceinline__ uint32_t stage_escapes(uint8_t* dst, const uint8_t* e
 template <int MAXB>
 __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_constant__ DecParams<MAXB> p) {
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_begin();
   const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
   const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;
   uint8_t* gbase = smem + (sbase - smem_u32(smem));
@@ -270,8 +271,9 @@ static cudaError_t launch_decode_t(const DecTensor* ts, int count, int32_t* stat
   if (err != cudaSuccess) return err;
   uint32_t ctas = (total + kDecWarps - 1) / kDecWarps;
   if (ctas > static_cast<uint32_t>(dev.sm_count)) ctas = dev.sm_count;
-  decode_kernel<MAXB><<<ctas, kDecWarps * 32, kDecSmem, stream>>>(p);
-  return cudaGetLastError();
+  void* args[] = {&p};
+  return launch_kernel(reinterpret_cast<const void*>(decode_kernel<MAXB>), dim3(ctas), dim3(kDecWarps * 32),
+                       kDecSmem, stream, args, false);
 }
 
 cudaError_t launch_decode(const DecTensor* ts, int count, int32_t* status, cudaStream_t stream,

@@ -159,6 +159,20 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return done != 0;
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched so
+// that it may be scheduled while the kernel before it on the stream is still
+// running, and every kernel lets the launch after it be scheduled as soon as
+// all its CTAs have started.  pdl_begin() does both: it allows the next
+// launch, then waits until every grid this one depends on has completed and
+// its memory operations are visible.  A kernel calls it before it touches
+// global memory, so stream order holds for all data; what overlaps is the
+// launch itself and the placement of CTAs on SMs that the previous grid has
+// left.  Without the launch attribute the wait returns at once.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Wait for phase `parity` of `bar` to complete, at most kWaitLimitNs.  Returns
 // false (and records ZC_ERR_TIMEOUT) if the limit is reached.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* status) {

@@ -116,9 +116,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;  // 1 KB aligned shared address
   uint8_t* gbase = smem + (sbase - smem_u32(smem));           // its generic pointer
   RoundShared* rs = reinterpret_cast<RoundShared*>(gbase + kEncGrpOff);
-  // A launch that follows as a programmatic dependent (the raw-bypass
-  // decision) may be scheduled now; it waits for this grid's completion.
-  asm volatile("griddepcontrol.launch_dependents;");
+  pdl_begin();
   const uint32_t step = gridDim.x;
 
   if (threadIdx.x == 0) {
@@ -428,8 +426,8 @@ static cudaError_t launch_encode_t(const EncTensor* ts, int count, WsHeader* ws,
   if (ctas > cap) ctas = cap;
   if (ctas == 0) ctas = 1;
   void* args[] = {&p};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(encode_kernel<MAXB>), dim3(ctas),
-                                     dim3(kEncThreads), args, kEncSmem, stream);
+  return launch_kernel(reinterpret_cast<const void*>(encode_kernel<MAXB>), dim3(ctas), dim3(kEncThreads), kEncSmem,
+                       stream, args, true);
 }
 
 cudaError_t launch_encode(const EncTensor* ts, int count, WsHeader* ws, Flag* flags, int32_t* status,

@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(const uint16_t* _
                                                                WsHeader* ws, uint8_t* cb_out, uint32_t* hist_out,
                                                                int32_t* status) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
+  pdl_begin();
   uint8_t* smem = smem_raw + ((128 - (smem_u32(smem_raw) & 127u)) & 127u);
   uint32_t* h = reinterpret_cast<uint32_t*>(smem + kHistBinOff);
   __shared__ uint32_t cnt[256];
@@ -132,8 +133,9 @@ cudaError_t launch_histogram(const uint16_t* in, uint64_t n, uint8_t* cb_out, ui
   const uint64_t cap = static_cast<uint64_t>(dev.sm_count) * static_cast<uint64_t>(per_sm);
   if (ctas > cap) ctas = cap;
   if (ctas == 0) ctas = 1;
-  hist_kernel<<<static_cast<unsigned>(ctas), kHistThreads, kHistSmem, stream>>>(in, n, ws, cb_out, hist_out, status);
-  return cudaGetLastError();
+  void* args[] = {&in, &n, &ws, &cb_out, &hist_out, &status};
+  return launch_kernel(reinterpret_cast<const void*>(hist_kernel), dim3(static_cast<unsigned>(ctas)),
+                       dim3(kHistThreads), kHistSmem, stream, args, false);
 }
 
 }  // namespace zc

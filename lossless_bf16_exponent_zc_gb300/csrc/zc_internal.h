@@ -61,6 +61,12 @@ struct KernelPrep {
 cudaError_t prepare_kernel(KernelPrep& kp, const void* fn, int threads, int smem_bytes, const DeviceInfo& dev,
                            int* per_sm);
 
+// Launches kernel `fn` (args: pointers to its parameters) on `stream` as a
+// programmatic dependent of the work before it (the kernel begins with
+// pdl_begin()), and cooperatively -- every CTA resident at once -- if asked.
+cudaError_t launch_kernel(const void* fn, dim3 grid, dim3 block, int smem_bytes, cudaStream_t stream, void** args,
+                          bool cooperative);
+
 // count <= kMaxBatch; flags = workspace flag array (one per tile of the launch).
 // adaptive: an escape overflow is not reported (launch_raw_switch decides).
 cudaError_t launch_encode(const EncTensor* ts, int count, WsHeader* ws, Flag* flags, int32_t* status,

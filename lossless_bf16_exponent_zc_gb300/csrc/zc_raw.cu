@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kRawThreads, 6) raw_switch_kernel(const __grid
   static_assert(MAXB <= 32, "one mask bit per tensor");
   __shared__ uint32_t raw_mask;
   if (threadIdx.x == 0) raw_mask = 0;
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // the encoder has finished and its writes are visible
+  pdl_begin();  // the encoder has finished and its writes are visible
   __syncthreads();
   for (int i = threadIdx.x; i < p.count; i += blockDim.x) {
     bool overflow;
@@ -156,19 +156,10 @@ static cudaError_t launch_raw_switch_t(const EncTensor* ts, int count, WsHeader*
   const uint64_t cap = 6ull * static_cast<uint64_t>(dev.sm_count);  // a full SM of them keeps ~96 KB of copies in flight
   if (ctas > cap) ctas = cap;
   if (ctas == 0) ctas = 1;
-  // programmatic dependent launch: it may start while the encoder runs and
-  // waits for it in griddepcontrol.wait
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
-  cfg.blockDim = dim3(kRawThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, raw_switch_kernel<MAXB>, p);
+  // it may start while the encoder runs and waits for it in pdl_begin()
+  void* args[] = {&p};
+  return launch_kernel(reinterpret_cast<const void*>(raw_switch_kernel<MAXB>), dim3(static_cast<unsigned>(ctas)),
+                       dim3(kRawThreads), 0, stream, args, false);
 }
 
 cudaError_t launch_raw_switch(const EncTensor* ts, int count, WsHeader* ws, int32_t* status, cudaStream_t stream,

@@ -129,6 +129,7 @@ __device__ __forceinline__ uint4 round_pack(const float (&acc)[8]) {
 template <bool REENC, bool RAW>
 __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_constant__ RedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_begin();
   const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
   const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;
   uint8_t* gbase = smem + (sbase - smem_u32(smem));
@@ -517,18 +518,15 @@ cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out,
       err = prepare_kernel(prep[1][raw], fn, kRedThreads, kRedSmem, dev, &per_sm);
       if (err != cudaSuccess) return err;
       void* args[] = {&p};
-      err = cudaLaunchCooperativeKernel(fn, dim3(ctas), dim3(kRedThreads), args, kRedSmem, stream);
+      err = launch_kernel(fn, dim3(ctas), dim3(kRedThreads), kRedSmem, stream, args, true);
     } else {
       if (p.ntiles == 0) return cudaSuccess;
       const void* fn = raw ? reinterpret_cast<const void*>(reduce_kernel<false, true>)
                            : reinterpret_cast<const void*>(reduce_kernel<false, false>);
       err = prepare_kernel(prep[0][raw], fn, kRedThreads, kRedSmem, dev, &per_sm);
       if (err != cudaSuccess) return err;
-      if (raw)
-        reduce_kernel<false, true><<<ctas, kRedThreads, kRedSmem, stream>>>(p);
-      else
-        reduce_kernel<false, false><<<ctas, kRedThreads, kRedSmem, stream>>>(p);
-      err = cudaGetLastError();
+      void* args[] = {&p};
+      err = launch_kernel(fn, dim3(ctas), dim3(kRedThreads), kRedSmem, stream, args, false);
     }
     if (err != cudaSuccess) return err;
   }

@@ -91,6 +91,7 @@ __device__ __forceinline__ void zq_lookup_run(const uint32_t* lut, uint4 v, uint
 // L2 -- and stores each at its offset.
 __global__ void __launch_bounds__(kQEncWarps * 32, 1) zq_encode_kernel(const __grid_constant__ QEncParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
+  pdl_begin();
   QEncShared& S = *reinterpret_cast<QEncShared*>(smem_raw);
   const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
   for (uint32_t i = threadIdx.x; i < 256; i += blockDim.x) S.lut[i] = p.code[i];
@@ -264,6 +265,7 @@ constexpr uint16_t kQBadCode = 0x8000u | (11u << 8);
 
 __global__ void __launch_bounds__(kQDecWarps * 32) zq_decode_kernel(const __grid_constant__ QDecParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
+  pdl_begin();
   QDecShared& S = *reinterpret_cast<QDecShared*>(smem_raw);
   const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
   const uint64_t nb = zq_blocks(p.n);
@@ -434,8 +436,8 @@ cudaError_t launch_zq_encode(const uint8_t* in, uint64_t n, const uint8_t width[
   if (ctas > cap) ctas = cap;
   if (ctas == 0) ctas = 1;
   void* args[] = {&p};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(zq_encode_kernel), dim3(ctas),
-                                     dim3(kQEncWarps * 32), args, smem, stream);
+  return launch_kernel(reinterpret_cast<const void*>(zq_encode_kernel), dim3(ctas), dim3(kQEncWarps * 32), smem,
+                       stream, args, true);
 }
 
 cudaError_t launch_zq_decode(const uint8_t* in, uint64_t in_bytes, uint64_t n, uint8_t* out, int32_t* status,
@@ -452,8 +454,9 @@ cudaError_t launch_zq_decode(const uint8_t* in, uint64_t in_bytes, uint64_t n, u
   const uint64_t cap = static_cast<uint64_t>(dev.sm_count) * static_cast<uint64_t>(per_sm);
   if (ctas > cap) ctas = cap;
   if (ctas == 0) ctas = 1;
-  zq_decode_kernel<<<static_cast<unsigned>(ctas), kQDecWarps * 32, smem, stream>>>(p);
-  return cudaGetLastError();
+  void* args[] = {&p};
+  return launch_kernel(reinterpret_cast<const void*>(zq_decode_kernel), dim3(static_cast<unsigned>(ctas)),
+                       dim3(kQDecWarps * 32), smem, stream, args, false);
 }
 
 }  // namespace zc
