@@ -213,6 +213,47 @@ def test_config_llama_bucket_batched(zc, scale):
         assert np.array_equal(host_u16(o.bf16), x), name
 
 
+@pytest.mark.parametrize("adaptive", [False, True])
+def test_batch_beyond_one_launch(zc, adaptive):
+    """70 tensors in one call (three launches of at most 32 tensors on the stream): empty, one value, ragged,
+    exactly one tile, several scan groups; a codebook per tensor (sigma from 1e-4 to 3e-2), every fifth tensor
+    uniformly random bit patterns (RAW when adaptive).  Every stream against the oracle, byte for byte."""
+    rng = np.random.default_rng(70)
+    sizes = [0, 1, 4096, 4097, 8 * 4096 + 3, 10 * 4096, 21 * 4096 + 1] * 10
+    xs, cbs = [], []
+    for i, n in enumerate(sizes):
+        sigma = float(10 ** rng.uniform(-4, math.log10(3e-2)))
+        x = (rng.integers(0, 65536, n, dtype=np.uint16) if i % 5 == 4
+             else workloads.gaussian(n=n, sigma=sigma, seed=700 + i) if n else np.zeros(0, np.uint16))
+        xs.append(x)
+        cbs.append(oracle.codebook_from_sigma(sigma))
+    items = []
+    for x, cb in zip(xs, cbs):
+        mb, eb = zc.compressed_size(x.size)
+        cap = max(zc.raw_spill(x.size), 16) if adaptive else max(eb, 16)
+        items.append(zc.BatchItem(bf16=dev(x) if x.size else torch.empty(0, dtype=torch.int16, device="cuda"),
+                                  main=torch.empty(mb, dtype=torch.uint8, device="cuda"),
+                                  esc=torch.empty(cap, dtype=torch.uint8, device="cuda"),
+                                  cb=zc.codebook_to_device(cb)))
+    st = zc.new_status()
+    ws = zc.workspace([x.size for x in xs])
+    (zc.compress_batched_adaptive if adaptive else zc.compress_batched)(items, ws, st)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0, zc.status_string(zc.status_value(st))
+    outs = []
+    for i, (it, x, cb) in enumerate(zip(items, xs, cbs)):
+        om, oe = oracle.compress_adaptive(x, cb)[:2] if adaptive else oracle.compress(x, cb)
+        n_esc = zc.header_n_esc(it.main)
+        assert_stream_equal(host_u8(it.main), host_u8(it.esc)[:n_esc], om, oe)
+        outs.append(zc.BatchItem(bf16=torch.empty(x.size, dtype=torch.int16, device="cuda"), main=it.main,
+                                 esc=it.esc))
+    zc.decompress_batched(outs, st)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0, zc.status_string(zc.status_value(st))
+    for o, x in zip(outs, xs):
+        assert np.array_equal(host_u16(o.bf16), x)
+
+
 @pytest.mark.slow
 def test_config_moe_payload_chunks(zc):
     """16384 x 4096 Student-t payload: one histogram codebook, 8 Zipf-sized destination chunks batched."""
