@@ -28,6 +28,7 @@ constexpr int kLinkThreads = 256;
 __global__ void __launch_bounds__(kLinkThreads) link_escapes_kernel(const uint8_t* __restrict__ main,
                                                                     const uint8_t* __restrict__ src,
                                                                     uint8_t* __restrict__ dst, uint64_t cap) {
+  pdl_begin();
   uint64_t n_esc = __ldcg(reinterpret_cast<const unsigned long long*>(main + 24));
   if (n_esc > cap) n_esc = cap;
   const uint64_t tid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -130,9 +131,15 @@ cudaError_t launch_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, u
     uint64_t blocks = (raw_spill(m) + kLinkThreads * 16 - 1) / (kLinkThreads * 16);
     if (blocks > static_cast<uint64_t>(dev.sm_count)) blocks = dev.sm_count;
     if (blocks == 0) blocks = 1;
-    link_escapes_kernel<<<static_cast<unsigned>(blocks), kLinkThreads, 0, sl>>>(recv_main(s), send_esc(s),
-                                                                                 recv_esc(s), esc_cap);
-    ZC_TRY(cudaGetLastError());
+    {
+      const uint8_t* lm = recv_main(s);
+      const uint8_t* le = send_esc(s);
+      uint8_t* ld = recv_esc(s);
+      uint64_t lc = esc_cap;
+      void* args[] = {&lm, &le, &ld, &lc};
+      ZC_TRY(launch_kernel(reinterpret_cast<const void*>(link_escapes_kernel), dim3(static_cast<unsigned>(blocks)),
+                           dim3(kLinkThreads), 0, sl, args, false));
+    }
     ZC_TRY(cudaEventRecord(ev.link[s], sl));
     // decompress chunk k from receive slot s
     ZC_TRY(cudaStreamWaitEvent(sd, ev.link[s], 0));
