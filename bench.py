@@ -205,6 +205,24 @@ def oracle_step(x: np.ndarray):
     return ya, yb
 
 
+def host_info() -> dict:
+    """The host the CPU legs ran on: logical CPUs, machine type, CPU model (from /proc/cpuinfo when present)."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    key, val = (t.strip() for t in line.split(":", 1))
+                    fields.setdefault(key.lower(), val)
+    except OSError:
+        pass
+    model = fields.get("model name") or fields.get("cpu model") or ""
+    if not model and "cpu part" in fields:  # Arm: implementer and part numbers
+        model = f"implementer {fields.get('cpu implementer', '?')} part {fields['cpu part']}"
+    return {"nproc": os.cpu_count(), "machine": platform.machine(), "cpu": model or platform.processor()}
+
+
 def cpu_baseline(x: np.ndarray, sample_log2: int) -> dict:
     m = min(x.size, 1 << sample_log2)
     sample = x[:m]
@@ -219,7 +237,7 @@ def cpu_baseline(x: np.ndarray, sample_log2: int) -> dict:
     return {"value": round(4 * 2 * m * reps / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"first 2^{int(math.log2(m))} elements of the workload, {reps} full step(s) "
                       f"(sigma and histogram codebooks, 2 compress + 2 decompress), single-threaded C, "
-                      f"{dt:.1f} s"}
+                      f"{dt:.1f} s", "host": host_info()}
 
 
 def run_reference(args):
@@ -243,7 +261,8 @@ def run_reference(args):
         "config": {"workload": WORKLOAD, "sample": f"first 2^{args.ref_sample_log2} elements per step",
                    "parallelism": "rank 0 only (CPU oracle)"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"first 2^{args.ref_sample_log2} elements of the workload per step"},
+                         "sample": f"first 2^{args.ref_sample_log2} elements of the workload per step",
+                         "host": host_info()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
