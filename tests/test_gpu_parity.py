@@ -459,6 +459,53 @@ def test_largest_tensor(zc):
 
 
 @pytest.mark.slow
+def test_largest_all_escape(zc):
+    """n = 2^32 - 1 values, none of whose exponents is in the codebook: n_esc = n, the escape offsets run up
+    to the u32 limit.  Round trip on the device; 16 seeded tiles of the main and escape streams against the
+    oracle; then decode-reduce-re-encode of the stream with itself (P = 2, x + x = 2x exactly, again all
+    escapes), its result and re-encoded stream checked on the same tiles."""
+    n = (1 << 32) - 1
+    xt = workloads.gaussian_on_device(n, 1e-3, seed=33)
+    cb = FAR_CODEBOOK
+    st = zc.new_status()
+    ws = zc.workspace(n)
+    main, esc = zc.compress(xt, zc.codebook_to_device(cb), ws, st)
+    y = zc.decompress(main, esc, n, st)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0, zc.status_string(zc.status_value(st))
+    assert zc.header_n_esc(main) == n
+    assert torch.equal(y, xt)
+    del y
+    ntiles = -(-n // 4096)
+    R = -(-4 * ntiles // 128) * 128
+    rng = np.random.default_rng(33)
+    tiles = sorted({0, ntiles // 2, ntiles - 2, ntiles - 1, *rng.integers(0, ntiles, 12).tolist()})
+
+    def check_stream(m_t, e_t, x_of_tile, cbook):
+        table = m_t[128:128 + 4 * ntiles].view(torch.int32)
+        n_esc = zc.header_n_esc(m_t)
+        for t in tiles:
+            tm, te = oracle.compress(x_of_tile(t), cbook)
+            assert np.array_equal(host_u8(m_t[128 + R + 5632 * t:128 + R + 5632 * (t + 1)]), tm[256:256 + 5632]), t
+            a = int(table[t].item()) & 0xFFFFFFFF
+            b = int(table[t + 1].item()) & 0xFFFFFFFF if t + 1 < ntiles else n_esc
+            assert b - a == te.size and np.array_equal(host_u8(e_t[a:b]), te), f"escapes of tile {t}"
+
+    def x_tile(t):
+        return host_u16(xt[4096 * t:min(n, 4096 * (t + 1))])
+
+    check_stream(main, esc, x_tile, cb)
+    out, om, oe = zc.decompress_reduce([main, main], [esc, esc], n, st, out_cb=zc.codebook_to_device(cb), ws=ws)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0, zc.status_string(zc.status_value(st))
+    assert zc.header_n_esc(om) == n
+    for t in tiles:
+        want = oracle.reduce([x_tile(t), x_tile(t)])
+        assert np.array_equal(host_u16(out[4096 * t:min(n, 4096 * (t + 1))]), want), f"reduced tile {t}"
+    check_stream(om, oe, lambda t: oracle.reduce([x_tile(t), x_tile(t)]), cb)
+
+
+@pytest.mark.slow
 def test_huge_reduce_byte_offsets_beyond_2pow31(zc):
     """Decode-reduce-re-encode of P = 2 shards of 2^31 + 777 values (2.8 GiB main streams, a 4 GiB result):
     24 seeded tiles of the result and of the re-encoded stream against the oracle's reduction of the same
