@@ -24,7 +24,8 @@
 //     independent coalesced loads; each lane decodes its runs with a 32-bit
 //     funnel-shift window over two words and a 2048-entry table indexed by
 //     the next 11 bits, which gives the symbol and its code length in one
-//     shared load.
+//     shared load; two symbols are decoded per window refill (a code is at
+//     most 11 bits, so the second one still lies within the next two words).
 #include "zc_device.cuh"
 #include "zc_internal.h"
 
@@ -367,6 +368,23 @@ __global__ void __launch_bounds__(kQDecWarps * 32) zq_decode_kernel(const __grid
       w2 = wbuf[idx];
       return e;
     };
+    // Two symbols per refill: a code is at most 11 bits, so after the first
+    // symbol the second starts at most 42 bits into (w0, w1, w2) and ends
+    // inside w1; one advance (at most one word) follows the pair.
+    auto decode_two = [&](uint32_t& ea, uint32_t& eb) {
+      ea = S.lut[__funnelshift_l(w1, w0, pos) >> 21];
+      const uint32_t p2 = pos + ((ea >> 8) & 15u);
+      const bool hi = p2 >= 32;
+      eb = S.lut[__funnelshift_l(hi ? w2 : w1, hi ? w1 : w0, p2 & 31u) >> 21];
+      badcode |= ea | eb;
+      const uint32_t p3 = p2 + ((eb >> 8) & 15u);
+      const bool adv = p3 >= 32;
+      pos = p3 & 31u;
+      w0 = adv ? w1 : w0;
+      w1 = adv ? w2 : w1;
+      idx += adv ? 1u : 0u;
+      w2 = wbuf[idx];
+    };
 #pragma unroll 1
     for (uint32_t j = 0; j < 8; j++) {
       const uint64_t i0 = base + zq_run_offset(lane, j);
@@ -375,7 +393,9 @@ __global__ void __launch_bounds__(kQDecWarps * 32) zq_decode_kernel(const __grid
         uint32_t o[4];
 #pragma unroll
         for (uint32_t q = 0; q < 4; q++) {
-          const uint32_t e0 = decode_one(), e1 = decode_one(), e2 = decode_one(), e3 = decode_one();
+          uint32_t e0, e1, e2, e3;
+          decode_two(e0, e1);
+          decode_two(e2, e3);
           o[q] = __byte_perm(__byte_perm(e0, e1, 0x0040), __byte_perm(e2, e3, 0x0040), 0x5410);
         }
         *reinterpret_cast<uint4*>(p.out + i0) = make_uint4(o[0], o[1], o[2], o[3]);
