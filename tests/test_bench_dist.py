@@ -55,3 +55,23 @@ def test_reference_arm_line(capsys):
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    host = line["cpu_baseline"]["host"]
+    assert host["nproc"] >= 1 and host["machine"]
+
+
+def test_host_info_reads_cpuinfo_fields(tmp_path, monkeypatch):
+    """The CPU model comes from /proc/cpuinfo: "model name" on x86, implementer and part numbers on Arm."""
+    import builtins
+    import bench
+    real_open = builtins.open
+    arm = "processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\nCPU part\t: 0xd4f\n"
+
+    def fake_open(path, *a, **k):
+        if path == "/proc/cpuinfo":
+            p = tmp_path / "cpuinfo"
+            p.write_text(arm)
+            return real_open(p, *a, **k)
+        return real_open(path, *a, **k)
+
+    monkeypatch.setattr(builtins, "open", fake_open)
+    assert bench.host_info()["cpu"] == "implementer 0x41 part 0xd4f"
