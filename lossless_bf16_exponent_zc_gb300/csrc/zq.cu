@@ -14,12 +14,11 @@
 //     packed most-significant-bit first into a 64-bit accumulator and leave
 //     as 32-bit words into the lane's shared-memory buffer.  The warp packs
 //     its 32 lanes' words behind the 8 words of lane counts and stores the
-//     block with consecutive lanes on consecutive words.  Each CTA owns a
-//     contiguous range of blocks: it sizes them first (lengths only),
-//     publishes its total and adds the totals of the CTAs before it (one
-//     bounded wait per launch, the workspace's epoch protocol, cooperative
-//     launch), then codes them again from L2 and stores them at their
-//     offsets.
+//     block with consecutive lanes on consecutive words.  Every symbol is
+//     coded once: a CTA codes a group of 16 blocks per round (one per warp)
+//     and keeps them on chip while its scan warp finds the group's offset
+//     from the totals other CTAs publish (the escape scan's window sums and
+//     epoch protocol, cooperative launch); a block is stored one round later.
 //   * Decoder: the block's words are copied to shared memory with batches of
 //     independent coalesced loads; each lane decodes its runs with a 32-bit
 //     funnel-shift window over two words and a 2048-entry table indexed by
@@ -37,7 +36,8 @@ constexpr uint32_t kQMagic = 0x3142515Au;      // "ZQB1"
 constexpr uint32_t kQLaneWordsMax = 44;         // 128 symbols x 11 bits
 constexpr uint32_t kQBlockWordsMax = 8 + 32 * kQLaneWordsMax;  // 1416
 constexpr uint32_t kQLaneStride = 45;           // words per lane buffer (odd: no bank conflicts)
-constexpr int kQEncWarps = 8;
+constexpr int kQEncWarps = 16;                 // coding warps; a group is 16 blocks
+constexpr int kQEncThreads = (kQEncWarps + 1) * 32;  // + the scan warp
 constexpr int kQDecWarps = 8;
 
 __host__ __device__ __forceinline__ uint64_t zq_blocks(uint64_t n) { return (n + kQBlock - 1) / kQBlock; }
@@ -62,8 +62,10 @@ struct QEncParams {
 // Shared memory of the encoder, per CTA.
 struct QEncShared {
   uint32_t lut[256];
-  uint32_t lanebuf[kQEncWarps][32 * kQLaneStride];
-  uint32_t packed[kQEncWarps][kQBlockWordsMax];
+  uint32_t lanebuf[kQEncWarps][32 * kQLaneStride];  // a lane's words of the block being coded
+  uint32_t packed[kQEncWarps][kQBlockWordsMax];     // a warp's block, packed, until its offset is known
+  uint32_t words[2][kQEncWarps];                    // block sizes of a round (slot = round mod 2)
+  uint32_t offs[2][kQEncWarps];                     // block word offsets of a round
 };
 
 // Run j of lane `lane` in block b (zero past n); *valid = its symbols below n.
@@ -84,13 +86,20 @@ __device__ __forceinline__ void zq_lookup_run(const uint32_t* lut, uint4 v, uint
   for (uint32_t t = 0; t < 16; t++) e[t] = t < valid ? lut[(w4[t >> 2] >> (8 * (t & 3))) & 0xFFu] : 0u;
 }
 
-// Design of the launch: CTA c owns the contiguous blocks [c B, c B + B).
-// Pass 1 sizes them (code lengths only) and leaves each block's word count in
-// its offset-table entry; the CTA publishes its total at once and learns its
-// base offset from the totals of the CTAs before it (one bounded wait, not one
-// per round).  Pass 2 codes the blocks again -- their input is mostly still in
-// L2 -- and stores each at its offset.
-__global__ void __launch_bounds__(kQEncWarps * 32, 1) zq_encode_kernel(const __grid_constant__ QEncParams p) {
+// Design of the launch: one CTA of 16 coding warps and 1 scan warp per SM.
+// Round r of CTA c codes group G = c + r C (C CTAs): blocks 16 G .. 16 G + 15,
+// one per coding warp.  A warp codes its block once, into its lane buffers
+// (its runs' 32-bit words) and their word counts; the scan warp adds the
+// group's 16 block sizes, publishes the group's total at once and finds the
+// group's first word offset as the offset after its CTA's previous group plus
+// the totals of the C - 1 groups in between (published by the CTAs that own
+// them, which never wait for this one).  Stores lag one round: after the
+// round's barrier a warp stores the block it packed in the previous round (at
+// the offset the scan warp posted meanwhile) and packs this round's block, so
+// the scan's wait overlaps the next round's coding.  The wait is bounded
+// (ZC_ERR_TIMEOUT); the launch is cooperative, so every group's owner is
+// resident.
+__global__ void __launch_bounds__(kQEncThreads, 1) zq_encode_kernel(const __grid_constant__ QEncParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   pdl_begin();
   QEncShared& S = *reinterpret_cast<QEncShared*>(smem_raw);
@@ -100,7 +109,7 @@ __global__ void __launch_bounds__(kQEncWarps * 32, 1) zq_encode_kernel(const __g
   const uint64_t tbl = zq_table_bytes(nb);
   uint32_t* table = reinterpret_cast<uint32_t*>(p.out + kQHeader);
   uint8_t* payload = p.out + kQHeader + tbl;
-  // fixed header fields and the rank table (payload words come with the last block)
+  // fixed header fields and the rank table (payload words come with the last group)
   if (blockIdx.x == 0 && warp == 0) {
     uint32_t* h = reinterpret_cast<uint32_t*>(p.out);
     for (uint32_t i = lane; i < kQHeader / 4; i += 32) {
@@ -125,122 +134,116 @@ __global__ void __launch_bounds__(kQEncWarps * 32, 1) zq_encode_kernel(const __g
   }
   __syncthreads();
   const uint32_t epoch = launch_epoch(p.ws);
-  const uint64_t per = (nb + gridDim.x - 1) / gridDim.x;  // blocks per CTA
-  const uint64_t b0 = static_cast<uint64_t>(blockIdx.x) * per;
-  const uint64_t b1 = b0 + per < nb ? b0 + per : nb;
+  const uint64_t groups = (nb + kQEncWarps - 1) / kQEncWarps;
+  const uint32_t R = blockIdx.x < groups
+                         ? static_cast<uint32_t>((groups - blockIdx.x + gridDim.x - 1) / gridDim.x)
+                         : 0u;  // rounds of this CTA
+  auto group_of = [&](uint32_t r) { return static_cast<uint64_t>(blockIdx.x) + static_cast<uint64_t>(r) * gridDim.x; };
 
-  // A warp's runs in coding order: run k is run k % 8 of its (k / 8)-th block.
-  // Four runs are loaded ahead (64 bytes per lane in flight).
-  const uint64_t first_b = b0 + warp;
-  const uint32_t nruns = first_b < b1 ? static_cast<uint32_t>(8 * ((b1 - first_b + kQEncWarps - 1) / kQEncWarps)) : 0u;
-  auto block_of = [&](uint32_t k) { return first_b + static_cast<uint64_t>(k >> 3) * kQEncWarps; };
-  auto load_k = [&](uint32_t k, uint32_t* valid) -> uint4 {
-    if (k >= nruns) {
-      *valid = 0;
-      return make_uint4(0u, 0u, 0u, 0u);
-    }
-    return zq_load_run(p.in, p.n, block_of(k), lane, k & 7u, valid);
-  };
-
-  // ---- pass 1: words of each block of this CTA (into its offset-table entry)
-  uint32_t cta_words = 0;  // lane 0 of each warp: this warp's blocks
-  {
-    uint32_t v0, v1, v2, v3, bits = 0;
+  if (warp < kQEncWarps) {
+    // ---------------- coding warps: block 16 G + warp of each group G
+    auto block_of = [&](uint32_t k) { return group_of(k >> 3) * kQEncWarps + warp; };  // run k's block
+    const uint32_t nruns = 8 * R;
+    auto load_k = [&](uint32_t k, uint32_t* valid) -> uint4 {
+      if (k >= nruns) {
+        *valid = 0;
+        return make_uint4(0u, 0u, 0u, 0u);
+      }
+      return zq_load_run(p.in, p.n, block_of(k), lane, k & 7u, valid);  // no symbols past n
+    };
+    uint32_t* lb = &S.lanebuf[warp][lane * kQLaneStride];
+    uint32_t* packed = S.packed[warp];
+    // Four runs are loaded ahead (64 bytes per lane in flight), across rounds.
+    uint32_t v0, v1, v2, v3;
     uint4 q0 = load_k(0, &v0), q1 = load_k(1, &v1), q2 = load_k(2, &v2), q3 = load_k(3, &v3);
+    bool prev_has = false;  // the block packed in the previous round, waiting for its offset ...
+    uint32_t prev_T = 0;    // ... and its words
 #pragma unroll 1
-    for (uint32_t k = 0; k < nruns; k++) {
-      uint32_t e[16];
-      zq_lookup_run(S.lut, q0, v0, e);
-      q0 = q1, v0 = v1, q1 = q2, v1 = v2, q2 = q3, v2 = v3;
-      q3 = load_k(k + 4, &v3);
+    for (uint32_t r = 0; r <= R; r++) {
+      const bool has = r < R && block_of(8 * r) < nb;
+      uint32_t wc = 0, T = 0;
+      if (r < R) {
+        unsigned long long acc = 0;  // codes most significant bit first; nacc bits used
+        uint32_t nacc = 0;
+#pragma unroll 1
+        for (uint32_t j = 0; j < 8; j++) {
+          // the run's 16 lookups first, all in flight at once (the word stores
+          // below would otherwise keep each lookup behind the previous store)
+          uint32_t e[16];
+          zq_lookup_run(S.lut, q0, v0, e);
+          q0 = q1, v0 = v1, q1 = q2, v1 = v2, q2 = q3, v2 = v3;
+          q3 = load_k(8 * r + j + 4, &v3);
+          // two codes at a time (at most 22 bits): one insertion and at most
+          // one full word per pair
 #pragma unroll
-      for (uint32_t t = 0; t < 16; t++) bits += e[t] >> 16;
-      if ((k & 7u) == 7u) {
-        const uint32_t T = 8 + warp_sum((bits + 31) / 32);
-        bits = 0;
-        if (lane == 0) {
-          table[block_of(k)] = T;
-          cta_words += T;
+          for (uint32_t t = 0; t < 16; t += 2) {
+            const uint32_t l1 = e[t + 1] >> 16;  // 0 past n
+            const uint32_t len = (e[t] >> 16) + l1;
+            const uint32_t code = ((e[t] & 0xFFFFu) << l1) | (e[t + 1] & 0xFFFFu);
+            acc |= static_cast<unsigned long long>(code) << ((64 - nacc - len) & 63);
+            nacc += len;
+            if (nacc >= 32) {
+              lb[wc++] = static_cast<uint32_t>(acc >> 32);
+              acc <<= 32;
+              nacc -= 32;
+            }
+          }
+        }
+        if (nacc > 0) lb[wc++] = static_cast<uint32_t>(acc >> 32);
+        T = has ? 8 + warp_sum(wc) : 0u;
+        if (lane == 0) S.words[r & 1][warp] = T;
+      }
+      __syncthreads();  // round r's sizes are in; round r - 1's offsets are posted
+      if (prev_has) {
+        const uint64_t off = S.offs[(r - 1) & 1][warp];
+        if (off + prev_T <= p.out_words) {
+          uint32_t* dst = reinterpret_cast<uint32_t*>(payload) + off;
+          for (uint32_t i = lane; i < prev_T; i += 32) dst[i] = packed[i];
+        } else if (lane == 0) {
+          set_status(p.status, ZC_ERR_OUT_OF_ROOM);
         }
       }
-    }
-  }
-  __shared__ uint32_t warp_words[kQEncWarps];
-  if (lane == 0) warp_words[warp] = cta_words;
-  __syncthreads();
-  // ---- the CTA's base: publish its total, add the totals of the CTAs before it
-  if (warp == 0) {
-    const uint32_t t = lane < kQEncWarps ? warp_words[lane] : 0u;
-    const uint32_t total = warp_sum(t);
-    if (lane == 0) st_relaxed(&p.flags[blockIdx.x].agg, (static_cast<unsigned long long>(epoch) << 32) | total);
-    bool timed_out;
-    const uint64_t base = window_sum(p.flags, 0u, blockIdx.x, epoch, p.status, &timed_out);
-    // block offsets: a running sum over this CTA's blocks, in order
-    uint64_t run = base;
-    for (uint64_t c = b0; c < b1; c += 32) {
-      const uint32_t w = c + lane < b1 ? table[c + lane] : 0u;
-      const uint32_t inc = warp_inclusive_scan(w);
-      if (c + lane < b1) table[c + lane] = static_cast<uint32_t>(run + inc - w);
-      run += __shfl_sync(kFull, inc, 31);
-    }
-    if (b1 == nb && b0 < b1 && lane == 0) *reinterpret_cast<unsigned long long*>(p.out + 24) = run;
-    if (b1 == nb)  // the offset table's padding
-      for (uint64_t o = kQHeader + 4 * nb + 4 * lane; o < kQHeader + tbl; o += 128)
-        *reinterpret_cast<uint32_t*>(p.out + o) = 0u;
-    scan_exit(p.ws, p.flags, epoch, gridDim.x);
-  }
-  __syncthreads();
-
-  // ---- pass 2: code each block and store it at its offset
-  uint32_t* lb = &S.lanebuf[warp][lane * kQLaneStride];
-  uint32_t* packed = S.packed[warp];
-  uint32_t v0, v1, v2, v3, nacc = 0, wc = 0;
-  unsigned long long acc = 0;  // codes most significant bit first; nacc bits used
-  uint4 q0 = load_k(0, &v0), q1 = load_k(1, &v1), q2 = load_k(2, &v2), q3 = load_k(3, &v3);
-#pragma unroll 1
-  for (uint32_t k = 0; k < nruns; k++) {
-    // the run's 16 lookups first, all in flight at once (the word stores
-    // below would otherwise keep each lookup behind the previous store)
-    uint32_t e[16];
-    zq_lookup_run(S.lut, q0, v0, e);
-    q0 = q1, v0 = v1, q1 = q2, v1 = v2, q2 = q3, v2 = v3;
-    q3 = load_k(k + 4, &v3);
-    // two codes at a time (at most 22 bits): one insertion and at most one
-    // full word per pair
-#pragma unroll
-    for (uint32_t t = 0; t < 16; t += 2) {
-      const uint32_t l1 = e[t + 1] >> 16;  // 0 past n
-      const uint32_t len = (e[t] >> 16) + l1;
-      const uint32_t code = ((e[t] & 0xFFFFu) << l1) | (e[t + 1] & 0xFFFFu);
-      acc |= static_cast<unsigned long long>(code) << ((64 - nacc - len) & 63);
-      nacc += len;
-      if (nacc >= 32) {
-        lb[wc++] = static_cast<uint32_t>(acc >> 32);
-        acc <<= 32;
-        nacc -= 32;
+      __syncwarp();
+      if (has) {  // pack: lane counts, then the lanes' words in lane order
+        const uint32_t inc = warp_inclusive_scan(wc);
+        const uint32_t pre = inc - wc;
+        reinterpret_cast<uint8_t*>(packed)[lane] = static_cast<uint8_t>(wc);
+        for (uint32_t i = 0; i < wc; i++) packed[8 + pre + i] = lb[i];
       }
+      __syncwarp();
+      prev_has = has;
+      prev_T = T;
     }
-    if ((k & 7u) != 7u) continue;
-    const uint64_t b = block_of(k);
-    if (nacc > 0) lb[wc++] = static_cast<uint32_t>(acc >> 32);
-    // pack: lane counts, then the lanes' words in lane order
-    const uint32_t inc = warp_inclusive_scan(wc);
-    const uint32_t pre = inc - wc;
-    const uint32_t T = 8 + __shfl_sync(kFull, inc, 31);
-    reinterpret_cast<uint8_t*>(packed)[lane] = static_cast<uint8_t>(wc);
-    for (uint32_t i = 0; i < wc; i++) packed[8 + pre + i] = lb[i];
-    __syncwarp();
-    const uint64_t off = table[b];
-    if (off + T <= p.out_words) {
-      uint32_t* dst = reinterpret_cast<uint32_t*>(payload) + off;
-      for (uint32_t i = lane; i < T; i += 32) dst[i] = packed[i];
-    } else if (lane == 0) {
-      set_status(p.status, ZC_ERR_OUT_OF_ROOM);
+  } else {
+    // ---------------- scan warp: each group's first word offset
+    uint64_t prev_incl = 0;  // offset after this CTA's previous group
+#pragma unroll 1
+    for (uint32_t r = 0; r <= R; r++) {
+      __syncthreads();  // round r's sizes are in
+      if (r == R) break;
+      const uint64_t G = group_of(r);
+      const uint32_t w = lane < kQEncWarps ? S.words[r & 1][lane] : 0u;
+      const uint32_t inc = warp_inclusive_scan(w);
+      const uint32_t total = __shfl_sync(kFull, inc, 31);
+      if (lane == 0) st_relaxed(&p.flags[G].agg, (static_cast<unsigned long long>(epoch) << 32) | total);
+      bool timed_out;
+      const uint32_t lo = r > 0 ? static_cast<uint32_t>(group_of(r - 1)) + 1u : 0u;
+      const uint64_t prefix = (r > 0 ? prev_incl : 0) +
+                              window_sum(p.flags, lo, static_cast<uint32_t>(G), epoch, p.status, &timed_out);
+      if (lane < kQEncWarps) {
+        const uint64_t off = prefix + inc - w;
+        S.offs[r & 1][lane] = static_cast<uint32_t>(off);
+        if (G * kQEncWarps + lane < nb) table[G * kQEncWarps + lane] = static_cast<uint32_t>(off);
+      }
+      prev_incl = prefix + total;
+      if (G + 1 == groups) {  // the last group: payload words and the offset table's padding
+        if (lane == 0) *reinterpret_cast<unsigned long long*>(p.out + 24) = prev_incl;
+        for (uint64_t o = kQHeader + 4 * nb + 4 * lane; o < kQHeader + tbl; o += 128)
+          *reinterpret_cast<uint32_t*>(p.out + o) = 0u;
+      }
+      __syncwarp();
     }
-    __syncwarp();
-    acc = 0;
-    nacc = 0;
-    wc = 0;
+    scan_exit(p.ws, p.flags, epoch, static_cast<uint32_t>(groups));
   }
 }
 
@@ -447,16 +450,16 @@ cudaError_t launch_zq_encode(const uint8_t* in, uint64_t n, const uint8_t width[
   static KernelPrep prep;
   int per_sm = 0;
   const int smem = static_cast<int>(sizeof(QEncShared));
-  cudaError_t err = prepare_kernel(prep, reinterpret_cast<const void*>(zq_encode_kernel), kQEncWarps * 32, smem, dev,
-                                   &per_sm);
+  cudaError_t err =
+      prepare_kernel(prep, reinterpret_cast<const void*>(zq_encode_kernel), kQEncThreads, smem, dev, &per_sm);
   if (err != cudaSuccess) return err;
   const uint32_t groups = static_cast<uint32_t>((nb + kQEncWarps - 1) / kQEncWarps);
-  uint32_t ctas = groups;  // at least 8 blocks per CTA, at most all resident CTAs
+  uint32_t ctas = groups;  // one group per CTA and round, at most all resident CTAs
   const uint32_t cap = static_cast<uint32_t>(dev.sm_count) * static_cast<uint32_t>(per_sm);
   if (ctas > cap) ctas = cap;
   if (ctas == 0) ctas = 1;
   void* args[] = {&p};
-  return launch_kernel(reinterpret_cast<const void*>(zq_encode_kernel), dim3(ctas), dim3(kQEncWarps * 32), smem,
+  return launch_kernel(reinterpret_cast<const void*>(zq_encode_kernel), dim3(ctas), dim3(kQEncThreads), smem,
                        stream, args, true);
 }
 
