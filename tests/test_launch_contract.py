@@ -1,0 +1,69 @@
+"""Source checks of the launch contract every libzc kernel relies on (no GPU).
+
+Every kernel is launched as a programmatic dependent launch, so it may start
+while the kernel before it on the stream is still running; stream order for
+data holds only because each kernel executes griddepcontrol.wait (pdl_begin())
+before it touches global memory.  These checks keep that true for every
+kernel in csrc/: each __global__ function calls pdl_begin() among its first
+statements, and no kernel is launched with the triple-chevron syntax (which
+would bypass launch_kernel and its attributes).
+"""
+import os
+import re
+
+CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "lossless_bf16_exponent_zc_gb300",
+                    "csrc")
+
+
+def _sources():
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(CSRC, name)) as f:
+                yield name, f.read()
+
+
+def _kernels(text):
+    """(name, body) of each __global__ function definition."""
+    for m in re.finditer(r"__global__\s+void\s+(?:__launch_bounds__\([^)]*\)\s+)?(\w+)\s*\(", text):
+        brace = text.index("{", m.end())
+        depth, i = 0, brace
+        while True:
+            if text[i] == "{":
+                depth += 1
+            elif text[i] == "}":
+                depth -= 1
+                if depth == 0:
+                    break
+            i += 1
+        yield m.group(1), text[brace + 1:i]
+
+
+def test_every_kernel_waits_for_its_predecessor_first():
+    found = 0
+    for name, text in _sources():
+        for kernel, body in _kernels(text):
+            found += 1
+            statements = [s.strip() for s in body.split(";") if s.strip()]
+            head = statements[:8]  # shared-memory addresses may be computed first
+            assert any(s.endswith("pdl_begin()") for s in head), f"{name}: {kernel} does not begin with pdl_begin()"
+            before = body[:body.index("pdl_begin()")]
+            # nothing before the wait may touch global memory
+            assert not re.search(r"\bp\.|__ldg|ld_relaxed|st_relaxed|atomic|tma_|cp_async", before), \
+                f"{name}: {kernel} accesses memory before pdl_begin()"
+    assert found >= 8  # encode, decode, reduce, histogram, raw switch, pipeline link, QLC encode and decode
+
+
+def test_no_triple_chevron_launches():
+    for name, text in _sources():
+        code = re.sub(r"//.*", "", text)
+        assert "<<<" not in code, f"{name} launches a kernel without launch_kernel()"
+
+
+def test_launch_kernel_sets_programmatic_serialization():
+    with open(os.path.join(CSRC, "zc_api.cu")) as f:
+        api = f.read()
+    body = api[api.index("cudaError_t launch_kernel("):]
+    body = body[:body.index("\n}\n")]
+    assert "cudaLaunchAttributeProgrammaticStreamSerialization" in body
+    assert "programmaticStreamSerializationAllowed = 1" in body
+    assert "cudaLaunchKernelExC" in body
