@@ -136,6 +136,15 @@ def test_stream_errors(zc):
         assert zc.status_value(st) == code, (code, zc.status_string(zc.status_value(st)))
 
 
+@pytest.mark.parametrize("widths", [DEFAULT, DYNAMIC])
+def test_several_rounds_and_a_partial_last_group(zc, widths):
+    """4917 blocks (a ragged last one): 308 groups of 16 blocks over at most one CTA per SM, so CTAs code two or
+    three groups each and the last group holds 5 blocks; the whole stream against the oracle's."""
+    n = (16 * 152 * 2 + 16 * 3 + 5) * 4096 - 77
+    x = workloads.fp8_gradient(n, seed=4917)
+    check(zc, x, widths, oracle.qlc_table_for(x))
+
+
 @pytest.mark.slow
 def test_full_size_ffn1(zc):
     n = 1 << 26
