@@ -16,6 +16,10 @@ Ops (device tensors; bf16 data as bfloat16 / int16 / uint16):
       the local stage of a zipped reduce-scatter (no re-encode).
   zc::pipelined_transfer(x, cb, chunk_elems, ws, status) -> int16[n]
       the chunked compress / link / decompress pipeline on three streams.
+  zc::zq_compress(x, widths, sym, ws, status) -> uint8[zq_max_bytes(n)]
+      Quad Length Codes of 1-byte symbols (uint8 / float8 e4m3), the table
+      given as its 8 region widths and 256-entry rank -> symbol list.
+  zc::zq_decompress(stream, n, status) -> uint8[n]
 ``ws`` and ``status`` are mutated (the workspace protocol and the device
 status word), and declared so.
 """
@@ -72,3 +76,24 @@ def pipelined_transfer(x: torch.Tensor, cb: torch.Tensor, chunk_elems: int, ws: 
 @pipelined_transfer.register_fake
 def _(x, cb, chunk_elems, ws, status):
     return x.new_empty(x.numel(), dtype=torch.int16)
+
+
+@torch.library.custom_op("zc::zq_compress", mutates_args=("ws", "status"))
+def zq_compress(x: torch.Tensor, widths: list[int], sym: list[int], ws: torch.Tensor,
+                status: torch.Tensor) -> torch.Tensor:
+    return zc.zq_compress(x.contiguous(), zc.zq_table(widths, sym), ws, status)
+
+
+@zq_compress.register_fake
+def _(x, widths, sym, ws, status):
+    return x.new_empty(zc.zq_max_bytes(x.numel()), dtype=torch.uint8)
+
+
+@torch.library.custom_op("zc::zq_decompress", mutates_args=("status",))
+def zq_decompress(stream: torch.Tensor, n: int, status: torch.Tensor) -> torch.Tensor:
+    return zc.zq_decompress(stream, n, status)
+
+
+@zq_decompress.register_fake
+def _(stream, n, status):
+    return stream.new_empty(n, dtype=torch.uint8)

@@ -17,7 +17,7 @@ from lossless_bf16_exponent_zc_gb300 import zc
 
 
 def test_ops_registered():
-    for name in ("compress", "decompress", "decompress_reduce", "pipelined_transfer"):
+    for name in ("compress", "decompress", "decompress_reduce", "pipelined_transfer", "zq_compress", "zq_decompress"):
         assert hasattr(torch.ops.zc, name)
     schema = torch.ops.zc.compress.default._schema
     mutated = {a.name for a in schema.arguments if a.alias_info is not None and a.alias_info.is_write}
@@ -45,6 +45,46 @@ def test_fake_tracing(n):
         g = make_fx(roundtrip, tracing_mode="fake")(x, cb, ws, st)
     targets = [str(node.target) for node in g.graph.nodes if node.op == "call_function"]
     assert any("zc.compress" in t for t in targets) and any("zc.decompress" in t for t in targets)
+
+
+@pytest.mark.parametrize("n", [1, 4096, 100_003])
+def test_fake_tracing_qlc(n):
+    from torch.fx.experimental.proxy_tensor import make_fx
+    from torch._subclasses.fake_tensor import FakeTensorMode
+    widths = list(oracle.QLC_DEFAULT_WIDTHS)
+    sym = list(range(256))
+
+    def roundtrip(x, ws, st):
+        s = torch.ops.zc.zq_compress(x, widths, sym, ws, st)
+        return s, torch.ops.zc.zq_decompress(s, x.numel(), st)
+
+    with FakeTensorMode():
+        x = torch.empty(n, dtype=torch.uint8, device="cuda")
+        ws = torch.empty(zc.workspace_size(n), dtype=torch.uint8, device="cuda")
+        st = torch.empty(1, dtype=torch.int32, device="cuda")
+        s, y = roundtrip(x, ws, st)
+        assert s.shape == (zc.zq_max_bytes(n),) and s.dtype == torch.uint8
+        assert y.shape == (n,) and y.dtype == torch.uint8 and y.device.type == "cuda"
+        g = make_fx(roundtrip, tracing_mode="fake")(x, ws, st)
+    targets = [str(node.target) for node in g.graph.nodes if node.op == "call_function"]
+    assert any("zc.zq_compress" in t for t in targets) and any("zc.zq_decompress" in t for t in targets)
+
+
+@pytest.mark.gpu
+def test_qlc_ops_match_oracle(zc):
+    x = workloads.fp8_ffn1(3 * 4096 + 777, seed=21)
+    sym = oracle.qlc_table_for(x)
+    widths = list(oracle.QLC_DEFAULT_WIDTHS)
+    ws, st = zc.workspace(x.size), zc.new_status()
+    xt = torch.from_numpy(x).cuda().view(torch.float8_e4m3fn)  # float8 tensors are coded by their bytes
+    s = torch.ops.zc.zq_compress(xt, widths, [int(v) for v in sym], ws, st)
+    want = oracle.qlc_compress(x, widths, sym)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0
+    assert np.array_equal(s[:want.size].cpu().numpy(), want)
+    y = torch.ops.zc.zq_decompress(s, x.size, st)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0 and np.array_equal(y.cpu().numpy(), x)
 
 
 @pytest.mark.gpu
