@@ -274,7 +274,11 @@ zc_status zc_decompress_reduce(int P, const void* const* h_mains, const void* co
  *     8-byte cudaMemsetAsync on `stream`.  Calls that overlap on the GPU (two
  *     streams at once) race: order them on one stream.
  *   - No cudaMalloc, cudaFree or allocating library routine is called.
- * Arguments, alignment and device errors as in zc_compress.
+ * Arguments, alignment and device errors as in zc_compress, except that no
+ * reset is needed after a device error (a caller could not reset the internal
+ * array anyway): each call clears the two counters itself, and the kernel
+ * advances the launch epoch on every path, a timeout included, so flags left
+ * by an earlier call never match a later one.
  */
 zc_status zc_compress_noalloc(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_main, void* d_esc,
                               uint64_t esc_capacity, int32_t* d_status, void* stream);
