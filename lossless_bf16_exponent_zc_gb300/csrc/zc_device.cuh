@@ -566,6 +566,35 @@ __device__ __forceinline__ void build_spread_tables(uint32_t* spread /* 3 x 256 
   }
 }
 
+// One spread table S(v) (bit j of byte v at bit 4j) held in NC lane copies,
+// interleaved: word v * NC + c holds S(v), and lane l reads copy l % NC.  A
+// lookup by 32 lanes with data-dependent bytes then touches bank (v * NC +
+// l % NC) mod 32, so NC = 32 puts every lane in its own bank (no conflicts,
+// 32 KB) and NC = 16 leaves at most two lanes per bank.  The three planes
+// share the table: the selector is S(p0) + 2 S(p1) + 4 S(p2), the bits being
+// disjoint.
+template <int NC>
+__device__ __forceinline__ void build_spread_replicated(uint32_t* tab) {
+  for (uint32_t i = threadIdx.x; i < 256u * NC; i += blockDim.x) {
+    const uint32_t v = i / NC;
+    uint32_t s = 0;
+#pragma unroll
+    for (int j = 0; j < 8; j++) s |= ((v >> j) & 1u) << (4 * j);
+    tab[i] = s;
+  }
+}
+
+// Permute selector of group k of a lane's plane words (nibble j = the 3-bit
+// code of element 8 lane + 256 k + j); `lb` = the table's shared address plus
+// 4 (lane % NC).
+template <int NC>
+__device__ __forceinline__ uint32_t spread_sel(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t k, uint32_t lb) {
+  const uint32_t s0 = lds32(lb + __byte_perm(w0, 0u, 0x4440u + k) * (4u * NC));
+  const uint32_t s1 = lds32(lb + __byte_perm(w1, 0u, 0x4440u + k) * (4u * NC));
+  const uint32_t s2 = lds32(lb + __byte_perm(w2, 0u, 0x4440u + k) * (4u * NC));
+  return s0 + 2u * s1 + 4u * s2;
+}
+
 // An exponent rotated right by one bit: (e & 1) << 7 | e >> 1.  In this form
 // the exponent's low bit sits where a bf16's low byte wants it (bit 7) and its
 // other seven bits where the high byte wants them (bits 0..6), so a bf16 is
@@ -695,87 +724,6 @@ __device__ __forceinline__ uint32_t decode_block(uint32_t tile, uint32_t blk, ui
     out[k].w = bf16_pair<1>(sm.y, r1);
   }
   return c;
-}
-
-// Code-0 positions (escapes) of block `blk` of a staged tile, per lane
-// (bit 8k + j <-> block element 256k + 8*lane + j).
-__device__ __forceinline__ uint32_t block_zero_mask(uint32_t tile, uint32_t blk, uint32_t n_tile) {
-  const uint32_t lane = lane_id();
-  const uint32_t b = tile + blk * kBlockBytes;
-  uint32_t z = ~(lds32(b + 1024 + lane * 4) | lds32(b + 1152 + lane * 4) | lds32(b + 1280 + lane * 4));
-  if (n_tile < kTile) z &= lane_valid_mask(blk, n_tile, lane);
-  return z;
-}
-
-// Decodes block `blk` of a staged tile for this lane, like decode_block, when
-// the tile-local rank of the block's first escape (`first`) is already known:
-// out[k] receives 8 bf16 values of block elements 256k + 8*lane + 0..7.
-// Escapes are patched only in the lanes that have some (lane-private scratch).
-// Returns the block's number of escapes.
-__device__ __forceinline__ uint32_t decode_one_block(uint32_t tile, uint32_t blk, uint32_t n_tile, uint32_t spread,
-                                                     DecTable dt, const EscSource& es, uint32_t first,
-                                                     uint8_t* scratch, uint4 out[4]) {
-  const uint32_t lane = lane_id();
-  const uint32_t b = tile + blk * kBlockBytes;
-  const uint32_t w0 = lds32(b + 1024 + lane * 4);
-  const uint32_t w1 = lds32(b + 1152 + lane * 4);
-  const uint32_t w2 = lds32(b + 1280 + lane * 4);
-  uint32_t z = ~(w0 | w1 | w2);
-  if (n_tile < kTile) z &= lane_valid_mask(blk, n_tile, lane);
-  const uint32_t c = __popc(z);
-  const uint32_t inc = warp_inclusive_scan(c);
-  uint32_t rank = first + inc - c;
-  uint4 exa, exb;  // ex words 0..3 and 4..7 (16-byte vectors: stored and reloaded without moves)
-  {
-    uint32_t sel[4];
-#pragma unroll
-    for (uint32_t k = 0; k < 4; k++)
-      sel[k] = spread_at(w0, k, spread) | spread_at(w1, k, spread + 1024) | spread_at(w2, k, spread + 2048);
-    exa.x = __byte_perm(dt.t0, dt.t1, sel[0] & 0xFFFFu);
-    exa.y = __byte_perm(dt.t0, dt.t1, sel[0] >> 16);
-    exa.z = __byte_perm(dt.t0, dt.t1, sel[1] & 0xFFFFu);
-    exa.w = __byte_perm(dt.t0, dt.t1, sel[1] >> 16);
-    exb.x = __byte_perm(dt.t0, dt.t1, sel[2] & 0xFFFFu);
-    exb.y = __byte_perm(dt.t0, dt.t1, sel[2] >> 16);
-    exb.z = __byte_perm(dt.t0, dt.t1, sel[3] & 0xFFFFu);
-    exb.w = __byte_perm(dt.t0, dt.t1, sel[3] >> 16);
-  }
-  const uint32_t total = __shfl_sync(kFull, inc, 31);
-  if (z) {
-    uint4* sp = reinterpret_cast<uint4*>(scratch + lane * 32);
-    sp[0] = exa;
-    sp[1] = exb;
-    uint32_t m = z;
-    uint8_t* dst = scratch + lane * 32;
-    if (first + total <= es.staged) {  // (warp-uniform) every escape of the block is staged
-      const uint8_t* src = es.smem + rank;
-      do {
-        const uint32_t p = __ffs(m) - 1;
-        m &= m - 1;
-        dst[p] = static_cast<uint8_t>(rot_exp(*src++));
-      } while (m);
-    } else {
-      while (m) {
-        const uint32_t p = __ffs(m) - 1;
-        m &= m - 1;
-        dst[p] = static_cast<uint8_t>(rot_exp(esc_byte(es, rank)));
-        rank++;
-      }
-    }
-    exa = sp[0];
-    exb = sp[1];
-  }
-#pragma unroll
-  for (uint32_t k = 0; k < 4; k++) {
-    const uint2 sm = lds64(b + k * 256 + lane * 8);
-    const uint32_t r0 = k == 0 ? exa.x : k == 1 ? exa.z : k == 2 ? exb.x : exb.z;
-    const uint32_t r1 = k == 0 ? exa.y : k == 1 ? exa.w : k == 2 ? exb.y : exb.w;
-    out[k].x = bf16_pair<0>(sm.x, r0);
-    out[k].y = bf16_pair<1>(sm.x, r0);
-    out[k].z = bf16_pair<0>(sm.y, r1);
-    out[k].w = bf16_pair<1>(sm.y, r1);
-  }
-  return total;
 }
 
 // acc[i] += bf16 value i of the 8 packed in v: each add takes the bf16 operand

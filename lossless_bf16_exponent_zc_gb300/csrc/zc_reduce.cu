@@ -12,7 +12,13 @@
 //     the 5632-byte tile and one for the 16-byte-aligned span holding its
 //     escape bytes, both completing on the stage's full barrier; the team's
 //     4 warps release the stage on its empty barrier.  Offset-table entries
-//     are prefetched a round ahead.
+//     are prefetched a round ahead, and each round's copies are planned for
+//     all shards at once (one shard per lane), so issuing a copy is short.
+//   * The code planes become permute selectors through one spread table kept
+//     in 32 lane copies, so the data-dependent lookups never conflict.
+//   * A block's escape ranks: a warp scan inside the block, and the totals of
+//     the tile's earlier blocks exchanged by the team's four warps through
+//     shared memory at one named barrier per copy.
 //   * Each consumer decodes its block straight into its sums (one fp32 += bf16
 //     add per value, the decoded half-word as the addend), rounds, stores, and
 //     -- when re-encoding -- encodes its block of the result from shared memory.
@@ -42,20 +48,21 @@ constexpr uint32_t kRedStageBytes = kTileBytes + kRedEscCap;
 constexpr uint32_t kRedEbuf = 512;                // staged output escapes per block and round
 constexpr int kRedSlots = 2;                      // rounds in flight for the output offsets
 constexpr uint32_t kGroupTilesR = kRedTeams;      // tiles per escape-scan group
+constexpr int kSpreadCopies = 32;
 // Shared-memory layout after 1 KB alignment.
-constexpr uint32_t kRSpread = 0;      // decode spread tables, 3 x 1 KB
-constexpr uint32_t kRLut = 3072;      // encoder LUT of the output codebook, 1 KB aligned
-constexpr uint32_t kRShard = 4096;    // per-shard tables, 64 x 16 B
-constexpr uint32_t kRRound = 5120;    // round bookkeeping (<= 512 B)
-constexpr uint32_t kRFlag = 5632;     // validity flags, then the RAW shard mask (u64)
-constexpr uint32_t kRBars = 5648;     // full / empty barriers, 2 x 4 teams x 4 stages
+constexpr uint32_t kRSpread = 0;                              // spread table, 32 lane copies (32 KB)
+constexpr uint32_t kRLut = kRSpread + 1024 * kSpreadCopies;  // encoder LUT of the output codebook, 1 KB aligned
+constexpr uint32_t kRShard = kRLut + 1024;                    // per-shard tables, 64 x 16 B
+constexpr uint32_t kRRound = kRShard + 1024;                  // round bookkeeping (<= 512 B)
+constexpr uint32_t kRFlag = kRRound + 512;                    // validity flags, then the RAW shard mask (u64)
+constexpr uint32_t kRBars = kRFlag + 16;                      // full / empty barriers, 2 x 4 teams x 4 stages
 constexpr uint32_t kRMeta = kRBars + 2 * kRedTeams * kRedStages * 8;  // stage metadata
-constexpr uint32_t kRScratch = 6272;  // per-consumer exponent scratch, 1 KB each
+constexpr uint32_t kRTot = kRMeta + kRedTeams * kRedStages * 16;      // block escape totals, 2 x 4 per team
+constexpr uint32_t kRScratch = (kRTot + kRedTeams * 2 * 16 + 127) / 128 * 128;  // per-consumer exponent scratch, 1 KB each
 constexpr uint32_t kREbuf = kRScratch + kRedCons * 1024;
 constexpr uint32_t kRYtile = kREbuf + kRedCons * kRedSlots * kRedEbuf;  // per-team rounded tile, 8 KB
 constexpr uint32_t kRStage = kRYtile + kRedTeams * 8192;
 constexpr uint32_t kRedSmem = 1024 + kRStage + kRedTeams * kRedStages * kRedStageBytes;
-static_assert(kRMeta + kRedTeams * kRedStages * 16 <= kRScratch, "reduce layout");
 static_assert(kRedSmem + 1024 <= 232448, "shared memory budget");
 
 struct RedParams {
@@ -149,7 +156,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     if (!__syncthreads_or(any)) return;
   }
 
-  build_spread_tables(spread);
+  build_spread_replicated<kSpreadCopies>(spread);
   if (threadIdx.x == 0) {
     flags_s[0] = flags_s[1] = 0;
     *raw_s = 0ull;
@@ -217,95 +224,112 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
   if (skip) {
     // nothing to do; the exit protocol below still runs
   } else if (warp >= kRedProd && warp < kRedScan) {
-    // ---------------- producer q: stage the P copies of the tiles of teams 2q, 2q + 1
+    // ---------------- producer q: stage the P copies of the tiles of teams 2q, 2q + 1, in the
+    // order the consumers take them.  What a copy needs (its escape range and its checks, the
+    // span of escape bytes to stage) is worked out once per round for every shard at once, one
+    // shard per lane, so that lane 0 only waits for the stage, writes 16 bytes and starts the
+    // two bulk copies: the issue of a copy is short, and the copies follow each other closely.
     const uint32_t t0 = (warp - kRedProd) * kTeamsPerProducer;
+    const uint32_t P = static_cast<uint32_t>(p.P);
     uint32_t uses[kTeamsPerProducer] = {};
-    // offsets [a, b) of tile 4G + t0 + u for shard `lane` (h = 0) and `lane + 32` (h = 1)
-    uint32_t cur_a[kTeamsPerProducer][2], cur_b[kTeamsPerProducer][2];
-    uint32_t nxt_a[kTeamsPerProducer][2], nxt_b[kTeamsPerProducer][2];
-    auto load_round = [&](uint32_t G, uint32_t (&oa)[kTeamsPerProducer][2], uint32_t (&ob)[kTeamsPerProducer][2]) {
+    // offsets [a, b) of the tile of team t0 + u in the next round, for shard lane + 32 h
+    uint32_t na[kTeamsPerProducer][2], nb[kTeamsPerProducer][2];
+    // the round's plan per team and shard: pa = the tile's first escape;
+    // pk = count | staged << 13 | (span / 16) << 23 | consistent << 31
+    uint32_t pa[kTeamsPerProducer][2], pk[kTeamsPerProducer][2];
+    auto load_offsets = [&](uint32_t G) {
 #pragma unroll
       for (int u = 0; u < kTeamsPerProducer; u++)
 #pragma unroll
         for (int h = 0; h < 2; h++) {
-          oa[u][h] = ob[u][h] = 0;
+          na[u][h] = nb[u][h] = 0;
           const uint32_t g = G * kGroupTilesR + t0 + u;
-          const int r = static_cast<int>(lane) + 32 * h;
-          if (G < ngroups && g < p.ntiles && r < p.P) {
+          const uint32_t r = lane + 32u * h;
+          if (G < ngroups && g < p.ntiles && r < P) {
             const uint32_t* tbl = reinterpret_cast<const uint32_t*>(p.s[r].main + kHeader);
-            oa[u][h] = __ldg(tbl + g);
+            na[u][h] = __ldg(tbl + g);
             const uint64_t bb = (g + 1 < p.ntiles) ? static_cast<uint64_t>(__ldg(tbl + g + 1)) : si[r].n_esc;
-            ob[u][h] = bb > 0xFFFFFFFFull ? 0xFFFFFFFFu : static_cast<uint32_t>(bb);
+            nb[u][h] = bb > 0xFFFFFFFFull ? 0xFFFFFFFFu : static_cast<uint32_t>(bb);
           }
         }
     };
-    load_round(blockIdx.x, cur_a, cur_b);
-    for (uint32_t G = blockIdx.x; G < ngroups; G += step) {
-      load_round(G + step, nxt_a, nxt_b);  // consumed next round; the loads complete meanwhile
-      for (int r = 0; r < p.P; r++) {
-        const uint32_t src = static_cast<uint32_t>(r & 31);
-        uint32_t a[kTeamsPerProducer], b[kTeamsPerProducer];
+    auto plan_round = [&]() {
+#pragma unroll
+      for (int h = 0; h < 2; h++) {
+        const uint32_t r = lane + 32u * h;
+        const uint64_t n_esc = r < P ? si[r].n_esc : 0ull;
+        const uint64_t buf = r < P ? p.s[r].esc_bytes : 0ull;
 #pragma unroll
         for (int u = 0; u < kTeamsPerProducer; u++) {
-          a[u] = __shfl_sync(kFull, r < 32 ? cur_a[u][0] : cur_a[u][1], src);
-          b[u] = __shfl_sync(kFull, r < 32 ? cur_b[u][0] : cur_b[u][1], src);
+          const uint32_t a = na[u][h], b = nb[u][h];
+          // (absent tiles and shards have a = b = 0; a RAW shard's offset table is
+          // zero and it stages nothing, so it is not checked)
+          const bool raw_r = RAW && r < P && ((*raw_s >> r) & 1ull);
+          const bool ok = raw_r || (a <= b && b <= n_esc && b - a <= kTile);
+          if (!ok) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
+          const uint32_t aa = ok ? a : 0, cnt = ok ? b - a : 0;
+          // escape bytes: the 16-byte-aligned span [aa - head, ...) that holds
+          // them, at most kRedEscCap bytes and never past the end of the
+          // buffer; ranks beyond it are read from global memory by consumers
+          const uint32_t head = aa & 15u;
+          const uint64_t base = aa - head;
+          uint32_t span = cnt == 0 ? 0u : (head + cnt + 15u) & ~15u;
+          if (span > kRedEscCap) span = kRedEscCap;
+          if (base + span > buf) span = base >= buf ? 0u : static_cast<uint32_t>((buf - base) & ~15ull);
+          const uint32_t staged = span <= head ? 0u : (span - head < cnt ? span - head : cnt);
+          pa[u][h] = aa;
+          pk[u][h] = cnt | (staged << 13) | ((span >> 4) << 23) | (ok ? 0x80000000u : 0u);
+        }
+      }
+    };
+    load_offsets(blockIdx.x);
+    for (uint32_t G = blockIdx.x; G < ngroups; G += step) {
+      plan_round();              // from this round's offsets
+      load_offsets(G + step);    // the next round's, consumed once this round is issued
+      for (int r = 0; r < p.P; r++) {
+        const uint32_t src = static_cast<uint32_t>(r & 31);
+        uint32_t ca[kTeamsPerProducer], ck[kTeamsPerProducer];
+#pragma unroll
+        for (int u = 0; u < kTeamsPerProducer; u++) {
+          ca[u] = __shfl_sync(kFull, r < 32 ? pa[u][0] : pa[u][1], src);
+          ck[u] = __shfl_sync(kFull, r < 32 ? pk[u][0] : pk[u][1], src);
         }
         if (lane == 0) {
-          const uint64_t n_esc = si[r].n_esc;
-          const uint64_t buf = p.s[r].esc_bytes;
 #pragma unroll
           for (int u = 0; u < kTeamsPerProducer; u++) {
             const uint32_t t = t0 + u;
             const uint32_t g = G * kGroupTilesR + t;
             if (g >= p.ntiles) continue;
             const uint32_t bi = t * kRedStages + uses[u] % kRedStages;
-            if (uses[u] >= kRedStages)
+            if (uses[u] >= static_cast<uint32_t>(kRedStages))
               mbar_wait_bounded(&empty_bar[bi], (uses[u] / kRedStages - 1) & 1u, p.status);
+            uses[u]++;
+            StageMeta m;
+            m.shard = static_cast<uint16_t>(r);
             if (RAW && ((*raw_s >> r) & 1ull)) {  // RAW shard: the consumers read global memory
-              StageMeta m;
               m.a = m.cnt = m.staged = 0;
-              m.shard = static_cast<uint16_t>(r);
               m.ok = kMetaOk | kMetaRaw;
               meta[bi] = m;
               mbar_arrive(&full_bar[bi]);
-              uses[u]++;
               continue;
             }
-            const bool ok = a[u] <= b[u] && b[u] <= n_esc && b[u] - a[u] <= kTile;
-            if (!ok) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
-            const uint32_t aa = ok ? a[u] : 0, cnt = ok ? b[u] - a[u] : 0;
-            // escape bytes: the 16-byte-aligned span [aa - head, ...) that holds
-            // them, at most kRedEscCap bytes and never past the end of the
-            // buffer; ranks beyond it are read from global memory by consumers
-            const uint32_t head = aa & 15u;
-            const uint64_t base = aa - head;
-            uint32_t span = cnt == 0 ? 0u : (head + cnt + 15u) & ~15u;
-            if (span > kRedEscCap) span = kRedEscCap;
-            if (base + span > buf) span = base >= buf ? 0u : static_cast<uint32_t>((buf - base) & ~15ull);
-            uint8_t* stage = gbase + kRStage + bi * kRedStageBytes;
-            StageMeta m;
-            m.a = aa;
-            m.cnt = cnt;
-            m.staged = span <= head ? 0u : (span - head < cnt ? span - head : cnt);
-            m.shard = static_cast<uint16_t>(r);
-            m.ok = ok;
+            const uint32_t span = ((ck[u] >> 23) & 0x3Fu) << 4;
+            m.a = ca[u];
+            m.cnt = ck[u] & 0x1FFFu;
+            m.staged = (ck[u] >> 13) & 0x3FFu;
+            m.ok = static_cast<uint16_t>(ck[u] >> 31);
             meta[bi] = m;
-            fence_proxy_async();
+            uint8_t* stage = gbase + kRStage + bi * kRedStageBytes;
+            // (the stage is only ever written by these bulk copies; the
+            // consumers' reads of its previous contents completed before their
+            // release of it, which the wait above observed)
             mbar_arrive_expect_tx(&full_bar[bi], kTileBytes + span);
             tma_load_1d(stage, tile_ptr(p.s[r].main, p.ntiles, g), kTileBytes, &full_bar[bi]);
-            if (span != 0) tma_load_1d(stage + kTileBytes, p.s[r].esc + base, span, &full_bar[bi]);
-            uses[u]++;
+            if (span != 0) tma_load_1d(stage + kTileBytes, p.s[r].esc + (ca[u] & ~15u), span, &full_bar[bi]);
           }
         }
         __syncwarp();
       }
-#pragma unroll
-      for (int u = 0; u < kTeamsPerProducer; u++)
-#pragma unroll
-        for (int h = 0; h < 2; h++) {
-          cur_a[u][h] = nxt_a[u][h];
-          cur_b[u][h] = nxt_b[u][h];
-        }
     }
   } else if (warp == kRedScan) {
     // ---------------- scan warp (re-encoding): the escape offsets of each group of output tiles
@@ -340,6 +364,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     const uint32_t ytile_s = sbase + kRYtile + t * 8192;  // shared address of the team's rounded tile
     uint16_t* ytile = reinterpret_cast<uint16_t*>(gbase + kRYtile + t * 8192);
     const uint32_t lut_s = sbase + kRLut;
+    const uint32_t spread_lb = sbase + kRSpread + 4 * (lane % kSpreadCopies);
     uint32_t k_item = 0;
 
     // output offsets posted for round j: write the table entry, header parts, escapes
@@ -405,25 +430,82 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
             continue;
           }
           const uint32_t tile_s = sbase + kRStage + bi * kRedStageBytes;
-          // escapes of the tile's earlier blocks: one warp reduction over their masks
-          uint32_t first = 0;
-          if (b != 0) {
-            uint32_t c = __popc(block_zero_mask(tile_s, 0, n_tile));
-            if (b > 1) c += __popc(block_zero_mask(tile_s, 1, n_tile));
-            if (b > 2) c += __popc(block_zero_mask(tile_s, 2, n_tile));
-            first = __reduce_add_sync(kFull, c);
+          const uint32_t blk_s = tile_s + b * kBlockBytes;
+          const uint32_t w0 = lds32(blk_s + 1024 + lane * 4);
+          const uint32_t w1 = lds32(blk_s + 1152 + lane * 4);
+          const uint32_t w2 = lds32(blk_s + 1280 + lane * 4);
+          uint32_t z = ~(w0 | w1 | w2);
+          if (n_tile < kTile) z &= lane_valid_mask(b, n_tile, lane);
+          // the block's escape ranks: a scan inside the block, and the totals of
+          // the tile's earlier blocks from the team's other three warps
+          const uint32_t c = __popc(z);
+          const uint32_t inc = warp_inclusive_scan(c);
+          const uint32_t total = __shfl_sync(kFull, inc, 31);
+          const uint32_t tot_s = sbase + kRTot + (t * 2 + (k_item & 1u)) * 16;
+          if (lane == 0) asm volatile("st.shared.u32 [%0], %1;" ::"r"(tot_s + 4 * b), "r"(total) : "memory");
+          // code planes -> permute selectors -> rotated exponents, while the totals meet
+          uint4 exa, exb;
+          {
+            uint32_t sel[4];
+#pragma unroll
+            for (uint32_t k = 0; k < 4; k++) sel[k] = spread_sel<kSpreadCopies>(w0, w1, w2, k, spread_lb);
+            const uint32_t t0 = si[m.shard].t0, t1 = si[m.shard].t1;
+            exa.x = __byte_perm(t0, t1, sel[0]);
+            exa.y = __byte_perm(t0, t1, sel[0] >> 16);
+            exa.z = __byte_perm(t0, t1, sel[1]);
+            exa.w = __byte_perm(t0, t1, sel[1] >> 16);
+            exb.x = __byte_perm(t0, t1, sel[2]);
+            exb.y = __byte_perm(t0, t1, sel[2] >> 16);
+            exb.z = __byte_perm(t0, t1, sel[3]);
+            exb.w = __byte_perm(t0, t1, sel[3] >> 16);
           }
-          DecTable dt;
-          dt.t0 = si[m.shard].t0;
-          dt.t1 = si[m.shard].t1;
-          EscSource es;
-          es.smem = gbase + kRStage + bi * kRedStageBytes + kTileBytes + (m.a & 15u);
-          es.glob = p.s[m.shard].esc + m.a;
-          es.staged = m.staged;
-          es.count = m.cnt;
+          // the team's four warps: every block total of this copy is written
+          // (the two buffers alternate; a buffer is rewritten only after all
+          // four warps have passed the next copy's barrier, so after their reads)
+          asm volatile("bar.sync %0, 128;" ::"r"(1 + t) : "memory");
+          const uint4 tt = lds128(tot_s);
+          const uint32_t first = (b > 0 ? tt.x : 0u) + (b > 1 ? tt.y : 0u) + (b > 2 ? tt.z : 0u);
+          if (b == 3 && m.ok && first + total != m.cnt && lane == 0) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
+          if (z) {
+            // patch escapes through the lane's 32 scratch bytes (bit q of z <-> byte q)
+            EscSource es;
+            es.smem = gbase + kRStage + bi * kRedStageBytes + kTileBytes + (m.a & 15u);
+            es.glob = p.s[m.shard].esc + m.a;
+            es.staged = m.staged;
+            es.count = m.cnt;
+            uint32_t rank = first + inc - c;
+            uint4* sp = reinterpret_cast<uint4*>(scratch + lane * 32);
+            sp[0] = exa;
+            sp[1] = exb;
+            uint32_t mz = z;
+            uint8_t* dst = scratch + lane * 32;
+            if (first + total <= es.staged) {  // (warp-uniform) every escape of the block is staged
+              const uint8_t* src = es.smem + rank;
+              do {
+                const uint32_t q = __ffs(mz) - 1;
+                mz &= mz - 1;
+                dst[q] = static_cast<uint8_t>(rot_exp(*src++));
+              } while (mz);
+            } else {
+              while (mz) {
+                const uint32_t q = __ffs(mz) - 1;
+                mz &= mz - 1;
+                dst[q] = static_cast<uint8_t>(rot_exp(esc_byte(es, rank)));
+                rank++;
+              }
+            }
+            exa = sp[0];
+            exb = sp[1];
+          }
           uint4 v[4];
-          const uint32_t zb = decode_one_block(tile_s, b, n_tile, sbase + kRSpread, dt, es, first, scratch, v);
-          if (b == 3 && m.ok && first + zb != m.cnt && lane == 0) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
+#pragma unroll
+          for (uint32_t k = 0; k < 4; k++) {
+            const uint2 sm = lds64(blk_s + k * 256 + lane * 8);
+            const uint32_t r0 = k == 0 ? exa.x : k == 1 ? exa.z : k == 2 ? exb.x : exb.z;
+            const uint32_t r1 = k == 0 ? exa.y : k == 1 ? exa.w : k == 2 ? exb.y : exb.w;
+            v[k] = make_uint4(bf16_pair<0>(sm.x, r0), bf16_pair<1>(sm.x, r0), bf16_pair<0>(sm.y, r1),
+                              bf16_pair<1>(sm.y, r1));
+          }
 #pragma unroll
           for (int k = 0; k < 4; k++) accumulate8(acc[k], v[k]);
           __syncwarp();
