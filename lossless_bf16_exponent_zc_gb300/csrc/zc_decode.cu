@@ -10,8 +10,9 @@
 // 16-byte cp.async copies stage the tile's escape bytes (up to 512 of them;
 // any excess is read straight from global memory), all completing on one
 // mbarrier; two stages are in flight per warp.  Code -> exponent goes
-// through byte permutes on an 8-byte table held in registers, with a 3 x 256
-// spread table in shared memory turning the three plane bytes into a permute
+// through byte permutes on an 8-byte table held in registers, with a spread
+// table in shared memory (16 lane copies, so data-dependent lookups put at
+// most two lanes on a bank) turning the three plane bytes into a permute
 // selector.  Output is written with 16-byte vector stores.  A RAW stream
 // (the raw bypass: the values' own bytes) skips the staging: each warp
 // copies its tiles' 8192 bytes with 16-byte loads and stores.
@@ -24,8 +25,9 @@ constexpr int kDecWarps = 16;
 constexpr int kDecStages = 2;
 constexpr uint32_t kDecEscCap = 512;  // escape bytes staged per tile (multiple of 16)
 constexpr uint32_t kDecStageBytes = kTileBytes + kDecEscCap;
-// (after 1 KB alignment) spread tables 3 KB, per-warp scratch 1 KB, barriers, stages
-constexpr uint32_t kDecScratchOff = 3 * 1024;
+constexpr int kDecSpreadCopies = 16;  // lane copies of the spread table (at most two lanes per bank)
+// (after 1 KB alignment) spread table 16 KB, per-warp scratch 1 KB, barriers, stages
+constexpr uint32_t kDecScratchOff = 1024 * kDecSpreadCopies;
 constexpr uint32_t kDecBarOff = kDecScratchOff + kDecWarps * 1024;
 constexpr uint32_t kDecStageOff = kDecBarOff + kDecWarps * 16;
 constexpr uint32_t kDecSmem = 1024 + kDecStageOff + kDecWarps * kDecStages * kDecStageBytes;
@@ -130,6 +132,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;
   uint8_t* gbase = smem + (sbase - smem_u32(smem));
   uint32_t* spread = reinterpret_cast<uint32_t*>(gbase);
+  const uint32_t spread_lb = sbase + 4 * (lane % kDecSpreadCopies);
   uint8_t* scratch = gbase + kDecScratchOff + warp * 1024;
   uint64_t* bar = reinterpret_cast<uint64_t*>(gbase + kDecBarOff + warp * 16);
   uint8_t* wstage = gbase + kDecStageOff + warp * kDecStages * kDecStageBytes;
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   // every tensor's header, read once per CTA (a warp's tiles cross many tensors)
   __shared__ HdrInfo hdr_cache[MAXB];
   for (int i = threadIdx.x; i < p.count; i += blockDim.x) hdr_cache[i] = read_header(p.t[i], i, p.status);
-  build_spread_tables(spread);
+  build_spread_replicated<kDecSpreadCopies>(spread);
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < kDecStages; s++) mbar_init(&bar[s], 33);  // 1 TMA arrival + 32 cp.async arrivals
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
 #pragma unroll 1
         for (uint32_t blk = 0; blk < 4; blk++) {
           uint4 v[4];
-          decode_block(tile_s, blk, n_tile, sbase, st_dt[s], es, run, scratch, v);
+          decode_block<kDecSpreadCopies>(tile_s, blk, n_tile, spread_lb, st_dt[s], es, run, scratch, v);
 #pragma unroll
           for (uint32_t k = 0; k < 4; k++) store8_guarded(out, blk * kBlock + k * 256 + lane * 8, n_left, v[k]);
         }

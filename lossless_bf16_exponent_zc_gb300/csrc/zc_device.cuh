@@ -553,19 +553,6 @@ __device__ __forceinline__ uint64_t window_sum(const Flag* flags, uint32_t lo, u
 }
 
 // ---------------------------------------------------------------- decode side
-// Spread tables: spread[b][v] puts bit j of byte v at bit 4j + b, so
-// spread[0][p0] | spread[1][p1] | spread[2][p2] is a byte-permute selector
-// whose nibble j is the 3-bit code of element j.
-__device__ __forceinline__ void build_spread_tables(uint32_t* spread /* 3 x 256 */) {
-  for (uint32_t i = threadIdx.x; i < 768; i += blockDim.x) {
-    const uint32_t b = i >> 8, v = i & 255u;
-    uint32_t s = 0;
-#pragma unroll
-    for (int j = 0; j < 8; j++) s |= ((v >> j) & 1u) << (4 * j + b);
-    spread[i] = s;
-  }
-}
-
 // One spread table S(v) (bit j of byte v at bit 4j) held in NC lane copies,
 // interleaved: word v * NC + c holds S(v), and lane l reads copy l % NC.  A
 // lookup by 32 lanes with data-dependent bytes then touches bank (v * NC +
@@ -642,20 +629,15 @@ __device__ __forceinline__ uint32_t esc_byte(const EscSource& s, uint32_t rank) 
   return 0;
 }
 
-// Spread-table lookup for byte k of plane word w: table b lives at shared
-// address `spread` + 1024 b (1 KB aligned, so the offset can be OR-ed in).
-__device__ __forceinline__ uint32_t spread_at(uint32_t w, uint32_t k, uint32_t table) {
-  const uint32_t off = k == 0 ? (w << 2) : (w >> (8 * k - 2));
-  return lds32((off & 0x3FCu) | table);
-}
-
 // Decodes block `blk` of a ZC1 tile held in shared memory (shared address
 // `tile`: 5632 B) for this lane: out[k] (k = 0..3) receives 4 words = 8 bf16
-// values of block elements 256k + 8*lane + 0..7.  `scratch` is this warp's
-// 1 KB exponent scratch.  `run` is the tile-local rank of the block's first
-// escape and is advanced past the block.  Returns the number of code-0
-// positions (escapes).
-__device__ __forceinline__ uint32_t decode_block(uint32_t tile, uint32_t blk, uint32_t n_tile, uint32_t spread,
+// values of block elements 256k + 8*lane + 0..7.  `spread_lb` is the lane's
+// base address in a spread table of NC lane copies (build_spread_replicated);
+// `scratch` is this warp's 1 KB exponent scratch.  `run` is the tile-local
+// rank of the block's first escape and is advanced past the block.  Returns
+// the number of code-0 positions (escapes).
+template <int NC>
+__device__ __forceinline__ uint32_t decode_block(uint32_t tile, uint32_t blk, uint32_t n_tile, uint32_t spread_lb,
                                                  DecTable dt, const EscSource& es, uint32_t& run, uint8_t* scratch,
                                                  uint4 out[4]) {
   const uint32_t lane = lane_id();
@@ -677,15 +659,14 @@ __device__ __forceinline__ uint32_t decode_block(uint32_t tile, uint32_t blk, ui
   {
     uint32_t sel[4];
 #pragma unroll
-    for (uint32_t k = 0; k < 4; k++)
-      sel[k] = spread_at(w0, k, spread) | spread_at(w1, k, spread + 1024) | spread_at(w2, k, spread + 2048);
-    exa.x = __byte_perm(dt.t0, dt.t1, sel[0] & 0xFFFFu);
+    for (uint32_t k = 0; k < 4; k++) sel[k] = spread_sel<NC>(w0, w1, w2, k, spread_lb);
+    exa.x = __byte_perm(dt.t0, dt.t1, sel[0]);
     exa.y = __byte_perm(dt.t0, dt.t1, sel[0] >> 16);
-    exa.z = __byte_perm(dt.t0, dt.t1, sel[1] & 0xFFFFu);
+    exa.z = __byte_perm(dt.t0, dt.t1, sel[1]);
     exa.w = __byte_perm(dt.t0, dt.t1, sel[1] >> 16);
-    exb.x = __byte_perm(dt.t0, dt.t1, sel[2] & 0xFFFFu);
+    exb.x = __byte_perm(dt.t0, dt.t1, sel[2]);
     exb.y = __byte_perm(dt.t0, dt.t1, sel[2] >> 16);
-    exb.z = __byte_perm(dt.t0, dt.t1, sel[3] & 0xFFFFu);
+    exb.z = __byte_perm(dt.t0, dt.t1, sel[3]);
     exb.w = __byte_perm(dt.t0, dt.t1, sel[3] >> 16);
   }
   if (z) {
