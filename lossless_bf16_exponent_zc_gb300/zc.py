@@ -60,8 +60,13 @@ class ZcTensor(ctypes.Structure):
 _lib = None
 
 
+def _sanitized() -> bool:
+    """ZC_SANITIZE=1 selects the ASan/UBSan build of the host code (CPU-side checks only)."""
+    return os.environ.get("ZC_SANITIZE") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.SAN_LIB if _sanitized() else _build.LIB
 
 
 def load() -> ctypes.CDLL:
@@ -69,7 +74,7 @@ def load() -> ctypes.CDLL:
     global _lib
     if _lib is not None:
         return _lib
-    path = _build.build()
+    path = _build.build(sanitize=_sanitized())
     if not os.path.exists(path):
         raise RuntimeError(f"libzc not found at {path}")
     lib = ctypes.CDLL(path)

@@ -26,6 +26,14 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "zc_oracle.c")
 _QSRC = os.path.join(_HERE, "qlc_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
+# ZC_SANITIZE=1: the same C built with AddressSanitizer and UndefinedBehaviorSanitizer
+# (a process that loads it must load the ASan runtime first, LD_PRELOAD)
+_SAN_LIB = os.path.join(_HERE, "liboracle_san.so")
+_SAN_FLAGS = ["-fsanitize=address,undefined", "-fno-sanitize-recover=undefined", "-fno-omit-frame-pointer", "-g"]
+
+
+def _sanitized() -> bool:
+    return os.environ.get("ZC_SANITIZE") == "1"
 _lock = threading.Lock()
 _lib = None
 
@@ -43,26 +51,31 @@ class OracleError(RuntimeError):
         self.code = code
 
 
-def build(force: bool = False) -> str:
-    """Compile zc_oracle.c into liboracle.so (plain C11, no fast-math, no FMA contraction)."""
+def build(force: bool = False, sanitize: bool | None = None) -> str:
+    """Compile zc_oracle.c into liboracle.so (plain C11, no fast-math, no FMA contraction).
+
+    sanitize (default: ZC_SANITIZE=1 in the environment) builds liboracle_san.so
+    instead, the same sources under AddressSanitizer and UndefinedBehaviorSanitizer."""
+    san = _sanitized() if sanitize is None else sanitize
+    lib = _SAN_LIB if san else _LIB
     with _lock:
         newest = max(os.path.getmtime(_SRC), os.path.getmtime(_QSRC))
-        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
-            tmp = _LIB + f".tmp{os.getpid()}"
+        if force or not os.path.exists(lib) or os.path.getmtime(lib) < newest:
+            tmp = lib + f".tmp{os.getpid()}"
             subprocess.check_call([
-                "gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
-                "-fno-fast-math", "-Wall", "-Wextra", "-o", tmp, _SRC, _QSRC, "-lm",
+                "gcc", "-std=c11", "-O1" if san else "-O2", "-fPIC", "-shared", "-ffp-contract=off",
+                "-fno-fast-math", "-Wall", "-Wextra"] + (_SAN_FLAGS if san else []) + [
+                "-o", tmp, _SRC, _QSRC, "-lm",
             ])
-            os.replace(tmp, _LIB)
-    return _LIB
+            os.replace(tmp, lib)
+    return lib
 
 
 def _load():
     global _lib
     if _lib is not None:
         return _lib
-    build()
-    lib = ctypes.CDLL(_LIB)
+    lib = ctypes.CDLL(build())
     u8p = ctypes.POINTER(ctypes.c_uint8)
     u16p = ctypes.POINTER(ctypes.c_uint16)
     u64p = ctypes.POINTER(ctypes.c_uint64)
