@@ -421,12 +421,31 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "workloads": per_workload,
             "cost_model": cost_model_context(zc, ops_report, per_workload, n, 2 * n / (mb + n_esc_b)),
+            # last, so that a reader of the line's tail sees every workload: fraction of measured HBM per op
+            "summary_frac_of_hbm": workload_summary(ops_report, per_workload),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def workload_summary(ops_report, per_workload):
+    """{workload: {op: fraction of the measured HBM peak}} for the step's ops and every workload section."""
+    out = {"gradient_2^26_step": {o: v["frac_of_hbm"] for o, v in ops_report.items()}}
+    for name, sec in (per_workload or {}).items():
+        if isinstance(sec, dict) and "frac_of_hbm" in sec:
+            out[name] = sec["frac_of_hbm"]
+        elif isinstance(sec, dict):
+            ops = {op: v["frac_of_hbm"] for op, v in sec.items() if isinstance(v, dict) and "frac_of_hbm" in v}
+            for sub, v in sec.items():  # one level further (raw bypass, QLC)
+                if isinstance(v, dict) and not ("frac_of_hbm" in v):
+                    ops.update({f"{sub}.{op}": w["frac_of_hbm"] for op, w in v.items()
+                                if isinstance(w, dict) and "frac_of_hbm" in w})
+            if ops:
+                out[name] = ops
+    return out
 
 
 def cost_model_context(zc, ops_report, per_workload, n, ratio):
@@ -531,6 +550,35 @@ def _time_ms(torch, fn, reps, warmup=2):
     return s.elapsed_time(e) / reps
 
 
+def _time_graph_ms(torch, fn, calls=20, replays=10):
+    """Per-call device time of fn with the host out of the way: `calls` calls captured in one CUDA graph,
+    replayed `replays` times.  Small calls timed back to back on a stream measure how fast the host submits
+    them; this measures the GPU.  None if the calls cannot be captured."""
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(calls):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(replays):
+            g.replay()
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / (calls * replays)
+    except Exception:  # capture unsupported here: report the stream timing only
+        return None
+
+
 def run_workloads(args, zc, torch, device, peak):
     """Per-kernel GB/s (uncompressed and algorithmic), HBM fraction, ratio and escape rate for the other
     workloads: the 2^20 Gaussian (L2-resident), the 9-tensor Llama-3-8B bucket (batched), the MoE payload
@@ -558,11 +606,16 @@ def run_workloads(args, zc, torch, device, peak):
     m_t = torch.empty(mb, dtype=torch.uint8, device=device)
     e_t = torch.empty(eb, dtype=torch.uint8, device=device)
     y = torch.empty(n, dtype=torch.int16, device=device)
-    tc = _time_ms(torch, lambda: zc.compress(xt, cb, ws, st, main=m_t, esc=e_t), 50)
+    fc = lambda: zc.compress(xt, cb, ws, st, main=m_t, esc=e_t)
+    tc = _time_ms(torch, fc, 50)
     k = zc.header_n_esc(m_t)
-    td = _time_ms(torch, lambda: zc.decompress(m_t, e_t, n, st, out=y), 50)
+    fd = lambda: zc.decompress(m_t, e_t, n, st, out=y)
+    td = _time_ms(torch, fd, 50)
+    gc, gd = _time_graph_ms(torch, fc), _time_graph_ms(torch, fd)
     out["gaussian_2^20_L2_resident"] = {"compress": entry(tc, 2 * n, 2 * n + mb + k),
                                         "decompress": entry(td, 2 * n, 2 * n + mb + k),
+                                        "graph_replay_us": {"compress": round(1e3 * gc, 2) if gc else None,
+                                                            "decompress": round(1e3 * gd, 2) if gd else None},
                                         "ratio": round(2 * n / (mb + k), 4), "escape_rate": round(k / n, 5)}
 
     # 2. Llama-3-8B layer bucket, one batched launch each way
@@ -638,15 +691,19 @@ def run_workloads(args, zc, torch, device, peak):
         y_ = torch.empty(m, dtype=torch.int16, device=device)
         om_ = torch.empty(mb_, dtype=torch.uint8, device=device)
         oe_ = torch.empty(eb_, dtype=torch.uint8, device=device)
-        reps = max(3, min(50, int(2e9 // (P * m * 2))))
-        t_ = _time_ms(torch, lambda: zc.decompress_reduce(mains_, escs_, m, st, out=y_, out_cb=cb_out, out_main=om_,
-                                                          out_esc=oe_, ws=ws_), reps)
+        reps = max(20, min(50, int(2e9 // (P * m * 2))))
+        fr = lambda: zc.decompress_reduce(mains_, escs_, m, st, out=y_, out_cb=cb_out, out_main=om_, out_esc=oe_,
+                                          ws=ws_)
+        t_ = _time_ms(torch, fr, reps)
+        g_ = _time_graph_ms(torch, fr) if m <= (1 << 22) else None
         in_bytes = sum(mb_ + zc.header_n_esc(a_) for a_ in mains_)
         k_out = zc.header_n_esc(om_)
         alg = in_bytes + 2 * m + mb_ + k_out
         r = entry(t_, 2 * P * m, alg)
         r.update({"shard_elements": m, "escape_rate_in": round((in_bytes - P * mb_) / (P * m), 5),
                   "escape_rate_out": round(k_out / m, 5)})
+        if g_ is not None:
+            r["graph_replay_us"] = round(1e3 * g_, 2)
         return r
 
     out["reduce_scatter_8x2^25"] = reduce_case(1 << 25)
@@ -695,7 +752,8 @@ def run_workloads(args, zc, torch, device, peak):
         torch.cuda.empty_cache()
     out["reduce_scatter_sweep_P8"] = [{"shard_bytes": r["shard_elements"] * 2, "ms": r["ms"],
                                        "GB_per_s_uncompressed": r["GB_per_s_uncompressed"],
-                                       "frac_of_hbm": r["frac_of_hbm"]} for r in sweep]
+                                       "frac_of_hbm": r["frac_of_hbm"],
+                                       "graph_replay_us": r.get("graph_replay_us")} for r in sweep]
     del base
 
     # 5. raw bypass [CCCL §3.3, §5.2]: adaptive compression of a 2^26 N(0, 1e-3) tensor (stays coded: the cost

@@ -9,6 +9,7 @@ if libzc cannot be loaded, every call raises.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 from dataclasses import dataclass
 from typing import Sequence
@@ -143,8 +144,20 @@ def _ptr(t: torch.Tensor | None) -> int | None:
     return t.data_ptr()
 
 
-def _stream(stream: torch.cuda.Stream | None = None) -> int:
-    return (stream or torch.cuda.current_stream()).cuda_stream
+def _current_raw_stream(device_index: int) -> int:
+    """The current stream's cudaStream_t on a device (torch's raw query: no Stream object is built)."""
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(device_index)
+    return torch.cuda.current_stream(device_index).cuda_stream
+
+
+def _stream(stream: torch.cuda.Stream | None = None, like: torch.Tensor | None = None) -> int:
+    """The cudaStream_t to launch on: the given stream, else the current stream of `like`'s device."""
+    if stream is not None:
+        return stream.cuda_stream
+    index = like.device.index if like is not None and like.device.index is not None else torch.cuda.current_device()
+    return _current_raw_stream(index)
 
 
 def _nelem16(x: torch.Tensor) -> int:
@@ -160,6 +173,7 @@ def codebook_from_sigma(sigma: float) -> np.ndarray:
     return np.frombuffer(bytes(cb), np.uint8).copy()
 
 
+@functools.lru_cache(maxsize=4096)
 def compressed_size(n: int) -> tuple[int, int]:
     m, e = ctypes.c_uint64(), ctypes.c_uint64()
     _check(load().zc_compressed_size(int(n), ctypes.byref(m), ctypes.byref(e)), "zc_compressed_size")
@@ -202,7 +216,7 @@ def histogram_topk(x: torch.Tensor, ws: torch.Tensor, status: torch.Tensor, cb_o
     if cb_out is None:
         cb_out = torch.empty(7, dtype=torch.uint8, device=x.device)
     rc = load().zc_histogram_topk(_ptr(x), n, _ptr(cb_out), _ptr(hist_out), _ptr(ws), ws.numel(), _ptr(status),
-                                  _stream(stream))
+                                  _stream(stream, status))
     _check(rc, "zc_histogram_topk")
     return cb_out, hist_out
 
@@ -217,7 +231,7 @@ def compress(x: torch.Tensor, cb: torch.Tensor, ws: torch.Tensor, status: torch.
     if esc is None:
         esc = torch.empty(max(eb, 16), dtype=torch.uint8, device=x.device)
     rc = load().zc_compress(_ptr(x), n, _ptr(cb), _ptr(main), _ptr(esc), esc.numel(), _ptr(ws), ws.numel(),
-                            _ptr(status), _stream(stream))
+                            _ptr(status), _stream(stream, status))
     _check(rc, "zc_compress")
     return main, esc
 
@@ -235,7 +249,7 @@ def compress_adaptive(x: torch.Tensor, cb: torch.Tensor, ws: torch.Tensor, statu
     if esc is None:
         esc = torch.empty(max(raw_spill(n), 16), dtype=torch.uint8, device=x.device)
     rc = load().zc_compress_adaptive(_ptr(x), n, _ptr(cb), _ptr(main), _ptr(esc), esc.numel(), _ptr(ws),
-                                     ws.numel(), _ptr(status), _stream(stream))
+                                     ws.numel(), _ptr(status), _stream(stream, status))
     _check(rc, "zc_compress_adaptive")
     return main, esc
 
@@ -246,7 +260,7 @@ def decompress(main: torch.Tensor, esc: torch.Tensor, n: int, status: torch.Tens
         out = torch.empty(n, dtype=torch.int16, device=main.device)
     eb = esc.numel() if esc_bytes is None else int(esc_bytes)
     rc = load().zc_decompress(_ptr(main), _ptr(esc) if esc is not None else None, eb, int(n), _ptr(out),
-                              _ptr(status), _stream(stream))
+                              _ptr(status), _stream(stream, status))
     _check(rc, "zc_decompress")
     return out
 
@@ -272,7 +286,7 @@ def decompress_reduce(mains: Sequence[torch.Tensor], escs: Sequence[torch.Tensor
     eb_arr = (ctypes.c_uint64 * P)(*sizes)
     rc = load().zc_decompress_reduce(P, mp, ep, eb_arr, int(n), _ptr(out), _ptr(out_cb), _ptr(out_main),
                                      _ptr(out_esc), out_esc.numel() if out_esc is not None else 0,
-                                     _ptr(ws), ws.numel() if ws is not None else 0, _ptr(status), _stream(stream))
+                                     _ptr(ws), ws.numel() if ws is not None else 0, _ptr(status), _stream(stream, status))
     _check(rc, "zc_decompress_reduce")
     return out, out_main, out_esc
 
@@ -300,7 +314,7 @@ def _descs(items: Sequence[BatchItem]):
 
 def compress_batched(items: Sequence[BatchItem], ws: torch.Tensor, status: torch.Tensor, stream=None) -> None:
     arr = _descs(items)
-    _check(load().zc_compress_batched(len(items), arr, _ptr(ws), ws.numel(), _ptr(status), _stream(stream)),
+    _check(load().zc_compress_batched(len(items), arr, _ptr(ws), ws.numel(), _ptr(status), _stream(stream, status)),
            "zc_compress_batched")
 
 
@@ -308,12 +322,12 @@ def compress_batched_adaptive(items: Sequence[BatchItem], ws: torch.Tensor, stat
                               stream=None) -> None:
     arr = _descs(items)
     _check(load().zc_compress_batched_adaptive(len(items), arr, _ptr(ws), ws.numel(), _ptr(status),
-                                               _stream(stream)), "zc_compress_batched_adaptive")
+                                               _stream(stream, status)), "zc_compress_batched_adaptive")
 
 
 def decompress_batched(items: Sequence[BatchItem], status: torch.Tensor, stream=None) -> None:
     arr = _descs(items)
-    _check(load().zc_decompress_batched(len(items), arr, _ptr(status), _stream(stream)), "zc_decompress_batched")
+    _check(load().zc_decompress_batched(len(items), arr, _ptr(status), _stream(stream, status)), "zc_decompress_batched")
 
 
 def transfer_pays(nbytes: int, bandwidth_gbps: float, latency_us: float, compress_gbps: float,
@@ -409,7 +423,7 @@ def zq_compress(x: torch.Tensor, table: ZqTable, ws: torch.Tensor, status: torch
     if out is None:
         out = torch.empty(zq_max_bytes(n), dtype=torch.uint8, device=x.device)
     rc = load().zq_compress(_ptr(x), n, ctypes.byref(table), _ptr(out), out.numel(), _ptr(ws), ws.numel(),
-                            _ptr(status), _stream(stream))
+                            _ptr(status), _stream(stream, status))
     _check(rc, "zq_compress")
     return out
 
@@ -427,7 +441,7 @@ def zq_decompress(stream_buf: torch.Tensor, n: int, status: torch.Tensor, out: t
     if out is None:
         out = torch.empty(n, dtype=torch.uint8, device=stream_buf.device)
     nb = stream_buf.numel() if in_bytes is None else int(in_bytes)
-    rc = load().zq_decompress(_ptr(stream_buf), nb, int(n), _ptr(out), _ptr(status), _stream(stream))
+    rc = load().zq_decompress(_ptr(stream_buf), nb, int(n), _ptr(out), _ptr(status), _stream(stream, status))
     _check(rc, "zq_decompress")
     return out
 
