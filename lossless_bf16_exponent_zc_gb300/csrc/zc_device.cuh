@@ -671,28 +671,30 @@ __device__ __forceinline__ uint32_t decode_block(uint32_t tile, uint32_t blk, ui
   }
   if (z) {
     // patch escapes through shared memory (bit p of z <-> byte p of ex)
-    uint4* sp = reinterpret_cast<uint4*>(scratch + lane * 32);
+    // bytes 0..15 of the lane at scratch[16 lane], bytes 16..31 at scratch[512 + 16 lane]:
+    // each 16-byte access of the warp then touches every bank once per quarter
+    uint4* sp = reinterpret_cast<uint4*>(scratch + lane * 16);
     sp[0] = exa;
-    sp[1] = exb;
+    sp[32] = exb;
     uint32_t m = z;
-    uint8_t* dst = scratch + lane * 32;
+    uint8_t* dst = scratch + lane * 16;  // byte q at dst[(q & 15) + 32 (q & 16)]
     if (run_end <= es.staged) {  // (warp-uniform) every escape of the block is staged
       const uint8_t* src = es.smem + rank;
       do {
         const uint32_t p = __ffs(m) - 1;
         m &= m - 1;
-        dst[p] = static_cast<uint8_t>(rot_exp(*src++));
+        dst[(p & 15u) + 32u * (p & 16u)] = static_cast<uint8_t>(rot_exp(*src++));
       } while (m);
     } else {
       while (m) {
         const uint32_t p = __ffs(m) - 1;
         m &= m - 1;
-        dst[p] = static_cast<uint8_t>(rot_exp(esc_byte(es, rank)));
+        dst[(p & 15u) + 32u * (p & 16u)] = static_cast<uint8_t>(rot_exp(esc_byte(es, rank)));
         rank++;
       }
     }
     exa = sp[0];
-    exb = sp[1];
+    exb = sp[32];
   }
 #pragma unroll
   for (uint32_t k = 0; k < 4; k++) {

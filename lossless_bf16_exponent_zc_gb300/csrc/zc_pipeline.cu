@@ -105,6 +105,15 @@ cudaError_t launch_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, u
   auto recv_esc = [&](int s) { return slots + (2 + s) * L.slot_bytes + L.main_bytes; };
   const uint64_t esc_cap = L.esc_bytes;
 
+  // On three distinct streams the compress and decompress stages get half of
+  // the SMs each: both kernels are persistent and ask for a whole SM's shared
+  // memory per CTA, so with full grids one stage would wait for the other to
+  // leave the GPU and the stages would not overlap.  (The encoder's
+  // cooperative grid then stays within half the SMs.)  On one stream they
+  // run one after the other and keep the whole GPU.
+  DeviceInfo half = dev;
+  if (sc != sd && dev.sm_count >= 2) half.sm_count = dev.sm_count / 2;
+
   Events ev;
   ZC_TRY(ev.create());
   // the other two streams start after everything already enqueued on the compress stream
@@ -120,8 +129,8 @@ cudaError_t launch_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, u
     // compress chunk k into send slot s once the link has taken chunk k - 2 out of it
     if (k >= 2) ZC_TRY(cudaStreamWaitEvent(sc, ev.link[s], 0));
     EncTensor t{in + k * c, send_main(s), send_esc(s), cb, m, esc_cap};
-    ZC_TRY(launch_encode(&t, 1, enc_ws, enc_flags, status, sc, dev, true));
-    ZC_TRY(launch_raw_switch(&t, 1, enc_ws, status, sc, dev));
+    ZC_TRY(launch_encode(&t, 1, enc_ws, enc_flags, status, sc, half, true));
+    ZC_TRY(launch_raw_switch(&t, 1, enc_ws, status, sc, half));
     ZC_TRY(cudaEventRecord(ev.comp[s], sc));
     // link: the static part (fixed-size main stream), then the dynamic part
     // (n_esc escape bytes, counted on the device), once receive slot s is free
@@ -144,7 +153,7 @@ cudaError_t launch_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, u
     // decompress chunk k from receive slot s
     ZC_TRY(cudaStreamWaitEvent(sd, ev.link[s], 0));
     DecTensor d{recv_main(s), recv_esc(s), out + k * c, m, esc_cap};
-    ZC_TRY(launch_decode(&d, 1, status, sd, dev));
+    ZC_TRY(launch_decode(&d, 1, status, sd, half));
     ZC_TRY(cudaEventRecord(ev.dec[s], sd));
   }
   // join: the compress and link streams continue after the last chunk is decoded

@@ -474,28 +474,30 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
             es.staged = m.staged;
             es.count = m.cnt;
             uint32_t rank = first + inc - c;
-            uint4* sp = reinterpret_cast<uint4*>(scratch + lane * 32);
+            // bytes 0..15 of the lane at scratch[16 lane], bytes 16..31 at scratch[512 + 16 lane]:
+            // each 16-byte access of the warp then touches every bank once per quarter
+            uint4* sp = reinterpret_cast<uint4*>(scratch + lane * 16);
             sp[0] = exa;
-            sp[1] = exb;
+            sp[32] = exb;
             uint32_t mz = z;
-            uint8_t* dst = scratch + lane * 32;
+            uint8_t* dst = scratch + lane * 16;  // byte q at dst[(q & 15) + 32 (q & 16)]
             if (first + total <= es.staged) {  // (warp-uniform) every escape of the block is staged
               const uint8_t* src = es.smem + rank;
               do {
                 const uint32_t q = __ffs(mz) - 1;
                 mz &= mz - 1;
-                dst[q] = static_cast<uint8_t>(rot_exp(*src++));
+                dst[(q & 15u) + 32u * (q & 16u)] = static_cast<uint8_t>(rot_exp(*src++));
               } while (mz);
             } else {
               while (mz) {
                 const uint32_t q = __ffs(mz) - 1;
                 mz &= mz - 1;
-                dst[q] = static_cast<uint8_t>(rot_exp(esc_byte(es, rank)));
+                dst[(q & 15u) + 32u * (q & 16u)] = static_cast<uint8_t>(rot_exp(esc_byte(es, rank)));
                 rank++;
               }
             }
             exa = sp[0];
-            exb = sp[1];
+            exb = sp[32];
           }
           uint4 v[4];
 #pragma unroll
