@@ -4,15 +4,17 @@
 // [ZipCCL §2.C] three 1-bit code arrays in column-major order, 128-byte
 // aligned blocks, asynchronous global->shared staging with double buffering.
 //
-// Design on sm_103a: a persistent, cooperatively launched grid, one CTA of 21
-// warps per SM.  The work unit of a warp is half a tile (2 blocks, 2048
-// values, one 4 KB TMA bulk copy into one of its two shared-memory stages).  A
-// CTA works through groups of 10 consecutive tiles (group G, G + C, ... for C
-// CTAs); encoding warp w takes half-tile w of each group.  The group is the
-// unit of the escape scan: the warps' escape counts meet in shared memory,
-// the last encoding warp to finish a group publishes the group's count at
-// once, the 21st "scan" warp finds the group's escape offset and posts the
-// group's offsets in shared memory.
+// Design on sm_103a: a persistent, cooperatively launched grid, one CTA of 12
+// warps per SM.  The work unit of a warp is a whole tile (4 blocks, 4096
+// values, one 8 KB TMA bulk copy into one of its two shared-memory stages): a
+// unit's fixed work (stage wait and refill, counts, offset-table entry, queue)
+// is spread over twice the values of a half-tile unit, and the 168 registers
+// of an 11-warp CTA hold four blocks' bookkeeping.  A CTA works through groups
+// of 11 consecutive tiles (group G, G + C, ... for C CTAs); encoding warp w
+// takes tile w of each group.  The group is the unit of the escape scan: the
+// warps' escape counts meet in shared memory, the last encoding warp to finish
+// a group publishes the group's count at once, the 12th "scan" warp finds the
+// group's escape offset and posts the group's offsets in shared memory.
 //
 // CTAs drift apart by several rounds (the order in which HBM serves their
 // loads), and a group's offset is known only once every group before it is
@@ -33,18 +35,30 @@
 
 namespace zc {
 
-constexpr int kEncWarps = 20;                   // encoding warps; warp 20 is the scan warp
+// Shape of the encoder (measured on 2^26 values, the batched MoE payload and
+// the batched Llama-3-8B bucket: whole-tile units on 11 warps beat half-tile
+// units on 20 warps by 2-4%, with identical streams).
+#ifndef ZC_ENC_UNIT_BLOCKS
+#define ZC_ENC_UNIT_BLOCKS 4  // blocks per warp unit: 4 (a tile) or 2 (half a tile)
+#endif
+#ifndef ZC_ENC_WARPS
+#define ZC_ENC_WARPS 11  // encoding warps (units per escape-scan group)
+#endif
+#ifndef ZC_ENC_RING
+#define ZC_ENC_RING 1024  // per-warp escape ring, bytes
+#endif
+constexpr int kEncWarps = ZC_ENC_WARPS;         // encoding warps; the next warp is the scan warp
 constexpr int kEncThreads = (kEncWarps + 1) * 32;
 constexpr int kEncStages = 2;
-constexpr uint32_t kUnitBlocks = 2;             // blocks per warp unit (half a tile)
+constexpr uint32_t kUnitBlocks = ZC_ENC_UNIT_BLOCKS;  // blocks per warp unit
 constexpr uint32_t kUnitElems = kUnitBlocks * kBlock;
 constexpr uint32_t kUnitsPerTile = kTile / kUnitElems;
 constexpr uint32_t kGroupUnits = kEncWarps;     // units per scan group (one per encoding warp)
 constexpr uint32_t kGroupTiles = kGroupUnits / kUnitsPerTile;
 constexpr uint32_t kEncStageBytes = kUnitElems * 2;  // 4096
 constexpr int kEncSlots = 16;                   // rounds in flight per warp (round slot = round mod 16)
-constexpr uint32_t kEncRing = 1024;             // per-warp escape ring (bytes, a power of two)
-constexpr uint32_t kEncRingUnitMax = 512;       // a unit with more escapes bypasses the ring
+constexpr uint32_t kEncRing = ZC_ENC_RING;      // per-warp escape ring (bytes, a power of two)
+constexpr uint32_t kEncRingUnitMax = kEncRing / 2;  // a unit with more escapes bypasses the ring
 constexpr uint32_t kEncQEntry = 16;             // bytes per queued round
 // After 1 KB alignment: per-warp LUTs (1 KB each, 1 KB aligned), per-warp stage
 // barriers, CTA round bookkeeping, per-warp round queues, per-warp escape
