@@ -798,6 +798,21 @@ def run_workloads(args, zc, torch, device, peak):
     cur = torch.cuda.current_stream()
     s3 = (cur, torch.cuda.Stream(device=device), torch.cuda.Stream(device=device))
     pipe = {"uncompressed_device_copy_ms": round(tcopy, 4)}
+    # the same transfer unchunked: compress the whole tensor, copy its main stream and escapes, decompress
+    wws = zc.workspace(n, device=device)
+    wm, we = torch.empty(mb, dtype=torch.uint8, device=device), torch.empty(n, dtype=torch.uint8, device=device)
+    rm, re_ = torch.empty_like(wm), torch.empty_like(we)
+    zc.compress(xt, cbg, wws, st, main=wm, esc=we)
+    kw = zc.header_n_esc(wm)
+
+    def whole():
+        zc.compress(xt, cbg, wws, st, main=wm, esc=we)
+        rm.copy_(wm)
+        re_[:kw].copy_(we[:kw])
+        zc.decompress(rm, re_, n, st, out=y, esc_bytes=kw)
+    tw = _time_ms(torch, whole, 10)
+    pipe["whole_tensor_compress_copy_decompress_ms"] = round(tw, 4)
+    del wws, wm, we, rm, re_
     for lg in (22, 24):
         chunk = 1 << lg
         pws = zc.pipeline_workspace(chunk, device=device)
@@ -805,11 +820,23 @@ def run_workloads(args, zc, torch, device, peak):
         ok = torch.equal(y, xt)
         t1 = _time_ms(torch, lambda: zc.pipelined_transfer(xt, cbg, chunk, pws, st, out=y, streams=(cur, cur, cur)),
                       10)
+        # the launch sequence captured once as a CUDA graph (zc_pipeline_plan_*) and replayed
+        y.zero_()
+        p3 = zc.pipeline_plan(xt, cbg, chunk, pws, st, out=y, overlap=True)
+        tp3 = _time_ms(torch, p3.launch, 10)
+        ok_plan = torch.equal(y, xt)
+        p1 = zc.pipeline_plan(xt, cbg, chunk, pws, st, out=y, overlap=False)
+        tp1 = _time_ms(torch, p1.launch, 10)
+        p3.close()
+        p1.close()
         pipe[f"chunks_2^{lg}"] = {
             "chunks": n // chunk,
             "three_streams": {"ms": round(t3, 4), "GB_per_s_uncompressed": round(2 * n / t3 / 1e6, 1)},
             "one_stream": {"ms": round(t1, 4), "GB_per_s_uncompressed": round(2 * n / t1 / 1e6, 1)},
-            "overlap_speedup": round(t1 / t3, 3), "round_trip_ok": bool(ok)}
+            "overlap_speedup": round(t1 / t3, 3), "round_trip_ok": bool(ok),
+            "plan_three_streams": {"ms": round(tp3, 4), "GB_per_s_uncompressed": round(2 * n / tp3 / 1e6, 1)},
+            "plan_one_stream": {"ms": round(tp1, 4)}, "plan_overlap_speedup": round(tp1 / tp3, 3),
+            "plan_vs_whole_tensor": round(tp3 / tw, 3), "plan_round_trip_ok": bool(ok_plan)}
         del pws
     out["pipelined_transfer_2^26"] = pipe
     del xt, y, yc

@@ -313,11 +313,11 @@ zc_status zc_compress_batched(int count, const zc_tensor* h_tensors, void* d_ws,
  * collective moves them over a link -- in chunks of chunk_elems values, with
  * three stages overlapped on three streams:
  *   stream_compress    chunk k      zc_compress_adaptive into send slot k % 2
- *   stream_link        chunk k - 1  the fixed-size main stream (one
- *                                   device-to-device copy: the static part),
- *                                   then exactly n_esc escape bytes, n_esc
- *                                   read on the device from the header that
- *                                   just arrived (the dynamic part)
+ *   stream_link        chunk k - 1  one copy kernel: the fixed-size main
+ *                                   stream (the static part, its size known
+ *                                   on the host) and exactly n_esc escape
+ *                                   bytes, n_esc read on the device from the
+ *                                   sender's header (the dynamic part)
  *   stream_decompress  chunk k - 2  zc_decompress from receive slot k % 2
  *                                   into d_out
  * On one GPU the receive slots (in the workspace) stand in for the peer's
@@ -342,6 +342,36 @@ zc_status zc_pipeline_workspace_size(uint64_t chunk_elems, uint64_t* bytes);
 zc_status zc_pipelined_transfer(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_out,
                                 uint64_t chunk_elems, void* d_ws, uint64_t ws_bytes, int32_t* d_status,
                                 void* stream_compress, void* stream_link, void* stream_decompress);
+
+/*
+ * Pipeline plan: the launch sequence of one zc_pipelined_transfer call (same
+ * arguments, same checks, same errors), captured once into an instantiated
+ * CUDA graph and replayed by zc_pipeline_plan_launch with a single launch.
+ * Each chunk costs five kernel launches and six event operations; once chunks
+ * are small the host submits them more slowly than the GPU runs them, and a
+ * replay removes that cost.
+ *   - overlap != 0: captured from three private streams, so the graph keeps
+ *     the three stages' overlap; overlap == 0: one stream, nothing overlaps.
+ *   - The plan holds the pointers it was made with (not their contents): a
+ *     launch reads d_in, d_cb and the workspace as they are when it runs and
+ *     writes d_out and *d_status.  The buffers must outlive the plan's last
+ *     launch; launches that share the workspace must be ordered (one stream).
+ *   - zc_pipeline_plan_create enqueues no device work; it creates and releases
+ *     streams and events and instantiates the graph (driver memory, no
+ *     library allocation of the caller's buffers).  On error *plan is NULL.
+ *   - zc_pipeline_plan_launch(plan, stream): the whole pipeline runs after the
+ *     work already on `stream`, and later work on `stream` sees d_out.  The
+ *     current device must be the one the plan was made on
+ *     (else ZC_ERR_INVALID_ARG).  A plan of n == 0 launches nothing.
+ *   - zc_pipeline_plan_destroy: releases the plan (NULL is accepted); a launch
+ *     still in flight completes.
+ */
+typedef struct zc_pipeline_plan_s* zc_pipeline_plan;
+zc_status zc_pipeline_plan_create(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_out,
+                                  uint64_t chunk_elems, void* d_ws, uint64_t ws_bytes, int32_t* d_status,
+                                  int overlap, zc_pipeline_plan* plan);
+zc_status zc_pipeline_plan_launch(zc_pipeline_plan plan, void* stream);
+zc_status zc_pipeline_plan_destroy(zc_pipeline_plan plan);
 
 /*
  * Cost models for deciding, on the host, whether compressing pays

@@ -2,9 +2,12 @@
 //
 // Host work only: argument validation, workspace layout, the sigma closed form
 // of [ZipCCL §2.A], and kernel launches on the caller's stream.  Nothing here
-// allocates, synchronises, or keeps per-call state.
+// allocates device memory, synchronises, or keeps per-call state; a pipeline
+// plan is an object the caller owns (a host struct and an instantiated CUDA
+// graph).
 #include <cmath>
 #include <cstring>
+#include <new>
 #include <vector>
 
 #include "zc_device.cuh"
@@ -327,6 +330,55 @@ zc_status zc_compress_batched_adaptive(int count, const zc_tensor* h_tensors, vo
   return compress_batched(count, h_tensors, d_ws, ws_bytes, d_status, stream, true);
 }
 
+struct zc_pipeline_plan_s {
+  cudaGraphExec_t exec;
+  int device;
+};
+static zc_status pipeline_args_ok(const void* d_in, uint64_t n, const uint8_t* d_cb, const void* d_out,
+                                  uint64_t chunk_elems, const void* d_ws, uint64_t ws_bytes, const int32_t* d_status) {
+  if (!d_status || !d_cb || !d_ws || ((!d_in || !d_out) && n) || chunk_elems == 0 || chunk_elems % 8 != 0)
+    return ZC_ERR_INVALID_ARG;
+  if (chunk_elems > kMaxN) return ZC_ERR_TOO_LARGE;
+  if (!aligned(d_in, 16) || !aligned(d_out, 16) || !aligned(d_ws, 256) || !aligned(d_status, 4))
+    return ZC_ERR_ALIGNMENT;
+  if (ws_bytes < pipeline_workspace_bytes(chunk_elems)) return ZC_ERR_WORKSPACE;
+  return ZC_OK;
+}
+zc_status zc_pipeline_plan_create(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_out,
+                                  uint64_t chunk_elems, void* d_ws, uint64_t ws_bytes, int32_t* d_status,
+                                  int overlap, zc_pipeline_plan* plan) {
+  if (!plan) return ZC_ERR_INVALID_ARG;
+  *plan = nullptr;
+  const zc_status a = pipeline_args_ok(d_in, n, d_cb, d_out, chunk_elems, d_ws, ws_bytes, d_status);
+  if (a != ZC_OK) return a;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return ZC_ERR_CUDA;
+  cudaGraphExec_t exec = nullptr;
+  if (capture_pipeline(static_cast<const uint16_t*>(d_in), n, d_cb, static_cast<uint16_t*>(d_out), chunk_elems,
+                       static_cast<uint8_t*>(d_ws), d_status, overlap != 0, dev, &exec) != cudaSuccess)
+    return ZC_ERR_CUDA;
+  zc_pipeline_plan p = new (std::nothrow) zc_pipeline_plan_s{exec, dev.device};
+  if (!p) {
+    if (exec) cudaGraphExecDestroy(exec);
+    return ZC_ERR_CUDA;
+  }
+  *plan = p;
+  return ZC_OK;
+}
+zc_status zc_pipeline_plan_launch(zc_pipeline_plan plan, void* stream) {
+  if (!plan) return ZC_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ZC_ERR_CUDA;
+  if (dev != plan->device) return ZC_ERR_INVALID_ARG;
+  if (!plan->exec) return ZC_OK;  // n == 0
+  return cuda_status(cudaGraphLaunch(plan->exec, as_stream(stream)));
+}
+zc_status zc_pipeline_plan_destroy(zc_pipeline_plan plan) {
+  if (!plan) return ZC_OK;
+  const cudaError_t e = plan->exec ? cudaGraphExecDestroy(plan->exec) : cudaSuccess;
+  delete plan;
+  return cuda_status(e);
+}
 zc_status zc_pipeline_workspace_size(uint64_t chunk_elems, uint64_t* bytes) {
   if (!bytes || chunk_elems == 0 || chunk_elems % 8 != 0) return ZC_ERR_INVALID_ARG;
   if (chunk_elems > kMaxN) return ZC_ERR_TOO_LARGE;
@@ -336,12 +388,8 @@ zc_status zc_pipeline_workspace_size(uint64_t chunk_elems, uint64_t* bytes) {
 zc_status zc_pipelined_transfer(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_out,
                                 uint64_t chunk_elems, void* d_ws, uint64_t ws_bytes, int32_t* d_status,
                                 void* stream_compress, void* stream_link, void* stream_decompress) {
-  if (!d_status || !d_cb || !d_ws || ((!d_in || !d_out) && n) || chunk_elems == 0 || chunk_elems % 8 != 0)
-    return ZC_ERR_INVALID_ARG;
-  if (chunk_elems > kMaxN) return ZC_ERR_TOO_LARGE;
-  if (!aligned(d_in, 16) || !aligned(d_out, 16) || !aligned(d_ws, 256) || !aligned(d_status, 4))
-    return ZC_ERR_ALIGNMENT;
-  if (ws_bytes < pipeline_workspace_bytes(chunk_elems)) return ZC_ERR_WORKSPACE;
+  const zc_status a = pipeline_args_ok(d_in, n, d_cb, d_out, chunk_elems, d_ws, ws_bytes, d_status);
+  if (a != ZC_OK) return a;
   DeviceInfo dev;
   if (device_info(&dev) != cudaSuccess) return ZC_ERR_CUDA;
   return cuda_status(launch_pipeline(static_cast<const uint16_t*>(d_in), n, d_cb, static_cast<uint16_t*>(d_out),

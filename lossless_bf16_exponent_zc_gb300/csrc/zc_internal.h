@@ -90,6 +90,12 @@ cudaError_t launch_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, u
                             uint8_t* ws, int32_t* status, cudaStream_t sc, cudaStream_t sl, cudaStream_t sd,
                             const DeviceInfo& dev);
 
+// The same launch sequence captured into an instantiated CUDA graph, from
+// three private streams (overlap) or one; *exec = nullptr when n == 0.
+cudaError_t capture_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, uint16_t* out, uint64_t c,
+                             uint8_t* ws, int32_t* status, bool overlap, const DeviceInfo& dev,
+                             cudaGraphExec_t* exec);
+
 cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out, const uint8_t* out_cb,
                           uint8_t* out_main, uint8_t* out_esc, uint64_t out_cap, WsHeader* ws, Flag* flags,
                           int32_t* status, cudaStream_t stream, const DeviceInfo& dev);

@@ -9,12 +9,18 @@
 // (the escape stream, n_esc bytes).
 //
 // On one GPU the link is a device-to-device copy into receive slots that stand
-// in for the peer's buffers.  The static part is one cudaMemcpyAsync of the
-// main stream (its size is known on the host); the dynamic part is sized on the
-// device: a small kernel reads n_esc from the header that just arrived and
-// copies exactly that many escape bytes -- the host never waits for a count.
-// Chunks are compressed adaptively, so an incompressible chunk travels RAW and
-// an escape slot of 5/8 of the chunk's values never overflows.
+// in for the peer's buffers, done by one kernel per chunk: the static part (the
+// main stream, whose size the host knows) and the dynamic part (exactly n_esc
+// escape bytes, n_esc read on the device from the sender's header, as a sender
+// sizes its second message) -- the host never waits for a count.  Chunks are
+// compressed adaptively, so an incompressible chunk travels RAW and an escape
+// slot of 5/8 of the chunk's values never overflows.
+//
+// Each chunk costs five launches and six event operations, which the host
+// submits more slowly than the GPU runs them once chunks are small.  A
+// pipeline plan captures the whole launch sequence once into a CUDA graph
+// (from three private streams, so the graph keeps the three-stage overlap) and
+// replays it with one launch.
 #include "zc_device.cuh"
 #include "zc_internal.h"
 
@@ -22,21 +28,30 @@ namespace zc {
 
 constexpr int kLinkThreads = 256;
 
-// Copies the dynamic part of a chunk: n_esc escape bytes, n_esc read from the
-// main stream's header (clamped to the slot's capacity; a bad count is then
-// caught by the decoder's header check).  Both buffers are 16-byte aligned.
-__global__ void __launch_bounds__(kLinkThreads) link_escapes_kernel(const uint8_t* __restrict__ main,
-                                                                    const uint8_t* __restrict__ src,
-                                                                    uint8_t* __restrict__ dst, uint64_t cap) {
+// The link of one chunk: the main stream (main_bytes, a multiple of 16) and
+// then n_esc escape bytes, n_esc read from the sender's header (clamped to the
+// slot's capacity; a bad count is then caught by the decoder's header check).
+// One index space of 16-byte pieces covers both parts; all four buffers are
+// 16-byte aligned.
+__global__ void __launch_bounds__(kLinkThreads) link_kernel(const uint8_t* __restrict__ send_main,
+                                                            uint8_t* __restrict__ recv_main, uint64_t main_bytes,
+                                                            const uint8_t* __restrict__ send_esc,
+                                                            uint8_t* __restrict__ recv_esc, uint64_t cap) {
   pdl_begin();
-  uint64_t n_esc = __ldcg(reinterpret_cast<const unsigned long long*>(main + 24));
+  uint64_t n_esc = __ldcg(reinterpret_cast<const unsigned long long*>(send_main + 24));
   if (n_esc > cap) n_esc = cap;
   const uint64_t tid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const uint64_t nthreads = static_cast<uint64_t>(gridDim.x) * blockDim.x;
-  const uint64_t vecs = n_esc / 16;
-  for (uint64_t i = tid; i < vecs; i += nthreads)
-    reinterpret_cast<uint4*>(dst)[i] = __ldcg(reinterpret_cast<const uint4*>(src) + i);
-  for (uint64_t i = 16 * vecs + tid; i < n_esc; i += nthreads) dst[i] = src[i];
+  const uint64_t main_vecs = main_bytes / 16;
+  const uint64_t vecs = main_vecs + n_esc / 16;
+  for (uint64_t i = tid; i < vecs; i += nthreads) {
+    if (i < main_vecs)
+      reinterpret_cast<uint4*>(recv_main)[i] = __ldcg(reinterpret_cast<const uint4*>(send_main) + i);
+    else
+      reinterpret_cast<uint4*>(recv_esc)[i - main_vecs] =
+          __ldcg(reinterpret_cast<const uint4*>(send_esc) + (i - main_vecs));
+  }
+  for (uint64_t i = 16 * (n_esc / 16) + tid; i < n_esc; i += nthreads) recv_esc[i] = send_esc[i];
 }
 
 // Workspace of a pipeline with chunks of c values: the encoder's workspace,
@@ -89,12 +104,10 @@ struct Events {
     if (e_ != cudaSuccess) return e_;          \
   } while (0)
 
-}  // namespace
-
-cudaError_t launch_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, uint16_t* out, uint64_t c,
-                            uint8_t* ws, int32_t* status, cudaStream_t sc, cudaStream_t sl, cudaStream_t sd,
-                            const DeviceInfo& dev) {
-  if (n == 0) return cudaSuccess;
+// Enqueues the whole pipeline on sc / sl / sd, using the caller's events.
+cudaError_t enqueue_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, uint16_t* out, uint64_t c,
+                             uint8_t* ws, int32_t* status, cudaStream_t sc, cudaStream_t sl, cudaStream_t sd,
+                             const DeviceInfo& dev, Events& ev) {
   const PipeLayout L = pipeline_layout(c);
   WsHeader* enc_ws = reinterpret_cast<WsHeader*>(ws);
   Flag* enc_flags = reinterpret_cast<Flag*>(ws + ZC_WORKSPACE_HEADER_BYTES);
@@ -114,8 +127,6 @@ cudaError_t launch_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, u
   DeviceInfo half = dev;
   if (sc != sd && dev.sm_count >= 2) half.sm_count = dev.sm_count / 2;
 
-  Events ev;
-  ZC_TRY(ev.create());
   // the other two streams start after everything already enqueued on the compress stream
   ZC_TRY(cudaEventRecord(ev.fork, sc));
   ZC_TRY(cudaStreamWaitEvent(sl, ev.fork, 0));
@@ -132,21 +143,24 @@ cudaError_t launch_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, u
     ZC_TRY(launch_encode(&t, 1, enc_ws, enc_flags, status, sc, half, true));
     ZC_TRY(launch_raw_switch(&t, 1, enc_ws, status, sc, half));
     ZC_TRY(cudaEventRecord(ev.comp[s], sc));
-    // link: the static part (fixed-size main stream), then the dynamic part
+    // link: the static part (fixed-size main stream) and the dynamic part
     // (n_esc escape bytes, counted on the device), once receive slot s is free
     ZC_TRY(cudaStreamWaitEvent(sl, ev.comp[s], 0));
     if (k >= 2) ZC_TRY(cudaStreamWaitEvent(sl, ev.dec[s], 0));
-    ZC_TRY(cudaMemcpyAsync(recv_main(s), send_main(s), main_bytes(m), cudaMemcpyDeviceToDevice, sl));
-    uint64_t blocks = (raw_spill(m) + kLinkThreads * 16 - 1) / (kLinkThreads * 16);
-    if (blocks > static_cast<uint64_t>(dev.sm_count)) blocks = dev.sm_count;
-    if (blocks == 0) blocks = 1;
     {
-      const uint8_t* lm = recv_main(s);
-      const uint8_t* le = send_esc(s);
-      uint8_t* ld = recv_esc(s);
+      const uint64_t mb = main_bytes(m);
+      uint64_t blocks = (mb + raw_spill(m) + kLinkThreads * 16 - 1) / (kLinkThreads * 16);
+      const uint64_t cap = 4ull * static_cast<uint64_t>(dev.sm_count);
+      if (blocks > cap) blocks = cap;
+      if (blocks == 0) blocks = 1;
+      const uint8_t* sm_ = send_main(s);
+      uint8_t* rm = recv_main(s);
+      const uint8_t* se = send_esc(s);
+      uint8_t* re = recv_esc(s);
       uint64_t lc = esc_cap;
-      void* args[] = {&lm, &le, &ld, &lc};
-      ZC_TRY(launch_kernel(reinterpret_cast<const void*>(link_escapes_kernel), dim3(static_cast<unsigned>(blocks)),
+      uint64_t lmb = mb;
+      void* args[] = {&sm_, &rm, &lmb, &se, &re, &lc};
+      ZC_TRY(launch_kernel(reinterpret_cast<const void*>(link_kernel), dim3(static_cast<unsigned>(blocks)),
                            dim3(kLinkThreads), 0, sl, args, false));
     }
     ZC_TRY(cudaEventRecord(ev.link[s], sl));
@@ -160,6 +174,46 @@ cudaError_t launch_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, u
   ZC_TRY(cudaStreamWaitEvent(sc, ev.dec[last], 0));
   ZC_TRY(cudaStreamWaitEvent(sl, ev.dec[last], 0));
   return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, uint16_t* out, uint64_t c,
+                            uint8_t* ws, int32_t* status, cudaStream_t sc, cudaStream_t sl, cudaStream_t sd,
+                            const DeviceInfo& dev) {
+  if (n == 0) return cudaSuccess;
+  Events ev;
+  ZC_TRY(ev.create());
+  return enqueue_pipeline(in, n, cb, out, c, ws, status, sc, sl, sd, dev, ev);
+}
+
+cudaError_t capture_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, uint16_t* out, uint64_t c,
+                             uint8_t* ws, int32_t* status, bool overlap, const DeviceInfo& dev,
+                             cudaGraphExec_t* exec) {
+  *exec = nullptr;
+  if (n == 0) return cudaSuccess;
+  // private streams: the capture depends on nothing the caller has enqueued
+  cudaStream_t st[3] = {nullptr, nullptr, nullptr};
+  const int ns = overlap ? 3 : 1;
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < ns && e == cudaSuccess; i++) e = cudaStreamCreateWithFlags(&st[i], cudaStreamNonBlocking);
+  if (e == cudaSuccess) {
+    Events ev;  // outlives the capture
+    e = ev.create();
+    if (e == cudaSuccess) e = cudaStreamBeginCapture(st[0], cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+      cudaStream_t sl = overlap ? st[1] : st[0], sd = overlap ? st[2] : st[0];
+      cudaError_t ee = enqueue_pipeline(in, n, cb, out, c, ws, status, st[0], sl, sd, dev, ev);
+      cudaGraph_t g = nullptr;
+      e = cudaStreamEndCapture(st[0], &g);  // always ends the capture, also after a failed enqueue
+      if (ee != cudaSuccess) e = ee;
+      if (e == cudaSuccess) e = cudaGraphInstantiateWithFlags(exec, g, 0);
+      if (g) cudaGraphDestroy(g);
+    }
+  }
+  for (int i = 0; i < ns; i++)
+    if (st[i]) cudaStreamDestroy(st[i]);
+  return e;
 }
 
 }  // namespace zc

@@ -110,10 +110,14 @@ def load() -> ctypes.CDLL:
                                              ctypes.POINTER(i32), dp, dp]
     lib.zc_pipeline_workspace_size.argtypes = [u64, u64p]
     lib.zc_pipelined_transfer.argtypes = [vp, u64, vp, vp, u64, vp, u64, vp, vp, vp, vp]
+    lib.zc_pipeline_plan_create.argtypes = [vp, u64, vp, vp, u64, vp, u64, vp, i32, ctypes.POINTER(vp)]
+    lib.zc_pipeline_plan_launch.argtypes = [vp, vp]
+    lib.zc_pipeline_plan_destroy.argtypes = [vp]
     for name in ("zc_codebook_from_sigma", "zc_compressed_size", "zc_workspace_size", "zc_histogram_topk",
                  "zc_compress", "zc_compress_adaptive", "zc_raw_spill", "zc_decompress", "zc_decompress_reduce",
                  "zc_compress_batched", "zc_compress_batched_adaptive", "zc_decompress_batched",
-                 "zc_pipeline_workspace_size", "zc_pipelined_transfer", "zq_default_widths",
+                 "zc_pipeline_workspace_size", "zc_pipelined_transfer", "zc_pipeline_plan_create",
+                 "zc_pipeline_plan_launch", "zc_pipeline_plan_destroy", "zq_default_widths",
                  "zq_table_from_histogram", "zq_max_bytes", "zq_compress", "zq_decompress", "zc_transfer_pays",
                  "zc_reduce_scatter_choose"):
         getattr(lib, name).restype = i32
@@ -381,6 +385,50 @@ def pipelined_transfer(x: torch.Tensor, cb: torch.Tensor, chunk_elems: int, ws: 
                                       _ptr(status), sc, sl, sd)
     _check(rc, "zc_pipelined_transfer")
     return out
+
+
+class PipelinePlan:
+    """zc_pipelined_transfer's launch sequence captured once into a CUDA graph; launch() replays it.
+
+    The plan keeps the tensors it was made with alive: each launch reads x, cb and ws as they are when it runs
+    (refill x in place for new data) and writes out and status.  Launches that share ws must be ordered."""
+
+    def __init__(self, x: torch.Tensor, cb: torch.Tensor, chunk_elems: int, ws: torch.Tensor,
+                 status: torch.Tensor, out: torch.Tensor | None = None, overlap: bool = True):
+        n = _nelem16(x)
+        if out is None:
+            out = torch.empty(n, dtype=torch.int16, device=x.device)
+        self.x, self.cb, self.ws, self.status, self.out = x, cb, ws, status, out
+        self._plan = ctypes.c_void_p()
+        with torch.cuda.device(x.device):
+            rc = load().zc_pipeline_plan_create(_ptr(x), n, _ptr(cb), _ptr(out), int(chunk_elems), _ptr(ws),
+                                                ws.numel(), _ptr(status), int(bool(overlap)),
+                                                ctypes.byref(self._plan))
+        _check(rc, "zc_pipeline_plan_create")
+
+    def launch(self, stream=None) -> torch.Tensor:
+        """Replays the pipeline on `stream` (default: the current stream of the plan's device, which must be the
+        current device); returns out."""
+        if self._plan is None:
+            raise RuntimeError("the plan was closed")
+        _check(load().zc_pipeline_plan_launch(self._plan, _stream(stream, self.status)), "zc_pipeline_plan_launch")
+        return self.out
+
+    def close(self) -> None:
+        if self._plan is not None:
+            _check(load().zc_pipeline_plan_destroy(self._plan), "zc_pipeline_plan_destroy")
+            self._plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # interpreter shutdown: nothing left to release into
+            pass
+
+
+def pipeline_plan(x: torch.Tensor, cb: torch.Tensor, chunk_elems: int, ws: torch.Tensor, status: torch.Tensor,
+                  out: torch.Tensor | None = None, overlap: bool = True) -> PipelinePlan:
+    return PipelinePlan(x, cb, chunk_elems, ws, status, out=out, overlap=overlap)
 
 
 # ------------------------------------------------------------------ QLC for FP8 (e4m3) bytes

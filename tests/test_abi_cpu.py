@@ -25,7 +25,8 @@ def test_library_exports_every_declared_symbol():
     assert {"zc_codebook_from_sigma", "zc_histogram_topk", "zc_compress", "zc_decompress", "zc_decompress_reduce",
             "zc_compressed_size", "zc_workspace_size", "zc_compress_batched", "zc_decompress_batched",
             "zc_status_string", "zc_version", "zc_compress_adaptive", "zc_compress_batched_adaptive",
-            "zc_raw_spill", "zc_pipeline_workspace_size", "zc_pipelined_transfer", "zq_default_widths",
+            "zc_raw_spill", "zc_pipeline_workspace_size", "zc_pipelined_transfer",
+            "zc_pipeline_plan_create", "zc_pipeline_plan_launch", "zc_pipeline_plan_destroy", "zq_default_widths",
             "zq_table_from_histogram", "zq_max_bytes", "zq_compress", "zq_decompress", "zc_transfer_pays",
             "zc_reduce_scatter_choose"} <= set(names)
     for name in names:
@@ -138,6 +139,27 @@ def test_pipeline_workspace_size():
                 None) == zc.ERR_ALIGNMENT
     assert _raw("zc_pipelined_transfer", fake, 10, fake, fake, 4096, fake, 100, status, None, None,
                 None) == zc.ERR_WORKSPACE
+
+
+def test_pipeline_plan_argument_errors():
+    """The plan applies zc_pipelined_transfer's checks before it captures anything; a failed create leaves
+    *plan NULL, and NULL plans are rejected (launch) or accepted (destroy)."""
+    import ctypes
+    fake, status = 1 << 20, 1 << 21
+    plan = ctypes.c_void_p(1234)
+    assert _raw("zc_pipeline_plan_create", fake, 10, fake, fake, 4100, fake, 1 << 30, status, 1,
+                ctypes.byref(plan)) == zc.ERR_INVALID_ARG
+    assert plan.value is None
+    assert _raw("zc_pipeline_plan_create", fake + 2, 10, fake, fake, 4096, fake, 1 << 30, status, 1,
+                ctypes.byref(plan)) == zc.ERR_ALIGNMENT
+    assert _raw("zc_pipeline_plan_create", fake, 10, fake, fake, 4096, fake, 100, status, 0,
+                ctypes.byref(plan)) == zc.ERR_WORKSPACE
+    assert _raw("zc_pipeline_plan_create", fake, 10, None, fake, 4096, fake, 1 << 30, status, 1,
+                ctypes.byref(plan)) == zc.ERR_INVALID_ARG
+    assert _raw("zc_pipeline_plan_create", fake, 10, fake, fake, 4096, fake, 1 << 30, status, 1,
+                None) == zc.ERR_INVALID_ARG
+    assert _raw("zc_pipeline_plan_launch", None, None) == zc.ERR_INVALID_ARG
+    assert _raw("zc_pipeline_plan_destroy", None) == zc.OK
 
 
 def test_qlc_host_functions_match_oracle():

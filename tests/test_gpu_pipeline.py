@@ -105,3 +105,55 @@ def test_pipeline_argument_errors(zc):
     with pytest.raises(zc.ZcError) as e:
         zc.pipelined_transfer(x, cb, 8192, ws, st)  # workspace sized for 4096-value chunks
     assert e.value.code == zc.ERR_WORKSPACE
+
+
+# ---------------------------------------------------------------- pipeline plans (the sequence as a CUDA graph)
+def check_plan(zc, plan, x, stream=None):
+    out = plan.launch(stream)
+    torch.cuda.synchronize()
+    assert zc.status_value(plan.status) == 0, zc.status_string(zc.status_value(plan.status))
+    got = out.cpu().numpy().view(np.uint16)
+    bad = np.nonzero(got != x)[0]
+    assert bad.size == 0, f"{bad.size} values differ, first at {bad[:8]}"
+
+
+@pytest.mark.parametrize("overlap", [True, False])
+@pytest.mark.parametrize("n,chunk", [
+    ((1 << 22) + 1234, 1 << 20),   # 5 chunks, ragged last
+    (100_000, 4104),               # chunk not a multiple of the tile size
+    (1 << 21, 1 << 16),            # 32 chunks
+])
+def test_plan_identity(zc, n, chunk, overlap):
+    x = workloads.gradient(n=n, sigma=1e-3, seed=n % 997)
+    plan = zc.pipeline_plan(dev(x), zc.codebook_to_device(oracle.codebook_from_sigma(1e-3)), chunk,
+                            zc.pipeline_workspace(chunk), zc.new_status(), overlap=overlap)
+    check_plan(zc, plan, x)
+    plan.close()
+
+
+def test_plan_replays_new_contents(zc):
+    """One plan, replayed over new values written into the same input buffer: Gaussian, then chunks that travel
+    RAW, then Gaussian again (the workspace's escape-scan state carries over between replays)."""
+    chunk, n = 1 << 16, 12 * (1 << 16) + 777
+    xt = torch.empty(n, dtype=torch.int16, device="cuda")
+    plan = zc.pipeline_plan(xt, zc.codebook_to_device(oracle.codebook_from_sigma(1e-3)), chunk,
+                            zc.pipeline_workspace(chunk), zc.new_status())
+    side = torch.cuda.Stream()
+    for i in range(4):
+        if i == 1:
+            x = np.concatenate([workloads.random_bits(n // 2, seed=i), workloads.gaussian(n - n // 2, sigma=1e-3)])
+        else:
+            x = workloads.gradient(n=n, sigma=1e-3, seed=300 + i)
+        xt.copy_(dev(x))
+        torch.cuda.synchronize()
+        check_plan(zc, plan, x, stream=side if i == 3 else None)
+
+
+def test_plan_empty(zc):
+    ws = zc.pipeline_workspace(4096)
+    plan = zc.pipeline_plan(torch.empty(0, dtype=torch.int16, device="cuda"),
+                            zc.codebook_to_device(oracle.codebook_from_sigma(1e-3)), 4096, ws, zc.new_status())
+    assert plan.launch().numel() == 0
+    plan.close()
+    with pytest.raises(RuntimeError):
+        plan.launch()
