@@ -780,6 +780,24 @@ __device__ __forceinline__ uint32_t launch_epoch(const WsHeader* ws) {
   return e == 0 ? 1u : e;
 }
 
+// Completion counts without full fences: relaxed reductions before a
+// __syncthreads, then one thread's acquire-release increment of a counter.
+// The barrier puts every thread's earlier accesses before the release, and
+// the increment that completes the count acquires those of every CTA.
+__device__ __forceinline__ void red_add_relaxed_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Exit protocol of a launch that uses escape-scan flags, run by each CTA's
 // scan warp once the CTA's last escape offsets are posted: from then on the
 // CTA neither reads nor writes a flag (its units' counts were published
@@ -787,16 +805,17 @@ __device__ __forceinline__ uint32_t launch_epoch(const WsHeader* ws) {
 // long ago, so the rest of the CTA may still be writing escapes.  The last
 // CTA to get here resets the exit counter and the test hook and publishes the
 // epoch; when the epoch wraps it clears every flag first, so a flag written
-// 2^32 launches earlier can never pass for a current one.  One atomic per CTA.
+// 2^32 launches earlier can never pass for a current one.  One atomic per CTA:
+// lane 0's acquire-release increment orders the CTA's flag accesses (the
+// encoding warps' count stores reached this warp through shared-memory
+// barriers first) before the count, and the CTA completing it acquires them
+// all; the kernel's end publishes what it writes next.
 __device__ __forceinline__ void scan_exit(WsHeader* ws, Flag* flags, uint32_t epoch, uint32_t total_units) {
   const uint32_t lane = lane_id();
   int last = 0;
-  if (lane == 0) {
-    __threadfence();
-    last = atomicAdd(&ws->exited, 1u) == gridDim.x - 1;
-  }
+  if (lane == 0) last = atom_add_acq_rel_gpu(&ws->exited, 1u) == gridDim.x - 1;
   if (!__shfl_sync(kFull, last, 0)) return;
-  __threadfence();
+  __syncwarp();
   const uint32_t maxt = max(*reinterpret_cast<volatile uint32_t*>(&ws->max_tiles), total_units);
   if (epoch == 0xFFFFFFFFu) {
     for (uint32_t i = lane; i < maxt; i += 32) flags[i] = Flag{0ull, 0ull};
@@ -808,7 +827,6 @@ __device__ __forceinline__ void scan_exit(WsHeader* ws, Flag* flags, uint32_t ep
     ws->exited = 0;
     ws->hold_tile = 0;
     ws->epoch = (epoch == 0xFFFFFFFFu) ? 0u : epoch;
-    __threadfence();
   }
 }
 

@@ -40,20 +40,6 @@ constexpr uint32_t kHistSmem = 128 + kHistStageOff + kHistStages * kHistChunk;
 static_assert(kHistStageOff % 128 == 0, "stage alignment");
 static_assert(kHistWarpUnits % 32 == 0, "whole pieces per lane");
 
-__device__ __forceinline__ void red_add_relaxed_gpu(uint32_t* p, uint32_t v) {
-  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 __device__ __forceinline__ void count_word(uint32_t* h, uint32_t w, uint32_t lane) {
   atomicAdd(&h[((w >> 7) & 0xFFu) * 32 + lane], 1u);
   atomicAdd(&h[((w >> 23) & 0xFFu) * 32 + lane], 1u);

@@ -121,21 +121,17 @@ __global__ void __launch_bounds__(kRawThreads, 6) raw_switch_kernel(const __grid
       }
     }
   }
-  // The last CTA writes the RAW headers once every CTA has read the counts.
+  // The last CTA writes the RAW headers once every CTA has read the counts
+  // (the barrier, then thread 0's acquire-release count of finished CTAs).
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(&p.ws->raw_done, 1u) == gridDim.x - 1) {
-      __threadfence();
-      for (int i = 0; i < p.count; i++) {
-        if (!((mask >> i) & 1u)) continue;
-        uint8_t* m = p.t[i].main;
-        *reinterpret_cast<uint32_t*>(m + 4) = ZC_VERSION | (kFlagRaw << 16);
-        *reinterpret_cast<unsigned long long*>(m + 24) = raw_spill(p.t[i].n);
-      }
-      p.ws->raw_done = 0;
-      __threadfence();
+  if (threadIdx.x == 0 && atom_add_acq_rel_gpu(&p.ws->raw_done, 1u) == gridDim.x - 1) {
+    for (int i = 0; i < p.count; i++) {
+      if (!((mask >> i) & 1u)) continue;
+      uint8_t* m = p.t[i].main;
+      *reinterpret_cast<uint32_t*>(m + 4) = ZC_VERSION | (kFlagRaw << 16);
+      *reinterpret_cast<unsigned long long*>(m + 24) = raw_spill(p.t[i].n);
     }
+    p.ws->raw_done = 0;
   }
 }
 

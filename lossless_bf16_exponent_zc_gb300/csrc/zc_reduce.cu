@@ -78,6 +78,7 @@ struct RedParams {
   WsHeader* ws;
   Flag* flags;
   int32_t* status;
+  int single;  // the RAW-capable launch runs alone and does the work whatever the shards are
 };
 
 struct ShardInfo {
@@ -132,7 +133,9 @@ __device__ __forceinline__ uint4 round_pack(const float (&acc)[8]) {
 // RAW = false: the launch for all-coded inputs; it leaves at once when a shard
 // is RAW.  RAW = true: the launch that follows it and does the work only when
 // some shard is RAW (its shard loop tests every copy for RAW; keeping that
-// test out of the all-coded kernel keeps its code as lean as before).
+// test out of the all-coded kernel keeps its code as lean as before).  A grid
+// of less than one CTA per SM is launch-bound: there the RAW-capable kernel
+// runs alone (p.single) and does the work for any shards.
 template <bool REENC, bool RAW>
 __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_constant__ RedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -149,7 +152,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(gbase + kRBars);
   uint64_t* empty_bar = full_bar + kRedTeams * kRedStages;
   StageMeta* meta = reinterpret_cast<StageMeta*>(gbase + kRMeta);
-  if (RAW) {  // nothing to do unless a shard is RAW: leave before touching anything
+  if (RAW && !p.single) {  // nothing to do unless a shard is RAW: leave before touching anything
     bool any = false;
     for (int r = threadIdx.x; r < p.P; r += blockDim.x)
       any |= __ldg(reinterpret_cast<const uint32_t*>(p.s[r].main) + 1) == (ZC_VERSION | (kFlagRaw << 16));
@@ -592,8 +595,10 @@ cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out,
   if (ctas > static_cast<uint32_t>(dev.sm_count)) ctas = dev.sm_count;
   if (ctas == 0) ctas = 1;
   // The all-coded launch, then the RAW-capable one; exactly one of them works.
+  // A grid below one CTA per SM gets the RAW-capable launch alone.
+  p.single = ngroups < static_cast<uint32_t>(dev.sm_count) ? 1 : 0;
   static KernelPrep prep[2][2];
-  for (int raw = 0; raw < 2; raw++) {
+  for (int raw = p.single; raw < 2; raw++) {
     int per_sm = 0;
     cudaError_t err;
     if (out_cb) {

@@ -326,6 +326,16 @@ def test_decompress_reduce_small(zc, P, m, reencode):
     _reduce_case(zc, P, m, reencode=reencode, seed=P * 7 + m % 13)
 
 
+@pytest.mark.parametrize("reencode", [True, False])
+def test_decompress_reduce_both_launch_paths(zc, reencode):
+    """A grid below one CTA per SM runs the RAW-capable kernel alone; from one CTA per SM on (4 tiles per CTA,
+    so >= 4 x SMs tiles) the all-coded kernel runs, followed by the RAW-capable one that leaves at once.  Sizes on
+    both sides of the switch, element by element against the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for m in (4096 * (4 * (sms - 1) - 1) + 55, 4 * 4096 * sms + 4096 + 9):
+        _reduce_case(zc, 3, m, reencode=reencode, seed=m % 101)
+
+
 FAR_CODEBOOK = np.array([1, 2, 3, 4, 5, 6, 7], dtype=np.uint8)  # no N(0, 1e-3) value has these exponents
 
 
