@@ -47,7 +47,7 @@ constexpr uint32_t kRedEscCap = 512;              // staged input escape bytes p
 constexpr uint32_t kRedStageBytes = kTileBytes + kRedEscCap;
 constexpr uint32_t kRedEbuf = 512;                // staged output escapes per block and round
 constexpr int kRedSlots = 2;                      // rounds in flight for the output offsets
-constexpr uint32_t kGroupTilesR = kRedTeams;      // tiles per escape-scan group
+constexpr uint32_t kGroupTilesR = kRedTeams;      // tiles per escape-scan group (1 for inputs of few tiles)
 constexpr int kSpreadCopies = 32;
 // Shared-memory layout after 1 KB alignment.
 constexpr uint32_t kRSpread = 0;                              // spread table, 32 lane copies (32 KB)
@@ -78,7 +78,8 @@ struct RedParams {
   WsHeader* ws;
   Flag* flags;
   int32_t* status;
-  int single;  // the RAW-capable launch runs alone and does the work whatever the shards are
+  int single;   // the RAW-capable launch runs alone and does the work whatever the shards are
+  uint32_t gt;  // tiles per escape-scan group: kGroupTilesR (one per team), or 1 (team 0 alone)
 };
 
 struct ShardInfo {
@@ -134,7 +135,7 @@ __device__ __forceinline__ uint4 round_pack(const float (&acc)[8]) {
 // is RAW.  RAW = true: the launch that follows it and does the work only when
 // some shard is RAW (its shard loop tests every copy for RAW; keeping that
 // test out of the all-coded kernel keeps its code as lean as before).  A grid
-// of less than one CTA per SM is launch-bound: there the RAW-capable kernel
+// of at most one CTA per SM is launch-bound: there the RAW-capable kernel
 // runs alone (p.single) and does the work for any shards.
 template <bool REENC, bool RAW>
 __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_constant__ RedParams p) {
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
   const bool skip = flags_s[0] != 0 || flags_s[1] != 0;
   const uint32_t epoch = REENC ? launch_epoch(p.ws) : 0u;
   const uint32_t hold = REENC ? launch_hold(p.ws) : 0u;
-  const uint32_t ngroups = (p.ntiles + kGroupTilesR - 1) / kGroupTilesR;
+  const uint32_t ngroups = (p.ntiles + p.gt - 1) / p.gt;
   const uint32_t step = gridDim.x;
   if (REENC && !skip && p.ntiles == 0 && blockIdx.x == 0 && warp == 0) {
     write_header_words(p.out_main, 0, p.out_cb);
@@ -246,9 +247,9 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
 #pragma unroll
         for (int h = 0; h < 2; h++) {
           na[u][h] = nb[u][h] = 0;
-          const uint32_t g = G * kGroupTilesR + t0 + u;
+          const uint32_t g = G * p.gt + t0 + u;
           const uint32_t r = lane + 32u * h;
-          if (G < ngroups && g < p.ntiles && r < P) {
+          if (t0 + u < p.gt && G < ngroups && g < p.ntiles && r < P) {
             const uint32_t* tbl = reinterpret_cast<const uint32_t*>(p.s[r].main + kHeader);
             na[u][h] = __ldg(tbl + g);
             const uint64_t bb = (g + 1 < p.ntiles) ? static_cast<uint64_t>(__ldg(tbl + g + 1)) : si[r].n_esc;
@@ -301,8 +302,8 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
 #pragma unroll
           for (int u = 0; u < kTeamsPerProducer; u++) {
             const uint32_t t = t0 + u;
-            const uint32_t g = G * kGroupTilesR + t;
-            if (g >= p.ntiles) continue;
+            const uint32_t g = G * p.gt + t;
+            if (t >= p.gt || g >= p.ntiles) continue;
             const uint32_t bi = t * kRedStages + uses[u] % kRedStages;
             if (uses[u] >= static_cast<uint32_t>(kRedStages))
               mbar_wait_bounded(&empty_bar[bi], (uses[u] / kRedStages - 1) & 1u, p.status);
@@ -401,8 +402,8 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     prev.done = true;
     uint32_t j = 0;
     for (uint32_t G = blockIdx.x; G < ngroups; G += step, j++) {
-      const uint32_t g = G * kGroupTilesR + t;
-      const bool has = g < p.ntiles;
+      const uint32_t g = G * p.gt + t;
+      const bool has = t < p.gt && g < p.ntiles;
       const uint64_t rem = has ? p.n - static_cast<uint64_t>(g) * kTile : 0;
       const uint32_t n_tile = rem >= kTile ? kTile : static_cast<uint32_t>(rem);
       float acc[4][8];
@@ -590,13 +591,17 @@ cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out,
   p.ws = ws;
   p.flags = flags;
   p.status = status;
-  const uint32_t ngroups = (p.ntiles + kGroupTilesR - 1) / kGroupTilesR;
+  // Inputs of at most one tile per SM take one tile per group (team 0 of each
+  // CTA): the P copies of a tile are decoded one after another by its team, so
+  // spreading the tiles over more SMs shortens the launch.
+  p.gt = p.ntiles <= static_cast<uint32_t>(dev.sm_count) ? 1u : kGroupTilesR;
+  const uint32_t ngroups = (p.ntiles + p.gt - 1) / p.gt;
   uint32_t ctas = ngroups;
   if (ctas > static_cast<uint32_t>(dev.sm_count)) ctas = dev.sm_count;
   if (ctas == 0) ctas = 1;
   // The all-coded launch, then the RAW-capable one; exactly one of them works.
-  // A grid below one CTA per SM gets the RAW-capable launch alone.
-  p.single = ngroups < static_cast<uint32_t>(dev.sm_count) ? 1 : 0;
+  // A grid of at most one CTA per SM gets the RAW-capable launch alone.
+  p.single = ngroups <= static_cast<uint32_t>(dev.sm_count) ? 1 : 0;
   static KernelPrep prep[2][2];
   for (int raw = p.single; raw < 2; raw++) {
     int per_sm = 0;
