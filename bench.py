@@ -170,8 +170,8 @@ KERNEL_SOURCES = {
 OP_KERNEL = {"histogram": "hist_kernel", "compress_hist_cb": "encode_kernel", "compress_sigma_cb": "encode_kernel",
              "decompress_hist_cb": "decode_kernel", "decompress_sigma_cb": "decode_kernel"}
 MEASURED_TRAFFIC = {  # kernel: (source hash, bytes per launch)
-    "encode_kernel": ("86aa5cb2471b363e", 183489536),
-    "decode_kernel": ("e079df33f1bf1f69", 167630592),
+    "encode_kernel": ("cbb73e321092d557", 183554304),
+    "decode_kernel": ("26da93e49aff50a5", 167835392),
 }
 
 
