@@ -596,6 +596,20 @@ def run_workloads(args, zc, torch, device, peak):
         return {"ms": round(ms, 4), "GB_per_s_uncompressed": round(n_unc / ms / 1e6, 1),
                 "alg_GB_per_s": round(alg / ms / 1e6, 1), "frac_of_hbm": round(alg / ms / 1e6 / peak, 4)}
 
+    # 0. the histogram on its own: two 2^26 N(0, 1e-3) tensors alternated, so every call reads from HBM and no
+    #    decompress output is being written back from L2 meanwhile (inside the gradient step it is)
+    ha = [workloads.gaussian_on_device(1 << 26, 1e-3, seed=40 + i, device=device) for i in range(2)]
+    hws = zc.workspace(1 << 26, device=device)
+    hcb = torch.empty(7, dtype=torch.uint8, device=device)
+    calls = [0]
+
+    def hist_alt():
+        zc.histogram_topk(ha[calls[0] & 1], hws, st, cb_out=hcb)
+        calls[0] += 1
+    th_alone = _time_ms(torch, hist_alt, 20)
+    out["histogram_2^26_alone"] = entry(th_alone, 2 << 26, 2 << 26)
+    del ha, hws
+
     # 1. gaussian 2^20, sigma codebook
     x = workloads.gaussian()
     n = x.size
