@@ -585,7 +585,7 @@ __device__ __forceinline__ uint32_t spread_sel(uint32_t w0, uint32_t w1, uint32_
 // An exponent rotated right by one bit: (e & 1) << 7 | e >> 1.  In this form
 // the exponent's low bit sits where a bf16's low byte wants it (bit 7) and its
 // other seven bits where the high byte wants them (bits 0..6), so a bf16 is
-// a bit-select between its sign-mantissa byte and this byte (see bf16_pair).
+// a bit-select between its sign-mantissa byte and this byte (see bf16_quad).
 __device__ __forceinline__ uint32_t rot_exp(uint32_t e) { return ((e >> 1) | (e << 7)) & 0xFFu; }
 
 // Code -> rotated exponent table as two words for __byte_perm: byte c of
@@ -602,15 +602,17 @@ __device__ __forceinline__ DecTable make_dec_table(const uint8_t cb[7]) {
   return d;
 }
 
-// Two packed bf16 values (elements 2h, 2h + 1 of a group of four) from the
-// group's sign-mantissa word `sm` (byte i = s << 7 | m of element i) and its
-// rotated-exponent word `rx` (byte i = rot_exp(e) of element i):
-// low byte = (e & 1) << 7 | m, high byte = s << 7 | e >> 1.
-template <int H>
-__device__ __forceinline__ uint32_t bf16_pair(uint32_t sm, uint32_t rx) {
-  const uint32_t a = __byte_perm(sm, rx, H ? 0x7362 : 0x5140);  // [sm, rx, sm, rx] per value
-  const uint32_t b = __byte_perm(sm, rx, H ? 0x3726 : 0x1504);  // [rx, sm, rx, sm] per value
-  return (a & 0x7F7F7F7Fu) | (b & 0x80808080u);
+// The four bf16 values of a group of four elements, as two packed pairs
+// (p0 = elements 0, 1; p1 = elements 2, 3), from the group's sign-mantissa
+// word `sm` (byte i = s << 7 | m of element i) and its rotated-exponent word
+// `rx` (byte i = rot_exp(e) of element i): two bit-selects give all four low
+// bytes ((e & 1) << 7 | m) and all four high bytes (s << 7 | e >> 1), two byte
+// permutes interleave them.
+__device__ __forceinline__ void bf16_quad(uint32_t sm, uint32_t rx, uint32_t& p0, uint32_t& p1) {
+  const uint32_t lo = (sm & 0x7F7F7F7Fu) | (rx & 0x80808080u);
+  const uint32_t hi = (rx & 0x7F7F7F7Fu) | (sm & 0x80808080u);
+  p0 = __byte_perm(lo, hi, 0x5140);
+  p1 = __byte_perm(lo, hi, 0x7362);
 }
 
 // Source of escape bytes for one (tile, stream): the first `staged` ranks sit
@@ -701,10 +703,8 @@ __device__ __forceinline__ uint32_t decode_block(uint32_t tile, uint32_t blk, ui
     const uint2 sm = lds64(b + k * 256 + lane * 8);
     const uint32_t r0 = k == 0 ? exa.x : k == 1 ? exa.z : k == 2 ? exb.x : exb.z;
     const uint32_t r1 = k == 0 ? exa.y : k == 1 ? exa.w : k == 2 ? exb.y : exb.w;
-    out[k].x = bf16_pair<0>(sm.x, r0);
-    out[k].y = bf16_pair<1>(sm.x, r0);
-    out[k].z = bf16_pair<0>(sm.y, r1);
-    out[k].w = bf16_pair<1>(sm.y, r1);
+    bf16_quad(sm.x, r0, out[k].x, out[k].y);
+    bf16_quad(sm.y, r1, out[k].z, out[k].w);
   }
   return c;
 }

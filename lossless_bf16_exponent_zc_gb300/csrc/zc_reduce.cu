@@ -509,8 +509,8 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
             const uint2 sm = lds64(blk_s + k * 256 + lane * 8);
             const uint32_t r0 = k == 0 ? exa.x : k == 1 ? exa.z : k == 2 ? exb.x : exb.z;
             const uint32_t r1 = k == 0 ? exa.y : k == 1 ? exa.w : k == 2 ? exb.y : exb.w;
-            v[k] = make_uint4(bf16_pair<0>(sm.x, r0), bf16_pair<1>(sm.x, r0), bf16_pair<0>(sm.y, r1),
-                              bf16_pair<1>(sm.y, r1));
+            bf16_quad(sm.x, r0, v[k].x, v[k].y);
+            bf16_quad(sm.y, r1, v[k].z, v[k].w);
           }
 #pragma unroll
           for (int k = 0; k < 4; k++) accumulate8(acc[k], v[k]);
