@@ -231,11 +231,12 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     // ---------------- producer q: stage the P copies of the tiles of teams 2q, 2q + 1, in the
     // order the consumers take them.  What a copy needs (its escape range and its checks, the
     // span of escape bytes to stage) is worked out once per round for every shard at once, one
-    // shard per lane, so that lane 0 only waits for the stage, writes 16 bytes and starts the
-    // two bulk copies: the issue of a copy is short, and the copies follow each other closely.
+    // shard per lane, so that issuing a copy is short: lane u waits for team 2q + u's stage,
+    // writes 16 bytes and starts the two bulk copies, both teams in the same instructions, and
+    // the copies follow each other closely.
     const uint32_t t0 = (warp - kRedProd) * kTeamsPerProducer;
     const uint32_t P = static_cast<uint32_t>(p.P);
-    uint32_t uses[kTeamsPerProducer] = {};
+    uint32_t uses = 0;  // copies this lane has started for its team (lanes < kTeamsPerProducer)
     // offsets [a, b) of the tile of team t0 + u in the next round, for shard lane + 32 h
     uint32_t na[kTeamsPerProducer][2], nb[kTeamsPerProducer][2];
     // the round's plan per team and shard: pa = the tile's first escape;
@@ -298,16 +299,22 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
           ca[u] = __shfl_sync(kFull, r < 32 ? pa[u][0] : pa[u][1], src);
           ck[u] = __shfl_sync(kFull, r < 32 ? pk[u][0] : pk[u][1], src);
         }
-        if (lane == 0) {
+        if (lane < static_cast<uint32_t>(kTeamsPerProducer)) {
+          // lane u serves team t0 + u: the teams' copies start in the same instructions
+          uint32_t cau = ca[0], cku = ck[0];
 #pragma unroll
-          for (int u = 0; u < kTeamsPerProducer; u++) {
-            const uint32_t t = t0 + u;
-            const uint32_t g = G * p.gt + t;
-            if (t >= p.gt || g >= p.ntiles) continue;
-            const uint32_t bi = t * kRedStages + uses[u] % kRedStages;
-            if (uses[u] >= static_cast<uint32_t>(kRedStages))
-              mbar_wait_bounded(&empty_bar[bi], (uses[u] / kRedStages - 1) & 1u, p.status);
-            uses[u]++;
+          for (int q = 1; q < kTeamsPerProducer; q++)
+            if (lane == static_cast<uint32_t>(q)) {
+              cau = ca[q];
+              cku = ck[q];
+            }
+          const uint32_t t = t0 + lane;
+          const uint32_t g = G * p.gt + t;
+          if (t < p.gt && g < p.ntiles) {
+            const uint32_t bi = t * kRedStages + uses % kRedStages;
+            if (uses >= static_cast<uint32_t>(kRedStages))
+              mbar_wait_bounded(&empty_bar[bi], (uses / kRedStages - 1) & 1u, p.status);
+            uses++;
             StageMeta m;
             m.shard = static_cast<uint16_t>(r);
             if (RAW && ((*raw_s >> r) & 1ull)) {  // RAW shard: the consumers read global memory
@@ -315,21 +322,21 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
               m.ok = kMetaOk | kMetaRaw;
               meta[bi] = m;
               mbar_arrive(&full_bar[bi]);
-              continue;
+            } else {
+              const uint32_t span = ((cku >> 23) & 0x3Fu) << 4;
+              m.a = cau;
+              m.cnt = cku & 0x1FFFu;
+              m.staged = (cku >> 13) & 0x3FFu;
+              m.ok = static_cast<uint16_t>(cku >> 31);
+              meta[bi] = m;
+              uint8_t* stage = gbase + kRStage + bi * kRedStageBytes;
+              // (the stage is only ever written by these bulk copies; the
+              // consumers' reads of its previous contents completed before their
+              // release of it, which the wait above observed)
+              mbar_arrive_expect_tx(&full_bar[bi], kTileBytes + span);
+              tma_load_1d(stage, tile_ptr(p.s[r].main, p.ntiles, g), kTileBytes, &full_bar[bi]);
+              if (span != 0) tma_load_1d(stage + kTileBytes, p.s[r].esc + (cau & ~15u), span, &full_bar[bi]);
             }
-            const uint32_t span = ((ck[u] >> 23) & 0x3Fu) << 4;
-            m.a = ca[u];
-            m.cnt = ck[u] & 0x1FFFu;
-            m.staged = (ck[u] >> 13) & 0x3FFu;
-            m.ok = static_cast<uint16_t>(ck[u] >> 31);
-            meta[bi] = m;
-            uint8_t* stage = gbase + kRStage + bi * kRedStageBytes;
-            // (the stage is only ever written by these bulk copies; the
-            // consumers' reads of its previous contents completed before their
-            // release of it, which the wait above observed)
-            mbar_arrive_expect_tx(&full_bar[bi], kTileBytes + span);
-            tma_load_1d(stage, tile_ptr(p.s[r].main, p.ntiles, g), kTileBytes, &full_bar[bi]);
-            if (span != 0) tma_load_1d(stage + kTileBytes, p.s[r].esc + (ca[u] & ~15u), span, &full_bar[bi]);
           }
         }
         __syncwarp();
