@@ -211,9 +211,10 @@ zc_status zc_raw_spill(uint64_t n, uint64_t* bytes);
 
 /*
  * zc_compress with the raw bypass ([CCCL §3.3], [CCCL §5.2]): encodes like
- * zc_compress, then a second launch on the same stream reads the escape count
- * on the device and rewrites the tensor as a RAW stream (format above) when
- * that is strictly smaller, i.e. when n_esc > zc_raw_spill(n) -- no host
+ * zc_compress; then, in the same launch, once every CTA has encoded its tiles
+ * (a grid barrier of the cooperative launch), the escape count is read on the
+ * device and the tensor is rewritten as a RAW stream (format above) when that
+ * is strictly smaller, i.e. when n_esc > zc_raw_spill(n) -- no host
  * synchronisation.  The header's flags tell which form was stored and n_esc
  * the escape bytes to send.  A coded form that overflows esc_capacity is not
  * an error when the RAW form fits; ZC_ERR_ESCAPE_OVERFLOW is reported only

@@ -19,7 +19,7 @@ LIB = os.path.join(LIBDIR, "libzc.so")
 SAN_BUILD = os.path.join(BUILD, "san")
 SAN_LIB = os.path.join(LIBDIR, "libzc_san.so")
 SAN_FLAGS = ["-fsanitize=address", "-fsanitize=undefined", "-fno-sanitize-recover=undefined", "-fno-omit-frame-pointer", "-g"]
-SOURCES = ["zc_api.cu", "zc_encode.cu", "zc_decode.cu", "zc_reduce.cu", "zc_hist.cu", "zc_noalloc.cu", "zc_raw.cu", "zc_pipeline.cu", "zq.cu"]
+SOURCES = ["zc_api.cu", "zc_encode.cu", "zc_decode.cu", "zc_reduce.cu", "zc_hist.cu", "zc_noalloc.cu", "zc_pipeline.cu", "zq.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

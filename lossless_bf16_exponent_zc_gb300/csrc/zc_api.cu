@@ -218,11 +218,8 @@ static zc_status compress_one(const void* d_in, uint64_t n, const uint8_t* d_cb,
   if (device_info(&dev) != cudaSuccess) return ZC_ERR_CUDA;
   EncTensor t{static_cast<const uint16_t*>(d_in), static_cast<uint8_t*>(d_main), static_cast<uint8_t*>(d_esc),
               d_cb, n, esc_capacity};
-  if (launch_encode(&t, 1, ws_header(d_ws), ws_flags(d_ws), d_status, as_stream(stream), dev, adaptive) !=
-      cudaSuccess)
-    return ZC_ERR_CUDA;
-  if (adaptive) return cuda_status(launch_raw_switch(&t, 1, ws_header(d_ws), d_status, as_stream(stream), dev));
-  return ZC_OK;
+  return cuda_status(launch_encode(&t, 1, ws_header(d_ws), ws_flags(d_ws), d_status, as_stream(stream), dev,
+                                   adaptive));
 }
 zc_status zc_compress(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_main, void* d_esc,
                       uint64_t esc_capacity, void* d_ws, uint64_t ws_bytes, int32_t* d_status, void* stream) {
@@ -316,7 +313,6 @@ static zc_status compress_batched(int count, const zc_tensor* h_tensors, void* d
                         static_cast<uint8_t*>(t.esc), t.cb, t.n, t.esc_bytes};
     }
     cudaError_t e = launch_encode(ts, m, ws_header(d_ws), ws_flags(d_ws), d_status, as_stream(stream), dev, adaptive);
-    if (e == cudaSuccess && adaptive) e = launch_raw_switch(ts, m, ws_header(d_ws), d_status, as_stream(stream), dev);
     if (e != cudaSuccess) return ZC_ERR_CUDA;
   }
   return ZC_OK;

@@ -37,8 +37,10 @@ struct WsHeader {
   uint32_t epoch;      // epoch tag of the last finished encoding launch
   uint32_t max_tiles;  // largest flag range ever used (cleared when the epoch wraps)
   uint32_t hist_done;  // CTAs of the running histogram launch that have finished
-  uint32_t raw_done;   // CTAs of the running raw-bypass launch that have finished
-  uint32_t pad[26];
+  uint32_t raw_done;   // CTAs of the running adaptive encoding launch done with a RAW rewrite
+  uint32_t raw_arrived;  // CTAs of the running adaptive encoding launch at its grid barrier
+  uint32_t raw_gen;      // generation of that barrier: bumped by the last CTA to arrive
+  uint32_t pad[24];
   uint32_t hist[256];  // global exponent bins, all zero between calls
 };
 static_assert(sizeof(WsHeader) <= ZC_WORKSPACE_HEADER_BYTES, "workspace header too large");
@@ -796,6 +798,39 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Barrier of every CTA of a grid whose CTAs are all resident (a cooperative
+// launch), run by thread 0 of each CTA between two __syncthreads.  The count
+// of arrivals is reset by the CTA that completes it, which then bumps the
+// generation word the others wait on (read before arriving), so the barrier
+// is ready for the next launch with no further round trip.  Bounded: after
+// kWaitLimitNs it records ZC_ERR_TIMEOUT and returns false.
+__device__ __forceinline__ bool grid_barrier(uint32_t* arrived, uint32_t* gen, int32_t* status) {
+  const uint32_t g = ld_relaxed_gpu(gen);
+  if (atom_add_acq_rel_gpu(arrived, 1u) == gridDim.x - 1) {
+    *arrived = 0;
+    st_release_gpu(gen, g + 1u);
+    return true;
+  }
+  if (ld_acquire_gpu(gen) != g) return true;
+  const unsigned long long t0 = global_ns();
+  while (ld_acquire_gpu(gen) == g) {
+    if (global_ns() - t0 > kWaitLimitNs) {
+      set_status(status, ZC_ERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
 }
 
 // Exit protocol of a launch that uses escape-scan flags, run by each CTA's

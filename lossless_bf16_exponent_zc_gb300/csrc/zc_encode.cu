@@ -82,7 +82,7 @@ struct EncParams {
   WsHeader* ws;
   Flag* flags;  // one per group
   int32_t* status;
-  int adaptive;  // an escape overflow is left to the raw-bypass launch that follows
+  int adaptive;  // the raw bypass runs at the end; an escape overflow is reported by it
 };
 
 // Tensor of global group G.  Every caller visits groups in increasing order,
@@ -122,6 +122,125 @@ struct QEntry {
 static_assert(sizeof(QEntry) == kEncQEntry, "queue entry size");
 static_assert(kEncRingUnitMax <= kEncRing, "a ring share fits the ring");
 static_assert((kEncRing & (kEncRing - 1)) == 0, "ring positions stay contiguous across 32-bit wrap-around");
+
+// ---------------------------------------------------------------- raw bypass
+// [CCCL §3.3] leaves tensors uncompressed when compressing them does not pay;
+// [CCCL §5.2] falls back to the uncompressed data when the ratio is near or
+// above 1.  With ZC1's fixed-size main stream the comparison is exact: both
+// forms send the same main stream, the coded form n_esc escape bytes, the RAW
+// form max(0, 2n - 5632 ntiles) spill bytes; RAW is chosen exactly when n_esc
+// exceeds the spill (and the spill fits the escape buffer).
+
+// Tensor T goes RAW; a tensor whose codebook repeats an entry was not encoded
+// (reported) and stays as it is.  *overflow: the coded form stays and its
+// escapes did not fit.
+__device__ __forceinline__ bool goes_raw(const EncTensor& T, bool* overflow) {
+  *overflow = false;
+  bool dup = false;
+  for (int a = 0; a < 7; a++)
+    for (int b = a + 1; b < 7; b++) dup |= __ldg(T.cb + a) == __ldg(T.cb + b);
+  if (dup) return false;
+  const uint64_t n_esc = __ldcg(reinterpret_cast<const unsigned long long*>(T.main + 24));
+  const uint64_t spill = raw_spill(T.n);
+  if (n_esc > spill && spill <= T.esc_cap) return true;
+  *overflow = n_esc > T.esc_cap;
+  return false;
+}
+
+// Rewrites T as a RAW stream, 16-byte pieces over the threads of the grid: the
+// offset table zeroed, the tile region and the spill filled from the input
+// (zero past 2n).  The header is written afterwards by the last CTA.
+__device__ __forceinline__ void raw_rewrite(const EncTensor& T, uint64_t tid, uint64_t nthreads) {
+  constexpr int kUnroll = 4;  // 16-byte copies in flight per thread
+  const uint64_t ntiles = num_tiles(T.n);
+  const uint64_t tbl = table_bytes(ntiles);  // a multiple of 128
+  const uint64_t region = static_cast<uint64_t>(kTileBytes) * ntiles;
+  const uint64_t spill = raw_spill(T.n), two_n = 2 * T.n;
+  uint8_t* tiles = T.main + kHeader + tbl;
+  const uint64_t table_chunks = tbl / 16;
+  const uint64_t image_chunks = (region + spill + 15) / 16;
+  auto load = [&](uint64_t b) -> uint4 {
+    if (b + 16 <= two_n) return __ldg(reinterpret_cast<const uint4*>(T.in + b / 2));
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    for (uint32_t j = 0; b + 2 * j < two_n; j++)
+      w[j >> 1] |= static_cast<uint32_t>(__ldg(T.in + b / 2 + j)) << (16 * (j & 1));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  };
+  auto store = [&](uint64_t b, uint4 v) {
+    if (b < region) {
+      *reinterpret_cast<uint4*>(tiles + b) = v;  // zero past 2n: the tile region's tail
+      return;
+    }
+    uint8_t* dst = T.esc + (b - region);
+    const uint64_t left = spill - (b - region);  // spill bytes from here, even
+    if (left >= 16) {
+      *reinterpret_cast<uint4*>(dst) = v;
+    } else {
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      for (uint32_t j = 0; 2 * j < left; j++)
+        reinterpret_cast<uint16_t*>(dst)[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+    }
+  };
+  for (uint64_t c = tid; c < table_chunks; c += nthreads)
+    *reinterpret_cast<uint4*>(T.main + kHeader + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
+  for (uint64_t c0 = tid; c0 < image_chunks; c0 += kUnroll * nthreads) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; u++) {
+      const uint64_t c = c0 + u * nthreads;
+      v[u] = c < image_chunks ? load(16 * c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; u++) {
+      const uint64_t c = c0 + u * nthreads;
+      if (c < image_chunks) store(16 * c, v[u]);
+    }
+  }
+}
+
+// The raw bypass of an adaptive launch, run by every thread once its CTA's
+// encoding is done.  The CTAs meet at a grid barrier (the launch is
+// cooperative), so every tensor's n_esc is final; each CTA reads the counts
+// and reaches the same verdict.  In the usual case nothing goes RAW and that
+// is all: no further launch, no counter.  Otherwise every thread of the grid
+// rewrites the RAW tensors, and the last CTA to finish -- after every CTA has
+// read the counts -- writes their RAW headers (flags and n_esc).
+template <int MAXB>
+__device__ __forceinline__ void raw_bypass(const EncParams<MAXB>& p) {
+  static_assert(MAXB <= 32, "one mask bit per tensor");
+  __shared__ uint32_t raw_mask;
+  __shared__ int raw_ok;
+  __syncthreads();  // this CTA's streams, headers included, are written
+  if (threadIdx.x == 0) {
+    raw_mask = 0;
+    raw_ok = grid_barrier(&p.ws->raw_arrived, &p.ws->raw_gen, p.status);
+  }
+  __syncthreads();
+  if (raw_ok) {
+    for (int i = threadIdx.x; i < p.count; i += blockDim.x) {
+      bool overflow;
+      if (goes_raw(p.t[i], &overflow)) atomicOr(&raw_mask, 1u << i);
+      if (overflow && blockIdx.x == 0) set_status(p.status, ZC_ERR_ESCAPE_OVERFLOW);
+    }
+  }
+  __syncthreads();
+  const uint32_t mask = raw_mask;
+  if (mask == 0) return;  // every CTA reached the same verdict
+  const uint64_t tid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const uint64_t nthreads = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  for (int i = 0; i < p.count; i++)
+    if ((mask >> i) & 1u) raw_rewrite(p.t[i], tid, nthreads);
+  __syncthreads();
+  if (threadIdx.x == 0 && atom_add_acq_rel_gpu(&p.ws->raw_done, 1u) == gridDim.x - 1) {
+    for (int i = 0; i < p.count; i++) {
+      if (!((mask >> i) & 1u)) continue;
+      uint8_t* m = p.t[i].main;
+      *reinterpret_cast<uint32_t*>(m + 4) = ZC_VERSION | (kFlagRaw << 16);
+      *reinterpret_cast<unsigned long long*>(m + 24) = raw_spill(p.t[i].n);
+    }
+    p.ws->raw_done = 0;
+  }
+}
 
 template <int MAXB>
 __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_constant__ EncParams<MAXB> p) {
@@ -408,6 +527,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
     }
     while (fin < j) finish(fin++);  // drain
   }
+  if (p.adaptive) raw_bypass(p);
 }
 
 template <int MAXB>

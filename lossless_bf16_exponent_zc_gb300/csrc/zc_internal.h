@@ -68,16 +68,12 @@ cudaError_t launch_kernel(const void* fn, dim3 grid, dim3 block, int smem_bytes,
                           bool cooperative);
 
 // count <= kMaxBatch; flags = workspace flag array (one per tile of the launch).
-// adaptive: an escape overflow is not reported (launch_raw_switch decides).
+// adaptive: the raw bypass in the same launch -- each tensor whose coded form
+// has more escapes than its RAW spill (and whose spill fits its escape
+// capacity) is rewritten as a RAW stream, the escape overflow of the others is
+// reported.
 cudaError_t launch_encode(const EncTensor* ts, int count, WsHeader* ws, Flag* flags, int32_t* status,
                           cudaStream_t stream, const DeviceInfo& dev, bool adaptive = false);
-
-// The raw bypass after an adaptive launch_encode of the same tensors: rewrites
-// each tensor whose coded form has more escapes than its RAW spill (and whose
-// spill fits its escape capacity) as a RAW stream; reports the escape overflow
-// of the others.  count <= kMaxBatch.
-cudaError_t launch_raw_switch(const EncTensor* ts, int count, WsHeader* ws, int32_t* status, cudaStream_t stream,
-                              const DeviceInfo& dev);
 
 cudaError_t launch_decode(const DecTensor* ts, int count, int32_t* status, cudaStream_t stream,
                           const DeviceInfo& dev);

@@ -148,7 +148,6 @@ cudaError_t enqueue_pipeline(const uint16_t* in, uint64_t n, const uint8_t* cb, 
     if (k >= 2) ZC_TRY(cudaStreamWaitEvent(sc, ev.link[s], 0));
     EncTensor t{in + k * c, send_main(s), send_esc(s), cb, m, esc_cap};
     ZC_TRY(launch_encode(&t, 1, enc_ws, enc_flags, status, sc, enc_part, true));
-    ZC_TRY(launch_raw_switch(&t, 1, enc_ws, status, sc, enc_part));
     ZC_TRY(cudaEventRecord(ev.comp[s], sc));
     // link: the static part (fixed-size main stream) and the dynamic part
     // (n_esc escape bytes, counted on the device), once receive slot s is free
