@@ -475,56 +475,69 @@ def run_e2e(args, zc, torch, device, x, mb, eb, world):
     read from the downloaded header), upload both streams again into separate receive buffers, decode from
     those and download both decoded tensors.  The two codebooks' paths run on two streams (each with its own
     workspace), and the host waits for each path's main stream on an event, so one path's copies overlap the
-    other's kernels and the link carries both directions at once."""
+    other's kernels.  Consecutive steps use two buffer sets in turn, so one step's upload runs while the
+    previous step's results download (the link carries both directions at once); a set is reused only after
+    its previous step has finished."""
     n = x.size
     x_h = torch.from_numpy(x.view(np.int16)).pin_memory()
-    y_h = [torch.empty(n, dtype=torch.int16).pin_memory() for _ in range(2)]
-    m_h = [torch.empty(mb, dtype=torch.uint8).pin_memory() for _ in range(2)]
-    e_h = [torch.empty(eb, dtype=torch.uint8).pin_memory() for _ in range(2)]
-    xt = torch.empty(n, dtype=torch.int16, device=device)
-    mains = [torch.empty(mb, dtype=torch.uint8, device=device) for _ in range(2)]
-    escs = [torch.empty(eb, dtype=torch.uint8, device=device) for _ in range(2)]
-    r_mains = [torch.empty(mb, dtype=torch.uint8, device=device) for _ in range(2)]
-    r_escs = [torch.empty(eb, dtype=torch.uint8, device=device) for _ in range(2)]
-    ys = [torch.empty(n, dtype=torch.int16, device=device) for _ in range(2)]
-    wss = [zc.workspace(n, device=device) for _ in range(2)]
-    st = zc.new_status(device=device)
-    cbs = [torch.empty(7, dtype=torch.uint8, device=device) for _ in range(2)]
     cb_pinned = torch.empty(7, dtype=torch.uint8).pin_memory()
     cb_pinned.numpy()[:] = zc.codebook_from_sigma(SIGMA)
-    streams = [torch.cuda.current_stream(device), torch.cuda.Stream(device=device)]
-    ev_in = torch.cuda.Event()
-    ev_main = [torch.cuda.Event() for _ in range(2)]
+    st = zc.new_status(device=device)
+
+    def buffer_set():
+        return {
+            "y_h": [torch.empty(n, dtype=torch.int16).pin_memory() for _ in range(2)],
+            "m_h": [torch.empty(mb, dtype=torch.uint8).pin_memory() for _ in range(2)],
+            "e_h": [torch.empty(eb, dtype=torch.uint8).pin_memory() for _ in range(2)],
+            "xt": torch.empty(n, dtype=torch.int16, device=device),
+            "mains": [torch.empty(mb, dtype=torch.uint8, device=device) for _ in range(2)],
+            "escs": [torch.empty(eb, dtype=torch.uint8, device=device) for _ in range(2)],
+            "r_mains": [torch.empty(mb, dtype=torch.uint8, device=device) for _ in range(2)],
+            "r_escs": [torch.empty(eb, dtype=torch.uint8, device=device) for _ in range(2)],
+            "ys": [torch.empty(n, dtype=torch.int16, device=device) for _ in range(2)],
+            "wss": [zc.workspace(n, device=device) for _ in range(2)],
+            "cbs": [torch.empty(7, dtype=torch.uint8, device=device) for _ in range(2)],
+            "streams": [torch.cuda.Stream(device=device) for _ in range(2)],
+            "ev_in": torch.cuda.Event(), "ev_main": [torch.cuda.Event() for _ in range(2)],
+            "ev_done": torch.cuda.Event(), "used": False}
+    sets = [buffer_set(), buffer_set()]
     moved = [0, 0]
+    k_step = [0]
 
     def step():
-        s0, s1 = streams
+        S = sets[k_step[0] & 1]
+        k_step[0] += 1
+        if S["used"]:
+            S["ev_done"].synchronize()                           # this set's previous step has finished
+        S["used"] = True
+        s0, s1 = S["streams"]
+        xt, cbs, wss = S["xt"], S["cbs"], S["wss"]
         with torch.cuda.stream(s0):
             xt.copy_(x_h, non_blocking=True)
             cbs[1].copy_(cb_pinned, non_blocking=True)
-            ev_in.record(s0)
+            S["ev_in"].record(s0)
             zc.histogram_topk(xt, wss[0], st, cb_out=cbs[0], stream=s0)
-        s1.wait_event(ev_in)
+        s1.wait_event(S["ev_in"])
         for i in range(2):                                       # encode, then the static part
-            with torch.cuda.stream(streams[i]):
-                zc.compress(xt, cbs[i], wss[i], st, main=mains[i], esc=escs[i], stream=streams[i])
-                m_h[i].copy_(mains[i], non_blocking=True)
-                ev_main[i].record(streams[i])
+            with torch.cuda.stream(S["streams"][i]):
+                zc.compress(xt, cbs[i], wss[i], st, main=S["mains"][i], esc=S["escs"][i], stream=S["streams"][i])
+                S["m_h"][i].copy_(S["mains"][i], non_blocking=True)
+                S["ev_main"][i].record(S["streams"][i])
         ks = []
         for i in range(2):
-            ev_main[i].synchronize()                             # this path's main stream has arrived
-            k = int.from_bytes(m_h[i][24:32].numpy().tobytes(), "little")
+            S["ev_main"][i].synchronize()                        # this path's main stream has arrived
+            k = int.from_bytes(S["m_h"][i][24:32].numpy().tobytes(), "little")
             ks.append(k)
-            with torch.cuda.stream(streams[i]):
+            with torch.cuda.stream(S["streams"][i]):
                 if k:
-                    e_h[i][:k].copy_(escs[i][:k], non_blocking=True)  # the dynamic part
-                r_mains[i].copy_(m_h[i], non_blocking=True)            # the receiving side uploads what arrived
+                    S["e_h"][i][:k].copy_(S["escs"][i][:k], non_blocking=True)  # the dynamic part
+                S["r_mains"][i].copy_(S["m_h"][i], non_blocking=True)          # the receiving side uploads it
                 if k:
-                    r_escs[i][:k].copy_(e_h[i][:k], non_blocking=True)
-                zc.decompress(r_mains[i], r_escs[i], n, st, out=ys[i], stream=streams[i])
-                y_h[i].copy_(ys[i], non_blocking=True)
-        streams[0].wait_stream(streams[1])
-        torch.cuda.current_stream(device).synchronize()
+                    S["r_escs"][i][:k].copy_(S["e_h"][i][:k], non_blocking=True)
+                zc.decompress(S["r_mains"][i], S["r_escs"][i], n, st, out=S["ys"][i], stream=S["streams"][i])
+                S["y_h"][i].copy_(S["ys"][i], non_blocking=True)
+        s0.wait_stream(s1)
+        S["ev_done"].record(s0)
         streams_b = 2 * mb + sum(ks)
         moved[0] = 2 * n + 7 + streams_b
         moved[1] = streams_b + 2 * 2 * n
@@ -541,13 +554,14 @@ def run_e2e(args, zc, torch, device, x, mb, eb, world):
         step()
     torch.cuda.synchronize()
     dt = max_over_ranks(time.perf_counter() - t0, world, device)
-    if not (torch.equal(y_h[0], x_h) and torch.equal(y_h[1], x_h)):
+    if not all(torch.equal(y, x_h) for S in sets for y in S["y_h"]):
         raise SystemExit("end-to-end round trip mismatch")
     value = sum_over_ranks(4 * 2 * n, world, device) * steps / dt / 1e9
     return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": moved[0],
             "d2h_bytes_per_step": moved[1], "steps": steps,
             "path": "host tensor -> device -> histogram + 2 compress -> host streams -> device -> "
-                    "2 decompress -> host tensors, pinned buffers, one stream per codebook"}
+                    "2 decompress -> host tensors, pinned buffers, one stream per codebook, two buffer sets "
+                    "(a step's upload overlaps the previous step's downloads)"}
 
 
 # ------------------------------------------------------------------ per-workload section
