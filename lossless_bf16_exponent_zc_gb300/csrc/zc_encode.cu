@@ -204,7 +204,10 @@ __device__ __forceinline__ void raw_rewrite(const EncTensor& T, uint64_t tid, ui
 // and reaches the same verdict.  In the usual case nothing goes RAW and that
 // is all: no further launch, no counter.  Otherwise every thread of the grid
 // rewrites the RAW tensors, and the last CTA to finish -- after every CTA has
-// read the counts -- writes their RAW headers (flags and n_esc).
+// read the counts -- writes their RAW headers (flags and n_esc).  A CTA whose
+// barrier wait runs out (ZC_ERR_TIMEOUT, after an earlier wait of the launch
+// ran out) skips the bypass; as after any device error, the workspace is
+// zeroed again before it is reused.
 template <int MAXB>
 __device__ __forceinline__ void raw_bypass(const EncParams<MAXB>& p) {
   static_assert(MAXB <= 32, "one mask bit per tensor");

@@ -142,3 +142,33 @@ def test_escape_scan_wait_is_bounded(zc):
     assert zc.status_value(st2) == 0
     om, oe = oracle.compress(x, cb)
     assert np.array_equal(main.cpu().numpy(), om)
+
+
+def test_adaptive_launch_after_a_bounded_wait(zc):
+    """An adaptive launch ends at a grid barrier of its CTAs before the raw bypass.  With the hold hook its
+    escape scan times out (ZC_ERR_TIMEOUT) yet every CTA still reaches the barrier, so the launch returns, the
+    barrier's arrival count is back to 0, and the same workspace then compresses adaptively again, coded and
+    RAW, byte for byte as the oracle."""
+    n = 40 * 4096
+    x = workloads.gradient(n=n, seed=8)
+    cb = oracle.codebook_from_sigma(1e-3)
+    ws = zc.workspace(n)
+    ws[0:4] = torch.tensor([1, 0, 0, 0], dtype=torch.uint8, device="cuda")   # hold unit 0
+    st = zc.new_status()
+    zc.compress_adaptive(dev(x), zc.codebook_to_device(cb), ws, st)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == zc.ERR_TIMEOUT
+    hdr = ws[:32].cpu().numpy().view(np.uint32)
+    assert hdr[0] == 0 and hdr[1] == 0           # hook and exit counter reset
+    assert hdr[5] == 0 and hdr[6] == 0           # RAW rewrite counter and barrier arrivals back to 0
+    gen = int(hdr[7])
+    for data, book in ((x, cb), (workloads.random_bits(n, seed=9), np.array([1, 2, 3, 4, 5, 6, 7], np.uint8))):
+        st2 = zc.new_status()
+        main, esc = zc.compress_adaptive(dev(data), zc.codebook_to_device(book), ws, st2)
+        torch.cuda.synchronize()
+        assert zc.status_value(st2) == 0
+        om, oe, _ = oracle.compress_adaptive(data, book)
+        assert np.array_equal(main.cpu().numpy(), om)
+        assert np.array_equal(esc[:oe.size].cpu().numpy(), oe)
+    hdr = ws[:32].cpu().numpy().view(np.uint32)
+    assert hdr[6] == 0 and int(hdr[7]) == gen + 2  # one barrier per launch
