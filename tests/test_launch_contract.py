@@ -50,7 +50,7 @@ def test_every_kernel_waits_for_its_predecessor_first():
             # nothing before the wait may touch global memory
             assert not re.search(r"\bp\.|__ldg|ld_relaxed|st_relaxed|atomic|tma_|cp_async", before), \
                 f"{name}: {kernel} accesses memory before pdl_begin()"
-    assert found >= 8  # encode, decode, reduce, histogram, raw switch, pipeline link, QLC encode and decode
+    assert found >= 7  # encode (with its raw bypass), decode, reduce, histogram, pipeline link, QLC encode and decode
 
 
 def test_no_triple_chevron_launches():
