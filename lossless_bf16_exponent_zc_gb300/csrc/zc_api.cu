@@ -13,7 +13,25 @@
 #include "zc_device.cuh"
 #include "zc_internal.h"
 
+#ifndef ZC_NO_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 using namespace zc;
+
+namespace {
+// An NVTX range named after the entry point around each call that enqueues
+// device work, so a profiler attributes kernels to the library call that
+// launched them (a pointer check per push and pop when no tool is attached).
+struct ApiRange {
+#ifndef ZC_NO_NVTX
+  explicit ApiRange(const char* name) { nvtxRangePushA(name); }
+  ~ApiRange() { nvtxRangePop(); }
+#else
+  explicit ApiRange(const char*) {}
+#endif
+};
+}  // namespace
 
 namespace {
 
@@ -188,6 +206,7 @@ zc_status zc_workspace_size(const uint64_t* h_ns, int count, uint64_t* bytes) {
 
 zc_status zc_histogram_topk(const void* d_in, uint64_t n, uint8_t* d_cb_out, uint32_t* d_hist_out, void* d_ws,
                             uint64_t ws_bytes, int32_t* d_status, void* stream) {
+  const ApiRange range_("zc_histogram_topk");
   if ((!d_in && n) || !d_cb_out || !d_status) return ZC_ERR_INVALID_ARG;
   if (n > kMaxN) return ZC_ERR_TOO_LARGE;
   if (!aligned(d_in, 16) || !aligned(d_status, 4) || (d_hist_out && !aligned(d_hist_out, 4)))
@@ -223,11 +242,13 @@ static zc_status compress_one(const void* d_in, uint64_t n, const uint8_t* d_cb,
 }
 zc_status zc_compress(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_main, void* d_esc,
                       uint64_t esc_capacity, void* d_ws, uint64_t ws_bytes, int32_t* d_status, void* stream) {
+  const ApiRange range_("zc_compress");
   return compress_one(d_in, n, d_cb, d_main, d_esc, esc_capacity, d_ws, ws_bytes, d_status, stream, false);
 }
 zc_status zc_compress_adaptive(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_main, void* d_esc,
                                uint64_t esc_capacity, void* d_ws, uint64_t ws_bytes, int32_t* d_status,
                                void* stream) {
+  const ApiRange range_("zc_compress_adaptive");
   return compress_one(d_in, n, d_cb, d_main, d_esc, esc_capacity, d_ws, ws_bytes, d_status, stream, true);
 }
 zc_status zc_raw_spill(uint64_t n, uint64_t* bytes) {
@@ -247,6 +268,7 @@ static zc_status validate_decode_tensor(const void* main, const void* esc, uint6
 
 zc_status zc_decompress(const void* d_main, const void* d_esc, uint64_t esc_bytes, uint64_t n, void* d_out,
                         int32_t* d_status, void* stream) {
+  const ApiRange range_("zc_decompress");
   if (!d_status) return ZC_ERR_INVALID_ARG;
   if (!aligned(d_status, 4)) return ZC_ERR_ALIGNMENT;
   if (zc_status s = validate_decode_tensor(d_main, d_esc, esc_bytes, n, d_out)) return s;
@@ -261,6 +283,7 @@ zc_status zc_decompress_reduce(int P, const void* const* h_mains, const void* co
                                const uint64_t* h_esc_bytes, uint64_t n, void* d_out, const uint8_t* d_out_cb,
                                void* d_out_main, void* d_out_esc, uint64_t out_esc_capacity, void* d_ws,
                                uint64_t ws_bytes, int32_t* d_status, void* stream) {
+  const ApiRange range_("zc_decompress_reduce");
   if (P < 1 || P > ZC_MAX_SHARDS || !h_mains || !h_escs || !h_esc_bytes || !d_status) return ZC_ERR_INVALID_ARG;
   if (n > kMaxN) return ZC_ERR_TOO_LARGE;
   if (!aligned(d_status, 4) || !aligned(d_out, 16)) return ZC_ERR_ALIGNMENT;
@@ -319,10 +342,12 @@ static zc_status compress_batched(int count, const zc_tensor* h_tensors, void* d
 }
 zc_status zc_compress_batched(int count, const zc_tensor* h_tensors, void* d_ws, uint64_t ws_bytes,
                               int32_t* d_status, void* stream) {
+  const ApiRange range_("zc_compress_batched");
   return compress_batched(count, h_tensors, d_ws, ws_bytes, d_status, stream, false);
 }
 zc_status zc_compress_batched_adaptive(int count, const zc_tensor* h_tensors, void* d_ws, uint64_t ws_bytes,
                                        int32_t* d_status, void* stream) {
+  const ApiRange range_("zc_compress_batched_adaptive");
   return compress_batched(count, h_tensors, d_ws, ws_bytes, d_status, stream, true);
 }
 
@@ -343,6 +368,7 @@ static zc_status pipeline_args_ok(const void* d_in, uint64_t n, const uint8_t* d
 zc_status zc_pipeline_plan_create(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_out,
                                   uint64_t chunk_elems, void* d_ws, uint64_t ws_bytes, int32_t* d_status,
                                   int overlap, zc_pipeline_plan* plan) {
+  const ApiRange range_("zc_pipeline_plan_create");
   if (!plan) return ZC_ERR_INVALID_ARG;
   *plan = nullptr;
   const zc_status a = pipeline_args_ok(d_in, n, d_cb, d_out, chunk_elems, d_ws, ws_bytes, d_status);
@@ -362,6 +388,7 @@ zc_status zc_pipeline_plan_create(const void* d_in, uint64_t n, const uint8_t* d
   return ZC_OK;
 }
 zc_status zc_pipeline_plan_launch(zc_pipeline_plan plan, void* stream) {
+  const ApiRange range_("zc_pipeline_plan_launch");
   if (!plan) return ZC_ERR_INVALID_ARG;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return ZC_ERR_CUDA;
@@ -384,6 +411,7 @@ zc_status zc_pipeline_workspace_size(uint64_t chunk_elems, uint64_t* bytes) {
 zc_status zc_pipelined_transfer(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_out,
                                 uint64_t chunk_elems, void* d_ws, uint64_t ws_bytes, int32_t* d_status,
                                 void* stream_compress, void* stream_link, void* stream_decompress) {
+  const ApiRange range_("zc_pipelined_transfer");
   const zc_status a = pipeline_args_ok(d_in, n, d_cb, d_out, chunk_elems, d_ws, ws_bytes, d_status);
   if (a != ZC_OK) return a;
   DeviceInfo dev;
@@ -470,6 +498,7 @@ zc_status zq_max_bytes(uint64_t n, uint64_t* bytes) {
 }
 zc_status zq_compress(const void* d_in, uint64_t n, const zq_table* h_table, void* d_out, uint64_t out_capacity,
                       void* d_ws, uint64_t ws_bytes, int32_t* d_status, void* stream) {
+  const ApiRange range_("zq_compress");
   if (!d_status || !h_table || !d_out || (!d_in && n)) return ZC_ERR_INVALID_ARG;
   if (n > kMaxN) return ZC_ERR_TOO_LARGE;
   if (!aligned(d_in, 16) || !aligned(d_out, 16) || !aligned(d_status, 4)) return ZC_ERR_ALIGNMENT;
@@ -485,6 +514,7 @@ zc_status zq_compress(const void* d_in, uint64_t n, const zq_table* h_table, voi
 }
 zc_status zq_decompress(const void* d_in, uint64_t in_bytes, uint64_t n, void* d_out, int32_t* d_status,
                         void* stream) {
+  const ApiRange range_("zq_decompress");
   if (!d_status || !d_in || (!d_out && n)) return ZC_ERR_INVALID_ARG;
   if (n > kMaxN) return ZC_ERR_TOO_LARGE;
   if (!aligned(d_in, 16) || !aligned(d_out, 16) || !aligned(d_status, 4)) return ZC_ERR_ALIGNMENT;
@@ -495,6 +525,7 @@ zc_status zq_decompress(const void* d_in, uint64_t in_bytes, uint64_t n, void* d
                                       d_status, as_stream(stream), dev));
 }
 zc_status zc_decompress_batched(int count, const zc_tensor* h_tensors, int32_t* d_status, void* stream) {
+  const ApiRange range_("zc_decompress_batched");
   if (count < 1 || !h_tensors || !d_status) return ZC_ERR_INVALID_ARG;
   if (!aligned(d_status, 4)) return ZC_ERR_ALIGNMENT;
   for (int i = 0; i < count; i++) {

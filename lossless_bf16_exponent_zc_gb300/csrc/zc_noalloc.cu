@@ -17,6 +17,10 @@
 #include "zc_device.cuh"
 #include "zc_internal.h"
 
+#ifndef ZC_NO_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 namespace {
 
 // Largest tensor this entry point encodes: 2^28 values (512 MiB of bf16).
@@ -49,10 +53,19 @@ zc_status scratch_for_current_device(void** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The call's NVTX range (as for the other entry points that enqueue work).
+struct NoAllocRange {
+#ifndef ZC_NO_NVTX
+  NoAllocRange() { nvtxRangePushA("zc_compress_noalloc"); }
+  ~NoAllocRange() { nvtxRangePop(); }
+#endif
+};
+
 }  // namespace
 
 extern "C" zc_status zc_compress_noalloc(const void* d_in, uint64_t n, const uint8_t* d_cb, void* d_main, void* d_esc,
                                          uint64_t esc_capacity, int32_t* d_status, void* stream) {
+  const NoAllocRange range_;
   if (!d_status || !d_main || !d_cb || (!d_in && n) || (!d_esc && esc_capacity)) return ZC_ERR_INVALID_ARG;
   if (n > kNoAllocMaxElems) return ZC_ERR_WORKSPACE;  // the fixed scratch covers at most 2^28 values
   if (!aligned16(d_in) || !aligned16(d_main) || !aligned16(d_esc) || (reinterpret_cast<uintptr_t>(d_status) & 3u))
