@@ -141,3 +141,112 @@ def zipped_reduce_scatter(x: torch.Tensor, cb_in: torch.Tensor, status: torch.Te
     out, out_main, out_esc = zc.decompress_reduce(recv_mains, recv_escs, m, status, out_cb=out_cb, ws=ws,
                                                   esc_bytes=k_in)
     return out, out_main, out_esc
+
+
+# ------------------------------------------------------------------ the reduce-scatter switcher [ZipCCL §2.D]
+def _max_over(value: float, group, device) -> float:
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def profile_link(group=None, small_bytes: int = 1 << 10, large_bytes: int = 1 << 24, reps: int = 5,
+                 device=None) -> tuple[float, float]:
+    """(bandwidth in GB/s per rank and direction, latency in us) of the group's point-to-point path, measured the
+    way the zipped exchange moves data: every rank exchanges one message with every other rank at once
+    (batch_isend_irecv), once with a small message (its time is the latency) and once with a large one (the extra
+    bytes over the extra time give the bandwidth).  Each time is the median of `reps` exchanges after one untimed
+    one, taken as the slowest rank's (so every rank gets the same model).  device: where the buffers live (the
+    current CUDA device for NCCL, the CPU for gloo).  A group of one rank has no link: (inf, 0)."""
+    import statistics
+    import time
+    rank, world = dist.get_rank(group), dist.get_world_size(group)
+    if world == 1:
+        return float("inf"), 0.0
+    if device is None:
+        device = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend(group) == "nccl" else "cpu"
+    on_gpu = torch.device(device).type == "cuda"
+
+    def exchange_time(nbytes: int) -> float:
+        send = [torch.zeros(nbytes, dtype=torch.uint8, device=device) for _ in range(world)]
+        recv = [torch.empty(nbytes, dtype=torch.uint8, device=device) for _ in range(world)]
+        ops = [op for p in range(world) if p != rank
+               for op in (dist.P2POp(dist.isend, send[p], _peer(p, group), group),
+                          dist.P2POp(dist.irecv, recv[p], _peer(p, group), group))]
+        times = []
+        for i in range(reps + 1):
+            dist.barrier(group=group)
+            if on_gpu:
+                torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            _run(ops)
+            if on_gpu:
+                torch.cuda.synchronize()
+            if i:
+                times.append(time.perf_counter() - t0)
+        return _max_over(statistics.median(times), group, device)
+
+    t_small = exchange_time(small_bytes)
+    t_large = exchange_time(large_bytes)
+    extra = (world - 1) * (large_bytes - small_bytes)  # bytes each rank sends beyond the small exchange
+    bandwidth = extra / max(t_large - t_small, 1e-9) / 1e9
+    return bandwidth, t_small * 1e6
+
+
+def profile_codec(sample: torch.Tensor, cb: torch.Tensor, status: torch.Tensor, P: int = 8,
+                  reps: int = 10) -> tuple[float, float, float]:
+    """(compress GB/s, decode-reduce GB/s, ratio) of libzc on a sample of the caller's data (a bf16 device tensor):
+    compress throughput of the sample's 2n bytes, zc_decompress_reduce throughput over P copies of its stream per
+    byte of the P inputs (the figure the reduce-scatter model takes for the receiving side), and the ratio 2n /
+    (main stream + escapes).  CUDA events on the current stream."""
+    n = sample.numel()
+    ws = zc.workspace(n, device=sample.device)
+    main, esc = zc.compress(sample, cb, ws, status)
+    k = zc.header_n_esc(main)
+
+    def timed(fn) -> float:
+        fn()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            fn()
+        e.record()
+        e.synchronize()
+        return s.elapsed_time(e) / reps * 1e-3  # seconds
+
+    t_c = timed(lambda: zc.compress(sample, cb, ws, status, main=main, esc=esc))
+    out = torch.empty(n, dtype=torch.int16, device=sample.device)
+    t_d = timed(lambda: zc.decompress_reduce([main] * P, [esc] * P, n, status, out=out, esc_bytes=[k] * P))
+    return 2 * n / t_c / 1e9, 2 * n * P / t_d / 1e9, 2 * n / (main.numel() + k)
+
+
+class ReduceScatterSwitcher:
+    """The reduce-scatter switcher of [ZipCCL §2.D]: it profiles the link (bandwidth, latency) and the codec
+    (throughput, ratio on a sample of the caller's data) once, when it is made, and then for each tensor picks
+    the native reduce-scatter (torch.distributed.reduce_scatter_tensor, summed the collective library's way) or
+    the zipped one (zipped_reduce_scatter: fp32 sums in rank order, one rounding) by zc_reduce_scatter_choose's two
+    time estimates.  link / codec: measured figures to use instead of profiling ((GB/s, us) and (GB/s, GB/s,
+    ratio))."""
+
+    def __init__(self, sample: torch.Tensor, cb: torch.Tensor, status: torch.Tensor, group=None,
+                 link: tuple[float, float] | None = None, codec: tuple[float, float, float] | None = None):
+        self.group, self.cb, self.status = group, cb, status
+        self.world = dist.get_world_size(group)
+        self.link = link if link is not None else profile_link(group, device=sample.device)
+        self.codec = codec if codec is not None else profile_codec(sample, cb, status, P=max(self.world, 1))
+
+    def zipped(self, nbytes: int) -> bool:
+        """True when the zipped reduce-scatter of nbytes per rank is estimated to be faster (one rank: never)."""
+        if self.world == 1:
+            return False
+        z, _, _ = zc.reduce_scatter_choose(int(nbytes), self.world, self.link[0], self.link[1], *self.codec)
+        return z
+
+    def __call__(self, x: torch.Tensor, out_cb: torch.Tensor | None = None, ws: torch.Tensor | None = None):
+        """Reduce-scatter (sum) of x (bf16 bits, P * m values) over the group; returns this rank's shard."""
+        if self.zipped(2 * x.numel()):
+            return zipped_reduce_scatter(x, self.cb, self.status, out_cb=out_cb, ws=ws, group=self.group)[0]
+        m = x.numel() // self.world
+        out = torch.empty(m, dtype=torch.bfloat16, device=x.device)
+        dist.reduce_scatter_tensor(out, x.view(torch.bfloat16), group=self.group)
+        return out.view(torch.int16)

@@ -4,8 +4,9 @@ exchange.exchange_streams -- the same code that moves device buffers over NCCL. 
 escape stream and escape count must equal what its sender wrote, byte for byte; pieces differ in size per
 pair (ragged), and some are RAW (incompressible data) or have no escapes at all.  Then the reduce-scatter
 semantics: rank r receives shard r of every rank, and the oracle's decode-reduce of what arrived must equal the
-rank-order fp32 sum of the shards' values (torch), rounded to bf16.  No kernel runs here; the device path
-(libzc compress -> exchange -> zc_decompress_reduce) is checked on the GPU.
+rank-order fp32 sum of the shards' values (torch), rounded to bf16.  Then the reduce-scatter switcher: its link
+profile (timed exchanges) and its choice on a given model.  No kernel runs here; the device path (libzc compress
+-> exchange -> zc_decompress_reduce, the codec profile) is checked on the GPU.
 """
 import os
 import socket
@@ -86,6 +87,22 @@ def _worker(rank, world, port, q):
             acc = acc + torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).float()
         want = acc.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
         assert np.array_equal(y, want), "reduced shard"
+        # 3. the switcher's start-up profile of the link: finite, positive and the same on every rank
+        bw, lat = exchange.profile_link(device="cpu", large_bytes=1 << 20, reps=3)
+        assert np.isfinite(bw) and bw > 0 and np.isfinite(lat) and lat > 0
+        got = [None] * world
+        dist.all_gather_object(got, (bw, lat))
+        assert all(g == (bw, lat) for g in got)
+        # and its choice is zc_reduce_scatter_choose's on the model it holds (no device work)
+        from lossless_bf16_exponent_zc_gb300 import zc
+        codec = (800.0, 600.0, 1.4)
+        for link in ((1.0, 5.0), (50.0, 5.0), (1e6, 1.0)):
+            sw = exchange.ReduceScatterSwitcher(torch.empty(0), None, None, link=link, codec=codec)
+            for nbytes in (1 << 10, 1 << 20, 1 << 28):
+                assert sw.zipped(nbytes) == zc.reduce_scatter_choose(nbytes, world, *link, *codec)[0]
+        slow = exchange.ReduceScatterSwitcher(torch.empty(0), None, None, link=(1.0, 5.0), codec=codec)
+        fast = exchange.ReduceScatterSwitcher(torch.empty(0), None, None, link=(1e6, 1.0), codec=codec)
+        assert slow.zipped(1 << 28) and not fast.zipped(1 << 28)
         dist.barrier()
         dist.destroy_process_group()
         q.put((rank, True, ""))

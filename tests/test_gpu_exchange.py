@@ -61,6 +61,18 @@ def _child(port, q):
         assert np.array_equal(yt.cpu().numpy().view(np.uint16), oy), "reduced shard"
         k = zc.header_n_esc(om)
         assert np.array_equal(om.cpu().numpy(), omain) and np.array_equal(oe[:k].cpu().numpy(), oesc)
+        # the switcher on one rank: no link, the codec profiled on a sample, the native path chosen
+        bw, lat = exchange.profile_link()
+        assert bw == float("inf") and lat == 0.0
+        sample = torch.from_numpy(workloads.gaussian(1 << 20, sigma=1e-3, seed=24).view(np.int16)).cuda()
+        cgbps, dgbps, ratio = exchange.profile_codec(sample, zc.codebook_to_device(cb), st, P=4, reps=3)
+        sm, se = oracle.compress(sample.cpu().numpy().view(np.uint16), cb)
+        assert cgbps > 0 and dgbps > 0 and abs(ratio - 2 * (1 << 20) / (sm.size + se.size)) < 1e-9
+        sw = exchange.ReduceScatterSwitcher(sample, zc.codebook_to_device(cb), st)
+        assert not sw.zipped(1 << 30)
+        assert torch.equal(sw(sample), sample)  # one rank: its shard is the whole tensor
+        torch.cuda.synchronize()
+        assert zc.status_value(st) == 0
         dist.destroy_process_group()
         q.put((True, ""))
     except Exception:
