@@ -348,7 +348,7 @@ zc_status zc_pipelined_transfer(const void* d_in, uint64_t n, const uint8_t* d_c
  * Pipeline plan: the launch sequence of one zc_pipelined_transfer call (same
  * arguments, same checks, same errors), captured once into an instantiated
  * CUDA graph and replayed by zc_pipeline_plan_launch with a single launch.
- * Each chunk costs five kernel launches and six event operations; once chunks
+ * Each chunk costs three kernel launches and up to seven event operations; once chunks
  * are small the host submits them more slowly than the GPU runs them, and a
  * replay removes that cost.
  *   - overlap != 0: captured from three private streams, so the graph keeps

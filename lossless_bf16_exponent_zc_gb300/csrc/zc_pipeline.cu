@@ -16,7 +16,7 @@
 // compressed adaptively, so an incompressible chunk travels RAW and an escape
 // slot of 5/8 of the chunk's values never overflows.
 //
-// Each chunk costs five launches and six event operations, which the host
+// Each chunk costs three launches and up to seven event operations, which the host
 // submits more slowly than the GPU runs them once chunks are small.  A
 // pipeline plan captures the whole launch sequence once into a CUDA graph
 // (from three private streams, so the graph keeps the three-stage overlap) and
