@@ -127,9 +127,16 @@ def test_worked_example_fixture(zc):
 
 
 # ------------------------------------------------------------------ histogram
-@pytest.mark.parametrize("n", [0, 1, 9, 4096 * 3 + 3, 1 << 20])
-def test_histogram_small(zc, n):
-    x = workloads.gradient(n=n, seed=21) if n else np.zeros(0, np.uint16)
+# sizes around the kernel's pieces: the tail of fewer than 8 values counted with plain loads, 32 KB chunks of
+# 16384 values (one partial), one chunk per CTA of a full grid and one more; random bits fill all 256 bins
+@pytest.mark.parametrize("n,kind", [(0, "g"), (1, "g"), (7, "g"), (8, "g"), (9, "g"), (4096 * 3 + 3, "g"),
+                                    (16383, "g"), (16384, "g"), (16385, "g"), (16384 * 152 + 29, "g"),
+                                    (16384 * 153, "g"), (1 << 20, "g"), (16384 * 5 + 13, "r")])
+def test_histogram_small(zc, n, kind):
+    if not n:
+        x = np.zeros(0, np.uint16)
+    else:
+        x = workloads.gradient(n=n, seed=21) if kind == "g" else workloads.random_bits(n, seed=22)
     st = zc.new_status()
     ws = zc.workspace(n)
     hist = torch.zeros(256, dtype=torch.int32, device="cuda")

@@ -157,3 +157,28 @@ def test_plan_empty(zc):
     plan.close()
     with pytest.raises(RuntimeError):
         plan.launch()
+
+
+def test_plan_first_call_in_a_fresh_process():
+    """A plan made before any other libzc call: each kernel's one-time preparation (shared-memory limit,
+    occupancy) then happens while the launch sequence is being captured.  Run in a fresh interpreter."""
+    import subprocess
+    import sys
+    code = r'''
+import numpy as np, torch, workloads, oracle
+from lossless_bf16_exponent_zc_gb300 import zc
+n, chunk = (1 << 20) + 24, 1 << 18
+x = workloads.gradient(n=n, sigma=1e-3, seed=3)
+xt = torch.from_numpy(x.view(np.int16)).cuda()
+plan = zc.pipeline_plan(xt, zc.codebook_to_device(oracle.codebook_from_sigma(1e-3)), chunk,
+                        zc.pipeline_workspace(chunk), zc.new_status())
+out = plan.launch()
+torch.cuda.synchronize()
+assert zc.status_value(plan.status) == 0
+assert np.array_equal(out.cpu().numpy().view(np.uint16), x)
+print("ok")
+'''
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
