@@ -57,6 +57,9 @@ def parse_args(argv=None):
     p.add_argument("--sweep-max-log2", type=int, default=29, help="largest reduce-scatter shard (elements)")
     p.add_argument("--profile", action="store_true",
                    help="for profiler runs: no clock sampling, no soak, no e2e, CPU or workload legs")
+    p.add_argument("--profile-pipeline", type=int, default=0, metavar="LOG2_CHUNK",
+                   help="for profiler runs: only the transfer pipeline plan on 2^26 values in chunks of "
+                        "2^LOG2_CHUNK (three streams), replayed 3 times, checked, no JSON line")
     a = p.parse_args(argv)
     if a.profile:
         a.no_e2e = a.no_cpu_baseline = a.no_workloads = True
@@ -909,8 +912,29 @@ def run_workloads(args, zc, torch, device, peak):
     return out
 
 
+def profile_pipeline(log2_chunk: int) -> int:
+    """The transfer pipeline plan alone, for a profiler's launch list: 2^26 N(0, 1e-3) values through compress
+    -> link -> decompress in chunks of 2^log2_chunk on three streams, replayed three times, output checked."""
+    import torch
+    from lossless_bf16_exponent_zc_gb300 import zc
+    n, chunk = 1 << 26, 1 << log2_chunk
+    xt = torch.from_numpy(workloads.gaussian(n, sigma=workloads.RS_SIGMA, seed=6).view(np.int16)).cuda()
+    cb = zc.codebook_to_device(zc.codebook_from_sigma(workloads.RS_SIGMA))
+    st = zc.new_status()
+    plan = zc.pipeline_plan(xt, cb, chunk, zc.pipeline_workspace(chunk), st)
+    for _ in range(3):
+        out = plan.launch()
+    torch.cuda.synchronize()
+    if zc.status_value(st) != 0 or not torch.equal(out, xt):
+        raise SystemExit("pipeline round trip failed")
+    plan.close()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.profile_pipeline:
+        return profile_pipeline(args.profile_pipeline)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
