@@ -478,9 +478,10 @@ def run_e2e(args, zc, torch, device, x, mb, eb, world):
     read from the downloaded header), upload both streams again into separate receive buffers, decode from
     those and download both decoded tensors.  The two codebooks' paths run on two streams (each with its own
     workspace), and the host waits for each path's main stream on an event, so one path's copies overlap the
-    other's kernels.  Consecutive steps use two buffer sets in turn, so one step's upload runs while the
-    previous step's results download (the link carries both directions at once); a set is reused only after
-    its previous step has finished."""
+    other's kernels.  Steps are software-pipelined over three buffer sets: step k + 1 uploads, encodes and
+    downloads its main streams before step k's receiving side is enqueued, so the link carries both directions
+    at once and the download queue never waits for an upload; a set is reused only after its previous step
+    has finished."""
     n = x.size
     x_h = torch.from_numpy(x.view(np.int16)).pin_memory()
     cb_pinned = torch.empty(7, dtype=torch.uint8).pin_memory()
@@ -503,13 +504,12 @@ def run_e2e(args, zc, torch, device, x, mb, eb, world):
             "streams": [torch.cuda.Stream(device=device) for _ in range(2)],
             "ev_in": torch.cuda.Event(), "ev_main": [torch.cuda.Event() for _ in range(2)],
             "ev_done": torch.cuda.Event(), "used": False}
-    sets = [buffer_set(), buffer_set()]
+    sets = [buffer_set() for _ in range(3)]
     moved = [0, 0]
-    k_step = [0]
 
-    def step():
-        S = sets[k_step[0] & 1]
-        k_step[0] += 1
+    def begin(k):
+        """Step k, first half: upload, codebooks, encode, download the main streams (static part)."""
+        S = sets[k % 3]
         if S["used"]:
             S["ev_done"].synchronize()                           # this set's previous step has finished
         S["used"] = True
@@ -521,22 +521,28 @@ def run_e2e(args, zc, torch, device, x, mb, eb, world):
             S["ev_in"].record(s0)
             zc.histogram_topk(xt, wss[0], st, cb_out=cbs[0], stream=s0)
         s1.wait_event(S["ev_in"])
-        for i in range(2):                                       # encode, then the static part
+        for i in range(2):
             with torch.cuda.stream(S["streams"][i]):
                 zc.compress(xt, cbs[i], wss[i], st, main=S["mains"][i], esc=S["escs"][i], stream=S["streams"][i])
                 S["m_h"][i].copy_(S["mains"][i], non_blocking=True)
                 S["ev_main"][i].record(S["streams"][i])
+
+    def finish(k):
+        """Step k, second half: escapes sized from the downloaded headers, the receiving side's uploads,
+        decode, download of the decoded tensors."""
+        S = sets[k % 3]
+        s0, s1 = S["streams"]
         ks = []
         for i in range(2):
             S["ev_main"][i].synchronize()                        # this path's main stream has arrived
-            k = int.from_bytes(S["m_h"][i][24:32].numpy().tobytes(), "little")
-            ks.append(k)
+            kk = int.from_bytes(S["m_h"][i][24:32].numpy().tobytes(), "little")
+            ks.append(kk)
             with torch.cuda.stream(S["streams"][i]):
-                if k:
-                    S["e_h"][i][:k].copy_(S["escs"][i][:k], non_blocking=True)  # the dynamic part
-                S["r_mains"][i].copy_(S["m_h"][i], non_blocking=True)          # the receiving side uploads it
-                if k:
-                    S["r_escs"][i][:k].copy_(S["e_h"][i][:k], non_blocking=True)
+                if kk:
+                    S["e_h"][i][:kk].copy_(S["escs"][i][:kk], non_blocking=True)  # the dynamic part
+                S["r_mains"][i].copy_(S["m_h"][i], non_blocking=True)            # the receiving side uploads it
+                if kk:
+                    S["r_escs"][i][:kk].copy_(S["e_h"][i][:kk], non_blocking=True)
                 zc.decompress(S["r_mains"][i], S["r_escs"][i], n, st, out=S["ys"][i], stream=S["streams"][i])
                 S["y_h"][i].copy_(S["ys"][i], non_blocking=True)
         s0.wait_stream(s1)
@@ -545,16 +551,22 @@ def run_e2e(args, zc, torch, device, x, mb, eb, world):
         moved[0] = 2 * n + 7 + streams_b
         moved[1] = streams_b + 2 * 2 * n
 
-    for _ in range(max(3, args.warmup)):
-        step()
+    def run(count):
+        """count whole steps, software-pipelined: step k + 1 begins before step k finishes."""
+        begin(0)
+        for k in range(count):
+            if k + 1 < count:
+                begin(k + 1)
+            finish(k)
+
+    run(max(3, args.warmup))
     steps = max(5, args.steps // 10)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(steps):
-        step()
+    run(steps)
     torch.cuda.synchronize()
     dt = max_over_ranks(time.perf_counter() - t0, world, device)
     if not all(torch.equal(y, x_h) for S in sets for y in S["y_h"]):
@@ -563,8 +575,8 @@ def run_e2e(args, zc, torch, device, x, mb, eb, world):
     return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": moved[0],
             "d2h_bytes_per_step": moved[1], "steps": steps,
             "path": "host tensor -> device -> histogram + 2 compress -> host streams -> device -> "
-                    "2 decompress -> host tensors, pinned buffers, one stream per codebook, two buffer sets "
-                    "(a step's upload overlaps the previous step's downloads)"}
+                    "2 decompress -> host tensors, pinned buffers, one stream per codebook, steps "
+                    "software-pipelined over three buffer sets"}
 
 
 # ------------------------------------------------------------------ per-workload section
