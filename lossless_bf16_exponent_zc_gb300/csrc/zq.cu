@@ -19,12 +19,13 @@
 //     and keeps them on chip while its scan warp finds the group's offset
 //     from the totals other CTAs publish (the escape scan's window sums and
 //     epoch protocol, cooperative launch); a block is stored one round later.
-//   * Decoder: the block's words are copied to shared memory with batches of
-//     independent coalesced loads; each lane decodes its runs with a 32-bit
-//     funnel-shift window over two words and a 2048-entry table indexed by
-//     the next 11 bits, which gives the symbol and its code length in one
-//     shared load; two symbols are decoded per window refill (a code is at
-//     most 11 bits, so the second one still lies within the next two words).
+//   * Decoder: the block's words arrive in shared memory with one TMA bulk
+//     copy per block (the block offsets are read one block ahead); each lane
+//     decodes its runs with a 32-bit funnel-shift window over two words and a
+//     2048-entry table indexed by the next 11 bits, which gives the symbol and
+//     its code length in one shared load; two symbols are decoded per window
+//     refill (a code is at most 11 bits, so the second one still lies within
+//     the next two words).
 #include "zc_device.cuh"
 #include "zc_internal.h"
 
@@ -38,7 +39,7 @@ constexpr uint32_t kQBlockWordsMax = 8 + 32 * kQLaneWordsMax;  // 1416
 constexpr uint32_t kQLaneStride = 45;           // words per lane buffer (odd: no bank conflicts)
 constexpr int kQEncWarps = 16;                 // coding warps; a group is 16 blocks
 constexpr int kQEncThreads = (kQEncWarps + 1) * 32;  // + the scan warp
-constexpr int kQDecWarps = 8;
+constexpr int kQDecWarps = 12;                 // 3 CTAs per SM: 36 decoding warps
 
 __host__ __device__ __forceinline__ uint64_t zq_blocks(uint64_t n) { return (n + kQBlock - 1) / kQBlock; }
 __host__ __device__ __forceinline__ uint64_t zq_table_bytes(uint64_t nb) { return (4 * nb + 127) / 128 * 128; }
@@ -256,16 +257,25 @@ struct QDecParams {
   int32_t* status;
 };
 
+// A warp's block buffer: the block lands at word (offset mod 4) of its row (a
+// bulk copy starts on a 16-byte boundary).  + 52 words: up to 3 words of that
+// shift, and a lane's window start advances at most 44 times (1408 bits) plus
+// 2 words of look-ahead, from at most word 1416.
+constexpr uint32_t kQDecRowWords = kQBlockWordsMax + 52;  // 1468: rows of 5872 bytes, 16-byte aligned
+
 struct QDecShared {
-  uint16_t lut[2048];  // next 11 bits -> (code length << 8) | symbol; bit 15 set: no valid code
+  uint32_t words[kQDecWarps][kQDecRowWords];
+  uint64_t bar[kQDecWarps];  // one mbarrier per warp: its block's bulk copy
+  uint16_t lut[2048];  // next 11 bits -> (symbol << 8) | code length; bit 7 set: no valid code
   uint32_t seen[8];    // byte values met in the rank table
   uint32_t start[9];   // first rank of each region
   int bad;
-  // + 48 words: a lane's window start advances at most 44 times (1408 bits)
-  // plus 2 words of look-ahead, from at most word 1416
-  uint32_t words[kQDecWarps][kQBlockWordsMax + 48];
 };
-constexpr uint16_t kQBadCode = 0x8000u | (11u << 8);
+// A table entry's low byte is the code length (bits 0-3) with the "no valid
+// code" flag in bit 7, so whole entries can be added to a bit position: bits
+// 0-5 of the sum stay exact while positions plus lengths stay below 64.
+constexpr uint16_t kQBadCode = 0x80u | 11u;
+constexpr uint32_t kQBadFlag = 0x80u;
 
 __global__ void __launch_bounds__(kQDecWarps * 32) zq_decode_kernel(const __grid_constant__ QDecParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -276,6 +286,10 @@ __global__ void __launch_bounds__(kQDecWarps * 32) zq_decode_kernel(const __grid
   const uint64_t tbl = zq_table_bytes(nb);
   // header checks (every CTA reaches the same verdict) and the 11-bit table
   if (threadIdx.x < 8) S.seen[threadIdx.x] = 0u;
+  if (lane == 0) {
+    mbar_init(&S.bar[warp], 1);
+    fence_mbar_init();
+  }
   if (threadIdx.x == 0) {
     const uint32_t* h = reinterpret_cast<const uint32_t*>(p.in);
     int err = 0;
@@ -316,34 +330,60 @@ __global__ void __launch_bounds__(kQDecWarps * 32) zq_decode_kernel(const __grid
     const uint32_t r = q >> 8;
     const uint32_t w = __ldg(p.in + 64 + r);
     const uint32_t rank = S.start[r] + (w == 0 ? 0u : ((q & 0xFFu) >> (8 - w)));
-    S.lut[q] = rank > 255 ? kQBadCode : static_cast<uint16_t>(((3 + w) << 8) | __ldg(p.in + 128 + rank));
+    S.lut[q] = rank > 255 ? kQBadCode : static_cast<uint16_t>((uint32_t(__ldg(p.in + 128 + rank)) << 8) | (3 + w));
   }
   __syncthreads();
   const uint64_t words = static_cast<uint64_t>(reinterpret_cast<const uint32_t*>(p.in)[6]) |
                          (static_cast<uint64_t>(reinterpret_cast<const uint32_t*>(p.in)[7]) << 32);
   const uint32_t* table = reinterpret_cast<const uint32_t*>(p.in + kQHeader);
   const uint32_t* payload = reinterpret_cast<const uint32_t*>(p.in + kQHeader + tbl);
-  uint32_t* wbuf = S.words[warp];
+  uint32_t* const row = S.words[warp];
+  // The payload starts on 16 bytes (the stream does, and the header and the
+  // offset table are whole 16-byte units); a block whose copy, rounded up to
+  // 16 bytes, would reach past the stream's end is loaded with plain loads.
+  const uint8_t* in_end = p.in + p.in_bytes;
   const uint64_t total_warps = static_cast<uint64_t>(gridDim.x) * kQDecWarps;
-  for (uint64_t b = static_cast<uint64_t>(blockIdx.x) * kQDecWarps + warp; b < nb; b += total_warps) {
-    const uint64_t off = __ldg(table + b);
-    const uint64_t end = b + 1 < nb ? static_cast<uint64_t>(__ldg(table + b + 1)) : words;
+  uint64_t next_off = 0, next_end = 0;  // offsets of the warp's next block, loaded one block ahead
+  auto load_offsets = [&](uint64_t bb) {
+    next_off = __ldg(table + bb);
+    next_end = bb + 1 < nb ? static_cast<uint64_t>(__ldg(table + bb + 1)) : words;
+  };
+  const uint64_t b_first = static_cast<uint64_t>(blockIdx.x) * kQDecWarps + warp;
+  if (b_first < nb) load_offsets(b_first);
+  uint32_t phase = 0;
+  for (uint64_t b = b_first; b < nb; b += total_warps) {
+    const uint64_t off = next_off, end = next_end;
+    if (b + total_warps < nb) load_offsets(b + total_warps);
     if (off + 8 > end || end > words || end - off > kQBlockWordsMax) {
       if (lane == 0) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
       continue;
     }
     const uint32_t T = static_cast<uint32_t>(end - off);
-    for (uint32_t k0 = 0; k0 < T; k0 += 8 * 32) {  // 8 independent loads in flight per lane
-      uint32_t t[8];
-#pragma unroll
-      for (uint32_t u = 0; u < 8; u++) {
-        const uint32_t k = k0 + 32 * u + lane;
-        t[u] = k < T ? __ldg(payload + off + k) : 0u;
+    const uint64_t c0 = off & ~3ull, c1 = (end + 3) & ~3ull;  // the copy: whole 16-byte units
+    const uint32_t* wbuf = row;
+    if (reinterpret_cast<const uint8_t*>(payload + c1) <= in_end) {
+      wbuf = row + (off & 3u);
+      if (lane == 0) {
+        fence_proxy_async();  // the previous block's reads of the row come first
+        const uint32_t bytes = static_cast<uint32_t>(4 * (c1 - c0));
+        mbar_arrive_expect_tx(&S.bar[warp], bytes);
+        tma_load_1d(row, payload + c0, bytes, &S.bar[warp]);
       }
+      mbar_wait_bounded(&S.bar[warp], phase, p.status);
+      phase ^= 1u;
+    } else {
+      for (uint32_t k0 = 0; k0 < T; k0 += 8 * 32) {  // 8 independent loads in flight per lane
+        uint32_t t[8];
 #pragma unroll
-      for (uint32_t u = 0; u < 8; u++) {
-        const uint32_t k = k0 + 32 * u + lane;
-        if (k < T) wbuf[k] = t[u];
+        for (uint32_t u = 0; u < 8; u++) {
+          const uint32_t k = k0 + 32 * u + lane;
+          t[u] = k < T ? __ldg(payload + off + k) : 0u;
+        }
+#pragma unroll
+        for (uint32_t u = 0; u < 8; u++) {
+          const uint32_t k = k0 + 32 * u + lane;
+          if (k < T) row[k] = t[u];
+        }
       }
     }
     __syncwarp();
@@ -362,7 +402,7 @@ __global__ void __launch_bounds__(kQDecWarps * 32) zq_decode_kernel(const __grid
     auto decode_one = [&]() -> uint32_t {  // returns the lookup entry, advances the window
       const uint32_t e = S.lut[__funnelshift_l(w1, w0, pos) >> 21];
       badcode |= e;
-      pos += (e >> 8) & 15u;
+      pos += e & 15u;
       const bool adv = pos >= 32;
       pos &= 31u;
       w0 = adv ? w1 : w0;
@@ -374,19 +414,21 @@ __global__ void __launch_bounds__(kQDecWarps * 32) zq_decode_kernel(const __grid
     // Two symbols per refill: a code is at most 11 bits, so after the first
     // symbol the second starts at most 42 bits into (w0, w1, w2) and ends
     // inside w1; one advance (at most one word) follows the pair.
+    // Positions add whole entries (pos + two lengths <= 53 < 64); the funnel
+    // shifts take the shift amount modulo 32.
     auto decode_two = [&](uint32_t& ea, uint32_t& eb) {
       ea = S.lut[__funnelshift_l(w1, w0, pos) >> 21];
-      const uint32_t p2 = pos + ((ea >> 8) & 15u);
-      const bool hi = p2 >= 32;
-      eb = S.lut[__funnelshift_l(hi ? w2 : w1, hi ? w1 : w0, p2 & 31u) >> 21];
+      const uint32_t p2 = pos + ea;
+      const bool hi = (p2 & 32u) != 0;
+      eb = S.lut[__funnelshift_l(hi ? w2 : w1, hi ? w1 : w0, p2) >> 21];
       badcode |= ea | eb;
-      const uint32_t p3 = p2 + ((eb >> 8) & 15u);
-      const bool adv = p3 >= 32;
+      const uint32_t p3 = p2 + eb;
+      const bool adv = (p3 & 32u) != 0;
       pos = p3 & 31u;
       w0 = adv ? w1 : w0;
       w1 = adv ? w2 : w1;
       idx += adv ? 1u : 0u;
-      w2 = wbuf[idx];
+      if (adv) w2 = wbuf[idx];
     };
 #pragma unroll 1
     for (uint32_t j = 0; j < 8; j++) {
@@ -399,16 +441,16 @@ __global__ void __launch_bounds__(kQDecWarps * 32) zq_decode_kernel(const __grid
           uint32_t e0, e1, e2, e3;
           decode_two(e0, e1);
           decode_two(e2, e3);
-          o[q] = __byte_perm(__byte_perm(e0, e1, 0x0040), __byte_perm(e2, e3, 0x0040), 0x5410);
+          o[q] = __byte_perm(__byte_perm(e0, e1, 0x0051), __byte_perm(e2, e3, 0x0051), 0x5410);
         }
         *reinterpret_cast<uint4*>(p.out + i0) = make_uint4(o[0], o[1], o[2], o[3]);
       } else {
-        for (uint32_t t = 0; t < valid; t++) p.out[i0 + t] = static_cast<uint8_t>(decode_one());
+        for (uint32_t t = 0; t < valid; t++) p.out[i0 + t] = static_cast<uint8_t>(decode_one() >> 8);
       }
     }
     // words consumed: the window started at word `first`, advanced idx - first - 2 times
     const uint32_t bits_used = 32u * (idx - first - 2u) + pos;
-    ok &= (badcode & 0x8000u) == 0;
+    ok &= (badcode & kQBadFlag) == 0;
     ok &= (bits_used + 31) / 32 == wc;
     if (!__all_sync(kFull, ok) && lane == 0) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
     __syncwarp();

@@ -136,6 +136,41 @@ def test_stream_errors(zc):
         assert zc.status_value(st) == code, (code, zc.status_string(zc.status_value(st)))
 
 
+def test_decode_stream_tail(zc):
+    """The decoder stages a block with one bulk copy of whole 16-byte units; where the last block's copy would
+    reach past in_bytes it takes plain loads instead.  Streams whose sizes cover every residue mod 16 decode from
+    buffers that end exactly at the stream; a stream that does not start on 16 bytes is refused."""
+    residues = set()
+    for k in range(12):
+        n = 3 * 4096 + 517 * k + 1
+        x = workloads.fp8_ffn1(n, seed=60 + k)
+        s = oracle.qlc_compress(x, DYNAMIC, oracle.qlc_table_for(x))
+        residues.add(s.size % 16)
+        st = zc.new_status()
+        y = zc.zq_decompress(torch.from_numpy(s).cuda(), n, st, in_bytes=s.size)
+        torch.cuda.synchronize()
+        assert zc.status_value(st) == 0 and np.array_equal(y.cpu().numpy(), x)
+    assert residues == {0, 4, 8, 12}
+    buf = torch.zeros(s.size + 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(zc.ZcError):
+        zc.zq_decompress(buf[4:], n, zc.new_status(), in_bytes=s.size)
+
+
+def test_corrupt_block_offset(zc):
+    """A block offset past the payload is a corrupt stream; the blocks around it still decode."""
+    n = 20 * 4096
+    x = workloads.fp8_ffn1(n, seed=78)
+    s = oracle.qlc_compress(x, DEFAULT, oracle.qlc_table_for(x))
+    bad = s.copy()
+    bad[384 + 4 * 7:384 + 4 * 8] = np.frombuffer(np.uint32(0x7FFFFFF0).tobytes(), np.uint8)
+    st = zc.new_status()
+    y = zc.zq_decompress(torch.from_numpy(bad).cuda(), n, st, in_bytes=bad.size)
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == zc.ERR_CORRUPT_STREAM
+    got = y.cpu().numpy()
+    assert np.array_equal(got[:6 * 4096], x[:6 * 4096]) and np.array_equal(got[8 * 4096:], x[8 * 4096:])
+
+
 @pytest.mark.parametrize("widths", [DEFAULT, DYNAMIC])
 def test_several_rounds_and_a_partial_last_group(zc, widths):
     """4917 blocks (a ragged last one): 308 groups of 16 blocks over at most one CTA per SM, so CTAs code two or
