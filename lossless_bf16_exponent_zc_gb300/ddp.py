@@ -5,7 +5,7 @@ histogram codebook, sends shard r to rank r, and rank r adds the P shards it rec
 rounding once to bf16 and re-encoding the result) followed by a zipped all-gather of the re-encoded shards (every
 rank sends its shard's streams to every rank and decodes all of them in one batched launch).  The sum is then
 divided by the number of ranks, as DDP averages gradients.  Every codec step runs in libzc's kernels; the
-exchanges are point-to-point sends (exchange.exchange_streams).  Buckets of other dtypes go through the
+exchanges are point-to-point sends (exchange.zipped_reduce_scatter, exchange.all_gather_streams).  Buckets of other dtypes go through the
 process group's own all-reduce.
 
     state = ZippedAllReduceState()
@@ -17,7 +17,7 @@ import torch
 import torch.distributed as dist
 
 from . import zc
-from .exchange import exchange_streams, zipped_reduce_scatter
+from .exchange import all_gather_streams, zipped_reduce_scatter
 
 
 class ZippedAllReduceState:
@@ -58,11 +58,7 @@ def zipped_allreduce(t: torch.Tensor, state: ZippedAllReduceState) -> torch.Tens
     cb, _ = zc.histogram_topk(x, state.workspace((world * m,)), state.status)
     _, om, oe = zipped_reduce_scatter(x, cb, state.status, out_cb=cb, ws=state.workspace((m,) * world),
                                       group=group)
-    mb, _ = zc.compressed_size(m)
-    rm, re, k = exchange_streams([om] * world, [oe] * world, [mb] * world, group)
-    out = torch.empty(world * m, dtype=torch.int16, device=t.device)
-    zc.decompress_batched([zc.BatchItem(bf16=out[r * m:(r + 1) * m], main=rm[r], esc=re[r], esc_bytes=k[r])
-                           for r in range(world)], state.status)
+    out = all_gather_streams(om, oe, m, state.status, group=group)
     t.copy_(out[:n].view(torch.bfloat16))
     if world > 1:
         t.div_(world)

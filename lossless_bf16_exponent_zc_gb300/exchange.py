@@ -12,6 +12,8 @@ device buffers over NCCL and host buffers over gloo.  The codec steps on either 
 compression of all outgoing pieces in one batched launch (with the raw bypass, so an incompressible piece
 travels as its own bytes), decompression of all incoming pieces in one batched launch, and, for the
 reduce-scatter, the fused decode + fp32 sum in rank order + round to bf16 (+ re-encode) of zc_decompress_reduce.
+The all-gather sends one rank's streams to every rank (zipped_all_gather compresses first; all_gather_streams
+takes streams a rank already holds, such as a reduce-scatter's re-encoded shard).
 Sizes handed to a receiver (recv_counts) are the caller's to know, as in any all-to-all: an MoE dispatch
 exchanges its token counts first.
 """
@@ -141,6 +143,38 @@ def zipped_reduce_scatter(x: torch.Tensor, cb_in: torch.Tensor, status: torch.Te
     out, out_main, out_esc = zc.decompress_reduce(recv_mains, recv_escs, m, status, out_cb=out_cb, ws=ws,
                                                   esc_bytes=k_in)
     return out, out_main, out_esc
+
+
+def all_gather_streams(main: torch.Tensor, esc: torch.Tensor, n: int, status: torch.Tensor,
+                       out: torch.Tensor | None = None, group=None) -> torch.Tensor:
+    """All-gather of a tensor already compressed: every rank holds the streams of its own n values (a ZC1 main
+    stream and its escape buffer, coded or RAW), sends them to every rank and decodes the streams of all ranks
+    in one batched launch.  Returns (or fills) world * n bf16 bit patterns (int16), rank r's values at
+    [r n, (r + 1) n).  Every rank's piece has n values, so every main stream has the size the size law
+    gives for n; the escape streams follow with the sizes their headers hold."""
+    world = dist.get_world_size(group)
+    mb, _ = zc.compressed_size(n)
+    if main.numel() != mb:
+        raise ValueError("the main stream does not hold n values")
+    recv_mains, recv_escs, k_in = exchange_streams([main] * world, [esc] * world, [mb] * world, group)
+    if out is None:
+        out = torch.empty(world * n, dtype=torch.int16, device=main.device)
+    elif out.numel() != world * n:
+        raise ValueError("out must hold world * n values")
+    zc.decompress_batched([zc.BatchItem(bf16=out[r * n:(r + 1) * n], main=recv_mains[r], esc=recv_escs[r],
+                                        esc_bytes=k_in[r]) for r in range(world)], status)
+    return out
+
+
+def zipped_all_gather(x: torch.Tensor, cb: torch.Tensor, status: torch.Tensor, ws: torch.Tensor | None = None,
+                      out: torch.Tensor | None = None, group=None) -> torch.Tensor:
+    """All-gather of bf16 tensors of equal size, compressed on the wire: each rank compresses its x once (with
+    the raw bypass, so an incompressible tensor travels as its own bytes), sends the streams to every rank, and
+    every rank decodes all of them in one batched launch.  Returns world * x.numel() bf16 bit patterns (int16),
+    rank r's tensor at [r n, (r + 1) n), bit for bit."""
+    n = x.numel()
+    (item,) = _compress_pieces([x.reshape(-1)], cb, status, ws)
+    return all_gather_streams(item.main, item.esc, n, status, out=out, group=group)
 
 
 # ------------------------------------------------------------------ the reduce-scatter switcher [ZipCCL §2.D]

@@ -1,8 +1,9 @@
 """The zipped collectives' device path: libzc's batched (adaptive) compression, the two-part exchange over
 NCCL, and libzc's decoders on the receiving side [ZipCCL §2.D].  One rank in a spawned child process (a box
 here has one GPU, so a rank exchanges with itself only; more ranks are covered on CPU by test_exchange_dist.py),
-against the oracle byte for byte: the all-to-all returns every piece bit for bit, the reduce-scatter's shard is
-the oracle's decode-reduce of the same streams and its re-encoded streams are the oracle's.
+against the oracle byte for byte: the all-to-all and the all-gather return every piece bit for bit (the
+all-gather also from streams the oracle wrote), the reduce-scatter's shard is the oracle's decode-reduce of the
+same streams and its re-encoded streams are the oracle's.
 """
 import os
 import socket
@@ -47,6 +48,25 @@ def _child(port, q):
                                            zc.codebook_to_device(cb), st)
         torch.cuda.synchronize()
         assert np.array_equal(yr.cpu().numpy().view(np.uint16), r), "RAW piece"
+        # all-gather: compressed once, decoded from what arrived (coded and RAW tensors, bf16 dtype kept)
+        g = exchange.zipped_all_gather(xt.view(torch.bfloat16), zc.codebook_to_device(cb), st)
+        gr = exchange.zipped_all_gather(torch.from_numpy(r.view(np.int16)).cuda(), zc.codebook_to_device(cb), st)
+        torch.cuda.synchronize()
+        assert zc.status_value(st) == 0, zc.status_string(zc.status_value(st))
+        assert np.array_equal(g.cpu().numpy().view(np.uint16), x), "all-gather"
+        assert np.array_equal(gr.cpu().numpy().view(np.uint16), r), "all-gather of a RAW tensor"
+        # all-gather of streams the oracle wrote (the receiving side decodes them)
+        om_, oe_ = oracle.compress(x, cb)
+        ga = exchange.all_gather_streams(torch.from_numpy(om_).cuda(),
+                                         torch.from_numpy(np.concatenate([oe_, np.zeros(16, np.uint8)])).cuda(), n, st)
+        torch.cuda.synchronize()
+        assert zc.status_value(st) == 0 and np.array_equal(ga.cpu().numpy().view(np.uint16), x), "oracle streams"
+        try:
+            exchange.all_gather_streams(torch.from_numpy(om_).cuda(), torch.zeros(16, dtype=torch.uint8).cuda(),
+                                        n + 4096, st)
+            raise AssertionError("a main stream of another size was accepted")
+        except ValueError:
+            pass
         # reduce-scatter with a re-encoded output
         m = 7 * 4096 + 5
         s = workloads.gaussian(m, sigma=1e-3, seed=23)
