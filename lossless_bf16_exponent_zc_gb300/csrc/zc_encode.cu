@@ -106,8 +106,6 @@ struct RoundShared {
   unsigned long long uprefix[kEncSlots][kEncWarps];  // exclusive escape offset of each warp's unit
   uint64_t cnt_bar[kEncSlots];                       // kEncWarps arrivals: all counts of the round are in
   uint64_t pre_bar[kEncSlots];                       // 1 arrival: the scan warp has posted the offsets
-  uint64_t meta_bar;                                 // 1 arrival: the scan warp has read the epoch and the hook
-  uint32_t epoch, hold;                              // ... which the encoding warps take from here
 };
 static_assert(sizeof(RoundShared) <= kEncGrpBytes, "round bookkeeping too large");
 
@@ -264,7 +262,6 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
       mbar_init(&rs->pre_bar[r], 1);
       rs->agg[r] = 0;
     }
-    mbar_init(&rs->meta_bar, 1);
   }
   const uint32_t w = warp < kEncWarps ? warp : 0;  // per-warp regions (the scan warp uses none)
   uint32_t* lut = reinterpret_cast<uint32_t*>(gbase + kEncLutOff + w * 1024);
@@ -320,6 +317,8 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   // (thread 0's round barriers were initialised before its fence above; no
   // fence after the copies: a release fence would wait for them)
   __syncthreads();
+  const uint32_t epoch = launch_epoch(p.ws);
+  const uint32_t hold = launch_hold(p.ws);
 
   // Tensors without tiles still get a header.
   if (blockIdx.x == 0 && warp == 0) {
@@ -337,15 +336,6 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
 
   if (warp == kEncWarps) {
     // ---------------- scan warp: the escape offsets of each group
-    uint32_t epoch = 0, arrival = kNoArrival;
-    if (lane == 0) {  // the launch's epoch and hook, for the whole CTA; then count the CTA in
-      epoch = launch_epoch(p.ws);
-      rs->epoch = epoch;
-      rs->hold = launch_hold(p.ws);
-      mbar_arrive(&rs->meta_bar);
-      arrival = scan_arrive(p.ws, epoch);
-    }
-    epoch = __shfl_sync(kFull, epoch, 0);
     int cur_ti = -1;
     const uint8_t* cur_cb = nullptr;
     bool cb_ok = true;
@@ -389,7 +379,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(&rs->pre_bar[r]);  // release: the offsets are visible to waiters
     }
-    scan_exit(p.ws, p.flags, epoch, p.total_groups, arrival);
+    scan_exit(p.ws, p.flags, epoch, p.total_groups);
   } else {
     // ---------------- encoding warps: unit `warp` of every group
     // Second half of round k, once its offsets are posted (slot k mod 16):
@@ -431,8 +421,6 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
     };
 
     uint32_t phase = 0;
-    uint32_t epoch = 0, hold = 0;  // the launch's epoch and hook (lane 0, from the first publication on)
-    bool have_meta = false;
     int cur_ti = -1;
     const uint8_t* cur_cb = nullptr;
     uint64_t cur_n = 0;            // the current tensor's size ...
@@ -493,12 +481,6 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
         rs->cnt[r][warp] = cnt;
         // the last warp of the group publishes the group's escape count right away
         const uint32_t old = atomicAdd(&rs->agg[r], (1u << 16) | cnt);
-        if (!have_meta) {  // the epoch and the hook, read by the scan warp (long since, by now)
-          mbar_wait_bounded(&rs->meta_bar, 0, p.status);
-          epoch = rs->epoch;
-          hold = rs->hold;
-          have_meta = true;
-        }
         if ((old >> 16) == kEncWarps - 1 && cb_ok && hold != G + 1) {
           const uint32_t agg = (old & 0xFFFFu) + cnt;
           const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;

@@ -103,8 +103,6 @@ struct RedRound {
   unsigned long long uprefix[kRedSlots][16];  // exclusive output escape offset of each block
   uint64_t cnt_bar[kRedSlots];
   uint64_t pre_bar[kRedSlots];
-  uint64_t meta_bar;     // 1 arrival: the scan warp has read the epoch and the hook ...
-  uint32_t epoch, hold;  // ... which the consumers take from here
 };
 static_assert(sizeof(RedRound) <= 512, "round bookkeeping too large");
 
@@ -175,7 +173,6 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
       mbar_init(&rs->cnt_bar[r], kRedCons);
       mbar_init(&rs->pre_bar[r], 1);
     }
-    mbar_init(&rs->meta_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -219,19 +216,8 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
   __syncthreads();
   if (!RAW && *raw_s != 0ull) return;  // the RAW-capable launch that follows does the work
   const bool skip = flags_s[0] != 0 || flags_s[1] != 0;
-  // (re-encoding: lane 0 of the scan warp reads the launch's epoch and hook for the
-  // CTA and counts the CTA in, scan_arrive)
-  uint32_t epoch = 0, arrival = kNoArrival;
-  if (REENC && warp == kRedScan) {
-    if (lane == 0) {
-      epoch = launch_epoch(p.ws);
-      rs->epoch = epoch;
-      rs->hold = launch_hold(p.ws);
-      mbar_arrive(&rs->meta_bar);
-      arrival = scan_arrive(p.ws, epoch);
-    }
-    epoch = __shfl_sync(kFull, epoch, 0);
-  }
+  const uint32_t epoch = REENC ? launch_epoch(p.ws) : 0u;
+  const uint32_t hold = REENC ? launch_hold(p.ws) : 0u;
   const uint32_t ngroups = (p.ntiles + p.gt - 1) / p.gt;
   const uint32_t step = gridDim.x;
   if (REENC && !skip && p.ntiles == 0 && blockIdx.x == 0 && warp == 0) {
@@ -379,7 +365,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
         __syncwarp();
         if (lane == 0) mbar_arrive(&rs->pre_bar[sl]);
       }
-      scan_exit(p.ws, p.flags, epoch, ngroups, arrival);
+      scan_exit(p.ws, p.flags, epoch, ngroups);
     }
   } else {
     // ---------------- consumers: team t, block b
@@ -418,8 +404,6 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
       __syncwarp();
     };
 
-    uint32_t c_epoch = 0, c_hold = 0;  // the launch's epoch and hook (lane 0, from the first publication on)
-    bool have_meta = false;
     RedPending prev;
     prev.has = prev.spilled = false;
     prev.done = true;
@@ -581,15 +565,9 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
         if (lane == 0) {
           rs->cnt[sl][warp] = cur.te.total;
           const uint32_t old = atomicAdd(&rs->agg[sl], (1u << 16) | cur.te.total);
-          if (!have_meta) {  // the epoch and the hook, read by the scan warp (long since, by now)
-            mbar_wait_bounded(&rs->meta_bar, 0, p.status);
-            c_epoch = rs->epoch;
-            c_hold = rs->hold;
-            have_meta = true;
-          }
-          if ((old >> 16) == kRedCons - 1 && c_hold != G + 1) {
+          if ((old >> 16) == kRedCons - 1 && hold != G + 1) {
             const uint32_t agg = (old & 0xFFFFu) + cur.te.total;
-            const unsigned long long tag = static_cast<unsigned long long>(c_epoch) << 32;
+            const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
             st_relaxed(&p.flags[G].agg, tag | agg);
           }
           mbar_arrive(&rs->cnt_bar[sl]);
@@ -601,7 +579,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     }
     if (REENC && j > 0 && !prev.done) finish(j - 1, prev);
   }
-  if (REENC && skip && warp == kRedScan) scan_exit(p.ws, p.flags, epoch, ngroups, arrival);  // (nothing was run)
+  if (REENC && skip && warp == kRedScan) scan_exit(p.ws, p.flags, epoch, ngroups);  // (nothing was run)
 }
 
 cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out, const uint8_t* out_cb,

@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(kQEncThreads, 1) zq_encode_kernel(const __grid
     if (nb == 0 && lane == 0) *reinterpret_cast<unsigned long long*>(p.out + 24) = 0ull;
   }
   __syncthreads();
+  const uint32_t epoch = launch_epoch(p.ws);
   const uint64_t groups = (nb + kQEncWarps - 1) / kQEncWarps;
   const uint32_t R = blockIdx.x < groups
                          ? static_cast<uint32_t>((groups - blockIdx.x + gridDim.x - 1) / gridDim.x)
@@ -216,12 +217,6 @@ __global__ void __launch_bounds__(kQEncThreads, 1) zq_encode_kernel(const __grid
     }
   } else {
     // ---------------- scan warp: each group's first word offset
-    uint32_t epoch = 0, arrival = kNoArrival;
-    if (lane == 0) {  // the launch's epoch (only this warp uses it); then count the CTA in
-      epoch = launch_epoch(p.ws);
-      arrival = scan_arrive(p.ws, epoch);
-    }
-    epoch = __shfl_sync(kFull, epoch, 0);
     uint64_t prev_incl = 0;  // offset after this CTA's previous group
 #pragma unroll 1
     for (uint32_t r = 0; r <= R; r++) {
@@ -249,7 +244,7 @@ __global__ void __launch_bounds__(kQEncThreads, 1) zq_encode_kernel(const __grid
       }
       __syncwarp();
     }
-    scan_exit(p.ws, p.flags, epoch, static_cast<uint32_t>(groups), arrival);
+    scan_exit(p.ws, p.flags, epoch, static_cast<uint32_t>(groups));
   }
 }
 
