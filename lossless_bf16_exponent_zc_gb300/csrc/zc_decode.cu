@@ -127,7 +127,7 @@ __device__ __forceinline__ uint32_t stage_escapes(uint8_t* dst, const uint8_t* e
 template <int MAXB>
 __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_constant__ DecParams<MAXB> p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  pdl_begin();
+  pdl_allow_dependents();
   const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
   const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;
   uint8_t* gbase = smem + (sbase - smem_u32(smem));
@@ -140,13 +140,15 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
 
   // every tensor's header, read once per CTA (a warp's tiles cross many tensors)
   __shared__ HdrInfo hdr_cache[MAXB];
-  for (int i = threadIdx.x; i < p.count; i += blockDim.x) hdr_cache[i] = read_header(p.t[i], i, p.status);
+  // shared-memory setup first: it overlaps the end of the previous kernel
   build_spread_replicated<kDecSpreadCopies>(spread);
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < kDecStages; s++) mbar_init(&bar[s], 33);  // 1 TMA arrival + 32 cp.async arrivals
     fence_mbar_init();
   }
+  pdl_wait();
+  for (int i = threadIdx.x; i < p.count; i += blockDim.x) hdr_cache[i] = read_header(p.t[i], i, p.status);
   __syncthreads();
 
   const uint32_t total_warps = gridDim.x * kDecWarps;

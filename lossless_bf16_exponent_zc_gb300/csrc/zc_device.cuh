@@ -164,15 +164,21 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // Programmatic dependent launch.  Every kernel of the library is launched so
 // that it may be scheduled while the kernel before it on the stream is still
 // running, and every kernel lets the launch after it be scheduled as soon as
-// all its CTAs have started.  pdl_begin() does both: it allows the next
-// launch, then waits until every grid this one depends on has completed and
-// its memory operations are visible.  A kernel calls it before it touches
-// global memory, so stream order holds for all data; what overlaps is the
-// launch itself and the placement of CTAs on SMs that the previous grid has
-// left.  Without the launch attribute the wait returns at once.
-__device__ __forceinline__ void pdl_begin() {
+// all its CTAs have started (pdl_allow_dependents, first thing).  pdl_wait()
+// waits until every grid this one depends on has completed and its memory
+// operations are visible; every thread calls it before it touches global
+// memory, so stream order holds for all data.  What overlaps is the launch
+// itself, the placement of CTAs on SMs that the previous grid has left, and
+// whatever setup a kernel does in shared memory alone before its wait
+// (mbarriers, lookup tables, cleared bins).  Without the launch attribute the
+// wait returns at once.  pdl_begin() is both, for kernels with no such setup.
+__device__ __forceinline__ void pdl_allow_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_begin() {
+  pdl_allow_dependents();
+  pdl_wait();
 }
 
 // Wait for phase `parity` of `bar` to complete, at most kWaitLimitNs.  Returns

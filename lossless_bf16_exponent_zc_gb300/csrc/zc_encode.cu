@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;  // 1 KB aligned shared address
   uint8_t* gbase = smem + (sbase - smem_u32(smem));           // its generic pointer
   RoundShared* rs = reinterpret_cast<RoundShared*>(gbase + kEncGrpOff);
-  pdl_begin();
+  pdl_allow_dependents();  // (the wait for the previous grid comes after the shared-memory setup)
   const uint32_t step = gridDim.x;
 
   if (threadIdx.x == 0) {
@@ -304,12 +304,13 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   };
   // Each encoding warp starts its first two loads before anything reads global
   // memory (the epoch, the test hook, codebooks), so HBM is busy from the start.
-  if (warp < kEncWarps) {
-    if (lane == 0) {
+  if (warp < kEncWarps && lane == 0) {
 #pragma unroll
-      for (int s = 0; s < kEncStages; s++) mbar_init(&bar[s], 1);
-      fence_mbar_init();
-    }
+    for (int s = 0; s < kEncStages; s++) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+  }
+  pdl_wait();
+  if (warp < kEncWarps) {
     __syncwarp();
 #pragma unroll
     for (int s = 0; s < kEncStages; s++) issue(s, blockIdx.x + s * step);

@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(const uint16_t* _
                                                                WsHeader* ws, uint8_t* cb_out, uint32_t* hist_out,
                                                                int32_t* status) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  pdl_begin();
+  pdl_allow_dependents();  // (the wait for the previous grid comes after the shared-memory setup)
   uint8_t* smem = smem_raw + ((128 - (smem_u32(smem_raw) & 127u)) & 127u);
   uint32_t* h = reinterpret_cast<uint32_t*>(smem + kHistBinOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kHistBarOff);
@@ -73,17 +73,20 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(const uint16_t* _
     mbar_arrive_expect_tx(&full[s], bytes);
     tma_load_1d(stage + s * kHistChunk, in + u0 * 8, bytes, &full[s]);
   };
-  // The producer starts the first copies before the bins are cleared.
+  // Barriers and cleared bins first (shared memory only: this overlaps the end
+  // of the previous kernel), then the producer starts the first copies.
   if (producer) {
     for (int s = 0; s < kHistStages; s++) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kHistCounters);
     }
     fence_mbar_init();
-    for (int s = 0; s < kHistStages; s++)
-      if (blockIdx.x + s * step < nchunks) issue(s, blockIdx.x + s * step);
   }
   for (uint32_t i = threadIdx.x; i < 256 * 32; i += blockDim.x) h[i] = 0;
+  pdl_wait();
+  if (producer)
+    for (int s = 0; s < kHistStages; s++)
+      if (blockIdx.x + s * step < nchunks) issue(s, blockIdx.x + s * step);
   __syncthreads();
 
   if (warp == kHistCounters) {

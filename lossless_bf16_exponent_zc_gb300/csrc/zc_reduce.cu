@@ -140,7 +140,7 @@ __device__ __forceinline__ uint4 round_pack(const float (&acc)[8]) {
 template <bool REENC, bool RAW>
 __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_constant__ RedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  pdl_begin();
+  pdl_allow_dependents();  // (the wait for the previous grid comes after the shared-memory setup)
   const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
   const uint32_t sbase = (smem_u32(smem) + 1023u) & ~1023u;
   uint8_t* gbase = smem + (sbase - smem_u32(smem));
@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
   uint64_t* empty_bar = full_bar + kRedTeams * kRedStages;
   StageMeta* meta = reinterpret_cast<StageMeta*>(gbase + kRMeta);
   if (RAW && !p.single) {  // nothing to do unless a shard is RAW: leave before touching anything
+    pdl_wait();
     bool any = false;
     for (int r = threadIdx.x; r < p.P; r += blockDim.x)
       any |= __ldg(reinterpret_cast<const uint32_t*>(p.s[r].main) + 1) == (ZC_VERSION | (kFlagRaw << 16));
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     }
     fence_mbar_init();
   }
+  if (!(RAW && !p.single)) pdl_wait();  // after the shared-memory setup, which overlaps the previous kernel
   __syncthreads();
   // validate every shard header (each CTA reaches the same verdict)
   for (int r = threadIdx.x; r < p.P; r += blockDim.x) {
