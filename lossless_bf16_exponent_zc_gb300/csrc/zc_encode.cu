@@ -271,6 +271,12 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   uint8_t* ring = gbase + kEncRingOff + w * kEncRing;
   uint8_t* wstage = gbase + kEncStageOff + w * kEncStages * kEncStageBytes;
   const uint32_t wstage_s = sbase + kEncStageOff + w * kEncStages * kEncStageBytes;
+  if (warp < kEncWarps && lane == 0) {
+#pragma unroll
+    for (int s = 0; s < kEncStages; s++) mbar_init(&bar[s], 1);
+    fence_mbar_init();  // (thread 0's round barriers above included)
+  }
+  pdl_wait();
   auto stage_ptr = [&](int s) { return reinterpret_cast<uint16_t*>(wstage + s * kEncStageBytes); };
   const uint32_t half = warp % kUnitsPerTile;  // this warp's half of each tile of a group
   uint32_t issue_ti = 0;  // running tensor index of issue()
@@ -304,12 +310,6 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   };
   // Each encoding warp starts its first two loads before anything reads global
   // memory (the epoch, the test hook, codebooks), so HBM is busy from the start.
-  if (warp < kEncWarps && lane == 0) {
-#pragma unroll
-    for (int s = 0; s < kEncStages; s++) mbar_init(&bar[s], 1);
-    fence_mbar_init();
-  }
-  pdl_wait();
   if (warp < kEncWarps) {
     __syncwarp();
 #pragma unroll

@@ -67,12 +67,6 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(const uint16_t* _
   const uint64_t nchunks = (units + kHistUnits - 1) / kHistUnits;
   const uint64_t step = gridDim.x;
   const bool producer = warp == kHistCounters && lane == 0;
-  auto issue = [&](int s, uint64_t c) {
-    const uint64_t u0 = c * kHistUnits;
-    const uint32_t bytes = static_cast<uint32_t>(units - u0 < kHistUnits ? units - u0 : kHistUnits) * 16u;
-    mbar_arrive_expect_tx(&full[s], bytes);
-    tma_load_1d(stage + s * kHistChunk, in + u0 * 8, bytes, &full[s]);
-  };
   // Barriers and cleared bins first (shared memory only: this overlaps the end
   // of the previous kernel), then the producer starts the first copies.
   if (producer) {
@@ -84,6 +78,12 @@ __global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(const uint16_t* _
   }
   for (uint32_t i = threadIdx.x; i < 256 * 32; i += blockDim.x) h[i] = 0;
   pdl_wait();
+  auto issue = [&](int s, uint64_t c) {
+    const uint64_t u0 = c * kHistUnits;
+    const uint32_t bytes = static_cast<uint32_t>(units - u0 < kHistUnits ? units - u0 : kHistUnits) * 16u;
+    mbar_arrive_expect_tx(&full[s], bytes);
+    tma_load_1d(stage + s * kHistChunk, in + u0 * 8, bytes, &full[s]);
+  };
   if (producer)
     for (int s = 0; s < kHistStages; s++)
       if (blockIdx.x + s * step < nchunks) issue(s, blockIdx.x + s * step);

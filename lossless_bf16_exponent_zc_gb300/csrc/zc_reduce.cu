@@ -153,14 +153,6 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(gbase + kRBars);
   uint64_t* empty_bar = full_bar + kRedTeams * kRedStages;
   StageMeta* meta = reinterpret_cast<StageMeta*>(gbase + kRMeta);
-  if (RAW && !p.single) {  // nothing to do unless a shard is RAW: leave before touching anything
-    pdl_wait();
-    bool any = false;
-    for (int r = threadIdx.x; r < p.P; r += blockDim.x)
-      any |= __ldg(reinterpret_cast<const uint32_t*>(p.s[r].main) + 1) == (ZC_VERSION | (kFlagRaw << 16));
-    if (!__syncthreads_or(any)) return;
-  }
-
   build_spread_replicated<kSpreadCopies>(spread);
   if (threadIdx.x == 0) {
     flags_s[0] = flags_s[1] = 0;
@@ -176,7 +168,13 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     }
     fence_mbar_init();
   }
-  if (!(RAW && !p.single)) pdl_wait();  // after the shared-memory setup, which overlaps the previous kernel
+  pdl_wait();  // after the shared-memory setup, which overlaps the previous kernel
+  if (RAW && !p.single) {  // nothing to do unless a shard is RAW: leave before touching the workspace
+    bool any = false;
+    for (int r = threadIdx.x; r < p.P; r += blockDim.x)
+      any |= __ldg(reinterpret_cast<const uint32_t*>(p.s[r].main) + 1) == (ZC_VERSION | (kFlagRaw << 16));
+    if (!__syncthreads_or(any)) return;
+  }
   __syncthreads();
   // validate every shard header (each CTA reaches the same verdict)
   for (int r = threadIdx.x; r < p.P; r += blockDim.x) {

@@ -102,11 +102,10 @@ __device__ __forceinline__ void zq_lookup_run(const uint32_t* lut, uint4 v, uint
 // resident.
 __global__ void __launch_bounds__(kQEncThreads, 1) zq_encode_kernel(const __grid_constant__ QEncParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  pdl_allow_dependents();
+  pdl_begin();
   QEncShared& S = *reinterpret_cast<QEncShared*>(smem_raw);
   const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
-  for (uint32_t i = threadIdx.x; i < 256; i += blockDim.x) S.lut[i] = p.code[i];  // (from the launch parameters)
-  pdl_wait();
+  for (uint32_t i = threadIdx.x; i < 256; i += blockDim.x) S.lut[i] = p.code[i];
   const uint64_t nb = zq_blocks(p.n);
   const uint64_t tbl = zq_table_bytes(nb);
   uint32_t* table = reinterpret_cast<uint32_t*>(p.out + kQHeader);

@@ -2,11 +2,16 @@
 
 Every kernel is launched as a programmatic dependent launch, so it may start
 while the kernel before it on the stream is still running; stream order for
-data holds only because each kernel executes griddepcontrol.wait (pdl_begin())
-before it touches global memory.  These checks keep that true for every
-kernel in csrc/: each __global__ function calls pdl_begin() among its first
-statements, and no kernel is launched with the triple-chevron syntax (which
-would bypass launch_kernel and its attributes).
+data holds only because each thread executes griddepcontrol.wait (pdl_wait(),
+or pdl_begin(), which also lets the next launch be scheduled) before it
+touches global memory.  A kernel may first set up shared memory (mbarriers,
+tables, cleared bins), which then overlaps the end of the previous kernel.
+These checks keep that true for every kernel in csrc/: each __global__
+function lets the next launch be scheduled among its first statements, and
+the source before its first wait names no global access (no launch
+parameters, loads, atomics or bulk copies); and no kernel is launched with
+the triple-chevron syntax (which would bypass launch_kernel and its
+attributes).
 """
 import os
 import re
@@ -43,13 +48,17 @@ def test_every_kernel_waits_for_its_predecessor_first():
     for name, text in _sources():
         for kernel, body in _kernels(text):
             found += 1
-            statements = [s.strip() for s in body.split(";") if s.strip()]
+            code = re.sub(r"//.*", "", body)
+            statements = [s.strip() for s in code.split(";") if s.strip()]
             head = statements[:8]  # shared-memory addresses may be computed first
-            assert any(s.endswith("pdl_begin()") for s in head), f"{name}: {kernel} does not begin with pdl_begin()"
-            before = body[:body.index("pdl_begin()")]
+            assert any(s.endswith(("pdl_begin()", "pdl_allow_dependents()")) for s in head), \
+                f"{name}: {kernel} does not let the next launch be scheduled first"
+            waits = [i for i in (code.find("pdl_begin()"), code.find("pdl_wait()")) if i >= 0]
+            assert waits, f"{name}: {kernel} never waits for the previous grid"
+            before = code[:min(waits)]
             # nothing before the wait may touch global memory
-            assert not re.search(r"\bp\.|__ldg|ld_relaxed|st_relaxed|atomic|tma_|cp_async", before), \
-                f"{name}: {kernel} accesses memory before pdl_begin()"
+            assert not re.search(r"\bp\.|__ldg|ld_relaxed|st_relaxed|atomic|tma_|cp_async|\bws->|\bin\s*[\[+]|launch_epoch|launch_hold",
+                                 before), f"{name}: {kernel} may access global memory before its wait"
     assert found >= 7  # encode (with its raw bypass), decode, reduce, histogram, pipeline link, QLC encode and decode
 
 
