@@ -13,7 +13,13 @@ read), would show up as a wrong byte:
 * histogram -> compress with the codebook the histogram just wrote;
 * one main / escape buffer pair reused by every round of compress + decompress;
 * decompress -> decompress_reduce -> re-encoded stream -> decompress;
-* compress on one stream, decompress on another after an event.
+* compress on one stream, decompress on another after an event;
+* the benchmark's step (histogram, compress with the histogram's and with
+  the sigma codebook, both decompressed) hundreds of times on one
+  workspace, back to back and with a synchronisation after every call: the
+  escape scan's per-launch state (epoch, counters) is handed from launch to
+  launch, and a slip there shows up as escape offsets that no longer match
+  the code planes, which the decoder reports.
 """
 import math
 
@@ -135,3 +141,42 @@ def test_cross_stream_event(zc):
     _check_status(zc, st)
     for x, y in zip(xs, outs):
         assert torch.equal(y, x)
+
+
+def test_long_runs_of_the_benchmark_step(zc):
+    n = 1 << 26
+    # the benchmark's own tensor: N(0, 1e-3) with outliers and special values
+    x = torch.from_numpy(workloads.gradient().view("int16")).cuda()
+    cb_sig = zc.codebook_to_device(oracle.codebook_from_sigma(1e-3))
+    cb_hist = torch.empty(7, dtype=torch.uint8, device="cuda")
+    st, ws = zc.new_status(), zc.workspace(n)
+    mb, eb = zc.compressed_size(n)
+    ma, mb_ = torch.empty(mb, dtype=torch.uint8, device="cuda"), torch.empty(mb, dtype=torch.uint8, device="cuda")
+    ea, eb_ = torch.empty(eb, dtype=torch.uint8, device="cuda"), torch.empty(eb, dtype=torch.uint8, device="cuda")
+    ya, yb = torch.empty_like(x), torch.empty_like(x)
+
+    def step():
+        zc.histogram_topk(x, ws, st, cb_out=cb_hist)
+        zc.compress(x, cb_hist, ws, st, main=ma, esc=ea)
+        zc.compress(x, cb_sig, ws, st, main=mb_, esc=eb_)
+        zc.decompress(ma, ea, n, st, out=ya)
+        zc.decompress(mb_, eb_, n, st, out=yb)
+
+    for _ in range(300):
+        step()
+    _check_status(zc, st)
+    for _ in range(100):
+        for call in (lambda: zc.histogram_topk(x, ws, st, cb_out=cb_hist),
+                     lambda: zc.compress(x, cb_hist, ws, st, main=ma, esc=ea),
+                     lambda: zc.compress(x, cb_sig, ws, st, main=mb_, esc=eb_),
+                     lambda: zc.decompress(ma, ea, n, st, out=ya),
+                     lambda: zc.decompress(mb_, eb_, n, st, out=yb)):
+            call()
+            _check_status(zc, st)
+    assert torch.equal(ya, x) and torch.equal(yb, x)
+    # the last streams are the ones a fresh workspace gives
+    ws2, st2 = zc.workspace(n), zc.new_status()
+    for cb, m in ((cb_hist, ma), (cb_sig, mb_)):
+        rm, _ = zc.compress(x, cb, ws2, st2)
+        _check_status(zc, st2)
+        assert torch.equal(rm, m)
