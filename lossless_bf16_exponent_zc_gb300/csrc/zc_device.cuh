@@ -26,14 +26,15 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
 // ---------------------------------------------------------------- workspace
 // The caller zero-fills the workspace once.  Every kernel returns it to a
-// reusable state: the exit counter is reset by the last CTA to leave, escape
+// reusable state: the exit counter is reset by the CTA that completes it, escape
 // scan flags are tagged with a per-launch epoch so stale flags of earlier
 // launches never match, and histogram bins are cleared by the last CTA.
 struct WsHeader {
   uint32_t hold_tile;  // test hook for the bounded waits: if non-zero, scan unit hold_tile - 1
-                       // publishes no count, so the scans that need it must time out; the
-                       // last CTA of the launch resets it to 0
-  uint32_t exited;     // CTAs of the running encoding launch that have left
+                       // publishes no count, so the scans that need it must time out; reset
+                       // to 0 by the launch (scan_exit)
+  uint32_t exited;     // CTAs of the running encoding launch that have read the epoch (that have
+                       // left, in the launch whose epoch wraps)
   uint32_t epoch;      // epoch tag of the last finished encoding launch
   uint32_t max_tiles;  // largest flag range ever used (cleared when the epoch wraps)
   uint32_t hist_done;  // CTAs of the running histogram launch that have finished
@@ -839,35 +840,60 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* arrived, uint32_t* gen, i
   return true;
 }
 
-// Exit protocol of a launch that uses escape-scan flags, run by each CTA's
-// scan warp once the CTA's last escape offsets are posted: from then on the
-// CTA neither reads nor writes a flag (its units' counts were published
-// before they reached the scan warp) and has read the epoch and the test hook
-// long ago, so the rest of the CTA may still be writing escapes.  The last
-// CTA to get here resets the exit counter and the test hook and publishes the
-// epoch; when the epoch wraps it clears every flag first, so a flag written
-// 2^32 launches earlier can never pass for a current one.  One atomic per CTA:
-// lane 0's acquire-release increment orders the CTA's flag accesses (the
-// encoding warps' count stores reached this warp through shared-memory
-// barriers first) before the count, and the CTA completing it acquires them
-// all; the kernel's end publishes what it writes next.
-__device__ __forceinline__ void scan_exit(WsHeader* ws, Flag* flags, uint32_t epoch, uint32_t total_units) {
+// Entry and exit of a launch that uses escape-scan flags.  Every thread that
+// needs the epoch or the test hook reads them from the workspace before a
+// barrier of its CTA, and after that barrier lane 0 of the CTA's scan warp
+// counts the CTA in with one acquire-release increment of the exit counter
+// (scan_arrive), whose result it needs only at the end.  The CTA that
+// completes the count therefore knows that every thread of the launch has
+// read both words (the barrier puts the CTA's reads before its increment),
+// so at the end of its own scan it publishes the epoch for the next launch
+// and resets the counter and the hook (scan_exit) without waiting for any
+// other CTA: the count's round trip to L2 overlaps the CTA's work instead of
+// ending the launch.  The launch whose epoch wraps (tag 2^32 - 1) clears
+// every flag, so a flag written 2^32 launches earlier can never pass for a
+// current one; that has to wait until no CTA reads or writes a flag, so that
+// launch counts CTAs when they leave instead, and the last to leave clears
+// the flags.
+constexpr uint32_t kNoArrival = 0xFFFFFFFFu;
+
+__device__ __forceinline__ uint32_t scan_arrive(WsHeader* ws, uint32_t epoch) {
+  return epoch == 0xFFFFFFFFu ? kNoArrival : atom_add_acq_rel_gpu(&ws->exited, 1u);
+}
+
+// Run by the whole scan warp once the CTA's last escape offsets are posted
+// (the CTA's units' counts were published before they reached this warp, and
+// the rest of the CTA may still be writing escapes); `arrival` is lane 0's
+// scan_arrive result.
+__device__ __forceinline__ void scan_exit(WsHeader* ws, Flag* flags, uint32_t epoch, uint32_t total_units,
+                                          uint32_t arrival) {
   const uint32_t lane = lane_id();
+  if (epoch != 0xFFFFFFFFu) {
+    if (__shfl_sync(kFull, arrival, 0) != gridDim.x - 1) return;
+    if (lane == 0) {
+      ws->max_tiles = max(*reinterpret_cast<volatile uint32_t*>(&ws->max_tiles), total_units);
+      ws->exited = 0;
+      ws->hold_tile = 0;
+      ws->epoch = epoch;
+    }
+    return;
+  }
+  // the wrap: the last CTA to leave clears the flags, then publishes epoch 0
+  // (lane 0's acquire-release increment orders the CTA's flag accesses before
+  // the count, and the CTA completing it acquires those of every CTA)
   int last = 0;
   if (lane == 0) last = atom_add_acq_rel_gpu(&ws->exited, 1u) == gridDim.x - 1;
   if (!__shfl_sync(kFull, last, 0)) return;
   __syncwarp();
   const uint32_t maxt = max(*reinterpret_cast<volatile uint32_t*>(&ws->max_tiles), total_units);
-  if (epoch == 0xFFFFFFFFu) {
-    for (uint32_t i = lane; i < maxt; i += 32) flags[i] = Flag{0ull, 0ull};
-    __threadfence();
-    __syncwarp();
-  }
+  for (uint32_t i = lane; i < maxt; i += 32) flags[i] = Flag{0ull, 0ull};
+  __threadfence();
+  __syncwarp();
   if (lane == 0) {
     ws->max_tiles = maxt;
     ws->exited = 0;
     ws->hold_tile = 0;
-    ws->epoch = (epoch == 0xFFFFFFFFu) ? 0u : epoch;
+    ws->epoch = 0u;
   }
 }
 

@@ -317,9 +317,11 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
   }
   // (thread 0's round barriers were initialised before its fence above; no
   // fence after the copies: a release fence would wait for them)
-  __syncthreads();
+  // the launch's epoch and test hook, read by every thread before the barrier
+  // that precedes the scan warp's count (scan_arrive)
   const uint32_t epoch = launch_epoch(p.ws);
   const uint32_t hold = launch_hold(p.ws);
+  __syncthreads();
 
   // Tensors without tiles still get a header.
   if (blockIdx.x == 0 && warp == 0) {
@@ -337,6 +339,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
 
   if (warp == kEncWarps) {
     // ---------------- scan warp: the escape offsets of each group
+    const uint32_t arrival = lane == 0 ? scan_arrive(p.ws, epoch) : kNoArrival;
     int cur_ti = -1;
     const uint8_t* cur_cb = nullptr;
     bool cb_ok = true;
@@ -380,7 +383,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(&rs->pre_bar[r]);  // release: the offsets are visible to waiters
     }
-    scan_exit(p.ws, p.flags, epoch, p.total_groups);
+    scan_exit(p.ws, p.flags, epoch, p.total_groups, arrival);
   } else {
     // ---------------- encoding warps: unit `warp` of every group
     // Second half of round k, once its offsets are posted (slot k mod 16):

@@ -213,11 +213,14 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
       }
     }
   }
+  // (re-encoding: the launch's epoch and test hook, read by every thread before the
+  // barrier that precedes the scan warp's count, scan_arrive)
+  const uint32_t epoch = REENC ? launch_epoch(p.ws) : 0u;
+  const uint32_t hold = REENC ? launch_hold(p.ws) : 0u;
   __syncthreads();
   if (!RAW && *raw_s != 0ull) return;  // the RAW-capable launch that follows does the work
   const bool skip = flags_s[0] != 0 || flags_s[1] != 0;
-  const uint32_t epoch = REENC ? launch_epoch(p.ws) : 0u;
-  const uint32_t hold = REENC ? launch_hold(p.ws) : 0u;
+  const uint32_t arrival = REENC && warp == kRedScan && lane == 0 ? scan_arrive(p.ws, epoch) : kNoArrival;
   const uint32_t ngroups = (p.ntiles + p.gt - 1) / p.gt;
   const uint32_t step = gridDim.x;
   if (REENC && !skip && p.ntiles == 0 && blockIdx.x == 0 && warp == 0) {
@@ -365,7 +368,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
         __syncwarp();
         if (lane == 0) mbar_arrive(&rs->pre_bar[sl]);
       }
-      scan_exit(p.ws, p.flags, epoch, ngroups);
+      scan_exit(p.ws, p.flags, epoch, ngroups, arrival);
     }
   } else {
     // ---------------- consumers: team t, block b
@@ -579,7 +582,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     }
     if (REENC && j > 0 && !prev.done) finish(j - 1, prev);
   }
-  if (REENC && skip && warp == kRedScan) scan_exit(p.ws, p.flags, epoch, ngroups);  // (nothing was run)
+  if (REENC && skip && warp == kRedScan) scan_exit(p.ws, p.flags, epoch, ngroups, arrival);  // (nothing was run)
 }
 
 cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out, const uint8_t* out_cb,

@@ -133,8 +133,8 @@ __global__ void __launch_bounds__(kQEncThreads, 1) zq_encode_kernel(const __grid
     }
     if (nb == 0 && lane == 0) *reinterpret_cast<unsigned long long*>(p.out + 24) = 0ull;
   }
+  const uint32_t epoch = launch_epoch(p.ws);  // (before the barrier that precedes scan_arrive)
   __syncthreads();
-  const uint32_t epoch = launch_epoch(p.ws);
   const uint64_t groups = (nb + kQEncWarps - 1) / kQEncWarps;
   const uint32_t R = blockIdx.x < groups
                          ? static_cast<uint32_t>((groups - blockIdx.x + gridDim.x - 1) / gridDim.x)
@@ -217,6 +217,7 @@ __global__ void __launch_bounds__(kQEncThreads, 1) zq_encode_kernel(const __grid
     }
   } else {
     // ---------------- scan warp: each group's first word offset
+    const uint32_t arrival = lane == 0 ? scan_arrive(p.ws, epoch) : kNoArrival;
     uint64_t prev_incl = 0;  // offset after this CTA's previous group
 #pragma unroll 1
     for (uint32_t r = 0; r <= R; r++) {
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(kQEncThreads, 1) zq_encode_kernel(const __grid
       }
       __syncwarp();
     }
-    scan_exit(p.ws, p.flags, epoch, static_cast<uint32_t>(groups));
+    scan_exit(p.ws, p.flags, epoch, static_cast<uint32_t>(groups), arrival);
   }
 }
 
