@@ -843,22 +843,29 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* arrived, uint32_t* gen, i
 // Entry and exit of a launch that uses escape-scan flags.  Every thread that
 // needs the epoch or the test hook reads them from the workspace before a
 // barrier of its CTA, and after that barrier lane 0 of the CTA's scan warp
-// counts the CTA in with one acquire-release increment of the exit counter
-// (scan_arrive), whose result it needs only at the end.  The CTA that
-// completes the count therefore knows that every thread of the launch has
-// read both words (the barrier puts the CTA's reads before its increment),
-// so at the end of its own scan it publishes the epoch for the next launch
-// and resets the counter and the hook (scan_exit) without waiting for any
-// other CTA: the count's round trip to L2 overlaps the CTA's work instead of
-// ending the launch.  The launch whose epoch wraps (tag 2^32 - 1) clears
-// every flag, so a flag written 2^32 launches earlier can never pass for a
-// current one; that has to wait until no CTA reads or writes a flag, so that
-// launch counts CTAs when they leave instead, and the last to leave clears
-// the flags.
+// counts the CTA in with one release increment of the exit counter
+// (scan_arrive): the encoders at once, with the result needed only at the
+// end, so that the count's round trip to L2 overlaps the CTA's work; the
+// decode-reduce at the end of its scan, since there an increment at the start
+// delays the scan warp's first look-back.  The CTA that completes the count
+// knows that every thread of the launch has read both words (the barrier puts
+// the CTA's reads before its increment), so at the end of its own scan it
+// publishes the epoch for the next launch and resets the counter and the hook
+// (scan_exit) without waiting for any other CTA.  The launch whose epoch
+// wraps (tag 2^32 - 1) clears every flag, so a flag written 2^32 launches
+// earlier can never pass for a current one; that has to wait until no CTA
+// reads or writes a flag, so that launch counts CTAs when they leave instead,
+// and the last to leave clears the flags.
 constexpr uint32_t kNoArrival = 0xFFFFFFFFu;
 
+// The increment is release-only (it orders the CTA's reads before it); the
+// CTA that completes the count acquires the other CTAs' increments with a
+// fence in scan_exit.
 __device__ __forceinline__ uint32_t scan_arrive(WsHeader* ws, uint32_t epoch) {
-  return epoch == 0xFFFFFFFFu ? kNoArrival : atom_add_acq_rel_gpu(&ws->exited, 1u);
+  if (epoch == 0xFFFFFFFFu) return kNoArrival;
+  uint32_t old;
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(&ws->exited) : "memory");
+  return old;
 }
 
 // Run by the whole scan warp once the CTA's last escape offsets are posted
@@ -871,6 +878,7 @@ __device__ __forceinline__ void scan_exit(WsHeader* ws, Flag* flags, uint32_t ep
   if (epoch != 0xFFFFFFFFu) {
     if (__shfl_sync(kFull, arrival, 0) != gridDim.x - 1) return;
     if (lane == 0) {
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");  // (acquires every CTA's increment and reads)
       ws->max_tiles = max(*reinterpret_cast<volatile uint32_t*>(&ws->max_tiles), total_units);
       ws->exited = 0;
       ws->hold_tile = 0;

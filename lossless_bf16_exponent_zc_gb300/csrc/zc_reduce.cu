@@ -153,6 +153,17 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(gbase + kRBars);
   uint64_t* empty_bar = full_bar + kRedTeams * kRedStages;
   StageMeta* meta = reinterpret_cast<StageMeta*>(gbase + kRMeta);
+  // A RAW-capable launch that follows the all-coded one has work only when a
+  // shard is RAW, which the headers tell after the wait: it checks before any
+  // setup, so that in the usual case it leaves at once.
+  const bool check_first = RAW && !p.single;
+  if (check_first) {
+    pdl_wait();
+    bool any = false;
+    for (int r = threadIdx.x; r < p.P; r += blockDim.x)
+      any |= __ldg(reinterpret_cast<const uint32_t*>(p.s[r].main) + 1) == (ZC_VERSION | (kFlagRaw << 16));
+    if (!__syncthreads_or(any)) return;
+  }
   build_spread_replicated<kSpreadCopies>(spread);
   if (threadIdx.x == 0) {
     flags_s[0] = flags_s[1] = 0;
@@ -168,13 +179,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     }
     fence_mbar_init();
   }
-  pdl_wait();  // after the shared-memory setup, which overlaps the previous kernel
-  if (RAW && !p.single) {  // nothing to do unless a shard is RAW: leave before touching the workspace
-    bool any = false;
-    for (int r = threadIdx.x; r < p.P; r += blockDim.x)
-      any |= __ldg(reinterpret_cast<const uint32_t*>(p.s[r].main) + 1) == (ZC_VERSION | (kFlagRaw << 16));
-    if (!__syncthreads_or(any)) return;
-  }
+  if (!check_first) pdl_wait();  // after the shared-memory setup, which overlaps the previous kernel
   __syncthreads();
   // validate every shard header (each CTA reaches the same verdict)
   for (int r = threadIdx.x; r < p.P; r += blockDim.x) {
@@ -220,8 +225,16 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
   __syncthreads();
   if (!RAW && *raw_s != 0ull) return;  // the RAW-capable launch that follows does the work
   const bool skip = flags_s[0] != 0 || flags_s[1] != 0;
-  const uint32_t arrival = REENC && warp == kRedScan && lane == 0 ? scan_arrive(p.ws, epoch) : kNoArrival;
   const uint32_t ngroups = (p.ntiles + p.gt - 1) / p.gt;
+  // The scan warp counts the CTA in at once in the RAW-capable kernel, which
+  // runs alone when every CTA has at most one group (there the count's round
+  // trip would otherwise end the launch), and at the end of its scan in the
+  // all-coded kernel of longer launches (an increment at the start delays the
+  // first look-back).
+  const uint32_t arrival = REENC && RAW && warp == kRedScan && lane == 0 ? scan_arrive(p.ws, epoch) : kNoArrival;
+  auto exit_scan = [&]() {
+    scan_exit(p.ws, p.flags, epoch, ngroups, RAW || lane != 0 ? arrival : scan_arrive(p.ws, epoch));
+  };
   const uint32_t step = gridDim.x;
   if (REENC && !skip && p.ntiles == 0 && blockIdx.x == 0 && warp == 0) {
     write_header_words(p.out_main, 0, p.out_cb);
@@ -368,7 +381,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
         __syncwarp();
         if (lane == 0) mbar_arrive(&rs->pre_bar[sl]);
       }
-      scan_exit(p.ws, p.flags, epoch, ngroups, arrival);
+      exit_scan();
     }
   } else {
     // ---------------- consumers: team t, block b
@@ -582,7 +595,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     }
     if (REENC && j > 0 && !prev.done) finish(j - 1, prev);
   }
-  if (REENC && skip && warp == kRedScan) scan_exit(p.ws, p.flags, epoch, ngroups, arrival);  // (nothing was run)
+  if (REENC && skip && warp == kRedScan) exit_scan();  // (nothing was run)
 }
 
 cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out, const uint8_t* out_cb,
