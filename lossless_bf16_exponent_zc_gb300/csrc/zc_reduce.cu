@@ -7,6 +7,11 @@
 //   * 16 consumer warps in 4 teams; team t owns tile 4G + t of each group G
 //     (G, G + C, ... for C CTAs) and warp b of the team owns block b of that
 //     tile, keeping its 1024 fp32 partial sums in registers (32 per lane).
+//     Inputs of at most one tile per SM give each CTA one tile instead, and
+//     the teams share its P copies: team t decodes copies t, t + 4, ... into
+//     shared memory and all 16 warps add each four, in rank order, to the sums
+//     of their 256 values (one warp per block and copy would leave the SM's
+//     schedulers a single warp each).
 //   * 2 producer warps, each serving two teams, stream the P compressed copies
 //     of a team's tile through the team's 4-stage ring: one TMA bulk copy for
 //     the 5632-byte tile and one for the 16-byte-aligned span holding its
@@ -136,8 +141,9 @@ __device__ __forceinline__ uint4 round_pack(const float (&acc)[8]) {
 // some shard is RAW (its shard loop tests every copy for RAW; keeping that
 // test out of the all-coded kernel keeps its code as lean as before).  A grid
 // of at most one CTA per SM is launch-bound: there the RAW-capable kernel
-// runs alone (p.single) and does the work for any shards.
-template <bool REENC, bool RAW>
+// runs alone (p.single) and does the work for any shards.  SPLIT = true: that
+// kernel for inputs of at most one tile per SM (one tile per CTA, gt == 1).
+template <bool REENC, bool RAW, bool SPLIT>
 __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_constant__ RedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_allow_dependents();  // (the wait for the previous grid comes after the shared-memory setup)
@@ -236,6 +242,13 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     scan_exit(p.ws, p.flags, epoch, ngroups, RAW || lane != 0 ? arrival : scan_arrive(p.ws, epoch));
   };
   const uint32_t step = gridDim.x;
+  // SPLIT (inputs of at most one tile per SM, gt == 1; a RAW-capable kernel):
+  // the four teams share each CTA's tile, team t decoding copies t, t + 4, ...
+  // into its 8 KB of the rounded-tile area, and after every four copies all 16
+  // consumer warps add them, in rank order, to the sums of their 256 values of
+  // the tile; team 0 then rounds and re-encodes as usual.
+  static_assert(RAW || !SPLIT, "the one-tile-per-CTA kernel is a RAW-capable one");
+  constexpr bool split = SPLIT;
   if (REENC && !skip && p.ntiles == 0 && blockIdx.x == 0 && warp == 0) {
     write_header_words(p.out_main, 0, p.out_cb);
     write_header_tail(p.out_main, 0, 0);
@@ -264,9 +277,9 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
 #pragma unroll
         for (int h = 0; h < 2; h++) {
           na[u][h] = nb[u][h] = 0;
-          const uint32_t g = G * p.gt + t0 + u;
+          const uint32_t g = split ? G : G * p.gt + t0 + u;
           const uint32_t r = lane + 32u * h;
-          if (t0 + u < p.gt && G < ngroups && g < p.ntiles && r < P) {
+          if ((split || t0 + u < p.gt) && G < ngroups && g < p.ntiles && r < P) {
             const uint32_t* tbl = reinterpret_cast<const uint32_t*>(p.s[r].main + kHeader);
             na[u][h] = __ldg(tbl + g);
             const uint64_t bb = (g + 1 < p.ntiles) ? static_cast<uint64_t>(__ldg(tbl + g + 1)) : si[r].n_esc;
@@ -325,8 +338,8 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
               cku = ck[q];
             }
           const uint32_t t = t0 + lane;
-          const uint32_t g = G * p.gt + t;
-          if (t < p.gt && g < p.ntiles) {
+          const uint32_t g = split ? G : G * p.gt + t;
+          if (split ? ((static_cast<uint32_t>(r) & 3u) == t && g < p.ntiles) : (t < p.gt && g < p.ntiles)) {
             const uint32_t bi = t * kRedStages + uses % kRedStages;
             if (uses >= static_cast<uint32_t>(kRedStages))
               mbar_wait_bounded(&empty_bar[bi], (uses / kRedStages - 1) & 1u, p.status);
@@ -425,16 +438,157 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     prev.done = true;
     uint32_t j = 0;
     for (uint32_t G = blockIdx.x; G < ngroups; G += step, j++) {
-      const uint32_t g = G * p.gt + t;
-      const bool has = t < p.gt && g < p.ntiles;
-      const uint64_t rem = has ? p.n - static_cast<uint64_t>(g) * kTile : 0;
+      const uint32_t g = split ? G : G * p.gt + t;
+      const bool work = split ? g < p.ntiles : (t < p.gt && g < p.ntiles);  // this team decodes copies of tile g
+      const bool has = work && (!split || t == 0);                          // ... and owns its output block b
+      const uint64_t rem = work ? p.n - static_cast<uint64_t>(g) * kTile : 0;
       const uint32_t n_tile = rem >= kTile ? kTile : static_cast<uint32_t>(rem);
       float acc[4][8];
 #pragma unroll
       for (int k = 0; k < 4; k++)
 #pragma unroll
         for (int i = 0; i < 8; i++) acc[k][i] = -0.0f;  // -0 + x == x for every x
-      if (has) {
+      if constexpr (SPLIT) {
+        if (work) {
+          // One staged copy of block b of tile g (the team's next stage): its 1024
+          // values as bf16 go to sink(v) (quarter k: 8 values per lane in v[k]),
+          // then the stage is released to the producer.  (The loop below the
+          // split path takes the same steps inline: through this helper the
+          // re-encoding all-coded kernel measured 1 us slower.)
+          auto take_copy = [&](uint32_t g, uint32_t n_tile, auto&& sink) {
+            const uint32_t s = k_item % kRedStages;
+            const uint32_t bi = t * kRedStages + s;
+            mbar_wait_bounded(&full_bar[bi], (k_item / kRedStages) & 1u, p.status);
+            const StageMeta m = meta[bi];
+            if (RAW && (m.ok & kMetaRaw)) {
+              // RAW shard: this block's values, 16 bytes per lane and chunk
+              const uint8_t* tiles = tile_ptr(p.s[m.shard].main, p.ntiles, 0);
+              const uint64_t region = static_cast<uint64_t>(kTileBytes) * p.ntiles;
+              const uint64_t b0 = 2 * (static_cast<uint64_t>(g) * kTile + b * kBlock + lane * 8);
+              uint4 v[4];
+#pragma unroll
+              for (int k = 0; k < 4; k++) v[k] = raw_load16(tiles, p.s[m.shard].esc, region, 2 * p.n, b0 + 512 * k);
+              sink(v);
+            } else {
+              const uint32_t tile_s = sbase + kRStage + bi * kRedStageBytes;
+              const uint32_t blk_s = tile_s + b * kBlockBytes;
+              const uint32_t w0 = lds32(blk_s + 1024 + lane * 4);
+              const uint32_t w1 = lds32(blk_s + 1152 + lane * 4);
+              const uint32_t w2 = lds32(blk_s + 1280 + lane * 4);
+              uint32_t z = ~(w0 | w1 | w2);
+              if (n_tile < kTile) z &= lane_valid_mask(b, n_tile, lane);
+              // the block's escape ranks: a scan inside the block, and the totals of
+              // the tile's earlier blocks from the team's other three warps
+              const uint32_t c = __popc(z);
+              const uint32_t inc = warp_inclusive_scan(c);
+              const uint32_t total = __shfl_sync(kFull, inc, 31);
+              const uint32_t tot_s = sbase + kRTot + (t * 2 + (k_item & 1u)) * 16;
+              if (lane == 0) asm volatile("st.shared.u32 [%0], %1;" ::"r"(tot_s + 4 * b), "r"(total) : "memory");
+              // code planes -> permute selectors -> rotated exponents, while the totals meet
+              uint4 exa, exb;
+              {
+                uint32_t sel[4];
+#pragma unroll
+                for (uint32_t k = 0; k < 4; k++) sel[k] = spread_sel<kSpreadCopies>(w0, w1, w2, k, spread_lb);
+                const uint32_t t0 = si[m.shard].t0, t1 = si[m.shard].t1;
+                exa.x = __byte_perm(t0, t1, sel[0]);
+                exa.y = __byte_perm(t0, t1, sel[0] >> 16);
+                exa.z = __byte_perm(t0, t1, sel[1]);
+                exa.w = __byte_perm(t0, t1, sel[1] >> 16);
+                exb.x = __byte_perm(t0, t1, sel[2]);
+                exb.y = __byte_perm(t0, t1, sel[2] >> 16);
+                exb.z = __byte_perm(t0, t1, sel[3]);
+                exb.w = __byte_perm(t0, t1, sel[3] >> 16);
+              }
+              // the team's four warps: every block total of this copy is written
+              // (the two buffers alternate; a buffer is rewritten only after all
+              // four warps have passed the next copy's barrier, so after their reads)
+              asm volatile("bar.sync %0, 128;" ::"r"(1 + t) : "memory");
+              const uint4 tt = lds128(tot_s);
+              const uint32_t first = (b > 0 ? tt.x : 0u) + (b > 1 ? tt.y : 0u) + (b > 2 ? tt.z : 0u);
+              if (b == 3 && m.ok && first + total != m.cnt && lane == 0) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
+              if (z) {
+                // patch escapes through the lane's 32 scratch bytes (bit q of z <-> byte q)
+                EscSource es;
+                es.smem = gbase + kRStage + bi * kRedStageBytes + kTileBytes + (m.a & 15u);
+                es.glob = p.s[m.shard].esc + m.a;
+                es.staged = m.staged;
+                es.count = m.cnt;
+                uint32_t rank = first + inc - c;
+                // bytes 0..15 of the lane at scratch[16 lane], bytes 16..31 at scratch[512 + 16 lane]:
+                // each 16-byte access of the warp then touches every bank once per quarter
+                uint4* sp = reinterpret_cast<uint4*>(scratch + lane * 16);
+                sp[0] = exa;
+                sp[32] = exb;
+                uint32_t mz = z;
+                uint8_t* dst = scratch + lane * 16;  // byte q at dst[(q & 15) + 32 (q & 16)]
+                if (first + total <= es.staged) {  // (warp-uniform) every escape of the block is staged
+                  const uint8_t* src = es.smem + rank;
+                  do {
+                    const uint32_t q = __ffs(mz) - 1;
+                    mz &= mz - 1;
+                    dst[(q & 15u) + 32u * (q & 16u)] = static_cast<uint8_t>(rot_exp(*src++));
+                  } while (mz);
+                } else {
+                  while (mz) {
+                    const uint32_t q = __ffs(mz) - 1;
+                    mz &= mz - 1;
+                    dst[(q & 15u) + 32u * (q & 16u)] = static_cast<uint8_t>(rot_exp(esc_byte(es, rank)));
+                    rank++;
+                  }
+                }
+                exa = sp[0];
+                exb = sp[32];
+              }
+              uint4 v[4];
+#pragma unroll
+              for (uint32_t k = 0; k < 4; k++) {
+                const uint2 sm = lds64(blk_s + k * 256 + lane * 8);
+                const uint32_t r0 = k == 0 ? exa.x : k == 1 ? exa.z : k == 2 ? exb.x : exb.z;
+                const uint32_t r1 = k == 0 ? exa.y : k == 1 ? exa.w : k == 2 ? exb.y : exb.w;
+                bf16_quad(sm.x, r0, v[k].x, v[k].y);
+                bf16_quad(sm.y, r1, v[k].z, v[k].w);
+              }
+              sink(v);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[bi]);  // release the stage to the producer
+            k_item++;
+          };
+          if (REENC && !prev.done && prev.spilled) {  // its escapes sit where this tile's copies go
+            finish(j - 1, prev);
+            prev.done = true;
+          }
+          // this thread's 8 values of the tile: elements 256 warp + 8 lane + i
+          const uint32_t idx = warp * 256 + lane * 8;
+          const uint32_t own_s = sbase + kRYtile + 2 * idx;
+          uint8_t* dec = gbase + kRYtile + t * 8192 + b * 2048;  // team t's decoded block b
+          const uint32_t P = static_cast<uint32_t>(p.P);
+          for (uint32_t q = 0; 4 * q < P; q++) {
+            if (4 * q + t < P)
+              take_copy(g, n_tile, [&](const uint4 (&v)[4]) {
+#pragma unroll
+                for (int k = 0; k < 4; k++) *reinterpret_cast<uint4*>(dec + k * 512 + lane * 16) = v[k];
+              });
+            asm volatile("bar.sync 5, 512;" ::: "memory");  // the 16 consumer warps: four copies decoded
+            for (uint32_t u = 0; u < 4 && 4 * q + u < P; u++) accumulate8(acc[0], lds128(own_s + u * 8192));
+            asm volatile("bar.sync 5, 512;" ::: "memory");  // ... and added
+          }
+          uint4 v = round_pack(acc[0]);
+          if (n_tile < kTile) {
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (uint32_t jj = 0; jj < 8; jj++)
+              if (idx + jj >= n_tile) w[jj >> 1] &= (jj & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+            v = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          if (p.out) store8_guarded(p.out + static_cast<uint64_t>(g) * kTile, idx, rem, v);
+          if (REENC) {
+            *reinterpret_cast<uint4*>(gbase + kRYtile + 2 * idx) = v;  // team 0's rounded tile
+            asm volatile("bar.sync 5, 512;" ::: "memory");
+          }
+        }
+      } else if (has) {
         // the P copies of this block, added in rank order
         for (int r = 0; r < p.P; r++) {
           const uint32_t s = k_item % kRedStages;
@@ -552,7 +706,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
         finish(j - 1, prev);
         prev.done = true;
       }
-      if (has) {
+      if (has && !split) {
         uint16_t* out = p.out ? p.out + static_cast<uint64_t>(g) * kTile : nullptr;
 #pragma unroll
         for (uint32_t k = 0; k < 4; k++) {
@@ -625,26 +779,24 @@ cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out,
   // The all-coded launch, then the RAW-capable one; exactly one of them works.
   // A grid of at most one CTA per SM gets the RAW-capable launch alone.
   p.single = ngroups <= static_cast<uint32_t>(dev.sm_count) ? 1 : 0;
-  static KernelPrep prep[2][2];
+  // [re-encode][kind]: all-coded, RAW-capable, RAW-capable with one tile per CTA (the teams share its copies)
+  static KernelPrep prep[2][3];
+  const void* const fns[2][3] = {
+      {reinterpret_cast<const void*>(reduce_kernel<false, false, false>),
+       reinterpret_cast<const void*>(reduce_kernel<false, true, false>),
+       reinterpret_cast<const void*>(reduce_kernel<false, true, true>)},
+      {reinterpret_cast<const void*>(reduce_kernel<true, false, false>),
+       reinterpret_cast<const void*>(reduce_kernel<true, true, false>),
+       reinterpret_cast<const void*>(reduce_kernel<true, true, true>)}};
+  const int re = out_cb ? 1 : 0;
+  if (!re && p.ntiles == 0) return cudaSuccess;
   for (int raw = p.single; raw < 2; raw++) {
+    const int kind = raw == 0 ? 0 : (p.gt == 1 ? 2 : 1);
     int per_sm = 0;
-    cudaError_t err;
-    if (out_cb) {
-      const void* fn = raw ? reinterpret_cast<const void*>(reduce_kernel<true, true>)
-                           : reinterpret_cast<const void*>(reduce_kernel<true, false>);
-      err = prepare_kernel(prep[1][raw], fn, kRedThreads, kRedSmem, dev, &per_sm);
-      if (err != cudaSuccess) return err;
-      void* args[] = {&p};
-      err = launch_kernel(fn, dim3(ctas), dim3(kRedThreads), kRedSmem, stream, args, true);
-    } else {
-      if (p.ntiles == 0) return cudaSuccess;
-      const void* fn = raw ? reinterpret_cast<const void*>(reduce_kernel<false, true>)
-                           : reinterpret_cast<const void*>(reduce_kernel<false, false>);
-      err = prepare_kernel(prep[0][raw], fn, kRedThreads, kRedSmem, dev, &per_sm);
-      if (err != cudaSuccess) return err;
-      void* args[] = {&p};
-      err = launch_kernel(fn, dim3(ctas), dim3(kRedThreads), kRedSmem, stream, args, false);
-    }
+    cudaError_t err = prepare_kernel(prep[re][kind], fns[re][kind], kRedThreads, kRedSmem, dev, &per_sm);
+    if (err != cudaSuccess) return err;
+    void* args[] = {&p};
+    err = launch_kernel(fns[re][kind], dim3(ctas), dim3(kRedThreads), kRedSmem, stream, args, re != 0);
     if (err != cudaSuccess) return err;
   }
   return cudaSuccess;

@@ -327,7 +327,8 @@ def _reduce_case(zc, P, m, sigma=1e-3, reencode=True, seed=5, cb_in=None, cb_out
     assert np.array_equal(host_u16(y), oy)
 
 
-@pytest.mark.parametrize("P,m", [(1, 5000), (2, 4096), (3, 3 * 4096 + 77), (8, 1 << 16), (64, 9000), (33, 4097)])
+@pytest.mark.parametrize("P,m", [(1, 5000), (2, 4096), (3, 3 * 4096 + 77), (5, 2 * 4096 + 1000), (8, 1 << 16),
+                                 (16, 3 * 4096), (64, 9000), (33, 4097)])
 @pytest.mark.parametrize("reencode", [True, False])
 def test_decompress_reduce_small(zc, P, m, reencode):
     _reduce_case(zc, P, m, reencode=reencode, seed=P * 7 + m % 13)
@@ -335,7 +336,8 @@ def test_decompress_reduce_small(zc, P, m, reencode):
 
 @pytest.mark.parametrize("reencode", [True, False])
 def test_decompress_reduce_launch_modes(zc, reencode):
-    """Up to one tile per SM, each CTA takes one tile (one team works); above that four (one per team).  A
+    """Up to one tile per SM, each CTA takes one tile (its four teams share the tile's copies: team t decodes
+    copies t, t + 4, ...); above that four (one per team).  A
     grid of at most one CTA per SM runs the RAW-capable kernel alone; beyond it the all-coded kernel runs,
     followed by the RAW-capable one that leaves at once.  Sizes on both sides of both switches, element by
     element against the oracle."""
