@@ -144,6 +144,46 @@ def test_escape_scan_wait_is_bounded(zc):
     assert np.array_equal(main.cpu().numpy(), om)
 
 
+@pytest.mark.parametrize("m", [12 * 4096 + 5, 700 * 4096])
+def test_reduce_escape_scan_wait_is_bounded(zc, m):
+    """The hold hook on a re-encoding decode-reduce: group 0 publishes no output escape count, so the scans of
+    the later groups give up after about a second with ZC_ERR_TIMEOUT and the launch returns; the hook and the
+    exit counter are reset, and the same workspace then reduces again byte for byte as the oracle.  One size
+    per launch shape: one tile per CTA (the teams share the copies), and four tiles per CTA in the all-coded
+    launch."""
+    import math
+    import time
+    P = 3
+    shards = workloads.rs_shards(P=P, m=m, sigma=1e-3, seed=17)
+    cb_in = oracle.codebook_from_sigma(1e-3)
+    cb_out = oracle.codebook_from_sigma(1e-3 * math.sqrt(P))
+    ws = zc.workspace(m)
+    st = zc.new_status()
+    streams = [zc.compress(dev(s), zc.codebook_to_device(cb_in), ws, st) for s in shards]
+    torch.cuda.synchronize()
+    assert zc.status_value(st) == 0
+    mains, escs = [a for a, _ in streams], [b for _, b in streams]
+    ws[0:4] = torch.tensor([1, 0, 0, 0], dtype=torch.uint8, device="cuda")   # hold group 0
+    st = zc.new_status()
+    t0 = time.time()
+    zc.decompress_reduce(mains, escs, m, st, out_cb=zc.codebook_to_device(cb_out), ws=ws)
+    torch.cuda.synchronize()
+    dt = time.time() - t0
+    assert zc.status_value(st) == zc.ERR_TIMEOUT
+    assert 0.5 < dt < 30
+    hdr = ws[:8].cpu().numpy().view(np.uint32)
+    assert hdr[0] == 0 and hdr[1] == 0          # hook and exit counter reset
+    st2 = zc.new_status()
+    y, om, oe = zc.decompress_reduce(mains, escs, m, st2, out_cb=zc.codebook_to_device(cb_out), ws=ws)
+    torch.cuda.synchronize()
+    assert zc.status_value(st2) == 0
+    omains, oescs = zip(*(oracle.compress(s, cb_in) for s in shards))
+    oy, orm, ore = oracle.decompress_reduce(list(omains), list(oescs), m, cb_out)
+    assert np.array_equal(y.cpu().numpy().view(np.uint16), oy)
+    assert np.array_equal(om.cpu().numpy(), orm)
+    assert np.array_equal(oe[:ore.size].cpu().numpy(), ore)
+
+
 def test_adaptive_launch_after_a_bounded_wait(zc):
     """An adaptive launch ends at a grid barrier of its CTAs before the raw bypass.  With the hold hook its
     escape scan times out (ZC_ERR_TIMEOUT) yet every CTA still reaches the barrier, so the launch returns, the
