@@ -33,8 +33,9 @@ struct WsHeader {
   uint32_t hold_tile;  // test hook for the bounded waits: if non-zero, scan unit hold_tile - 1
                        // publishes no count, so the scans that need it must time out; reset
                        // to 0 by the launch (scan_exit)
-  uint32_t exited;     // CTAs of the running encoding launch that have read the epoch (that have
-                       // left, in the launch whose epoch wraps)
+  uint32_t exited;     // CTAs of the running encoding launch counted in once they have read the
+                       // epoch (after their scan, in the decode-reduce's long launches; as they
+                       // leave, in the launch whose epoch wraps)
   uint32_t epoch;      // epoch tag of the last finished encoding launch
   uint32_t max_tiles;  // largest flag range ever used (cleared when the epoch wraps)
   uint32_t hist_done;  // CTAs of the running histogram launch that have finished

@@ -75,3 +75,25 @@ def test_host_info_reads_cpuinfo_fields(tmp_path, monkeypatch):
 
     monkeypatch.setattr(builtins, "open", fake_open)
     assert bench.host_info()["cpu"] == "implementer 0x41 part 0xd4f"
+
+
+def test_traffic_record_follows_code_not_comments(tmp_path, monkeypatch):
+    """A measured DRAM traffic figure is tied to the kernel's code: comment and whitespace edits keep it, a
+    code edit turns it into null."""
+    import shutil
+    import bench
+    csrc = tmp_path / "lossless_bf16_exponent_zc_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in bench.KERNEL_SOURCES["encode_kernel"]:
+        shutil.copy(os.path.join(bench.ROOT, "lossless_bf16_exponent_zc_gb300", "csrc", f), csrc / f)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.source_hash("encode_kernel")
+    main = csrc / bench.KERNEL_SOURCES["encode_kernel"][0]
+    text = main.read_text()
+    main.write_text("// a new comment line\n" + text.replace("\n", "  \n", 3) + "\n\n")
+    assert bench.source_hash("encode_kernel") == h0
+    monkeypatch.setitem(bench.MEASURED_TRAFFIC, "encode_kernel", (h0, 123))
+    assert bench.measured_traffic("encode_kernel") == 123
+    main.write_text(text + "\nconstexpr int kAnotherConstant = 1;\n")
+    assert bench.source_hash("encode_kernel") != h0
+    assert bench.measured_traffic("encode_kernel") is None
