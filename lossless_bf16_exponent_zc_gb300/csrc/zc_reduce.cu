@@ -228,10 +228,36 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
   // barrier that precedes the scan warp's count, scan_arrive)
   const uint32_t epoch = REENC ? launch_epoch(p.ws) : 0u;
   const uint32_t hold = REENC ? launch_hold(p.ws) : 0u;
+  // Producer warps: offsets [a, b) of the tile of team pt0 + u in a round, for
+  // shard lane + 32 h.  The first round's are loaded here, so that they arrive
+  // while the headers are checked; the end of a shard's last tile is the
+  // header's escape count, read directly.
+  const uint32_t ngroups = (p.ntiles + p.gt - 1) / p.gt;
+  const uint32_t pt0 = (warp - kRedProd) * kTeamsPerProducer;
+  uint32_t na[kTeamsPerProducer][2], nb[kTeamsPerProducer][2];
+  auto load_offsets = [&](uint32_t G) {
+#pragma unroll
+    for (int u = 0; u < kTeamsPerProducer; u++)
+#pragma unroll
+      for (int h = 0; h < 2; h++) {
+        na[u][h] = nb[u][h] = 0;
+        const uint32_t g = SPLIT ? G : G * p.gt + pt0 + u;
+        const uint32_t r = lane + 32u * h;
+        if ((SPLIT || pt0 + u < p.gt) && G < ngroups && g < p.ntiles && r < static_cast<uint32_t>(p.P)) {
+          const uint32_t* hdr = reinterpret_cast<const uint32_t*>(p.s[r].main);
+          const uint32_t* tbl = reinterpret_cast<const uint32_t*>(p.s[r].main + kHeader);
+          na[u][h] = __ldg(tbl + g);
+          const uint64_t bb = (g + 1 < p.ntiles)
+                                  ? static_cast<uint64_t>(__ldg(tbl + g + 1))
+                                  : static_cast<uint64_t>(__ldg(hdr + 6)) | (static_cast<uint64_t>(__ldg(hdr + 7)) << 32);
+          nb[u][h] = bb > 0xFFFFFFFFull ? 0xFFFFFFFFu : static_cast<uint32_t>(bb);
+        }
+      }
+  };
+  if (warp >= kRedProd && warp < kRedScan) load_offsets(blockIdx.x);
   __syncthreads();
   if (!RAW && *raw_s != 0ull) return;  // the RAW-capable launch that follows does the work
   const bool skip = flags_s[0] != 0 || flags_s[1] != 0;
-  const uint32_t ngroups = (p.ntiles + p.gt - 1) / p.gt;
   // The scan warp counts the CTA in at once in the RAW-capable kernel, which
   // runs alone when every CTA has at most one group (there the count's round
   // trip would otherwise end the launch), and at the end of its scan in the
@@ -266,27 +292,9 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     const uint32_t t0 = (warp - kRedProd) * kTeamsPerProducer;
     const uint32_t P = static_cast<uint32_t>(p.P);
     uint32_t uses = 0;  // copies this lane has started for its team (lanes < kTeamsPerProducer)
-    // offsets [a, b) of the tile of team t0 + u in the next round, for shard lane + 32 h
-    uint32_t na[kTeamsPerProducer][2], nb[kTeamsPerProducer][2];
     // the round's plan per team and shard: pa = the tile's first escape;
     // pk = count | staged << 13 | (span / 16) << 23 | consistent << 31
     uint32_t pa[kTeamsPerProducer][2], pk[kTeamsPerProducer][2];
-    auto load_offsets = [&](uint32_t G) {
-#pragma unroll
-      for (int u = 0; u < kTeamsPerProducer; u++)
-#pragma unroll
-        for (int h = 0; h < 2; h++) {
-          na[u][h] = nb[u][h] = 0;
-          const uint32_t g = split ? G : G * p.gt + t0 + u;
-          const uint32_t r = lane + 32u * h;
-          if ((split || t0 + u < p.gt) && G < ngroups && g < p.ntiles && r < P) {
-            const uint32_t* tbl = reinterpret_cast<const uint32_t*>(p.s[r].main + kHeader);
-            na[u][h] = __ldg(tbl + g);
-            const uint64_t bb = (g + 1 < p.ntiles) ? static_cast<uint64_t>(__ldg(tbl + g + 1)) : si[r].n_esc;
-            nb[u][h] = bb > 0xFFFFFFFFull ? 0xFFFFFFFFu : static_cast<uint32_t>(bb);
-          }
-        }
-    };
     auto plan_round = [&]() {
 #pragma unroll
       for (int h = 0; h < 2; h++) {
@@ -316,7 +324,6 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
         }
       }
     };
-    load_offsets(blockIdx.x);
     for (uint32_t G = blockIdx.x; G < ngroups; G += step) {
       plan_round();              // from this round's offsets
       load_offsets(G + step);    // the next round's, consumed once this round is issued
