@@ -201,7 +201,7 @@ __device__ __forceinline__ void raw_rewrite(const EncTensor& T, uint64_t tid, ui
 // The raw bypass of an adaptive launch, run by every thread once its CTA's
 // encoding is done.  The CTAs meet at a grid barrier (the launch is
 // cooperative), so every tensor's n_esc is final; each CTA reads the counts
-// and reaches the same verdict.  In the usual case nothing goes RAW and that
+// and reaches the same decision.  In the usual case nothing goes RAW and that
 // is all: no further launch, no counter.  Otherwise every thread of the grid
 // rewrites the RAW tensors, and the last CTA to finish -- after every CTA has
 // read the counts -- writes their RAW headers (flags and n_esc).  A CTA whose
@@ -228,7 +228,7 @@ __device__ __forceinline__ void raw_bypass(const EncParams<MAXB>& p) {
   }
   __syncthreads();
   const uint32_t mask = raw_mask;
-  if (mask == 0) return;  // every CTA reached the same verdict
+  if (mask == 0) return;  // every CTA reached the same decision
   const uint64_t tid = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const uint64_t nthreads = static_cast<uint64_t>(gridDim.x) * blockDim.x;
   for (int i = 0; i < p.count; i++)
@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
       if (static_cast<int>(ti) != cur_ti) {
         cur_ti = static_cast<int>(ti);
         const uint8_t* cb = p.t[ti].cb;
-        if (cb != cur_cb) {  // tensors that share a codebook share the verdict
+        if (cb != cur_cb) {  // tensors that share a codebook share the decision
           cur_cb = cb;
           cb_ok = true;
 #pragma unroll
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_kernel(const __grid_con
         cur_tiles = T.main + kHeader + table_bytes(cur_ntiles);
         cur_g0 = p.group_start[ti];
         if (T.cb != cur_cb) {  // tensors that share a codebook (same pointer) share the table
-          cb_ok = build_enc_lut(lut, T.cb);  // every warp of the group reaches the same verdict
+          cb_ok = build_enc_lut(lut, T.cb);  // every warp of the group reaches the same decision
           cur_cb = T.cb;
           if (!cb_ok && lane == 0) set_status(p.status, ZC_ERR_DUP_CODEBOOK);
         }

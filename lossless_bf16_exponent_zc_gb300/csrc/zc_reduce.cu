@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
   }
   if (!check_first) pdl_wait();  // after the shared-memory setup, which overlaps the previous kernel
   __syncthreads();
-  // validate every shard header (each CTA reaches the same verdict)
+  // validate every shard header (each CTA reaches the same decision)
   for (int r = threadIdx.x; r < p.P; r += blockDim.x) {
     const uint32_t* w = reinterpret_cast<const uint32_t*>(p.s[r].main);
     const uint64_t n = static_cast<uint64_t>(__ldg(w + 2)) | (static_cast<uint64_t>(__ldg(w + 3)) << 32);

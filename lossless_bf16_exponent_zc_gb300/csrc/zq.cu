@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kQDecWarps * 32) zq_decode_kernel(const __grid
   const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
   const uint64_t nb = zq_blocks(p.n);
   const uint64_t tbl = zq_table_bytes(nb);
-  // header checks (every CTA reaches the same verdict) and the 11-bit table
+  // header checks (every CTA reaches the same decision) and the 11-bit table
   if (threadIdx.x < 8) S.seen[threadIdx.x] = 0u;
   if (lane == 0) {
     mbar_init(&S.bar[warp], 1);
