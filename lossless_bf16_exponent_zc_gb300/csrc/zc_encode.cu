@@ -8,9 +8,10 @@
 // warps per SM.  The work unit of a warp is a whole tile (4 blocks, 4096
 // values, one 8 KB TMA bulk copy into one of its two shared-memory stages): a
 // unit's fixed work (stage wait and refill, counts, offset-table entry, queue)
-// is spread over twice the values of a half-tile unit, and the 168 registers
-// of an 11-warp CTA hold four blocks' bookkeeping.  A CTA works through groups
-// of 11 consecutive tiles (group G, G + C, ... for C CTAs); encoding warp w
+// is spread over twice the values of a half-tile unit, and the registers an
+// 11-warp CTA may use (up to 168 a thread) hold four blocks' bookkeeping.  A
+// CTA works through groups of 11 consecutive tiles (group G, G + C, ... for C
+// CTAs); encoding warp w
 // takes tile w of each group.  The group is the unit of the escape scan: the
 // warps' escape counts meet in shared memory, the last encoding warp to finish
 // a group publishes the group's count at once, the 12th "scan" warp finds the
