@@ -11,11 +11,11 @@
 // is spread over twice the values of a half-tile unit, and the registers an
 // 11-warp CTA may use (up to 168 a thread) hold four blocks' bookkeeping.  A
 // CTA works through groups of 11 consecutive tiles (group G, G + C, ... for C
-// CTAs); encoding warp w
-// takes tile w of each group.  The group is the unit of the escape scan: the
-// warps' escape counts meet in shared memory, the last encoding warp to finish
-// a group publishes the group's count at once, the 12th "scan" warp finds the
-// group's escape offset and posts the group's offsets in shared memory.
+// CTAs); encoding warp w takes tile w of each group.  The group is the unit
+// of the escape scan: the warps' escape counts meet in shared memory, the
+// last encoding warp to finish a group publishes the group's count at once,
+// the 12th "scan" warp finds the group's escape offset and posts the group's
+// offsets in shared memory.
 //
 // CTAs drift apart by several rounds (the order in which HBM serves their
 // loads), and a group's offset is known only once every group before it is
