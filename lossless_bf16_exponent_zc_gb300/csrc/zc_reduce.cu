@@ -7,8 +7,8 @@
 //   * 16 consumer warps in 4 teams; team t owns tile 4G + t of each group G
 //     (G, G + C, ... for C CTAs) and warp b of the team owns block b of that
 //     tile, keeping its 1024 fp32 partial sums in registers (32 per lane).
-//     Inputs of at most one tile per SM give each CTA one tile instead, and
-//     the teams share its P copies: team t decodes copies t, t + 4, ... into
+//     Inputs of at most two tiles per SM give each CTA one tile per round
+//     instead, and the teams share its P copies: team t decodes copies t, t + 4, ... into
 //     shared memory and all 16 warps add each four, in rank order, to the sums
 //     of their 256 values (one warp per block and copy would leave the SM's
 //     schedulers a single warp each).
@@ -142,7 +142,7 @@ __device__ __forceinline__ uint4 round_pack(const float (&acc)[8]) {
 // test out of the all-coded kernel keeps its code as lean as before).  A grid
 // of at most one CTA per SM is launch-bound: there the RAW-capable kernel
 // runs alone (p.single) and does the work for any shards.  SPLIT = true: that
-// kernel for inputs of at most one tile per SM (one tile per CTA, gt == 1).
+// kernel for inputs of at most two tiles per SM (one tile per group, gt == 1).
 template <bool REENC, bool RAW, bool SPLIT>
 __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_constant__ RedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -268,12 +268,12 @@ __global__ void __launch_bounds__(kRedThreads, 1) reduce_kernel(const __grid_con
     scan_exit(p.ws, p.flags, epoch, ngroups, RAW || lane != 0 ? arrival : scan_arrive(p.ws, epoch));
   };
   const uint32_t step = gridDim.x;
-  // SPLIT (inputs of at most one tile per SM, gt == 1; a RAW-capable kernel):
-  // the four teams share each CTA's tile, team t decoding copies t, t + 4, ...
+  // SPLIT (inputs of at most two tiles per SM, gt == 1; a RAW-capable kernel):
+  // the four teams share each of the CTA's tiles, team t decoding copies t, t + 4, ...
   // into its 8 KB of the rounded-tile area, and after every four copies all 16
   // consumer warps add them, in rank order, to the sums of their 256 values of
   // the tile; team 0 then rounds and re-encodes as usual.
-  static_assert(RAW || !SPLIT, "the one-tile-per-CTA kernel is a RAW-capable one");
+  static_assert(RAW || !SPLIT, "the SPLIT kernel is a RAW-capable one");
   constexpr bool split = SPLIT;
   if (REENC && !skip && p.ntiles == 0 && blockIdx.x == 0 && warp == 0) {
     write_header_words(p.out_main, 0, p.out_cb);
@@ -775,17 +775,20 @@ cudaError_t launch_reduce(const Shard* shards, int P, uint64_t n, uint16_t* out,
   p.ws = ws;
   p.flags = flags;
   p.status = status;
-  // Inputs of at most one tile per SM take one tile per group (team 0 of each
-  // CTA): the P copies of a tile are decoded one after another by its team, so
-  // spreading the tiles over more SMs shortens the launch.
-  p.gt = p.ntiles <= static_cast<uint32_t>(dev.sm_count) ? 1u : kGroupTilesR;
+  // Inputs of at most two tiles per SM take one tile per group, and the four
+  // teams of a CTA share each tile's P copies (SPLIT): with four tiles per CTA
+  // a team decodes a tile's copies one after another, so on few tiles the
+  // launch would be as long as P serial copies on a quarter of the SMs.
+  const bool split = p.ntiles <= 2u * static_cast<uint32_t>(dev.sm_count);
+  p.gt = split ? 1u : kGroupTilesR;
   const uint32_t ngroups = (p.ntiles + p.gt - 1) / p.gt;
   uint32_t ctas = ngroups;
   if (ctas > static_cast<uint32_t>(dev.sm_count)) ctas = dev.sm_count;
   if (ctas == 0) ctas = 1;
   // The all-coded launch, then the RAW-capable one; exactly one of them works.
-  // A grid of at most one CTA per SM gets the RAW-capable launch alone.
-  p.single = ngroups <= static_cast<uint32_t>(dev.sm_count) ? 1 : 0;
+  // A grid of at most one group per CTA, and the SPLIT shape, get the
+  // RAW-capable launch alone.
+  p.single = split || ngroups <= static_cast<uint32_t>(dev.sm_count) ? 1 : 0;
   // [re-encode][kind]: all-coded, RAW-capable, RAW-capable with one tile per CTA (the teams share its copies)
   static KernelPrep prep[2][3];
   const void* const fns[2][3] = {

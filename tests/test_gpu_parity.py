@@ -336,13 +336,14 @@ def test_decompress_reduce_small(zc, P, m, reencode):
 
 @pytest.mark.parametrize("reencode", [True, False])
 def test_decompress_reduce_launch_modes(zc, reencode):
-    """Up to one tile per SM, each CTA takes one tile (its four teams share the tile's copies: team t decodes
-    copies t, t + 4, ...); above that four (one per team).  A
+    """Up to two tiles per SM, each CTA takes one tile per round (its four teams share the tile's copies: team t
+    decodes copies t, t + 4, ...) in the RAW-capable kernel alone; above that four (one per team).  A
     grid of at most one CTA per SM runs the RAW-capable kernel alone; beyond it the all-coded kernel runs,
     followed by the RAW-capable one that leaves at once.  Sizes on both sides of both switches, element by
     element against the oracle."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    for m in (4096 * sms, 4096 * sms + 1, 4096 * (4 * (sms - 1) - 1) + 55, 4 * 4096 * sms + 4096 + 9):
+    for m in (4096 * sms, 4096 * sms + 1, 2 * 4096 * sms, 2 * 4096 * sms + 7, 4096 * (4 * (sms - 1) - 1) + 55,
+              4 * 4096 * sms + 4096 + 9):
         _reduce_case(zc, 3, m, reencode=reencode, seed=m % 101)
 
 

@@ -208,11 +208,11 @@ def test_raw_header_errors(zc):
         assert zc.status_value(st) == zc.ERR_BAD_HEADER
 
 
-@pytest.mark.parametrize("n", [4096 * 8 + 1234, 6913, 4096 * 400 + 5, 4096 * 700 + 77])
+@pytest.mark.parametrize("n", [4096 * 8 + 1234, 6913, 4096 * 250 + 3, 4096 * 400 + 5, 4096 * 700 + 77])
 def test_reduce_over_raw_and_coded_shards(zc, n):
     """A zipped reduce-scatter receives whatever each sender chose: mixed RAW and coded shards.  Sizes for each
-    launch mode: one tile per CTA (the teams share the copies), four tiles per CTA in one launch, and the
-    all-coded launch that leaves for the RAW-capable one."""
+    launch mode: one tile per CTA and round (the teams share the copies; one or two rounds), four tiles per CTA
+    in one launch, and the all-coded launch that leaves for the RAW-capable one."""
     P = 5
     cb_in = oracle.codebook_from_sigma(1e-3)
     cb_out = oracle.codebook_from_sigma(1e-3 * np.sqrt(P))
