@@ -133,7 +133,8 @@ __global__ void __launch_bounds__(kQEncThreads, 1) zq_encode_kernel(const __grid
     }
     if (nb == 0 && lane == 0) *reinterpret_cast<unsigned long long*>(p.out + 24) = 0ull;
   }
-  const uint32_t epoch = launch_epoch(p.ws);  // (before the barrier that precedes scan_arrive)
+  const uint32_t epoch = launch_epoch(p.ws);  // (both before the barrier that precedes scan_arrive)
+  const uint32_t hold = launch_hold(p.ws);    // test hook: group hold - 1 publishes no size
   __syncthreads();
   const uint64_t groups = (nb + kQEncWarps - 1) / kQEncWarps;
   const uint32_t R = blockIdx.x < groups
@@ -227,7 +228,8 @@ __global__ void __launch_bounds__(kQEncThreads, 1) zq_encode_kernel(const __grid
       const uint32_t w = lane < kQEncWarps ? S.words[r & 1][lane] : 0u;
       const uint32_t inc = warp_inclusive_scan(w);
       const uint32_t total = __shfl_sync(kFull, inc, 31);
-      if (lane == 0) st_relaxed(&p.flags[G].agg, (static_cast<unsigned long long>(epoch) << 32) | total);
+      if (lane == 0 && static_cast<uint64_t>(hold) != G + 1)
+        st_relaxed(&p.flags[G].agg, (static_cast<unsigned long long>(epoch) << 32) | total);
       bool timed_out;
       const uint32_t lo = r > 0 ? static_cast<uint32_t>(group_of(r - 1)) + 1u : 0u;
       const uint64_t prefix = (r > 0 ? prev_incl : 0) +

@@ -180,6 +180,26 @@ def test_several_rounds_and_a_partial_last_group(zc, widths):
     check(zc, x, widths, oracle.qlc_table_for(x))
 
 
+@pytest.mark.parametrize("n", [40 * 4096 + 9, (16 * 152 * 2 + 5) * 4096])
+def test_escape_scan_wait_is_bounded(zc, n):
+    """The workspace's hold hook on the QLC encoder: group 0 publishes no size, so the block-offset scans of the
+    later groups give up after about a second with ZC_ERR_TIMEOUT and the launch returns; the hook and the exit
+    counter are reset, and the same workspace then compresses again byte for byte as the oracle.  One size
+    with one group per CTA, one with several."""
+    import time
+    x = workloads.fp8_ffn1(n, seed=77)
+    sym = oracle.qlc_table_for(x)
+    ws = zc.workspace(n)
+    ws[0:4] = torch.tensor([1, 0, 0, 0], dtype=torch.uint8, device="cuda")   # hold group 0
+    t0 = time.time()
+    gpu_encode(zc, x, DEFAULT, sym, ws=ws, expect=zc.ERR_TIMEOUT)
+    dt = time.time() - t0
+    assert 0.5 < dt < 30
+    hdr = ws[:8].cpu().numpy().view(np.uint32)
+    assert hdr[0] == 0 and hdr[1] == 0          # hook and exit counter reset
+    check(zc, x, DEFAULT, sym, ws=ws)
+
+
 @pytest.mark.slow
 def test_full_size_ffn1(zc):
     n = 1 << 26
