@@ -148,11 +148,33 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     fence_mbar_init();
   }
   pdl_wait();
-  for (int i = threadIdx.x; i < p.count; i += blockDim.x) hdr_cache[i] = read_header(p.t[i], i, p.status);
-  __syncthreads();
-
   const uint32_t total_warps = gridDim.x * kDecWarps;
   const uint32_t gw = blockIdx.x * kDecWarps + warp;
+  // The first stages' offset-table entries are loaded with the headers (the end
+  // of a tensor's last tile is its header's escape count, read directly), so
+  // the escape ranges are known once the headers are.
+  uint64_t pre_a[kDecStages], pre_b[kDecStages];
+  {
+    uint32_t ti0 = 0;
+#pragma unroll
+    for (int s = 0; s < kDecStages; s++) {
+      const uint32_t g = gw + s * total_warps;
+      pre_a[s] = pre_b[s] = 0;
+      if (g < p.total_tiles) {
+        const uint32_t ti = dec_locate(p, g, ti0);
+        const DecTensor& T = p.t[ti];
+        const uint32_t lt = g - p.tile_start[ti];
+        const uint64_t ntiles = num_tiles(T.n);
+        const uint32_t* hw = reinterpret_cast<const uint32_t*>(T.main);
+        const uint32_t* tbl = reinterpret_cast<const uint32_t*>(T.main + kHeader);
+        pre_a[s] = __ldg(tbl + lt);
+        pre_b[s] = (lt + 1 < ntiles) ? static_cast<uint64_t>(__ldg(tbl + lt + 1))
+                                     : static_cast<uint64_t>(__ldg(hw + 6)) | (static_cast<uint64_t>(__ldg(hw + 7)) << 32);
+      }
+    }
+  }
+  for (int i = threadIdx.x; i < p.count; i += blockDim.x) hdr_cache[i] = read_header(p.t[i], i, p.status);
+  __syncthreads();
   auto stage_ptr = [&](int s) { return wstage + s * kDecStageBytes; };
 
   HdrInfo issue_hdr;
@@ -161,7 +183,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   bool st_ok[kDecStages], st_raw[kDecStages];
   DecTable st_dt[kDecStages];  // code table of the staged tile's tensor (read when it was issued)
   uint32_t issue_ti = 0;  // running tensor index of issue()
-  auto issue = [&](int s, uint32_t g) {
+  auto issue = [&](int s, uint32_t g, bool first) {
     const uint32_t ti = dec_locate(p, g, issue_ti);
     const DecTensor& T = p.t[ti];
     if (issue_hdr.ti != static_cast<int>(ti)) issue_hdr = hdr_cache[ti];
@@ -170,7 +192,14 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     bool ok = issue_hdr.ok;
     st_raw[s] = issue_hdr.raw;
     if (!issue_hdr.raw) {
-      tile_escape_range(T, issue_hdr, lt, a, cnt, ok);
+      if (first) {
+        const uint64_t aa = pre_a[s], bb = pre_b[s];
+        ok = ok && aa <= bb && bb <= issue_hdr.n_esc && bb - aa <= kTile;
+        a = ok ? static_cast<uint32_t>(aa) : 0;
+        cnt = ok ? static_cast<uint32_t>(bb - aa) : 0;
+      } else {
+        tile_escape_range(T, issue_hdr, lt, a, cnt, ok);
+      }
       if (!ok && issue_hdr.ok && lane == 0) set_status(p.status, ZC_ERR_CORRUPT_STREAM);
     }
     uint8_t* sp = stage_ptr(s);
@@ -193,7 +222,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
 #pragma unroll
   for (int s = 0; s < kDecStages; s++) {
     const uint32_t g = gw + s * total_warps;
-    if (g < p.total_tiles) issue(s, g);
+    if (g < p.total_tiles) issue(s, g, true);
   }
 
   uint32_t run_ti = 0;
@@ -249,7 +278,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
       }
       __syncwarp();
       const uint32_t gn = g + kDecStages * total_warps;
-      if (gn < p.total_tiles) issue(s, gn);
+      if (gn < p.total_tiles) issue(s, gn, false);
     }
   }
 }
